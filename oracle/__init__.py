@@ -1,0 +1,133 @@
+"""fp64 CPU oracle for the row-wise RMSNorm forward.
+
+TEST INFRASTRUCTURE ONLY.  The tests, the package smoke check and the
+benchmark's CPU baseline (and its ``--impl reference`` arm) may import this
+module; the CUDA library and its Python binding never do.  It shares no code
+with the CUDA path: the arithmetic lives in ``oracle.c`` (plain C, binary64),
+built here with gcc into ``oracle/_build/liboracle.so``.
+
+What it computes is the RMSNorm of "Build a GPU compiler from scratch: from
+PyTorch to CUDA via multi-level IR (Emmy)" (introduction and section "Tensor
+IR": square, sum, divide by the count, add epsilon, rsqrt, two multiplies)
+and "CuTeDSL at Perplexity", section "QK Norm" (rsqrt of the mean square plus
+EPS, times the element, times the weight, cast back to the element type).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_OUT_DIR, "liboracle.so")
+
+F32, BF16, F16 = 0, 1, 2
+_FMT = {"f32": F32, "bf16": BF16, "f16": F16}
+_STORAGE = {F32: np.float32, BF16: np.uint16, F16: np.uint16}
+
+_lib = None
+
+
+def fmt_code(dtype) -> int:
+    """Accept 'f32' / 'bf16' / 'f16' or an integer code."""
+    if isinstance(dtype, str):
+        return _FMT[dtype]
+    return int(dtype)
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c with gcc (plain C11, -O2, no SIMD intrinsics)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    stale = (not os.path.exists(_LIB_PATH)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC)
+             or os.path.getmtime(_LIB_PATH) < os.path.getmtime(os.path.join(_HERE, "oracle.h")))
+    if force or stale:
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
+                       check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    global _lib
+    if _lib is None:
+        l = ctypes.CDLL(build())
+        vp, i64, f32, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+        for name in ("oracle_rmsnorm_f64", "oracle_rmsnorm"):
+            getattr(l, name).argtypes = [vp, vp, vp, i64, i64, f32, i32]
+            getattr(l, name).restype = i32
+        for name in ("oracle_widen_array", "oracle_round_array"):
+            getattr(l, name).argtypes = [vp, vp, i64, i32]
+            getattr(l, name).restype = i32
+        l.oracle_round_value.argtypes = [ctypes.c_double, i32]
+        l.oracle_round_value.restype = ctypes.c_double
+        _lib = l
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _check_storage(a: np.ndarray, fmt: int) -> np.ndarray:
+    want = _STORAGE[fmt]
+    if a.dtype != want:
+        raise TypeError(f"format {fmt} wants storage {np.dtype(want)}, got {a.dtype}")
+    return np.ascontiguousarray(a)
+
+
+def rmsnorm_f64(x: np.ndarray, w: np.ndarray, eps: float, dtype) -> np.ndarray:
+    """y = x * rsqrt(mean(x^2) + eps) * w per row, in binary64 (unrounded).
+
+    ``x`` is [rows, hidden] storage (float32, or uint16 bit patterns for
+    bf16/f16); ``w`` is [hidden] of the same storage."""
+    fmt = fmt_code(dtype)
+    x = _check_storage(x, fmt)
+    w = _check_storage(w, fmt)
+    rows, hidden = x.shape
+    if w.shape != (hidden,):
+        raise ValueError("weight must have shape [hidden]")
+    y = np.empty((rows, hidden), dtype=np.float64)
+    rc = lib().oracle_rmsnorm_f64(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(eps), fmt)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_f64 rejected its arguments")
+    return y
+
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float, dtype) -> np.ndarray:
+    """The oracle's result rounded (nearest-even, from binary64) to the
+    element format; returned in the same storage as ``x``."""
+    fmt = fmt_code(dtype)
+    x = _check_storage(x, fmt)
+    w = _check_storage(w, fmt)
+    rows, hidden = x.shape
+    if w.shape != (hidden,):
+        raise ValueError("weight must have shape [hidden]")
+    y = np.empty((rows, hidden), dtype=_STORAGE[fmt])
+    rc = lib().oracle_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(eps), fmt)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm rejected its arguments")
+    return y
+
+
+def widen(a: np.ndarray, dtype) -> np.ndarray:
+    """Exact binary64 values of stored elements."""
+    fmt = fmt_code(dtype)
+    a = _check_storage(a, fmt)
+    out = np.empty(a.shape, dtype=np.float64)
+    lib().oracle_widen_array(_ptr(a), _ptr(out), a.size, fmt)
+    return out
+
+
+def round_to(v: np.ndarray, dtype) -> np.ndarray:
+    """Round binary64 values to the format, nearest-even, in its storage."""
+    fmt = fmt_code(dtype)
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    out = np.empty(v.shape, dtype=_STORAGE[fmt])
+    lib().oracle_round_array(_ptr(v), _ptr(out), v.size, fmt)
+    return out

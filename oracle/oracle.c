@@ -1,0 +1,242 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU restatement of the row-wise RMSNorm forward.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the oracle that the CUDA path is
+ * checked against.  Only the test suite, the package's smoke check and the
+ * benchmark's CPU-baseline / reference arm may load it.  The product path
+ * (the CUDA library under rmsnorm_fwd_gb300/) never calls, links or includes
+ * anything from here, and this file includes nothing from there.
+ *
+ * What it computes (one row i of a row-major [rows, hidden] tensor):
+ *
+ *   "Build a GPU compiler from scratch: from PyTorch to CUDA via multi-level
+ *    IR (Emmy)", introduction (the RMSNorm running example) and section
+ *    "Tensor IR" (the arithmetic steps: square, sum, divide by the count,
+ *    add epsilon, rsqrt, two multiplies):
+ *
+ *        S   = sum_j x[i,j]^2
+ *        r   = 1 / sqrt(S / hidden + eps)
+ *        y   = x[i,j] * r * w[j]
+ *
+ *   "CuTeDSL at Perplexity", section "QK Norm": the same statistic taken as
+ *   rsqrt(sum / head_dim + EPS), each element scaled by that factor and by
+ *   its weight, the result cast back to the input's element type.
+ *
+ * Every value is widened exactly to IEEE binary64 and every operation runs in
+ * binary64, left to right, with no blocking, fusion or reordering.  The final
+ * rounding to a 16-bit format is done directly from binary64 with
+ * round-to-nearest-even (no intermediate binary32 step, so no double
+ * rounding).
+ *
+ * Formats: 0 = IEEE binary32, 1 = bfloat16, 2 = IEEE binary16.  16-bit
+ * values travel as raw uint16 bit patterns.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <string.h>
+
+/* ---- exact widening of one stored element to binary64 ------------------ */
+
+static double widen_f32(uint32_t bits)
+{
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f; /* every binary32 value is exactly a binary64 value */
+}
+
+/* bfloat16: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits. */
+static double widen_bf16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 7) & 0xFF;
+    int frac = bits & 0x7F;
+    double mag;
+    if (expo == 0xFF)
+        mag = frac ? NAN : INFINITY;
+    else if (expo == 0)
+        mag = ldexp((double)frac, -126 - 7); /* subnormal: frac * 2^-133 */
+    else
+        mag = ldexp((double)(128 + frac), expo - 127 - 7);
+    return sign ? -mag : mag;
+}
+
+/* binary16: 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits. */
+static double widen_f16(uint16_t bits)
+{
+    int sign = (bits >> 15) & 1;
+    int expo = (bits >> 10) & 0x1F;
+    int frac = bits & 0x3FF;
+    double mag;
+    if (expo == 0x1F)
+        mag = frac ? NAN : INFINITY;
+    else if (expo == 0)
+        mag = ldexp((double)frac, -14 - 10); /* subnormal: frac * 2^-24 */
+    else
+        mag = ldexp((double)(1024 + frac), expo - 15 - 10);
+    return sign ? -mag : mag;
+}
+
+double oracle_widen(const void *base, int64_t index, int fmt)
+{
+    if (fmt == ORACLE_F32) {
+        uint32_t b;
+        memcpy(&b, (const char *)base + 4 * index, 4);
+        return widen_f32(b);
+    }
+    uint16_t h;
+    memcpy(&h, (const char *)base + 2 * index, 2);
+    return fmt == ORACLE_BF16 ? widen_bf16(h) : widen_f16(h);
+}
+
+/* ---- round binary64 to a narrow binary format, nearest-even ------------ */
+
+/*
+ * A binary format with p significand bits (counting the hidden bit), minimum
+ * normal exponent emin and maximum exponent emax.  The representable numbers
+ * in the binade [2^e, 2^(e+1)) are integer multiples of 2^(e-p+1); below 2^emin
+ * they are multiples of 2^(emin-p+1).  Rounding a = |v| therefore means: take
+ * the spacing q of the binade a falls in, round a/q to the nearest integer
+ * with ties to even (rint() under the default rounding mode does exactly
+ * that, and a/q is exact because q is a power of two), and multiply back.
+ * Results above the largest finite value become infinity.
+ */
+static double round_to_format(double v, int p, int emin, int emax)
+{
+    if (isnan(v) || isinf(v) || v == 0.0)
+        return v;
+    double a = fabs(v);
+    int k;
+    frexp(a, &k);          /* a = m * 2^k with m in [0.5, 1): a in [2^(k-1), 2^k) */
+    int e = k - 1;
+    if (e < emin)
+        e = emin;
+    int qexp = e - (p - 1);
+    double n = rint(ldexp(a, -qexp));
+    double r = ldexp(n, qexp);
+    double maxfinite = ldexp((double)((1 << p) - 1), emax - p + 1);
+    if (r > maxfinite)
+        r = INFINITY;
+    return v < 0 ? -r : r;
+}
+
+/* Encode a value that is already exactly representable in the format. */
+static uint16_t encode_narrow(double v, int p, int emin, int ebits)
+{
+    uint16_t sign = signbit(v) ? (uint16_t)(1u << 15) : 0;
+    int fbits = p - 1;
+    uint16_t expmask = (uint16_t)((1u << ebits) - 1);
+    if (isnan(v))
+        return (uint16_t)(sign | (expmask << fbits) | (1u << (fbits - 1)));
+    if (isinf(v))
+        return (uint16_t)(sign | (expmask << fbits));
+    double a = fabs(v);
+    if (a == 0.0)
+        return sign;
+    int bias = 1 - emin;
+    if (a < ldexp(1.0, emin)) { /* subnormal: a = frac * 2^(emin - fbits) */
+        uint16_t frac = (uint16_t)ldexp(a, -(emin - fbits));
+        return (uint16_t)(sign | frac);
+    }
+    int k;
+    frexp(a, &k);
+    int e = k - 1;
+    uint16_t frac = (uint16_t)(ldexp(a, -(e - fbits)) - ldexp(1.0, fbits));
+    return (uint16_t)(sign | ((uint16_t)(e + bias) << fbits) | frac);
+}
+
+double oracle_round_value(double v, int fmt)
+{
+    switch (fmt) {
+    case ORACLE_F32:
+        return round_to_format(v, 24, -126, 127);
+    case ORACLE_BF16:
+        return round_to_format(v, 8, -126, 127);
+    default:
+        return round_to_format(v, 11, -14, 15);
+    }
+}
+
+void oracle_store(double v, void *base, int64_t index, int fmt)
+{
+    double r = oracle_round_value(v, fmt);
+    if (fmt == ORACLE_F32) {
+        float f = (float)r; /* exact: r is already a binary32 value */
+        memcpy((char *)base + 4 * index, &f, 4);
+        return;
+    }
+    uint16_t h = fmt == ORACLE_BF16 ? encode_narrow(r, 8, -126, 8)
+                                    : encode_narrow(r, 11, -14, 5);
+    memcpy((char *)base + 2 * index, &h, 2);
+}
+
+/* ---- the method --------------------------------------------------------- */
+
+/*
+ * One row: square every element, sum them, divide the sum by the row length,
+ * add epsilon, take the reciprocal square root, then multiply each element
+ * by that factor and by its weight.  The statistic S is a row-local value
+ * and is never stored.
+ */
+static double row_factor(const void *x, int64_t row, int64_t hidden, double eps, int fmt)
+{
+    double S = 0.0;
+    for (int64_t j = 0; j < hidden; ++j) {
+        double xv = oracle_widen(x, row * hidden + j, fmt);
+        S += xv * xv;
+    }
+    double mean = S / (double)hidden;
+    return 1.0 / sqrt(mean + eps);
+}
+
+int oracle_rmsnorm_f64(const void *x, const void *w, double *y, int64_t rows,
+                       int64_t hidden, float eps, int fmt)
+{
+    if (rows < 0 || hidden <= 0 || fmt < 0 || fmt > 2)
+        return -1;
+    double e = (double)eps; /* both sides see the same binary32 epsilon */
+    for (int64_t i = 0; i < rows; ++i) {
+        double r = row_factor(x, i, hidden, e, fmt);
+        for (int64_t j = 0; j < hidden; ++j) {
+            double xv = oracle_widen(x, i * hidden + j, fmt);
+            double wv = oracle_widen(w, j, fmt);
+            y[i * hidden + j] = xv * r * wv;
+        }
+    }
+    return 0;
+}
+
+int oracle_rmsnorm(const void *x, const void *w, void *y, int64_t rows,
+                   int64_t hidden, float eps, int fmt)
+{
+    if (rows < 0 || hidden <= 0 || fmt < 0 || fmt > 2)
+        return -1;
+    double e = (double)eps;
+    for (int64_t i = 0; i < rows; ++i) {
+        double r = row_factor(x, i, hidden, e, fmt);
+        for (int64_t j = 0; j < hidden; ++j) {
+            double xv = oracle_widen(x, i * hidden + j, fmt);
+            double wv = oracle_widen(w, j, fmt);
+            oracle_store(xv * r * wv, y, i * hidden + j, fmt);
+        }
+    }
+    return 0;
+}
+
+int oracle_round_array(const double *v, void *out, int64_t n, int fmt)
+{
+    if (n < 0 || fmt < 0 || fmt > 2)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        oracle_store(v[i], out, i, fmt);
+    return 0;
+}
+
+int oracle_widen_array(const void *in, double *out, int64_t n, int fmt)
+{
+    if (n < 0 || fmt < 0 || fmt > 2)
+        return -1;
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = oracle_widen(in, i, fmt);
+    return 0;
+}

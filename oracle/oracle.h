@@ -1,0 +1,47 @@
+/*
+ * oracle.h -- interface of the fp64 CPU oracle for the row-wise RMSNorm
+ * forward.  TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and
+ * the benchmark's CPU baseline; never by the CUDA library.
+ *
+ * Element formats: ORACLE_F32 (IEEE binary32), ORACLE_BF16 (bfloat16 bit
+ * patterns as uint16), ORACLE_F16 (IEEE binary16 bit patterns as uint16).
+ * All arrays are host memory, row-major, rows x hidden, contiguous.
+ * Functions return 0 on success and -1 on a bad argument.
+ */
+#ifndef RMSNORM_ORACLE_H
+#define RMSNORM_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1, ORACLE_F16 = 2 };
+
+/* y[i, j] = x[i, j] * (1 / sqrt(sum_k x[i, k]^2 / hidden + eps)) * w[j], in
+ * binary64, written as binary64 (no final rounding). */
+int oracle_rmsnorm_f64(const void *x, const void *w, double *y, int64_t rows,
+                       int64_t hidden, float eps, int fmt);
+
+/* The same result rounded to the element format with round-to-nearest-even
+ * directly from binary64. */
+int oracle_rmsnorm(const void *x, const void *w, void *y, int64_t rows,
+                   int64_t hidden, float eps, int fmt);
+
+/* Exact widening of n stored elements to binary64. */
+int oracle_widen_array(const void *in, double *out, int64_t n, int fmt);
+
+/* Round n binary64 values to the format (nearest-even, overflow to inf). */
+int oracle_round_array(const double *v, void *out, int64_t n, int fmt);
+
+/* Single-element helpers behind the array functions. */
+double oracle_widen(const void *base, int64_t index, int fmt);
+double oracle_round_value(double v, int fmt);
+void oracle_store(double v, void *base, int64_t index, int fmt);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif
