@@ -1,0 +1,449 @@
+"""RMSNorm forward benchmark on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
+
+A step is one RMSNorm forward over one batch: the headline workload is the
+prefill-shaped batch, 16384 rows x 4096 hidden, bf16 in/out, fp32
+accumulation, eps 1e-6 (x ~ N(0,1), weight ~ N(1,0.1), seeded).  Inputs are
+resident in HBM before the timed region; consecutive steps rotate over
+several input/output sets whose total is larger than the 129 MB L2, so every
+step reads x from HBM.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and torch.cuda.synchronize() on both sides; CUDA events on the launching
+stream, one pair around the whole region and one pair around every launch
+(the kernel's average duration, for the roofline); max over ranks.  SM clocks
+and throttle reasons are sampled with nvidia-smi during the timed region.
+
+value = algorithmic bytes (read x + read weight + write y) of every step of
+every rank / the slowest rank's time, in GB/s.  e2e = the same metric through
+the public API with the step's input copied host->device from pinned memory
+and the result copied back, every step.  cpu_baseline = the fp64 CPU oracle
+timed on this host on a bounded sample of the same workload.
+
+--impl reference times the oracle itself (there is no other implementation
+of this path to compare with): rank 0 only, each step a bounded sample of the
+workload, same metric and unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from rmsnorm_fwd_gb300 import inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "RMSNorm achieved HBM GB/s (% of GB300 peak) and rows/s at 16384x4096 bf16"
+UNIT = "GB/s"
+
+
+# ----------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value: float, dist, device=None) -> float:
+    """Max over ranks (identity on one process)."""
+    if dist is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist, device=None):
+    if dist is None:
+        return
+    if device is not None:
+        dist.barrier(device_ids=[device.index])
+    else:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------- clocks
+
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of one GPU while the timed region runs."""
+
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.lines: list[str] = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={CLOCK_FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(self.period)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)  # let the first samples land before the region starts
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        return time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm, smax = float(parts[0]), float(parts[1])
+            except ValueError:
+                continue
+            rows.append((ts, sm, smax, parts[3:]))
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        if not inside and rows:  # a very short region: take the nearest sample
+            inside = [min(rows, key=lambda r: abs(r[0] - 0.5 * (t0 + t1)))]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, val in zip(names[1:], r[3][1:]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
+
+
+# ----------------------------------------------------------------- peaks, traffic
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            v = float(json.load(fh)["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "rmsnorm_fwd_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str, variant: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    src = kernel_source_hash()
+    for m in re.finditer(r"^workload=(\S+) variant=(\S+) src=(\S+) dram_bytes_per_launch=(\d+)",
+                         text, flags=re.M):
+        if m.group(1) == workload and m.group(2) == variant and m.group(3) == src:
+            return int(m.group(4))
+    return None
+
+
+# ----------------------------------------------------------------- CPU oracle
+
+def oracle_sample(wl, seconds: float, max_rows: int | None = None):
+    """Time the CPU oracle, as it stands, on leading rows of the workload
+    until `seconds` of work (one thread).  Returns (GB/s, rows/s, rows done,
+    seconds)."""
+    import oracle
+    block = max(1, min(wl.rows, 256))
+    sample = wl.with_shape(block)
+    x, w = inputs.make_inputs(sample)
+    oracle.rmsnorm(x[:1], w, wl.eps, wl.dtype)  # load the library outside the clock
+    done = 0
+    t0 = time.perf_counter()
+    while True:
+        n = block if max_rows is None else max(1, min(block, max_rows - done))
+        oracle.rmsnorm(x[:n], w, wl.eps, wl.dtype)
+        done += n
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_rows is not None and done >= max_rows):
+            break
+    es = inputs.ITEMSIZE[wl.dtype]
+    bytes_done = 2 * done * wl.hidden * es + wl.hidden * es
+    return bytes_done / el / 1e9, done / el, done, el
+
+
+def run_reference(args, world, rank):
+    """--impl reference: the oracle timed on the host cores (rank 0 only)."""
+    if rank != 0:
+        return 0
+    import oracle
+    wl = inputs.WORKLOADS[args.workload]
+    es = inputs.ITEMSIZE[wl.dtype]
+    x, w = inputs.make_inputs(wl.with_shape(min(wl.rows, 64)))
+    oracle.rmsnorm(x[:1], w, wl.eps, wl.dtype)
+    t0 = time.perf_counter()
+    oracle.rmsnorm(x[:8], w, wl.eps, wl.dtype)
+    t_row = (time.perf_counter() - t0) / 8
+    budget = args.reference_budget_s / max(1, args.steps + args.warmup)
+    rows_per_step = int(max(1, min(x.shape[0], budget / max(t_row, 1e-9))))
+    xs = x[:rows_per_step]
+    for _ in range(args.warmup):
+        oracle.rmsnorm(xs, w, wl.eps, wl.dtype)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.rmsnorm(xs, w, wl.eps, wl.dtype)
+    el = time.perf_counter() - t0
+    step_bytes = 2 * rows_per_step * wl.hidden * es + wl.hidden * es
+    value = step_bytes * args.steps / el / 1e9
+    sample = (f"{rows_per_step} of {wl.rows} rows x {wl.hidden} per step "
+              f"({wl.dtype}, seeded workload inputs), {args.steps} steps")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
+                   "io_dtype": wl.dtype, "rows_per_step_sampled": rows_per_step},
+        "rows_per_s": round(rows_per_step * args.steps / el, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+
+def to_torch(a, dtype: str, torch):
+    if dtype == "f32":
+        return torch.from_numpy(a)
+    import numpy as np
+    return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16 if dtype == "bf16"
+                                                      else torch.float16)
+
+
+def run_ours(args, world, rank, local):
+    import torch
+
+    import rmsnorm_fwd_gb300 as rn
+
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "bench.py needs a CUDA device (GB300)"}), flush=True)
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    wl = inputs.WORKLOADS[args.workload]
+    es = inputs.ITEMSIZE[wl.dtype]
+    step_bytes = wl.bytes_per_call
+
+    x_np, w_np = inputs.make_inputs(wl, seed=rank)
+    x_host = to_torch(x_np, wl.dtype, torch)
+    w_host = to_torch(w_np, wl.dtype, torch)
+    set_bytes = 2 * wl.rows * wl.hidden * es
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
+    xs = [x_host.to(device) for _ in range(nsets)]
+    ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    w = w_host.to(device)
+
+    rn.ensure_context(local)
+    stream = torch.cuda.current_stream(device)
+    sptr = stream.cuda_stream
+    plan = rn.Plan()
+    dt = rn.DTYPE_CODES[wl.dtype]
+    rn.rmsnorm_fwd_ex(xs[0].data_ptr(), w.data_ptr(), ys[0].data_ptr(), wl.rows, wl.hidden,
+                      wl.eps, dt, sptr, rn.VARIANT_AUTO, plan)
+    variant = rn.VARIANT_NAMES[plan.variant]
+    fwd = rn._load().rmsnorm_fwd_ex
+    xp = [t.data_ptr() for t in xs]
+    yp = [t.data_ptr() for t in ys]
+    wp = w.data_ptr()
+    pref = rn.ctypes.byref(plan)  # launch exactly the selector's plan every step
+
+    def step(i):
+        rc = fwd(xp[i % nsets], wp, yp[i % nsets], wl.rows, wl.hidden, wl.eps, dt, sptr, 0, pref)
+        if rc != rn.OK:
+            raise rn.RmsnormError(rc, "rmsnorm_fwd_ex")
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_e = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(local)
+    sampler.start()
+    barrier(dist, device)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(K):
+        ev_b[i].record(stream)
+        step(i)
+        ev_e[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    t_wall1 = time.time()
+    sampler.stop()
+    total_ms = start.elapsed_time(end)
+    kernel_ms = sum(b.elapsed_time(e) for b, e in zip(ev_b, ev_e)) / K
+    max_ms = reduce_max(total_ms, dist, device)
+    max_kernel_ms = reduce_max(kernel_ms, dist, device)
+    clocks = sampler.summary(t_wall0, t_wall1)
+    status = rn.rmsnorm_get_device_status()
+
+    # ---- e2e through the public API: pinned host in, pinned host out
+    E = args.e2e_steps
+    xh = x_host.pin_memory()
+    wh = w_host.pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    xd, yd, wd = xs[0], ys[0], torch.empty_like(w)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(wh, non_blocking=True)
+        rn.rmsnorm_fwd(xd.data_ptr(), wd.data_ptr(), yd.data_ptr(), wl.rows, wl.hidden, wl.eps,
+                       dt, sptr)
+        yh.copy_(yd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(E):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist, device)
+    e2e_ms = reduce_max(e0.elapsed_time(e1), dist, device)
+    e2e_gbs = world * E * step_bytes / (e2e_ms / 1e3) / 1e9
+
+    value = world * K * step_bytes / (max_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    achieved = step_bytes / (max_kernel_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(max_ms / K, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+        if wl.dtype == "bf16" else wl.dtype, "data": "synthetic",
+        "config": {
+            "workload": wl.name, "rows": wl.rows, "hidden": wl.hidden, "eps": wl.eps,
+            "io_dtype": wl.dtype, "accumulate": "f32", "variant": variant,
+            "plan": plan.as_dict(),
+            "l2": (f"inputs larger than L2: {nsets} rotating x/y sets of "
+                   f"{set_bytes / 1e6:.0f} MB ({nsets * set_bytes / 1e6:.0f} MB) vs 129 MB L2"),
+            "parallelism": f"replicas x{world} (rows are independent; no collective)",
+        },
+        "rows_per_s": round(world * K * wl.rows / (max_ms / 1e3), 1),
+        "pct_of_peak": round(100 * value / peak, 2),
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "traffic": ncu_traffic(wl.name, variant),
+                     "algorithmic_bytes_per_launch": step_bytes,
+                     "kernel_ms_avg": round(max_kernel_ms, 6)},
+        "e2e": {"value": round(e2e_gbs, 2), "unit": UNIT, "steps": E,
+                "h2d_bytes_per_step": int(xh.numel() * xh.element_size()
+                                          + wh.numel() * wh.element_size()),
+                "d2h_bytes_per_step": int(yh.numel() * yh.element_size())},
+        "clocks": clocks,
+        "device_status": status,
+    }
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
+        gbs, rps, rows_done, el = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": round(gbs, 5), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": (f"first {min(wl.rows, 256)} rows of the same seeded workload, repeated: "
+                       f"{rows_done} rows x {wl.hidden} in {el:.1f} s, one thread"),
+            "rows_per_s": round(rps, 2)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-budget-s", type=float, default=60.0)
+    args = ap.parse_args(argv)
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

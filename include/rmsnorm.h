@@ -1,0 +1,204 @@
+/*
+ * rmsnorm.h -- C ABI of the GB300 (sm_103a) row-wise RMSNorm forward library
+ * (librmsnorm.so).
+ *
+ * The operation.  "Build a GPU compiler from scratch: from PyTorch to CUDA via
+ * multi-level IR (Emmy)", introduction and section "Tensor IR": for every row
+ * take the mean of the squared elements, add epsilon, take the reciprocal
+ * square root, and scale every element by that factor and by its learned
+ * weight; section "Loop IR": all of it is one fused kernel whose row
+ * statistic never leaves the chip.  "CuTeDSL at Perplexity", section "QK
+ * Norm": the squares are summed in fp32, the factor is rsqrt(sum/n + EPS),
+ * each output is weight * (x * factor) cast back to the input's element type,
+ * and the store may overwrite the input.
+ *
+ *   y[i, j] = round( (x[i, j] * r_i) * w[j] ),   r_i = rsqrt( sum_j x[i, j]^2 / hidden + eps )
+ *
+ * computed in fp32 on the device and rounded to the element type with
+ * round-to-nearest-even.
+ *
+ * Memory layout.  x and y are row-major [rows, hidden], contiguous (row
+ * stride = hidden elements); weight is [hidden].  x, weight and y share one
+ * element type.  All three are DEVICE pointers owned by the caller; the
+ * library never frees or retains them.  The only memory the library itself
+ * allocates is a 4-byte device status word per device (rmsnorm_create) and
+ * its host-side context.
+ *
+ * Aliasing.  y == x (exactly in place) is allowed.  Any other overlap between
+ * y and x, or between y and weight, is rejected with RMSNORM_ERR_ALIASING.
+ *
+ * Asynchrony and errors.  rmsnorm_fwd only validates and enqueues at most
+ * one kernel on `stream` (a cudaStream_t passed as void*; NULL = the legacy
+ * default stream); it never synchronises.  Argument errors are reported
+ * before anything is enqueued.  A launch failure returns RMSNORM_ERR_CUDA.
+ * Device-side faults the kernels can detect themselves (a bounded wait that
+ * ran out) are recorded in the device status word, read with
+ * rmsnorm_get_device_status.  No function throws across this boundary and
+ * none aborts the process.
+ *
+ * Threads.  All functions may be called from any host thread; the context
+ * table is guarded by a mutex.  Contexts are per CUDA device: create on each
+ * device you use, with that device current.
+ */
+#ifndef RMSNORM_H
+#define RMSNORM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type shared by x, weight and y. */
+typedef enum {
+    RMSNORM_F32 = 0,  /* IEEE binary32 */
+    RMSNORM_BF16 = 1, /* bfloat16 */
+    RMSNORM_F16 = 2   /* IEEE binary16 */
+} rmsnorm_dtype_t;
+
+typedef enum {
+    RMSNORM_OK = 0,
+    RMSNORM_ERR_INVALID_ARG = 1,        /* null pointer, rows < 0, hidden <= 0, eps < 0 or NaN, bad plan */
+    RMSNORM_ERR_UNSUPPORTED_DTYPE = 2,  /* dtype not one of rmsnorm_dtype_t */
+    RMSNORM_ERR_NOT_INITIALIZED = 3,    /* no rmsnorm_create on the current device */
+    RMSNORM_ERR_ALIASING = 4,           /* y partially overlaps x, or overlaps weight */
+    RMSNORM_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
+    RMSNORM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device status word) */
+    RMSNORM_ERR_MISALIGNED = 7,         /* a forced vector variant got pointers it cannot load */
+    RMSNORM_ERR_UNSUPPORTED_DEVICE = 8, /* current device is not compute capability 10.x */
+    RMSNORM_ERR_VARIANT = 9             /* forced variant cannot take this shape */
+} rmsnorm_status_t;
+
+/* Kernel variants.  AUTO lets the selector choose from (rows, hidden, dtype,
+ * pointer alignment, SM count). */
+typedef enum {
+    RMSNORM_VARIANT_AUTO = 0,
+    /* A group of 4..32 lanes of one warp per row; the row stays in registers;
+     * the reduction is warp shuffles only.  Small hidden. */
+    RMSNORM_VARIANT_WARP_PER_ROW = 1,
+    /* One thread block per row; the row stays in registers; warp shuffles,
+     * then one float per warp through shared memory.  Medium/large hidden. */
+    RMSNORM_VARIANT_CTA_PER_ROW = 2,
+    /* Persistent blocks (one or two per SM) stream whole rows global ->
+     * shared with cp.async.bulk into a ring of slots guarded by mbarriers
+     * (bounded waits); one consumer warp per row.  Large hidden. */
+    RMSNORM_VARIANT_STAGED = 3,
+    /* Decode shapes: the block-per-row body with grid <= SM count and a
+     * grid-stride row loop. */
+    RMSNORM_VARIANT_PERSISTENT = 4,
+    /* Any hidden and any element alignment: scalar loads, two passes over
+     * the row (the second from cache).  Fallback for ragged shapes. */
+    RMSNORM_VARIANT_GENERIC = 5
+} rmsnorm_variant_t;
+
+/* A launch plan: what the selector chose.  Filled by rmsnorm_plan. */
+typedef struct {
+    int32_t variant;         /* rmsnorm_variant_t (never AUTO) */
+    int32_t vec_bytes;       /* bytes per vector access: 16 or 32; 0 = scalar */
+    int32_t threads_per_row; /* threads cooperating on one row (staged: 32) */
+    int32_t vecs_per_thread; /* register-resident vectors per thread per row */
+    int32_t block_threads;   /* threads per block */
+    int32_t rows_per_block;  /* rows a block works on at once */
+    int32_t stages;          /* staged: row slots in shared memory; else 0 */
+    int32_t grid;            /* blocks launched (0 when rows == 0) */
+    int32_t smem_bytes;      /* dynamic shared memory per block */
+    int32_t kernel_index;    /* internal instantiation index */
+} rmsnorm_plan_t;
+
+/* Create (or add a reference to) the context of the CURRENT CUDA device:
+ * queries SM count, shared memory limits and compute capability (must be
+ * 10.x; the kernels are built for sm_103a), allocates the device status word.
+ * Idempotent and reference counted.  Returns RMSNORM_OK,
+ * RMSNORM_ERR_UNSUPPORTED_DEVICE or RMSNORM_ERR_CUDA. */
+int rmsnorm_create(void);
+
+/* Drop one reference to the current device's context; at zero the status
+ * word is freed.  Returns RMSNORM_ERR_NOT_INITIALIZED if there is none. */
+int rmsnorm_destroy(void);
+
+/* y = RMSNorm(x) * weight, per row (see the top of this file).
+ *   x       device pointer, [rows, hidden] elements of `dtype`
+ *   weight  device pointer, [hidden] elements of `dtype`
+ *   y       device pointer, [rows, hidden]; may equal x
+ *   rows    >= 0 (0 returns RMSNORM_OK and launches nothing)
+ *   hidden  >= 1
+ *   eps     >= 0, finite (added to the mean square before the rsqrt)
+ *   dtype   rmsnorm_dtype_t
+ *   stream  cudaStream_t (as void*); NULL = legacy default stream
+ * Enqueues one kernel; does not synchronise. */
+int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                float eps, int dtype, void *stream);
+
+/* rmsnorm_fwd with a forced variant (RMSNORM_VARIANT_AUTO = selector's choice)
+ * and an optional plan override: when `plan` is non-NULL and plan->variant
+ * is not AUTO, that exact plan is launched after validation against the
+ * shape (benchmark sweeps); when `plan` is non-NULL and plan->variant is
+ * AUTO, the chosen plan is written back into it. */
+int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                   float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan);
+
+/* The selector, host only (touches no memory behind the pointers and no
+ * GPU): the plan rmsnorm_fwd_ex would launch for these arguments on a device
+ * with `sm_count` SMs and `smem_optin` bytes of opt-in shared memory per
+ * block.  Pointer values are used only for their alignment.  Returns
+ * RMSNORM_OK, RMSNORM_ERR_INVALID_ARG, RMSNORM_ERR_UNSUPPORTED_DTYPE,
+ * RMSNORM_ERR_MISALIGNED or RMSNORM_ERR_VARIANT. */
+int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows, int64_t hidden,
+                 int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out);
+
+/* One compiled kernel instantiation, for building explicit plans (tuning
+ * sweeps).  tpr / nv / block of 0 mean "chosen at launch". */
+typedef struct {
+    int32_t variant;   /* WARP_PER_ROW, CTA_PER_ROW (also used for PERSISTENT), STAGED, GENERIC */
+    int32_t dtype;     /* rmsnorm_dtype_t */
+    int32_t vec_bytes; /* 16 / 32; 0 = scalar */
+    int32_t tpr;       /* threads per row fixed at compile time (warp-per-row) */
+    int32_t nv;        /* vectors per thread fixed at compile time */
+    int32_t block;     /* block size fixed at compile time, or the largest allowed */
+} rmsnorm_kernel_info_t;
+
+/* SM count and opt-in shared memory per block of the current device, as
+ * cached by rmsnorm_create (the values the selector uses).  Returns
+ * RMSNORM_OK, RMSNORM_ERR_NOT_INITIALIZED or RMSNORM_ERR_INVALID_ARG. */
+int rmsnorm_device_limits(int *sm_count, int *smem_optin);
+
+/* Number of compiled kernel instantiations (host only, no GPU needed). */
+int rmsnorm_kernel_count(void);
+
+/* Describe instantiation `index` (0 <= index < rmsnorm_kernel_count()).
+ * Returns RMSNORM_OK or RMSNORM_ERR_INVALID_ARG. */
+int rmsnorm_kernel_info(int index, rmsnorm_kernel_info_t *out);
+
+/* Variant of the last successful launch on the calling thread (0 if none). */
+int rmsnorm_last_variant(void);
+
+/* Copy the current device's status word to *status (RMSNORM_OK, or the
+ * first device-side error recorded since the last read) and clear it.
+ * Synchronises the device's legacy default stream.  Returns RMSNORM_OK,
+ * RMSNORM_ERR_NOT_INITIALIZED, RMSNORM_ERR_INVALID_ARG or RMSNORM_ERR_CUDA. */
+int rmsnorm_get_device_status(int *status);
+
+/* Upper bound, in nanoseconds of %globaltimer, on every spin-wait inside the
+ * staged kernel (default 1e9 = one second).  After it runs out the kernel
+ * records RMSNORM_ERR_DEVICE_TIMEOUT, waits (again bounded) for its own
+ * copies in flight, and returns.  0 restores the default. */
+int rmsnorm_set_wait_limit_ns(uint64_t limit_ns);
+
+/* Failure-detection test hook: launch the staged kernel on a valid shape
+ * with its row copies withheld, so every consumer wait runs out after
+ * `limit_ns`; the kernel then records RMSNORM_ERR_DEVICE_TIMEOUT and returns
+ * without touching y.  No fault, trap or hang is involved. */
+int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int64_t rows,
+                                int64_t hidden, int dtype, uint64_t limit_ns, void *stream);
+
+/* Static text for a status code. */
+const char *rmsnorm_status_string(int status);
+
+/* Library version, (major << 16) | minor. */
+int rmsnorm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_H */

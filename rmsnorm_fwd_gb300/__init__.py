@@ -1,0 +1,269 @@
+"""Row-wise RMSNorm forward for GB300 (sm_103a): hand-written CUDA kernels
+behind the C ABI of ``include/rmsnorm.h`` (``librmsnorm.so``).
+
+This module is the thin Python binding: the functions below have the C
+names and only marshal arguments (pointers, sizes, the stream handle) into
+the library.  Every step of the computation runs in the library's kernels;
+there is no Python, PyTorch or CPU fallback.  If the library cannot be built
+or loaded, the first call raises.
+
+PyTorch is used only for device memory and streams (``rms_norm`` takes
+tensors, reads their data pointers and the current stream, and calls
+``rmsnorm_fwd``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+# element types (rmsnorm_dtype_t)
+F32, BF16, F16 = 0, 1, 2
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16"}
+DTYPE_CODES = {"f32": F32, "bf16": BF16, "f16": F16}
+
+# status codes (rmsnorm_status_t)
+OK = 0
+ERR_INVALID_ARG = 1
+ERR_UNSUPPORTED_DTYPE = 2
+ERR_NOT_INITIALIZED = 3
+ERR_ALIASING = 4
+ERR_CUDA = 5
+ERR_DEVICE_TIMEOUT = 6
+ERR_MISALIGNED = 7
+ERR_UNSUPPORTED_DEVICE = 8
+ERR_VARIANT = 9
+
+# variants (rmsnorm_variant_t)
+VARIANT_AUTO = 0
+VARIANT_WARP_PER_ROW = 1
+VARIANT_CTA_PER_ROW = 2
+VARIANT_STAGED = 3
+VARIANT_PERSISTENT = 4
+VARIANT_GENERIC = 5
+VARIANT_NAMES = {0: "auto", 1: "warp_per_row", 2: "cta_per_row", 3: "staged", 4: "persistent",
+                 5: "generic"}
+
+
+class RmsnormError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({rmsnorm_status_string(status)})")
+
+
+class Plan(ctypes.Structure):
+    """rmsnorm_plan_t."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "variant", "vec_bytes", "threads_per_row", "vecs_per_thread", "block_threads",
+        "rows_per_block", "stages", "grid", "smem_bytes", "kernel_index")]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+class KernelInfo(ctypes.Structure):
+    """rmsnorm_kernel_info_t."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "variant", "dtype", "vec_bytes", "tpr", "nv", "block")]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    from . import _build
+    return _build.LIB
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        from . import _build
+        path = _build.build()  # compiles in-tree if stale; raises if nvcc is missing
+        lib = ctypes.CDLL(path, mode=ctypes.RTLD_GLOBAL)
+        vp, i64, i32, f32, u64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float,
+                                  ctypes.c_uint64)
+        pp = ctypes.POINTER(Plan)
+        sig = {
+            "rmsnorm_create": ([], i32),
+            "rmsnorm_destroy": ([], i32),
+            "rmsnorm_fwd": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
+            "rmsnorm_fwd_ex": ([vp, vp, vp, i64, i64, f32, i32, vp, i32, pp], i32),
+            "rmsnorm_plan": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, pp], i32),
+            "rmsnorm_last_variant": ([], i32),
+            "rmsnorm_kernel_count": ([], i32),
+            "rmsnorm_device_limits": ([ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
+                                      i32),
+            "rmsnorm_kernel_info": ([i32, ctypes.POINTER(KernelInfo)], i32),
+            "rmsnorm_get_device_status": ([ctypes.POINTER(ctypes.c_int)], i32),
+            "rmsnorm_set_wait_limit_ns": ([u64], i32),
+            "rmsnorm_test_staged_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
+            "rmsnorm_status_string": ([i32], ctypes.c_char_p),
+            "rmsnorm_version": ([], i32),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != OK:
+        raise RmsnormError(rc, where)
+
+
+# ------------------------------------------------------------------ C names
+
+def rmsnorm_create() -> None:
+    _check(_load().rmsnorm_create(), "rmsnorm_create")
+
+
+def rmsnorm_destroy() -> None:
+    _check(_load().rmsnorm_destroy(), "rmsnorm_destroy")
+
+
+def rmsnorm_fwd(x: int, weight: int, y: int, rows: int, hidden: int, eps: float, dtype: int,
+                stream: int | None) -> None:
+    """Raw call: device pointers as integers, stream as a cudaStream_t integer."""
+    _check(_load().rmsnorm_fwd(x, weight, y, rows, hidden, eps, dtype, stream or None),
+           "rmsnorm_fwd")
+
+
+def rmsnorm_fwd_ex(x: int, weight: int, y: int, rows: int, hidden: int, eps: float, dtype: int,
+                   stream: int | None, variant: int = VARIANT_AUTO,
+                   plan: Plan | None = None) -> Plan | None:
+    ref = ctypes.byref(plan) if plan is not None else None
+    _check(_load().rmsnorm_fwd_ex(x, weight, y, rows, hidden, eps, dtype, stream or None,
+                                  variant, ref), "rmsnorm_fwd_ex")
+    return plan
+
+
+def rmsnorm_plan(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int, sm_count: int,
+                 smem_optin: int, variant: int = VARIANT_AUTO) -> Plan:
+    p = Plan()
+    _check(_load().rmsnorm_plan(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant,
+                                ctypes.byref(p)), "rmsnorm_plan")
+    return p
+
+
+def rmsnorm_plan_status(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int,
+                        sm_count: int, smem_optin: int, variant: int = VARIANT_AUTO):
+    """(status, plan) without raising."""
+    p = Plan()
+    rc = _load().rmsnorm_plan(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant,
+                              ctypes.byref(p))
+    return rc, p
+
+
+def rmsnorm_device_limits() -> tuple[int, int]:
+    """(SM count, opt-in shared memory per block) of the current device."""
+    a, b = ctypes.c_int(0), ctypes.c_int(0)
+    _check(_load().rmsnorm_device_limits(ctypes.byref(a), ctypes.byref(b)),
+           "rmsnorm_device_limits")
+    return a.value, b.value
+
+
+def rmsnorm_kernel_count() -> int:
+    return _load().rmsnorm_kernel_count()
+
+
+def rmsnorm_kernel_info(index: int) -> KernelInfo:
+    k = KernelInfo()
+    _check(_load().rmsnorm_kernel_info(index, ctypes.byref(k)), "rmsnorm_kernel_info")
+    return k
+
+
+def kernels() -> list[dict]:
+    """Every compiled instantiation, with its index."""
+    return [dict(index=i, **rmsnorm_kernel_info(i).as_dict()) for i in range(rmsnorm_kernel_count())]
+
+
+def rmsnorm_last_variant() -> int:
+    return _load().rmsnorm_last_variant()
+
+
+def rmsnorm_get_device_status() -> int:
+    v = ctypes.c_int(0)
+    _check(_load().rmsnorm_get_device_status(ctypes.byref(v)), "rmsnorm_get_device_status")
+    return v.value
+
+
+def rmsnorm_set_wait_limit_ns(limit_ns: int) -> None:
+    _check(_load().rmsnorm_set_wait_limit_ns(limit_ns), "rmsnorm_set_wait_limit_ns")
+
+
+def rmsnorm_test_staged_timeout(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int,
+                                limit_ns: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_test_staged_timeout(x, weight, y, rows, hidden, dtype, limit_ns,
+                                               stream or None), "rmsnorm_test_staged_timeout")
+
+
+def rmsnorm_status_string(status: int) -> str:
+    return _load().rmsnorm_status_string(status).decode()
+
+
+def rmsnorm_version() -> int:
+    return _load().rmsnorm_version()
+
+
+# ------------------------------------------------------------------ tensors
+
+_created = set()
+
+
+def ensure_context(device_index: int) -> None:
+    """rmsnorm_create on `device_index` once per process."""
+    if device_index in _created:
+        return
+    import torch
+    with torch.cuda.device(device_index):
+        rmsnorm_create()
+    _created.add(device_index)
+
+
+def torch_dtype_code(dt) -> int:
+    import torch
+    table = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}
+    if dt not in table:
+        raise TypeError(f"unsupported dtype {dt}")
+    return table[dt]
+
+
+def rms_norm(x, weight, eps: float, out=None, variant: int = VARIANT_AUTO, plan: Plan | None = None,
+             stream=None):
+    """y = x * rsqrt(mean(x^2, -1) + eps) * weight through rmsnorm_fwd_ex.
+
+    ``x``: CUDA tensor [..., hidden], contiguous; ``weight``: [hidden], same
+    dtype and device; ``out``: optional preallocated output (may be ``x``).
+    Runs on ``stream`` (default: PyTorch's current stream)."""
+    import torch
+    if not (x.is_cuda and weight.is_cuda):
+        raise ValueError("rms_norm takes CUDA tensors (there is no CPU path)")
+    if x.dtype != weight.dtype:
+        raise TypeError("x and weight must share a dtype")
+    if not x.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("x and weight must be contiguous")
+    hidden = x.shape[-1]
+    if weight.numel() != hidden:
+        raise ValueError("weight must have hidden elements")
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must match x (shape, dtype, contiguous)")
+    ensure_context(x.device.index)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    rows = x.numel() // hidden if hidden else 0
+    with torch.cuda.device(x.device.index):
+        rmsnorm_fwd_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), rows, hidden, float(eps),
+                       torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
+    return out

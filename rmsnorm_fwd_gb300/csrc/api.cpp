@@ -1,0 +1,365 @@
+// api.cpp -- the C ABI (include/rmsnorm.h): per-device contexts, argument
+// validation, plan selection and the launch.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstdlib>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "internal.h"
+
+namespace rmsnorm {
+
+const KernelDesc *kernel_table(int *n)
+{
+    static KernelDesc table[256];
+    static int count = [] {
+        int c = 0;
+        const KernelDesc *(*parts[])(int *) = {rowreg_kernels_f32, rowreg_kernels_bf16,
+                                                rowreg_kernels_f16, staged_kernels,
+                                                generic_kernels};
+        for (auto part : parts) {
+            int m = 0;
+            const KernelDesc *t = part(&m);
+            for (int i = 0; i < m && c < 256; ++i)
+                table[c++] = t[i];
+        }
+        return c;
+    }();
+    *n = count;
+    return table;
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull; // one second
+
+struct DeviceCtx {
+    int refs = 0;
+    int sm_count = 0;
+    int smem_optin = 0;
+    int *status = nullptr; // device word
+};
+
+std::mutex g_mu;
+DeviceCtx g_ctx[kMaxDevices];
+std::atomic<uint64_t> g_wait_limit{kDefaultWaitLimitNs};
+thread_local int t_last_variant = 0;
+
+bool log_enabled()
+{
+    static const bool on = [] {
+        const char *e = std::getenv("RMSNORM_LOG");
+        return e && e[0] == '1';
+    }();
+    return on;
+}
+
+// Looks up the current device's context (copy taken under the lock).
+int current_ctx(DeviceCtx *out, int *dev_out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return RMSNORM_ERR_NOT_INITIALIZED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_ctx[dev].refs <= 0)
+        return RMSNORM_ERR_NOT_INITIALIZED;
+    *out = g_ctx[dev];
+    if (dev_out)
+        *dev_out = dev;
+    return RMSNORM_OK;
+}
+
+bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes)
+{
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + static_cast<uintptr_t>(bbytes) && b0 < a0 + static_cast<uintptr_t>(abytes);
+}
+
+int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
+               int dtype)
+{
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
+        return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || hidden <= 0 || !(eps >= 0.f) || !std::isfinite(eps))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (!w || (rows > 0 && (!x || !y)))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (rows > 0) {
+        const int64_t es = dtype == RMSNORM_F32 ? 4 : 2;
+        if (rows > INT64_MAX / 4 / hidden)
+            return RMSNORM_ERR_INVALID_ARG;
+        const int64_t bytes = rows * hidden * es;
+        if (y != x && ranges_overlap(x, bytes, y, bytes))
+            return RMSNORM_ERR_ALIASING;
+        if (ranges_overlap(w, hidden * es, y, bytes))
+            return RMSNORM_ERR_ALIASING;
+    }
+    return RMSNORM_OK;
+}
+
+int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
+           int dtype, void *stream, int variant, rmsnorm_plan_t *plan, uint32_t flags,
+           uint64_t limit_ns)
+{
+    int rc = check_args(x, w, y, rows, hidden, eps, dtype);
+    if (rc != RMSNORM_OK)
+        return rc;
+    DeviceCtx ctx;
+    rc = current_ctx(&ctx, nullptr);
+    if (rc != RMSNORM_OK)
+        return rc;
+    if (rows == 0) {
+        if (plan && plan->variant == RMSNORM_VARIANT_AUTO)
+            *plan = rmsnorm_plan_t{};
+        return RMSNORM_OK;
+    }
+
+    rmsnorm_plan_t p;
+    if (plan && plan->variant != RMSNORM_VARIANT_AUTO) {
+        p = *plan;
+        rc = validate_plan(p, x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin);
+    } else {
+        rc = plan_launch(x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, variant, &p);
+    }
+    if (rc != RMSNORM_OK)
+        return rc;
+
+    int n = 0;
+    const KernelDesc *table = kernel_table(&n);
+    const KernelDesc &d = table[p.kernel_index];
+    LaunchArgs a;
+    a.x = x;
+    a.w = w;
+    a.y = y;
+    a.rows = rows;
+    a.hidden = static_cast<int32_t>(hidden);
+    a.eps = eps;
+    a.status = ctx.status;
+    a.wait_limit_ns = limit_ns;
+    a.flags = flags;
+    a.stream = static_cast<cudaStream_t>(stream);
+    if (log_enabled())
+        std::fprintf(stderr,
+                     "rmsnorm: rows=%lld hidden=%lld dtype=%d -> variant=%d vec=%d tpr=%d nv=%d "
+                     "block=%d grid=%d stages=%d smem=%d kernel=%d\n",
+                     static_cast<long long>(rows), static_cast<long long>(hidden), dtype,
+                     p.variant, p.vec_bytes, p.threads_per_row, p.vecs_per_thread,
+                     p.block_threads, p.grid, p.stages, p.smem_bytes, p.kernel_index);
+    if (d.launch(p, a) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    t_last_variant = p.variant;
+    if (plan && plan->variant == RMSNORM_VARIANT_AUTO)
+        *plan = p;
+    return RMSNORM_OK;
+}
+
+} // namespace
+} // namespace rmsnorm
+
+using namespace rmsnorm;
+
+extern "C" {
+
+int rmsnorm_create(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return RMSNORM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceCtx &c = g_ctx[dev];
+    if (c.refs > 0) {
+        ++c.refs;
+        return RMSNORM_OK;
+    }
+    int major = 0, minor = 0, sms = 0, optin = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    // The kernels are compiled for sm_103a only.
+    if (major != 10 || minor != 3)
+        return RMSNORM_ERR_UNSUPPORTED_DEVICE;
+    int *status = nullptr;
+    if (cudaMalloc(&status, sizeof(int)) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) {
+        cudaFree(status);
+        return RMSNORM_ERR_CUDA;
+    }
+    int n = 0;
+    const KernelDesc *t = kernel_table(&n);
+    for (int i = 0; i < n; ++i) {
+        if (t[i].variant == RMSNORM_VARIANT_STAGED &&
+            cudaFuncSetAttribute(t[i].func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+                cudaSuccess) {
+            cudaFree(status);
+            return RMSNORM_ERR_CUDA;
+        }
+    }
+    c.sm_count = sms;
+    c.smem_optin = optin;
+    c.status = status;
+    c.refs = 1;
+    return RMSNORM_OK;
+}
+
+int rmsnorm_destroy(void)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return RMSNORM_ERR_NOT_INITIALIZED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceCtx &c = g_ctx[dev];
+    if (c.refs <= 0)
+        return RMSNORM_ERR_NOT_INITIALIZED;
+    if (--c.refs == 0) {
+        cudaFree(c.status);
+        c = DeviceCtx{};
+    }
+    return RMSNORM_OK;
+}
+
+int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                float eps, int dtype, void *stream)
+{
+    return launch(x, weight, y, rows, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                  0u, g_wait_limit.load());
+}
+
+int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                   float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan)
+{
+    return launch(x, weight, y, rows, hidden, eps, dtype, stream, variant, plan, 0u,
+                  g_wait_limit.load());
+}
+
+int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows, int64_t hidden,
+                 int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out)
+{
+    return plan_launch(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant, out);
+}
+
+int rmsnorm_device_limits(int *sm_count, int *smem_optin)
+{
+    if (!sm_count || !smem_optin)
+        return RMSNORM_ERR_INVALID_ARG;
+    DeviceCtx ctx;
+    int rc = current_ctx(&ctx, nullptr);
+    if (rc != RMSNORM_OK)
+        return rc;
+    *sm_count = ctx.sm_count;
+    *smem_optin = ctx.smem_optin;
+    return RMSNORM_OK;
+}
+
+int rmsnorm_kernel_count(void)
+{
+    int n = 0;
+    kernel_table(&n);
+    return n;
+}
+
+int rmsnorm_kernel_info(int index, rmsnorm_kernel_info_t *out)
+{
+    int n = 0;
+    const KernelDesc *t = kernel_table(&n);
+    if (!out || index < 0 || index >= n)
+        return RMSNORM_ERR_INVALID_ARG;
+    const KernelDesc &d = t[index];
+    out->variant = d.variant;
+    out->dtype = d.dtype;
+    out->vec_bytes = d.vec_bytes;
+    out->tpr = d.tpr;
+    out->nv = d.nv;
+    out->block = d.block;
+    return RMSNORM_OK;
+}
+
+int rmsnorm_last_variant(void)
+{
+    return t_last_variant;
+}
+
+int rmsnorm_get_device_status(int *status)
+{
+    if (!status)
+        return RMSNORM_ERR_INVALID_ARG;
+    DeviceCtx ctx;
+    int rc = current_ctx(&ctx, nullptr);
+    if (rc != RMSNORM_OK)
+        return rc;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, ctx.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (cudaMemset(ctx.status, 0, sizeof(int)) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    *status = v;
+    return RMSNORM_OK;
+}
+
+int rmsnorm_set_wait_limit_ns(uint64_t limit_ns)
+{
+    g_wait_limit.store(limit_ns ? limit_ns : kDefaultWaitLimitNs);
+    return RMSNORM_OK;
+}
+
+int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int64_t rows,
+                                int64_t hidden, int dtype, uint64_t limit_ns, void *stream)
+{
+    if (rows <= 0 || limit_ns == 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    return launch(x, weight, y, rows, hidden, 0.f, dtype, stream, RMSNORM_VARIANT_STAGED, nullptr,
+                  kFlagWithholdCopies, limit_ns);
+}
+
+const char *rmsnorm_status_string(int status)
+{
+    switch (status) {
+    case RMSNORM_OK:
+        return "ok";
+    case RMSNORM_ERR_INVALID_ARG:
+        return "invalid argument";
+    case RMSNORM_ERR_UNSUPPORTED_DTYPE:
+        return "unsupported dtype";
+    case RMSNORM_ERR_NOT_INITIALIZED:
+        return "no context on the current device (call rmsnorm_create)";
+    case RMSNORM_ERR_ALIASING:
+        return "y partially overlaps x or overlaps weight";
+    case RMSNORM_ERR_CUDA:
+        return "CUDA runtime error";
+    case RMSNORM_ERR_DEVICE_TIMEOUT:
+        return "a bounded device-side wait ran out";
+    case RMSNORM_ERR_MISALIGNED:
+        return "pointers or row length not aligned for the forced vector variant";
+    case RMSNORM_ERR_UNSUPPORTED_DEVICE:
+        return "device is not compute capability 10.3 (sm_103a)";
+    case RMSNORM_ERR_VARIANT:
+        return "the forced variant or plan cannot take this shape";
+    default:
+        return "unknown status";
+    }
+}
+
+int rmsnorm_version(void)
+{
+    return (1 << 16) | 0;
+}
+
+} // extern "C"

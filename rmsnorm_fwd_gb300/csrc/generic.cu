@@ -1,0 +1,78 @@
+// generic.cu -- RMSNorm for any hidden size and any element alignment.
+//
+// One thread block per row (grid-stride), scalar element accesses, two
+// passes over the row: the first accumulates the fp32 sum of squares, the
+// block reduces it (warp shuffles, then one float per warp through shared
+// memory), the second re-reads x (now in L1/L2) and writes y.  This is the
+// fallback for rows whose byte length or pointers do not allow 16-byte
+// vectors; the arithmetic is the same as the vector kernels' (sum of
+// squares, divide by the count, add epsilon, rsqrt, then (x * r) * w rounded
+// to the element type -- "Build a GPU compiler from scratch ... (Emmy)",
+// section "Tensor IR"; "CuTeDSL at Perplexity", section "QK Norm").
+#include "internal.h"
+#include "device_common.cuh"
+
+namespace rmsnorm {
+namespace {
+
+template <int DT>
+__global__ void __launch_bounds__(1024)
+generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+                    int32_t hidden, float eps)
+{
+    using E = Elem<DT>;
+    __shared__ float part[2][32];
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const float n = static_cast<float>(hidden);
+
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+        const int64_t base = row * hidden;
+        float s = 0.f;
+        for (int j = t; j < hidden; j += blockDim.x) {
+            const float v = E::widen1(x, base + j);
+            s = fmaf(v, v, s);
+        }
+        s = group_allreduce<32>(s);
+        if (lane == 0)
+            part[it & 1][warp] = s;
+        // Also orders every pass-one read of this row before any pass-two
+        // write (in-place calls).
+        __syncthreads();
+        float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
+        tot = group_allreduce<32>(tot);
+        const float r = row_factor(tot, n, eps);
+        for (int j = t; j < hidden; j += blockDim.x) {
+            const float v = E::widen1(x, base + j);
+            E::store1(y, base + j, (v * r) * E::widen1(w, j));
+        }
+    }
+}
+
+template <int DT>
+cudaError_t launch_generic(const rmsnorm_plan_t &p, const LaunchArgs &a)
+{
+    generic_rows_kernel<DT><<<p.grid, p.block_threads, 0, a.stream>>>(a.x, a.w, a.y, a.rows,
+                                                                       a.hidden, a.eps);
+    return cudaGetLastError();
+}
+
+#define GENERIC_ENTRY(DT)                                                                      \
+    KernelDesc{RMSNORM_VARIANT_GENERIC, DT, 0, 0, 0, 0, &launch_generic<DT>,                  \
+               reinterpret_cast<const void *>(&generic_rows_kernel<DT>)}
+
+const KernelDesc kTable[] = {GENERIC_ENTRY(RMSNORM_F32), GENERIC_ENTRY(RMSNORM_BF16),
+                             GENERIC_ENTRY(RMSNORM_F16)};
+
+} // namespace
+
+const KernelDesc *generic_kernels(int *n)
+{
+    *n = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
+    return kTable;
+}
+
+} // namespace rmsnorm

@@ -1,0 +1,84 @@
+// internal.h -- shared between the host side (api.cpp, select.cpp) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "rmsnorm.h"
+
+#if defined(__CUDACC__)
+#define RMSNORM_HD __host__ __device__
+#else
+#define RMSNORM_HD
+#endif
+
+namespace rmsnorm {
+
+// Everything one launch needs besides the plan.
+struct LaunchArgs {
+    const void *x;
+    const void *w;
+    void *y;
+    int64_t rows;
+    int32_t hidden;
+    float eps;
+    int *status;            // device status word (staged variant's bounded waits)
+    uint64_t wait_limit_ns; // bound on every spin-wait, %globaltimer ns
+    uint32_t flags;         // kFlagWithholdCopies: failure-detection test only
+    cudaStream_t stream;
+};
+
+constexpr uint32_t kFlagWithholdCopies = 1u;
+
+using LaunchFn = cudaError_t (*)(const rmsnorm_plan_t &, const LaunchArgs &);
+
+// One compiled kernel instantiation.
+struct KernelDesc {
+    int32_t variant;     // WARP_PER_ROW, CTA_PER_ROW (also PERSISTENT), STAGED, GENERIC
+    int32_t dtype;       // rmsnorm_dtype_t
+    int32_t vec_bytes;   // 16 / 32; 0 = scalar
+    int32_t tpr;         // threads per row, compile time (warp kernels); 0 = runtime
+    int32_t nv;          // vectors per thread, compile time; 0 = runtime loop
+    int32_t block;       // threads per block, compile time; 0 = runtime
+    LaunchFn launch;
+    const void *func;    // the __global__ function (attributes)
+};
+
+// Per translation unit tables, concatenated by kernel_table().
+const KernelDesc *rowreg_kernels_f32(int *n);
+const KernelDesc *rowreg_kernels_bf16(int *n);
+const KernelDesc *rowreg_kernels_f16(int *n);
+const KernelDesc *staged_kernels(int *n);
+const KernelDesc *generic_kernels(int *n);
+
+const KernelDesc *kernel_table(int *n);
+
+// Staged variant's shared-memory layout (host and device agree on it).
+struct StagedLayout {
+    int32_t row_bytes;   // hidden * element size (multiple of 16)
+    int32_t slot_stride; // row_bytes rounded up to 128
+    int32_t bar_bytes;   // mbarrier area (2 per slot + 1 weight + flag), rounded to 128
+    int32_t smem_bytes;  // total dynamic shared memory
+};
+
+RMSNORM_HD inline StagedLayout staged_layout(int32_t row_bytes, int32_t stages)
+{
+    StagedLayout L;
+    L.row_bytes = row_bytes;
+    L.slot_stride = (row_bytes + 127) / 128 * 128;
+    L.bar_bytes = ((2 * stages + 2) * 8 + 127) / 128 * 128;
+    L.smem_bytes = L.bar_bytes + L.slot_stride * (stages + 1); // +1: the weight row
+    return L;
+}
+
+// Host-side selector (select.cpp).
+int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
+                int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out);
+
+// Checks a caller-supplied plan against the shape and the kernel table.
+int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const void *y,
+                  int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin);
+
+} // namespace rmsnorm

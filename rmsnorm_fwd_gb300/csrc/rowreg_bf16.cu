@@ -1,0 +1,18 @@
+// rowreg_bf16.cu -- bf16 instantiations of the register-resident kernels
+// (one translation unit per element type so they compile in parallel).
+#include "rowreg.cuh"
+
+namespace rmsnorm {
+namespace rowreg {
+namespace {
+const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_BF16)};
+} // namespace
+} // namespace rowreg
+
+const KernelDesc *rowreg_kernels_bf16(int *n)
+{
+    *n = static_cast<int>(sizeof(rowreg::kTable) / sizeof(rowreg::kTable[0]));
+    return rowreg::kTable;
+}
+
+} // namespace rmsnorm

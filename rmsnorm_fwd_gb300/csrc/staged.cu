@@ -1,0 +1,283 @@
+// staged.cu -- RMSNorm with rows staged in shared memory by bulk copies.
+//
+// Persistent blocks (grid <= SMs x blocks per SM).  Warp 0, lane 0 is the
+// producer: it streams each of its block's rows global -> shared with one
+// cp.async.bulk into a ring of `stages` slots, each slot guarded by a "full"
+// mbarrier (completed by the copy's transaction bytes) and an "empty"
+// mbarrier (completed by the consumer).  Warps 1..C are consumers, one row at
+// a time each: wait for the slot, sum the squares from shared memory in
+// fp32, reduce across the warp with shuffles, r = rsqrt(S / hidden + eps),
+// then read the slot again, scale by r and the weight (staged once per block
+// in its own slot), store y with 16-byte vector stores, and release the
+// slot.  HBM sees one read of x, one write of y and one read of the weight
+// per block; the row statistic stays in registers ("Build a GPU compiler
+// from scratch ... (Emmy)", sections "Tensor IR" and "Loop IR").
+//
+// Slot s holds rows k = s, s + stages, ...; consumer c takes k = c, c + C,
+// ...; `stages` is a multiple of C so each slot always has the same consumer
+// and mbarrier parity waits are never ambiguous.
+//
+// Every spin-wait is bounded by `limit_ns` of %globaltimer.  A wait that runs
+// out records RMSNORM_ERR_DEVICE_TIMEOUT in the status word, raises the
+// block's abort flag, and the producer then waits (again bounded) for every
+// copy it issued before the block exits, so no copy lands in shared memory
+// that has been handed to another block.  Nothing here traps.
+#include "internal.h"
+#include "device_common.cuh"
+
+namespace rmsnorm {
+namespace {
+
+__device__ inline uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ inline void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    return ok != 0;
+}
+
+__device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ inline uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ inline void record_timeout(int *status)
+{
+    atomicCAS(status, 0, static_cast<int>(RMSNORM_ERR_DEVICE_TIMEOUT));
+}
+
+// Single-thread bounded wait.  Returns false if the limit ran out or (when
+// abort_flag is non-null) the block's abort flag went up.
+__device__ inline bool wait_one(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                const volatile int *abort_flag)
+{
+    if (mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = globaltimer();
+    for (;;) {
+        if (mbar_try_wait(bar, parity))
+            return true;
+        if (abort_flag && *abort_flag)
+            return false;
+        if (globaltimer() - t0 > limit_ns)
+            return false;
+    }
+}
+
+// Whole-warp bounded wait: every lane observes the phase (acquire) before
+// any lane reads the slot; lane 0 decides, for the warp, when to give up.
+__device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_ns,
+                                 const volatile int *abort_flag, int lane)
+{
+    uint64_t t0 = 0;
+    bool timing = false;
+    for (;;) {
+        const bool done = mbar_try_wait(bar, parity);
+        if (__all_sync(0xFFFFFFFFu, done))
+            return true;
+        int give_up = 0;
+        if (lane == 0) {
+            const uint64_t now = globaltimer();
+            if (!timing) {
+                t0 = now;
+                timing = true;
+            }
+            give_up = (*abort_flag != 0) || (now - t0 > limit_ns);
+        }
+        if (__shfl_sync(0xFFFFFFFFu, give_up, 0))
+            return false;
+    }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(32 * 17)
+staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+                   int32_t hidden, float eps, int32_t stages, int *status, uint64_t limit_ns,
+                   uint32_t flags)
+{
+    using E = Elem<DT>;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int32_t row_bytes = hidden * E::kSize;
+    const StagedLayout L = staged_layout(row_bytes, stages);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    // full[s] = bars[s], empty[s] = bars[stages + s], weight = bars[2 * stages]
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * stages + 1);
+    unsigned char *wsm = smem + L.bar_bytes;
+    unsigned char *slots = wsm + L.slot_stride;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int consumers = (blockDim.x >> 5) - 1;
+    const int64_t my_rows =
+        rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(smem_u32(&bars[s]), 1);
+            mbar_init(smem_u32(&bars[stages + s]), 1);
+        }
+        mbar_init(smem_u32(&bars[2 * stages]), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+
+    const uint32_t wbar = smem_u32(&bars[2 * stages]);
+
+    if (warp == 0) {
+        if (lane != 0)
+            return;
+        // ---------------- producer
+        mbar_arrive_expect_tx(wbar, static_cast<uint32_t>(row_bytes));
+        bulk_copy_g2s(smem_u32(wsm), w, static_cast<uint32_t>(row_bytes), wbar);
+
+        const char *xb = static_cast<const char *>(x);
+        int64_t issued = 0;
+        if (!(flags & kFlagWithholdCopies)) {
+            for (int64_t k = 0; k < my_rows; ++k) {
+                const int s = static_cast<int>(k % stages);
+                if (k >= stages) {
+                    const uint32_t par = static_cast<uint32_t>(((k / stages) - 1) & 1);
+                    if (!wait_one(smem_u32(&bars[stages + s]), par, limit_ns, abort_flag)) {
+                        if (!*abort_flag)
+                            record_timeout(status);
+                        *abort_flag = 1;
+                        break;
+                    }
+                }
+                if (*abort_flag)
+                    break;
+                const int64_t row = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
+                const uint32_t fb = smem_u32(&bars[s]);
+                mbar_arrive_expect_tx(fb, static_cast<uint32_t>(row_bytes));
+                bulk_copy_g2s(smem_u32(slots + static_cast<int64_t>(s) * L.slot_stride),
+                              xb + row * row_bytes, static_cast<uint32_t>(row_bytes), fb);
+                issued = k + 1;
+            }
+        }
+        // Drain: every copy this block issued has landed before it exits.
+        if (!wait_one(wbar, 0, limit_ns, nullptr))
+            record_timeout(status);
+        const int64_t first = issued > stages ? issued - stages : 0;
+        for (int64_t k = first; k < issued; ++k) {
+            const int s = static_cast<int>(k % stages);
+            if (!wait_one(smem_u32(&bars[s]), static_cast<uint32_t>((k / stages) & 1), limit_ns,
+                          nullptr))
+                record_timeout(status);
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    const int c = warp - 1;
+    if (!wait_warp(wbar, 0, limit_ns, abort_flag, lane)) {
+        if (lane == 0) {
+            if (!*abort_flag)
+                record_timeout(status);
+            *abort_flag = 1;
+        }
+        return;
+    }
+    const int nvec = row_bytes / 16;
+    const float n = static_cast<float>(hidden);
+    char *yb = static_cast<char *>(y);
+
+    for (int64_t k = c; k < my_rows; k += consumers) {
+        const int s = static_cast<int>(k % stages);
+        const uint32_t par = static_cast<uint32_t>((k / stages) & 1);
+        if (!wait_warp(smem_u32(&bars[s]), par, limit_ns, abort_flag, lane)) {
+            if (lane == 0) {
+                if (!*abort_flag)
+                    record_timeout(status);
+                *abort_flag = 1;
+            }
+            return;
+        }
+        const unsigned char *src = slots + static_cast<int64_t>(s) * L.slot_stride;
+
+        float acc = 0.f;
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+            acc = sumsq<DT, 16>(xv, acc);
+        }
+        acc = group_allreduce<32>(acc);
+        const float r = row_factor(acc, n, eps);
+
+        const int64_t row = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
+        char *yr = yb + row * row_bytes;
+#pragma unroll 4
+        for (int v = lane; v < nvec; v += 32) {
+            const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+            const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+            Vec<16> o;
+            scale<DT, 16>(o, xv, wv, r);
+            st_stream(yr + static_cast<int64_t>(v) * 16, o);
+        }
+        __syncwarp();
+        if (lane == 0)
+            mbar_arrive(smem_u32(&bars[stages + s]));
+    }
+}
+
+template <int DT>
+cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
+{
+    staged_rows_kernel<DT><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
+        a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, a.status, a.wait_limit_ns, a.flags);
+    return cudaGetLastError();
+}
+
+#define STAGED_ENTRY(DT)                                                                       \
+    KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, &launch_staged<DT>,                  \
+               reinterpret_cast<const void *>(&staged_rows_kernel<DT>)}
+
+const KernelDesc kTable[] = {STAGED_ENTRY(RMSNORM_F32), STAGED_ENTRY(RMSNORM_BF16),
+                             STAGED_ENTRY(RMSNORM_F16)};
+
+} // namespace
+
+const KernelDesc *staged_kernels(int *n)
+{
+    *n = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
+    return kTable;
+}
+
+} // namespace rmsnorm

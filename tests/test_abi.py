@@ -1,0 +1,195 @@
+"""C ABI checks that need no GPU: the library builds for sm_103a, loads, and
+exports every function include/*.h declares; argument validation; the
+host-side selector."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import rmsnorm_fwd_gb300 as rn
+from rmsnorm_fwd_gb300 import inputs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SMS = 152
+OPTIN = 232448  # opt-in shared memory per block on sm_100-class parts (227 KiB)
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(", src):
+            name = m.group(1)
+            # a declaration: preceded by a return type on the same statement
+            if name.startswith("rmsnorm_"):
+                names.add(name)
+    return names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = rn._load()
+    names = declared_functions()
+    assert {"rmsnorm_create", "rmsnorm_fwd", "rmsnorm_destroy"} <= names
+    for name in sorted(names):
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    # exported with C linkage (no mangling): dlsym by the plain name worked above
+    assert rn.rmsnorm_version() >> 16 == 1
+
+
+def test_library_is_in_tree():
+    path = rn.library_path()
+    assert os.path.commonpath([path, ROOT]) == ROOT
+    assert os.path.exists(path)
+
+
+def test_status_strings():
+    for code in range(10):
+        s = rn.rmsnorm_status_string(code)
+        assert s and s != "unknown status"
+    assert rn.rmsnorm_status_string(999) == "unknown status"
+
+
+# ------------------------------------------------------------- validation (no GPU touched)
+
+FAKE = 1 << 40  # never dereferenced: every case below fails validation first
+
+
+def call(x, w, y, rows, hidden, eps, dtype):
+    return rn._load().rmsnorm_fwd(x, w, y, rows, hidden, eps, dtype, None)
+
+
+def test_bad_dtype():
+    assert call(FAKE, FAKE + 2 ** 30, FAKE + 2 ** 31, 4, 64, 1e-6, 7) == rn.ERR_UNSUPPORTED_DTYPE
+
+
+@pytest.mark.parametrize("rows,hidden,eps", [(-1, 64, 1e-6), (4, 0, 1e-6), (4, -3, 1e-6),
+                                             (4, 64, -1e-6), (4, 64, float("nan")),
+                                             (4, 64, float("inf"))])
+def test_bad_shape_or_eps(rows, hidden, eps):
+    assert call(FAKE, FAKE + 2 ** 30, FAKE + 2 ** 31, rows, hidden, eps, rn.BF16) == \
+        rn.ERR_INVALID_ARG
+
+
+def test_null_pointers():
+    assert call(0, FAKE, FAKE + 2 ** 31, 4, 64, 1e-6, rn.BF16) == rn.ERR_INVALID_ARG
+    assert call(FAKE, 0, FAKE + 2 ** 31, 4, 64, 1e-6, rn.BF16) == rn.ERR_INVALID_ARG
+    assert call(FAKE, FAKE + 2 ** 30, 0, 4, 64, 1e-6, rn.BF16) == rn.ERR_INVALID_ARG
+
+
+def test_partial_overlap_rejected():
+    # y starts one row into x: partial overlap
+    assert call(FAKE, FAKE + 2 ** 30, FAKE + 128, 4, 64, 1e-6, rn.BF16) == rn.ERR_ALIASING
+    # y overlaps the weight
+    assert call(FAKE, FAKE + 2 ** 30, FAKE + 2 ** 30 - 64, 4, 64, 1e-6, rn.BF16) == \
+        rn.ERR_ALIASING
+
+
+def test_no_context_without_gpu():
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    # valid arguments: the context lookup fails (no device) before any launch
+    rc = call(FAKE, FAKE + 2 ** 30, FAKE + 2 ** 31, 4, 64, 1e-6, rn.BF16)
+    assert rc in (rn.ERR_CUDA, rn.ERR_NOT_INITIALIZED)
+    assert rn._load().rmsnorm_create() in (rn.ERR_CUDA, rn.ERR_UNSUPPORTED_DEVICE)
+
+
+# ------------------------------------------------------------- selector (host only)
+
+A = 1 << 30  # 1 GiB-aligned fake addresses
+
+
+def plan(rows, hidden, dtype, variant=rn.VARIANT_AUTO, xoff=0, sms=SMS):
+    return rn.rmsnorm_plan_status(A + xoff, 3 * A, 5 * A + xoff, rows, hidden, dtype, sms,
+                                  OPTIN, variant)
+
+
+def test_selector_on_the_workloads():
+    expect = {
+        "f32_64x128": rn.VARIANT_WARP_PER_ROW,
+        "embed_bf16_8192x1024": rn.VARIANT_WARP_PER_ROW,
+        "decode_bf16_1x4096": rn.VARIANT_PERSISTENT,
+        "decode_bf16_8x4096": rn.VARIANT_PERSISTENT,
+        "decode_bf16_32x4096": rn.VARIANT_PERSISTENT,
+    }
+    for name, wl in inputs.WORKLOADS.items():
+        rc, p = plan(wl.rows, wl.hidden, rn.DTYPE_CODES[wl.dtype])
+        assert rc == rn.OK, name
+        assert p.variant != rn.VARIANT_GENERIC, name
+        if name in expect:
+            assert p.variant == expect[name], (name, p.as_dict())
+        assert p.grid >= 1 and p.block_threads % 32 == 0 and p.block_threads <= 1024
+
+
+def test_decode_one_block_per_row():
+    for rows in (1, 8, 32):
+        rc, p = plan(rows, 4096, rn.BF16)
+        assert rc == rn.OK and p.variant == rn.VARIANT_PERSISTENT
+        assert p.grid == rows
+        assert p.vecs_per_thread * p.threads_per_row * 8 >= 4096
+
+
+def test_persistent_grid_capped_by_sms():
+    rc, p = plan(100000, 4096, rn.BF16, rn.VARIANT_PERSISTENT)
+    assert rc == rn.OK and p.grid <= SMS * (2048 // p.block_threads)
+
+
+def test_capacity_covers_row():
+    for dt, es in ((rn.F32, 4), (rn.BF16, 2), (rn.F16, 2)):
+        for hidden in (8, 64, 128, 1000, 1024, 2880, 4096, 5120, 7168, 8192, 16384, 32768):
+            if hidden * es % 16:
+                continue
+            for v in (rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT):
+                rc, p = plan(4096, hidden, dt, v)
+                if rc == rn.OK:
+                    cap = p.threads_per_row * p.vecs_per_thread * p.vec_bytes // es
+                    assert cap >= hidden, (dt, hidden, v, p.as_dict())
+
+
+def test_ragged_rows_go_generic():
+    for hidden in (1, 3, 7, 9, 31, 33, 127, 129, 1023, 1025, 8191):
+        rc, p = plan(64, hidden, rn.BF16)
+        assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC, hidden
+
+
+def test_misaligned_pointer_goes_generic_or_is_refused_when_forced():
+    rc, p = plan(64, 4096, rn.BF16, xoff=2)
+    assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC
+    for v in (rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_STAGED):
+        rc, _ = plan(64, 4096, rn.BF16, v, xoff=2)
+        assert rc == rn.ERR_MISALIGNED
+
+
+def test_forced_variant_that_cannot_fit():
+    rc, _ = plan(64, 16384, rn.BF16, rn.VARIANT_WARP_PER_ROW)  # 2048 vectors > 32 x 16
+    assert rc == rn.ERR_VARIANT
+    rc, _ = plan(64, 1 << 20, rn.BF16, rn.VARIANT_STAGED)  # 2 MiB row > shared memory
+    assert rc == rn.ERR_VARIANT
+
+
+def test_staged_plan_fits_and_is_consistent():
+    for hidden in (2880, 4096, 5120, 7168, 16384, 32768):
+        for dt in (rn.BF16, rn.F16, rn.F32):
+            rc, p = plan(65536, hidden, dt, rn.VARIANT_STAGED)
+            es = 4 if dt == rn.F32 else 2
+            if hidden * es * 3 + 1024 > OPTIN:
+                assert rc == rn.ERR_VARIANT
+                continue
+            assert rc == rn.OK, (hidden, dt)
+            consumers = p.block_threads // 32 - 1
+            assert p.stages % consumers == 0 and p.stages >= 2
+            assert p.smem_bytes <= OPTIN
+            assert p.grid <= SMS
+
+
+def test_huge_row_still_planned():
+    rc, p = plan(4, 1 << 22, rn.BF16)
+    assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC
+
+
+def test_plan_struct_layout():
+    assert ctypes.sizeof(rn.Plan) == 40

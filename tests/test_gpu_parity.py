@@ -1,0 +1,223 @@
+"""GPU parity: the CUDA library (through the C ABI) against the fp64 CPU
+oracle on the same seeded inputs.
+
+* every workload shape, in the launch configuration the benchmark uses
+  (the selector's automatic plan), compared in full where the oracle is quick
+  and on sampled rows for the 65536-row wide-hidden shapes;
+* every variant forced on every shape it accepts, over a grid of hidden
+  sizes (powers of two, ragged, non-power-of-two LLM sizes) and row counts
+  (0, 1, 2, 31, 160, 161);
+* in place (y == x), guard bytes around y, misaligned pointers, zero rows,
+  eps = 0, a non-default stream.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import rmsnorm_fwd_gb300 as rn
+from rmsnorm_fwd_gb300 import inputs
+
+from _parity import compare, from_device, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rn.ensure_context(0)
+    yield
+    torch.cuda.synchronize()
+    assert rn.rmsnorm_get_device_status() == rn.OK
+
+
+def run(x_np, w_np, eps, dtype, variant=rn.VARIANT_AUTO, plan=None):
+    x = to_device(x_np, dtype)
+    w = to_device(w_np, dtype)
+    y = rn.rms_norm(x, w, eps, variant=variant, plan=plan)
+    torch.cuda.synchronize()
+    return from_device(y, dtype)
+
+
+# ------------------------------------------------------------------ workloads
+
+SMALL = ["f32_64x128", "embed_bf16_8192x1024", "decode_bf16_1x4096", "decode_bf16_8x4096",
+         "decode_bf16_32x4096", "prefill_bf16_16384x4096"]
+WIDE = [n for n in inputs.WORKLOADS if n.startswith("wide_")]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_workload_full_compare(name):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    y = run(x, w, wl.eps, wl.dtype)
+    s = compare(y, x, w, wl.eps, wl.dtype)
+    assert s["rows"] == wl.rows
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", WIDE)
+def test_wide_workload_sampled(name):
+    """65536 rows at 7168/5120/2880: full GPU run, 384 sampled rows checked."""
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    y = run(x, w, wl.eps, wl.dtype)
+    compare(y, x, w, wl.eps, wl.dtype, rows_idx=sample_rows(wl.rows, 384, seed=wl.key))
+    # every row is finite (weights U(0,2), eps > 0)
+    assert np.isfinite(oracle.widen(y[::97], wl.dtype)).all()
+
+
+@pytest.mark.parametrize("variant", [rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
+                                     rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT,
+                                     rn.VARIANT_GENERIC])
+def test_headline_shape_every_variant(variant):
+    wl = inputs.WORKLOADS["prefill_bf16_16384x4096"]
+    x, w = inputs.make_inputs(wl)
+    y = run(x, w, wl.eps, wl.dtype, variant=variant)
+    compare(y, x, w, wl.eps, wl.dtype)
+
+
+# ------------------------------------------------------------------ edge grid
+
+HIDDEN = [1, 2, 3, 7, 8, 9, 31, 33, 127, 128, 129, 1000, 1023, 1024, 1025, 2880, 4096, 5120,
+          7168, 8191, 16384, 32768]
+ROWS = [0, 1, 2, 31, 160, 161]
+VARIANTS = [rn.VARIANT_AUTO, rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
+            rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT, rn.VARIANT_GENERIC]
+
+
+def accepts(rows, hidden, dtype, variant):
+    """Whether the selector takes this forced variant (host-only query)."""
+    if rows == 0:
+        return True
+    sms, optin = rn.rmsnorm_device_limits()
+    base = 1 << 30
+    rc, _ = rn.rmsnorm_plan_status(base, 3 * base, 5 * base, rows, hidden, rn.DTYPE_CODES[dtype],
+                                   sms, optin, variant)
+    return rc == rn.OK
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("hidden", HIDDEN)
+def test_edge_grid(dtype, hidden):
+    checked = 0
+    for rows in ROWS:
+        x, w = inputs.random_case(rows, hidden, dtype, seed=rows)
+        for v in VARIANTS:
+            if not accepts(rows, hidden, dtype, v):
+                continue
+            y = run(x, w, 1e-6, dtype, variant=v)
+            compare(y, x, w, 1e-6, dtype)
+            checked += 1
+    assert checked > 0
+
+
+# ------------------------------------------------------------------ properties
+
+def test_in_place():
+    for name in ("embed_bf16_8192x1024", "decode_bf16_32x4096", "f32_64x128"):
+        wl = inputs.WORKLOADS[name]
+        x_np, w_np = inputs.make_inputs(wl)
+        for v in (rn.VARIANT_AUTO, rn.VARIANT_GENERIC, rn.VARIANT_STAGED, rn.VARIANT_CTA_PER_ROW):
+            if not accepts(wl.rows, wl.hidden, wl.dtype, v):
+                continue
+            x = to_device(x_np, wl.dtype)
+            w = to_device(w_np, wl.dtype)
+            rn.rms_norm(x, w, wl.eps, out=x, variant=v)
+            torch.cuda.synchronize()
+            compare(from_device(x, wl.dtype), x_np, w_np, wl.eps, wl.dtype)
+
+
+def test_guard_bytes_untouched():
+    for dtype, hidden in (("bf16", 4096), ("f16", 7168), ("f32", 128), ("bf16", 1025)):
+        rows = 161
+        x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=3)
+        x = to_device(x_np, dtype)
+        w = to_device(w_np, dtype)
+        pad = 4096
+        buf = torch.full((rows * hidden + 2 * pad,), 77.0, dtype=x.dtype, device="cuda")
+        y = buf[pad:pad + rows * hidden].view(rows, hidden)
+        for v in (rn.VARIANT_AUTO, rn.VARIANT_STAGED, rn.VARIANT_GENERIC):
+            if not accepts(rows, hidden, dtype, v):
+                continue
+            rn.rms_norm(x, w, 1e-6, out=y, variant=v)
+            torch.cuda.synchronize()
+            assert (buf[:pad] == 77.0).all() and (buf[pad + rows * hidden:] == 77.0).all()
+            compare(from_device(y, dtype), x_np, w_np, 1e-6, dtype)
+
+
+def test_misaligned_pointers_use_generic_and_match():
+    dtype, rows, hidden = "bf16", 33, 4096
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=4)
+    x_full = to_device(np.concatenate([np.zeros(1, np.uint16), x_np.ravel()]), dtype)
+    x = x_full[1:].view(rows, hidden)  # 2-byte offset
+    w = to_device(w_np, dtype)
+    y = rn.rms_norm(x, w, 1e-6)
+    assert rn.rmsnorm_last_variant() == rn.VARIANT_GENERIC
+    torch.cuda.synchronize()
+    compare(from_device(y, dtype), x_np, w_np, 1e-6, dtype)
+    with pytest.raises(rn.RmsnormError) as e:
+        rn.rms_norm(x, w, 1e-6, variant=rn.VARIANT_CTA_PER_ROW)
+    assert e.value.status == rn.ERR_MISALIGNED
+
+
+def test_zero_rows_and_eps_zero():
+    dtype = "bf16"
+    x_np = np.zeros((4, 256), np.uint16)
+    _, w_np = inputs.random_case(4, 256, dtype, seed=5)
+    for v in (rn.VARIANT_AUTO, rn.VARIANT_GENERIC, rn.VARIANT_STAGED):
+        y = run(x_np, w_np, 0.0, dtype, variant=v)  # 0 * inf -> NaN, as in the oracle
+        compare(y, x_np, w_np, 0.0, dtype)
+        y = run(x_np, w_np, 1e-5, dtype, variant=v)
+        assert (oracle.widen(y, dtype) == 0).all()
+
+
+def test_dynamic_range_rows():
+    """Rows scaled from 1e-3 to 1e3 (log-uniform), f16 and bf16."""
+    for dtype in ("f16", "bf16"):
+        rng = np.random.default_rng(11)
+        z = rng.standard_normal((256, 5120)).astype(np.float32)
+        z *= (10.0 ** rng.uniform(-3, 3, (256, 1))).astype(np.float32)
+        x_np = inputs.to_storage(z, dtype)
+        _, w_np = inputs.random_case(1, 5120, dtype, seed=6, w_dist="u0_2")
+        for v in (rn.VARIANT_AUTO, rn.VARIANT_STAGED, rn.VARIANT_CTA_PER_ROW):
+            compare(run(x_np, w_np, 1e-5, dtype, variant=v), x_np, w_np, 1e-5, dtype)
+
+
+def test_non_default_stream():
+    wl = inputs.WORKLOADS["embed_bf16_8192x1024"]
+    x_np, w_np = inputs.make_inputs(wl)
+    x = to_device(x_np, wl.dtype)
+    w = to_device(w_np, wl.dtype)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        y = rn.rms_norm(x, w, wl.eps)
+    s.synchronize()
+    compare(from_device(y, wl.dtype), x_np, w_np, wl.eps, wl.dtype)
+
+
+def test_raw_c_abi_call():
+    """rmsnorm_fwd called with raw pointers and a raw stream handle."""
+    wl = inputs.WORKLOADS["decode_bf16_8x4096"]
+    x_np, w_np = inputs.make_inputs(wl)
+    x = to_device(x_np, wl.dtype)
+    w = to_device(w_np, wl.dtype)
+    y = torch.empty_like(x)
+    rn.rmsnorm_fwd(x.data_ptr(), w.data_ptr(), y.data_ptr(), wl.rows, wl.hidden, wl.eps, rn.BF16,
+                   torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    compare(from_device(y, wl.dtype), x_np, w_np, wl.eps, wl.dtype)
+
+
+def test_plan_written_back_and_replayed():
+    wl = inputs.WORKLOADS["prefill_bf16_16384x4096"]
+    x_np, w_np = inputs.make_inputs(wl)
+    p = rn.Plan()
+    y1 = run(x_np, w_np, wl.eps, wl.dtype, plan=p)
+    assert p.variant != rn.VARIANT_AUTO and p.grid > 0
+    y2 = run(x_np, w_np, wl.eps, wl.dtype, plan=p)  # explicit plan path
+    assert np.array_equal(y1, y2)
