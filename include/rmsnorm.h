@@ -155,6 +155,9 @@ typedef struct {
     int32_t tpr;       /* threads per row fixed at compile time (warp-per-row) */
     int32_t nv;        /* vectors per thread fixed at compile time */
     int32_t block;     /* block size fixed at compile time, or the largest allowed */
+    int32_t min_blocks;   /* resident blocks per SM the build was register-capped for; 0 = none */
+    int32_t cache_policy; /* 0 plain, 1 L2 256-byte prefetch hint, 2 streaming (.cs) loads and
+                           * stores, 3 staged rows written back by bulk copies */
 } rmsnorm_kernel_info_t;
 
 /* SM count and opt-in shared memory per block of the current device, as
@@ -168,6 +171,15 @@ int rmsnorm_kernel_count(void);
 /* Describe instantiation `index` (0 <= index < rmsnorm_kernel_count()).
  * Returns RMSNORM_OK or RMSNORM_ERR_INVALID_ARG. */
 int rmsnorm_kernel_info(int index, rmsnorm_kernel_info_t *out);
+
+/* Host-only check of an explicit plan against a call's arguments on a device
+ * with `sm_count` SMs and `smem_optin` bytes of opt-in shared memory per
+ * block: the check rmsnorm_fwd_ex applies before launching a caller-supplied
+ * plan.  Pointer values are used only for their alignment.  Returns
+ * RMSNORM_OK or the status rmsnorm_fwd_ex would return. */
+int rmsnorm_validate_plan(const rmsnorm_plan_t *plan, const void *x, const void *weight,
+                          const void *y, int64_t rows, int64_t hidden, int dtype, int sm_count,
+                          int smem_optin);
 
 /* Variant of the last successful launch on the calling thread (0 if none). */
 int rmsnorm_last_variant(void);

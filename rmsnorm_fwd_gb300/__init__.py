@@ -64,7 +64,7 @@ class Plan(ctypes.Structure):
 class KernelInfo(ctypes.Structure):
     """rmsnorm_kernel_info_t."""
     _fields_ = [(name, ctypes.c_int32) for name in (
-        "variant", "dtype", "vec_bytes", "tpr", "nv", "block")]
+        "variant", "dtype", "vec_bytes", "tpr", "nv", "block", "min_blocks", "cache_policy")]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -100,6 +100,7 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_plan": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, pp], i32),
             "rmsnorm_last_variant": ([], i32),
             "rmsnorm_kernel_count": ([], i32),
+            "rmsnorm_validate_plan": ([pp, vp, vp, vp, i64, i64, i32, i32, i32], i32),
             "rmsnorm_device_limits": ([ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int)],
                                       i32),
             "rmsnorm_kernel_info": ([i32, ctypes.POINTER(KernelInfo)], i32),
@@ -171,6 +172,13 @@ def rmsnorm_device_limits() -> tuple[int, int]:
     _check(_load().rmsnorm_device_limits(ctypes.byref(a), ctypes.byref(b)),
            "rmsnorm_device_limits")
     return a.value, b.value
+
+
+def rmsnorm_validate_plan(plan: Plan, x: int, weight: int, y: int, rows: int, hidden: int,
+                          dtype: int, sm_count: int, smem_optin: int) -> int:
+    """Status rmsnorm_fwd_ex would give this explicit plan (host only)."""
+    return _load().rmsnorm_validate_plan(ctypes.byref(plan), x, weight, y, rows, hidden, dtype,
+                                         sm_count, smem_optin)
 
 
 def rmsnorm_kernel_count() -> int:

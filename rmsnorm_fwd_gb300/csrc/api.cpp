@@ -252,6 +252,15 @@ int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows,
     return plan_launch(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant, out);
 }
 
+int rmsnorm_validate_plan(const rmsnorm_plan_t *plan, const void *x, const void *weight,
+                          const void *y, int64_t rows, int64_t hidden, int dtype, int sm_count,
+                          int smem_optin)
+{
+    if (!plan)
+        return RMSNORM_ERR_INVALID_ARG;
+    return validate_plan(*plan, x, weight, y, rows, hidden, dtype, sm_count, smem_optin);
+}
+
 int rmsnorm_device_limits(int *sm_count, int *smem_optin)
 {
     if (!sm_count || !smem_optin)
@@ -285,6 +294,8 @@ int rmsnorm_kernel_info(int index, rmsnorm_kernel_info_t *out)
     out->tpr = d.tpr;
     out->nv = d.nv;
     out->block = d.block;
+    out->min_blocks = d.minb;
+    out->cache_policy = d.cache;
     return RMSNORM_OK;
 }
 

@@ -85,20 +85,45 @@ template <int VB> struct alignas(VB) Vec {
     uint32_t w[kWords];
 };
 
-// Streaming load of x: not kept in L1 (each byte is read once).  No .nc: x
-// may be the output too (in-place), so the read-only path is not used.
+// Streaming load of x.  No .nc: x may be the output too (in-place), so the
+// read-only path is not used.  Cache policy CP:
+//   0: not kept in L1 (each byte is read once);
+//   1: as 0, plus a 256-byte L2 prefetch hint (whole DRAM bursts);
+//   2: .cs (streaming, evict-first in L1 and L2).
+template <int CP>
 __device__ inline void ld_stream(Vec<16> &v, const void *p)
 {
-    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                 : "l"(p));
+    if (CP == 1)
+        asm volatile("ld.global.L1::no_allocate.L2::256B.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
+    else if (CP == 2)
+        asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                     : "l"(p));
 }
+template <int CP>
 __device__ inline void ld_stream(Vec<32> &v, const void *p)
 {
-    asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                 : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
-                   "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
-                 : "l"(p));
+    if (CP == 1)
+        asm volatile("ld.global.L1::no_allocate.L2::256B.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                       "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                     : "l"(p));
+    else if (CP == 2)
+        asm volatile("ld.global.cs.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                       "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                     : "l"(p));
+    else
+        asm volatile("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]),
+                       "=r"(v.w[5]), "=r"(v.w[6]), "=r"(v.w[7])
+                     : "l"(p));
 }
 
 // Weight load: read-only for the whole kernel (y never overlaps it), reused
@@ -117,19 +142,45 @@ __device__ inline void ld_weight(Vec<32> &v, const void *p)
                  : "l"(p));
 }
 
-// Output store: written once, not re-read by this kernel.
+// Output store: written once, not re-read by this kernel.  CP as for loads
+// (2 = .cs streaming store, otherwise not allocated in L1).
+template <int CP>
 __device__ inline void st_stream(void *p, const Vec<16> &v)
 {
-    asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};"
-                 ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
-                 : "memory");
+    if (CP == 2)
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                     ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                     : "memory");
+    else
+        asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};"
+                     ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3])
+                     : "memory");
 }
+template <int CP>
 __device__ inline void st_stream(void *p, const Vec<32> &v)
 {
-    asm volatile("st.global.L1::no_allocate.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
-                 ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]),
-                   "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
-                 : "memory");
+    if (CP == 2)
+        asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]),
+                       "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                     : "memory");
+    else
+        asm volatile("st.global.L1::no_allocate.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                     ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]),
+                       "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                     : "memory");
+}
+
+// Hides the vector's words from the compiler's value numbering, so the fp32
+// unpacked copies made for the sum of squares are not kept alive until the
+// scale pass (the scale pass unpacks the words again; that costs one integer
+// op per element and saves two registers per packed word).
+template <int VB>
+__device__ inline void reuse_barrier(Vec<VB> &v)
+{
+#pragma unroll
+    for (int k = 0; k < Vec<VB>::kWords; ++k)
+        asm("mov.b32 %0, %0;" : "+r"(v.w[k]));
 }
 
 // Sum of squares of one vector, accumulated into s (fp32).

@@ -61,7 +61,7 @@ cudaError_t launch_generic(const rmsnorm_plan_t &p, const LaunchArgs &a)
 }
 
 #define GENERIC_ENTRY(DT)                                                                      \
-    KernelDesc{RMSNORM_VARIANT_GENERIC, DT, 0, 0, 0, 0, &launch_generic<DT>,                  \
+    KernelDesc{RMSNORM_VARIANT_GENERIC, DT, 0, 0, 0, 0, 0, 0, &launch_generic<DT>,                  \
                reinterpret_cast<const void *>(&generic_rows_kernel<DT>)}
 
 const KernelDesc kTable[] = {GENERIC_ENTRY(RMSNORM_F32), GENERIC_ENTRY(RMSNORM_BF16),

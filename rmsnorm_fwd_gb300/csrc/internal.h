@@ -42,6 +42,9 @@ struct KernelDesc {
     int32_t tpr;         // threads per row, compile time (warp kernels); 0 = runtime
     int32_t nv;          // vectors per thread, compile time; 0 = runtime loop
     int32_t block;       // threads per block, compile time; 0 = runtime
+    int32_t minb;        // occupancy floor asked of the compiler (blocks per SM); 0 = none
+    int32_t cache;       // memory path: 0 plain, 1 L2 256B prefetch, 2 streaming (.cs),
+                         // 3 staged rows stored by bulk copies
     LaunchFn launch;
     const void *func;    // the __global__ function (attributes)
 };

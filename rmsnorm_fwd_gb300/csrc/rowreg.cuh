@@ -16,6 +16,12 @@
 // compile-time constant for the warp-per-row body and an upper bound
 // (__launch_bounds__) for the block-per-row body ("CuTeDSL at Perplexity",
 // section "Prefill and decode specialization").
+//
+// Occupancy is what sets the bandwidth of an HBM-bound row kernel: a block
+// cannot store a row before all of it has arrived, so the bytes in flight per
+// SM are (resident rows) x (row bytes).  MINB > 0 asks the compiler for at
+// least MINB resident blocks per SM (a register cap) and loads the weight
+// after the reduction instead of holding it in registers across rows.
 #pragma once
 
 #include "internal.h"
@@ -35,35 +41,31 @@ __device__ inline void vzero(Vec<VB> &v)
 // ---------------------------------------------------------------- warp-per-row
 
 // TPR lanes (4..32, power of two) per row, BLOCK/TPR rows per block per
-// iteration, grid-stride over rows.  Row r is handled in the iteration in
-// which its group's base row reaches it; the loop bound is block-uniform so
-// every lane takes part in every shuffle.
-template <int DT, int VB, int TPR, int NV, int BLOCK>
-__global__ void __launch_bounds__(BLOCK)
+// iteration, grid-stride over rows.  The loop bound is block-uniform so every
+// lane takes part in every shuffle.
+template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
+__global__ void __launch_bounds__(BLOCK, MINB > 0 ? MINB : 1)
 warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                  int32_t hidden, float eps)
 {
     using E = Elem<DT>;
-    constexpr int VPE = VB / E::kSize;     // elements per vector
-    constexpr int GROUPS = BLOCK / TPR;    // rows per block per iteration
-    constexpr bool W_HELD = NV * VB <= 64; // keep the weight slice in registers
+    constexpr int VPE = VB / E::kSize;                     // elements per vector
+    constexpr int GROUPS = BLOCK / TPR;                    // rows per block per iteration
+    constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;    // weight slice kept in registers
 
     const int nvec = hidden / VPE;
     const int t = threadIdx.x % TPR;
     const int g = threadIdx.x / TPR;
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
-    const char *xb = static_cast<const char *>(x);
-    const char *wb = static_cast<const char *>(w);
-    char *yb = static_cast<char *>(y);
+    const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
     if (W_HELD) {
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * TPR;
-            if (v < nvec)
-                ld_weight(wv[k], wb + static_cast<int64_t>(v) * VB);
+            if (t + k * TPR < nvec)
+                ld_weight(wv[k], wt + k * TPR * VB);
             else
                 vzero(wv[k]);
         }
@@ -73,15 +75,15 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
          base += static_cast<int64_t>(gridDim.x) * GROUPS) {
         const int64_t row = base + g;
         const bool active = row < rows;
-        const char *xr = xb + row * row_bytes;
-        char *yr = yb + row * row_bytes;
+        const int64_t off = row * row_bytes + t * VB;
+        const char *xr = static_cast<const char *>(x) + off;
+        char *yr = static_cast<char *>(y) + off;
 
         Vec<VB> xv[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * TPR;
-            if (active && v < nvec)
-                ld_stream(xv[k], xr + static_cast<int64_t>(v) * VB);
+            if (active && t + k * TPR < nvec)
+                ld_stream<CP>(xv[k], xr + k * TPR * VB);
             else
                 vzero(xv[k]);
         }
@@ -91,20 +93,22 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
             s = sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<TPR>(s);
         const float r = row_factor(s, n, eps);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            reuse_barrier(xv[k]);
 
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * TPR;
-            if (active && v < nvec) {
+            if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
                 if (W_HELD) {
                     scale<DT, VB>(o, xv[k], wv[W_HELD ? k : 0], r);
                 } else {
                     Vec<VB> wk;
-                    ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                    ld_weight(wk, wt + k * TPR * VB);
                     scale<DT, VB>(o, xv[k], wk, r);
                 }
-                st_stream(yr + static_cast<int64_t>(v) * VB, o);
+                st_stream<CP>(yr + k * TPR * VB, o);
             }
         }
     }
@@ -114,36 +118,35 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 
 // blockDim.x threads (a multiple of 32, <= MAXT) per row, grid-stride over
 // rows.  Warp totals go through a double-buffered shared array so one
-// __syncthreads per row suffices.
-template <int DT, int VB, int NV, int MAXT>
-__global__ void __launch_bounds__(MAXT)
+// __syncthreads per row suffices.  TPRC > 0 fixes blockDim.x = TPRC at
+// compile time (vector offsets become immediates).
+template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC>
+__global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                 int32_t hidden, float eps)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
-    constexpr bool W_HELD = NV * VB <= 64;
+    constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;
     __shared__ float part[2][32];
 
     const int nvec = hidden / VPE;
     const int t = threadIdx.x;
-    const int tpr = blockDim.x;
+    const int tpr = TPRC > 0 ? TPRC : blockDim.x;
     const int lane = t & 31;
     const int warp = t >> 5;
     const int nwarps = tpr >> 5;
+    const int stride = tpr * VB; // bytes between a thread's consecutive vectors
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
-    const char *xb = static_cast<const char *>(x);
-    const char *wb = static_cast<const char *>(w);
-    char *yb = static_cast<char *>(y);
+    const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
     if (W_HELD) {
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * tpr;
-            if (v < nvec)
-                ld_weight(wv[k], wb + static_cast<int64_t>(v) * VB);
+            if (t + k * tpr < nvec)
+                ld_weight(wv[k], wt + k * stride);
             else
                 vzero(wv[k]);
         }
@@ -151,14 +154,14 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
-        const char *xr = xb + row * row_bytes;
-        char *yr = yb + row * row_bytes;
+        const int64_t off = row * row_bytes + t * VB;
+        const char *xr = static_cast<const char *>(x) + off;
+        char *yr = static_cast<char *>(y) + off;
         Vec<VB> xv[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * tpr;
-            if (v < nvec)
-                ld_stream(xv[k], xr + static_cast<int64_t>(v) * VB);
+            if (t + k * tpr < nvec)
+                ld_stream<CP>(xv[k], xr + k * stride);
             else
                 vzero(xv[k]);
         }
@@ -167,26 +170,30 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
         for (int k = 0; k < NV; ++k)
             s = sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<32>(s);
-        if (lane == 0)
-            part[it & 1][warp] = s;
-        __syncthreads();
-        float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
-        tot = group_allreduce<32>(tot);
-        const float r = row_factor(tot, n, eps);
+        if (TPRC != 32) {
+            if (lane == 0)
+                part[it & 1][warp] = s;
+            __syncthreads();
+            const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
+            s = group_allreduce<32>(tot);
+        }
+        const float r = row_factor(s, n, eps);
+#pragma unroll
+        for (int k = 0; k < NV; ++k)
+            reuse_barrier(xv[k]);
 
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            const int v = t + k * tpr;
-            if (v < nvec) {
+            if (t + k * tpr < nvec) {
                 Vec<VB> o;
                 if (W_HELD) {
                     scale<DT, VB>(o, xv[k], wv[W_HELD ? k : 0], r);
                 } else {
                     Vec<VB> wk;
-                    ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                    ld_weight(wk, wt + k * stride);
                     scale<DT, VB>(o, xv[k], wk, r);
                 }
-                st_stream(yr + static_cast<int64_t>(v) * VB, o);
+                st_stream<CP>(yr + k * stride, o);
             }
         }
     }
@@ -194,42 +201,63 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
 // ---------------------------------------------------------------- launchers
 
-template <int DT, int VB, int TPR, int NV, int BLOCK>
+template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
 cudaError_t launch_warp(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    warp_rows_kernel<DT, VB, TPR, NV, BLOCK><<<p.grid, BLOCK, 0, a.stream>>>(
+    warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP><<<p.grid, BLOCK, 0, a.stream>>>(
         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
     return cudaGetLastError();
 }
 
-template <int DT, int VB, int NV, int MAXT>
+template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC>
 cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    cta_rows_kernel<DT, VB, NV, MAXT><<<p.grid, p.block_threads, 0, a.stream>>>(
+    cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC><<<p.grid, p.block_threads, 0, a.stream>>>(
         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
     return cudaGetLastError();
 }
 
 constexpr int kWarpBlock = 256;
 
-#define WARP_ENTRY(DT, VB, TPR, NV)                                                            \
-    KernelDesc{RMSNORM_VARIANT_WARP_PER_ROW, DT, VB, TPR, NV, kWarpBlock,                     \
-               &launch_warp<DT, VB, TPR, NV, kWarpBlock>,                                      \
-               reinterpret_cast<const void *>(&warp_rows_kernel<DT, VB, TPR, NV, kWarpBlock>)}
+#define WARP_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
+    KernelDesc{RMSNORM_VARIANT_WARP_PER_ROW, DT, VB, TPR, NV, kWarpBlock, MINB, CP,           \
+               &launch_warp<DT, VB, TPR, NV, kWarpBlock, MINB, CP>,                            \
+               reinterpret_cast<const void *>(                                                 \
+                   &warp_rows_kernel<DT, VB, TPR, NV, kWarpBlock, MINB, CP>)}
 
-#define CTA_ENTRY(DT, VB, NV, MAXT)                                                            \
-    KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, NV, MAXT, &launch_cta<DT, VB, NV, MAXT>, \
-               reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, MAXT>)}
+#define CTA_ENTRY(DT, VB, NV, MAXT, MINB, CP)                                                  \
+    KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, NV, MAXT, MINB, CP,                    \
+               &launch_cta<DT, VB, NV, MAXT, MINB, CP, 0>,                                     \
+               reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, 0>)}
 
+// Block of exactly TPR threads (compile time).
+#define CTAF_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
+    KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, TPR, NV, TPR, MINB, CP,                   \
+               &launch_cta<DT, VB, NV, TPR, MINB, CP, TPR>,                                    \
+               reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, TPR, MINB, CP, TPR>)}
+
+// The instantiations every element type gets.
+//   warp-per-row: (VB, TPR, NV, MINB, CP)
+//   block-per-row, runtime block size <= MAXT: (VB, NV, MAXT, MINB, CP)
+//   block-per-row, block size fixed at TPR: (VB, TPR, NV, MINB, CP)
+// MINB caps registers so at least MINB blocks of MAXT threads fit on an SM
+// (65536 registers): MAXT x MINB = 2048 -> 32 registers per thread.
 #define ROWREG_SET(DT)                                                                         \
-    WARP_ENTRY(DT, 16, 4, 1), WARP_ENTRY(DT, 16, 8, 1), WARP_ENTRY(DT, 16, 8, 2),             \
-        WARP_ENTRY(DT, 16, 16, 1), WARP_ENTRY(DT, 16, 16, 2), WARP_ENTRY(DT, 16, 32, 1),      \
-        WARP_ENTRY(DT, 16, 32, 2), WARP_ENTRY(DT, 16, 32, 4), WARP_ENTRY(DT, 16, 32, 8),      \
-        WARP_ENTRY(DT, 16, 32, 16), WARP_ENTRY(DT, 32, 32, 1), WARP_ENTRY(DT, 32, 32, 2),     \
-        WARP_ENTRY(DT, 32, 32, 4), WARP_ENTRY(DT, 32, 32, 8), CTA_ENTRY(DT, 16, 1, 1024),     \
-        CTA_ENTRY(DT, 16, 2, 1024), CTA_ENTRY(DT, 16, 3, 1024), CTA_ENTRY(DT, 16, 4, 1024),   \
-        CTA_ENTRY(DT, 16, 6, 512), CTA_ENTRY(DT, 16, 8, 512), CTA_ENTRY(DT, 32, 1, 1024),     \
-        CTA_ENTRY(DT, 32, 2, 1024), CTA_ENTRY(DT, 32, 4, 512)
+    WARP_ENTRY(DT, 16, 4, 1, 0, 0), WARP_ENTRY(DT, 16, 8, 1, 0, 0),                           \
+        WARP_ENTRY(DT, 16, 8, 2, 0, 0), WARP_ENTRY(DT, 16, 16, 1, 0, 0),                      \
+        WARP_ENTRY(DT, 16, 16, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 1, 0, 0),                     \
+        WARP_ENTRY(DT, 16, 32, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 4, 0, 0),                     \
+        WARP_ENTRY(DT, 16, 32, 2, 8, 0), WARP_ENTRY(DT, 16, 32, 4, 8, 0),                     \
+        WARP_ENTRY(DT, 32, 32, 1, 0, 0), WARP_ENTRY(DT, 32, 32, 2, 0, 0),                     \
+        CTA_ENTRY(DT, 16, 1, 1024, 0, 0), CTA_ENTRY(DT, 16, 1, 1024, 2, 1),                   \
+        CTA_ENTRY(DT, 16, 2, 256, 8, 0), CTA_ENTRY(DT, 16, 2, 256, 8, 1),                     \
+        CTA_ENTRY(DT, 16, 2, 1024, 2, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                    \
+        CTA_ENTRY(DT, 16, 4, 256, 6, 0), CTA_ENTRY(DT, 16, 4, 256, 6, 1),                     \
+        CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 16, 8, 512, 0, 1),                    \
+        CTA_ENTRY(DT, 32, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 2, 256, 8, 1),                    \
+        CTA_ENTRY(DT, 32, 2, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
+        CTAF_ENTRY(DT, 16, 256, 2, 8, 1), CTAF_ENTRY(DT, 16, 128, 4, 12, 1),                  \
+        CTAF_ENTRY(DT, 16, 512, 1, 0, 0)
 
 } // namespace rowreg
 } // namespace rmsnorm

@@ -44,15 +44,16 @@ int round_up(int v, int m)
     return (v + m - 1) / m * m;
 }
 
-// Finds the table entry for (variant, dtype, vec_bytes, tpr, nv); -1 if none.
-int find_kernel(int variant, int dtype, int vec_bytes, int tpr, int nv)
+// Finds the table entry for (variant, dtype, vec_bytes, tpr, nv, cache) with
+// no occupancy cap; -1 if none.
+int find_kernel(int variant, int dtype, int vec_bytes, int tpr, int nv, int cache = 0)
 {
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
         if (d.variant == variant && d.dtype == dtype && d.vec_bytes == vec_bytes &&
-            d.tpr == tpr && d.nv == nv)
+            d.tpr == tpr && d.nv == nv && d.cache == cache && d.minb == 0)
             return i;
     }
     return -1;
@@ -115,7 +116,8 @@ int plan_warp(const Shape &s, int vb, rmsnorm_plan_t *p)
     int64_t best_cap = INT64_MAX;
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
-        if (d.variant != RMSNORM_VARIANT_WARP_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb)
+        if (d.variant != RMSNORM_VARIANT_WARP_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb ||
+            d.minb != 0 || d.cache != 0)
             continue;
         const int64_t cap = int64_t(d.tpr) * d.nv;
         if (cap < nvec)
@@ -156,7 +158,8 @@ int plan_cta(const Shape &s, int vb, bool persistent, rmsnorm_plan_t *p)
     double best_score = 1e30;
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
-        if (d.variant != RMSNORM_VARIANT_CTA_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb)
+        if (d.variant != RMSNORM_VARIANT_CTA_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb ||
+            d.minb != 0 || d.cache != 0 || d.tpr != 0)
             continue;
         const int64_t need = (nvec + d.nv - 1) / d.nv;
         const int64_t tpr = std::max<int64_t>(32, (need + 31) / 32 * 32);
@@ -331,11 +334,16 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
     case RMSNORM_VARIANT_CTA_PER_ROW:
         if (p.block_threads > d.block || int64_t(p.block_threads) * d.nv < nvec)
             return RMSNORM_ERR_VARIANT;
+        if (d.tpr != 0 && p.block_threads != d.tpr) // block size fixed at compile time
+            return RMSNORM_ERR_VARIANT;
         break;
     case RMSNORM_VARIANT_STAGED: {
         const int consumers = p.block_threads / 32 - 1;
         if (consumers < 1 || consumers > kStagedMaxConsumers || p.stages < 1 ||
             p.stages > kStagedMaxStages || p.stages % consumers != 0 || s.row_bytes > INT_MAX / 4)
+            return RMSNORM_ERR_VARIANT;
+        // Bulk-store mode releases a slot one row later: each consumer needs two.
+        if (d.cache == 3 && p.stages < 2 * consumers)
             return RMSNORM_ERR_VARIANT;
         const int need = staged_layout(static_cast<int>(s.row_bytes), p.stages).smem_bytes;
         if (p.smem_bytes != need || need > smem_optin || p.grid > rows)

@@ -69,6 +69,27 @@ __device__ inline void bulk_copy_g2s(uint32_t dst, const void *src, uint32_t byt
                  : "memory");
 }
 
+// y row <- shared slot, tracked in this thread's bulk-async group.
+__device__ inline void bulk_copy_s2g(void *dst, uint32_t src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src),
+                 "r"(bytes)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ inline void bulk_wait_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ inline void bulk_wait_all()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ inline uint64_t globaltimer()
 {
     uint64_t t;
@@ -124,7 +145,11 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
     }
 }
 
-template <int DT>
+// TMA_STORE: the consumer writes y back into its slot and one lane streams
+// the row to global memory with a bulk copy; the slot is handed back to the
+// producer once that copy has finished reading it.  Otherwise y is stored
+// from registers with 16-byte vector stores.
+template <int DT, bool TMA_STORE>
 __global__ void __launch_bounds__(32 * 17)
 staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                    int32_t hidden, float eps, int32_t stages, int *status, uint64_t limit_ns,
@@ -218,6 +243,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
     const int nvec = row_bytes / 16;
     const float n = static_cast<float>(hidden);
     char *yb = static_cast<char *>(y);
+    int prev_slot = -1; // TMA_STORE: slot whose bulk store may still be reading
 
     for (int64_t k = c; k < my_rows; k += consumers) {
         const int s = static_cast<int>(k % stages);
@@ -227,6 +253,8 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                 if (!*abort_flag)
                     record_timeout(status);
                 *abort_flag = 1;
+                if (TMA_STORE)
+                    bulk_wait_all(); // own stores still read the slots
             }
             return;
         }
@@ -243,34 +271,63 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
 
         const int64_t row = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
         char *yr = yb + row * row_bytes;
+        if (TMA_STORE) {
+            unsigned char *dst = slots + static_cast<int64_t>(s) * L.slot_stride;
 #pragma unroll 4
-        for (int v = lane; v < nvec; v += 32) {
-            const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
-            const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
-            Vec<16> o;
-            scale<DT, 16>(o, xv, wv, r);
-            st_stream(yr + static_cast<int64_t>(v) * 16, o);
+            for (int v = lane; v < nvec; v += 32) {
+                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
+                const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                Vec<16> o;
+                scale<DT, 16>(o, xv, wv, r);
+                *reinterpret_cast<Vec<16> *>(dst + v * 16) = o;
+            }
+            // The slot's new contents must be visible to the bulk copy (async proxy).
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) {
+                bulk_copy_s2g(yr, smem_u32(dst), static_cast<uint32_t>(row_bytes));
+                // The previous row's copy has finished reading its slot: release it.
+                bulk_wait_read<1>();
+                if (prev_slot >= 0)
+                    mbar_arrive(smem_u32(&bars[stages + prev_slot]));
+            }
+            prev_slot = s;
+        } else {
+#pragma unroll 4
+            for (int v = lane; v < nvec; v += 32) {
+                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                Vec<16> o;
+                scale<DT, 16>(o, xv, wv, r);
+                st_stream<0>(yr + static_cast<int64_t>(v) * 16, o);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bars[stages + s]));
         }
-        __syncwarp();
-        if (lane == 0)
-            mbar_arrive(smem_u32(&bars[stages + s]));
+    }
+    if (TMA_STORE && lane == 0) {
+        bulk_wait_all(); // every y row written before the block exits
+        if (prev_slot >= 0)
+            mbar_arrive(smem_u32(&bars[stages + prev_slot]));
     }
 }
 
-template <int DT>
+template <int DT, bool TS>
 cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    staged_rows_kernel<DT><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
+    staged_rows_kernel<DT, TS><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
         a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, a.status, a.wait_limit_ns, a.flags);
     return cudaGetLastError();
 }
 
-#define STAGED_ENTRY(DT)                                                                       \
-    KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, &launch_staged<DT>,                  \
-               reinterpret_cast<const void *>(&staged_rows_kernel<DT>)}
+#define STAGED_ENTRY(DT, TS)                                                                   \
+    KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, 0, TS ? 3 : 0, &launch_staged<DT, TS>, \
+               reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS>)}
 
-const KernelDesc kTable[] = {STAGED_ENTRY(RMSNORM_F32), STAGED_ENTRY(RMSNORM_BF16),
-                             STAGED_ENTRY(RMSNORM_F16)};
+const KernelDesc kTable[] = {STAGED_ENTRY(RMSNORM_F32, false), STAGED_ENTRY(RMSNORM_BF16, false),
+                             STAGED_ENTRY(RMSNORM_F16, false), STAGED_ENTRY(RMSNORM_F32, true),
+                             STAGED_ENTRY(RMSNORM_BF16, true), STAGED_ENTRY(RMSNORM_F16, true)};
 
 } // namespace
 

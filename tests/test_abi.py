@@ -193,3 +193,44 @@ def test_huge_row_still_planned():
 
 def test_plan_struct_layout():
     assert ctypes.sizeof(rn.Plan) == 40
+
+
+def test_per_kernel_parity_plans_are_valid():
+    """The explicit plans the GPU per-kernel test launches all pass the
+    library's own plan validation (checked here, host only)."""
+    import sys
+    sys.path.insert(0, os.path.dirname(__file__))
+    import test_gpu_kernels as tk
+    n = 0
+    for k in rn.kernels():
+        es = tk.ES[k["dtype"]]
+        for hidden, pd in tk.plans_for(k, 37, SMS, OPTIN):
+            rc = rn.rmsnorm_validate_plan(rn.Plan(**pd), A, 3 * A, 5 * A, 37, hidden, k["dtype"],
+                                          SMS, OPTIN)
+            assert rc == rn.OK, (k, hidden, pd, rc)
+            n += 1
+    assert n > 500
+
+
+def test_validation_rejects_bad_plans():
+    rc, p = plan(64, 4096, rn.BF16, rn.VARIANT_CTA_PER_ROW)
+    assert rc == rn.OK
+    bad = rn.Plan(**p.as_dict())
+    bad.block_threads = 33
+    assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 64, 4096, rn.BF16, SMS, OPTIN) != rn.OK
+    bad = rn.Plan(**p.as_dict())
+    bad.kernel_index = 10 ** 6
+    assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 64, 4096, rn.BF16, SMS, OPTIN) != rn.OK
+    bad = rn.Plan(**p.as_dict())
+    bad.block_threads = 32  # too few threads for the row
+    assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 64, 4096, rn.BF16, SMS, OPTIN) == \
+        rn.ERR_VARIANT
+    # a plan for another element type
+    assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, 64, 4096, rn.F16, SMS, OPTIN) != rn.OK
+    rc, sp = plan(4096, 4096, rn.BF16, rn.VARIANT_STAGED)
+    bad = rn.Plan(**sp.as_dict())
+    bad.smem_bytes += 16
+    assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 4096, 4096, rn.BF16, SMS, OPTIN) != rn.OK
+    bad = rn.Plan(**sp.as_dict())
+    bad.stages += 1  # no longer a multiple of the consumer count
+    assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 4096, 4096, rn.BF16, SMS, OPTIN) != rn.OK
