@@ -76,6 +76,11 @@ def test_wide_workload_sampled(name):
 def test_headline_shape_every_variant(variant):
     wl = inputs.WORKLOADS["prefill_bf16_16384x4096"]
     x, w = inputs.make_inputs(wl)
+    if not accepts(wl.rows, wl.hidden, wl.dtype, variant):
+        with pytest.raises(rn.RmsnormError) as e:
+            run(x, w, wl.eps, wl.dtype, variant=variant)
+        assert e.value.status == rn.ERR_VARIANT
+        return
     y = run(x, w, wl.eps, wl.dtype, variant=variant)
     compare(y, x, w, wl.eps, wl.dtype)
 
