@@ -62,7 +62,8 @@ const KernelDesc *kernel_table(int *n);
 struct StagedLayout {
     int32_t row_bytes;   // hidden * element size (multiple of 16)
     int32_t slot_stride; // row_bytes rounded up to 128
-    int32_t bar_bytes;   // mbarrier area (2 per slot + 1 weight + flag), rounded to 128
+    int32_t bar_bytes;   // mbarriers (2 per slot + weight + abort flag) and the
+                         // consumer groups' reduction scratch, rounded to 128
     int32_t smem_bytes;  // total dynamic shared memory
 };
 
@@ -71,7 +72,7 @@ RMSNORM_HD inline StagedLayout staged_layout(int32_t row_bytes, int32_t stages)
     StagedLayout L;
     L.row_bytes = row_bytes;
     L.slot_stride = (row_bytes + 127) / 128 * 128;
-    L.bar_bytes = ((2 * stages + 2) * 8 + 127) / 128 * 128;
+    L.bar_bytes = ((2 * stages + 2) * 8 + 256 + 127) / 128 * 128;
     L.smem_bytes = L.bar_bytes + L.slot_stride * (stages + 1); // +1: the weight row
     return L;
 }

@@ -241,7 +241,8 @@ constexpr int kWarpBlock = 256;
 //   block-per-row, runtime block size <= MAXT: (VB, NV, MAXT, MINB, CP)
 //   block-per-row, block size fixed at TPR: (VB, TPR, NV, MINB, CP)
 // MINB caps registers so at least MINB blocks of MAXT threads fit on an SM
-// (65536 registers): MAXT x MINB = 2048 -> 32 registers per thread.
+// (65536 registers): MAXT x MINB = 2048 -> 32 registers per thread.  The
+// selector (select.cpp) names these entries by their parameters.
 #define ROWREG_SET(DT)                                                                         \
     WARP_ENTRY(DT, 16, 4, 1, 0, 0), WARP_ENTRY(DT, 16, 8, 1, 0, 0),                           \
         WARP_ENTRY(DT, 16, 8, 2, 0, 0), WARP_ENTRY(DT, 16, 16, 1, 0, 0),                      \
@@ -249,15 +250,12 @@ constexpr int kWarpBlock = 256;
         WARP_ENTRY(DT, 16, 32, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 4, 0, 0),                     \
         WARP_ENTRY(DT, 16, 32, 2, 8, 0), WARP_ENTRY(DT, 16, 32, 4, 8, 0),                     \
         WARP_ENTRY(DT, 32, 32, 1, 0, 0), WARP_ENTRY(DT, 32, 32, 2, 0, 0),                     \
-        CTA_ENTRY(DT, 16, 1, 1024, 0, 0), CTA_ENTRY(DT, 16, 1, 1024, 2, 1),                   \
-        CTA_ENTRY(DT, 16, 2, 256, 8, 0), CTA_ENTRY(DT, 16, 2, 256, 8, 1),                     \
-        CTA_ENTRY(DT, 16, 2, 1024, 2, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                    \
-        CTA_ENTRY(DT, 16, 4, 256, 6, 0), CTA_ENTRY(DT, 16, 4, 256, 6, 1),                     \
-        CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 16, 8, 512, 0, 1),                    \
-        CTA_ENTRY(DT, 32, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 2, 256, 8, 1),                    \
-        CTA_ENTRY(DT, 32, 2, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
-        CTAF_ENTRY(DT, 16, 256, 2, 8, 1), CTAF_ENTRY(DT, 16, 128, 4, 12, 1),                  \
-        CTAF_ENTRY(DT, 16, 512, 1, 0, 0)
+        CTA_ENTRY(DT, 16, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 1, 1024, 2, 1),                   \
+        CTA_ENTRY(DT, 16, 2, 1024, 2, 1), CTA_ENTRY(DT, 32, 2, 1024, 0, 1),                   \
+        CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
+        CTA_ENTRY(DT, 16, 2, 256, 8, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                     \
+        CTA_ENTRY(DT, 16, 4, 256, 6, 1), CTA_ENTRY(DT, 16, 4, 512, 2, 1),                     \
+        CTA_ENTRY(DT, 16, 8, 512, 0, 1), CTAF_ENTRY(DT, 16, 512, 1, 0, 0)
 
 } // namespace rowreg
 } // namespace rmsnorm

@@ -28,6 +28,7 @@ constexpr int kSmemPerSm = 233472;               // 228 KiB per SM on sm_100-cla
 constexpr int kSmemReservedPerBlock = 1024;
 constexpr int kStagedMaxStages = 32;
 constexpr int kStagedMaxConsumers = 16;
+constexpr int kStagedMaxNamedGroups = 15; // named barriers 1..15 (0 is __syncthreads)
 
 int elem_size(int dtype)
 {
@@ -103,109 +104,206 @@ int plan_generic(const Shape &s, rmsnorm_plan_t *p)
     return p->kernel_index >= 0 ? RMSNORM_OK : RMSNORM_ERR_VARIANT;
 }
 
-// ---- warp-per-row: TPR lanes x NV vectors of 16 (or 32) bytes per row
-int plan_warp(const Shape &s, int vb, rmsnorm_plan_t *p)
+// Exact lookup of a register-resident instantiation by its parameters.
+int find_rowreg(int variant, int dtype, int vb, int tpr, int nv, int maxt, int minb, int cache)
 {
-    clear(p);
-    if (vb == 16 ? !s.a16 : !s.a32)
-        return RMSNORM_ERR_MISALIGNED;
-    const int64_t nvec = s.row_bytes / vb;
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
-    int best = -1;
-    int64_t best_cap = INT64_MAX;
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
-        if (d.variant != RMSNORM_VARIANT_WARP_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb ||
-            d.minb != 0 || d.cache != 0)
-            continue;
-        const int64_t cap = int64_t(d.tpr) * d.nv;
-        if (cap < nvec)
-            continue;
-        // Smallest capacity that covers the row; on ties the wider group
-        // (fewer serial vectors per thread).
-        if (cap < best_cap || (cap == best_cap && d.tpr > t[best].tpr)) {
-            best = i;
-            best_cap = cap;
-        }
+        if (d.variant == variant && d.dtype == dtype && d.vec_bytes == vb && d.tpr == tpr &&
+            d.nv == nv && d.block == maxt && d.minb == minb && d.cache == cache)
+            return i;
     }
-    if (best < 0)
+    return -1;
+}
+
+// Registers per thread the compiler may use under __launch_bounds__(maxt,
+// minb): the 64 Ki register file shared by minb blocks, in steps of 8.
+int reg_cap(int maxt, int minb)
+{
+    if (minb <= 0)
+        return 128; // no cap asked for; the wide bodies use about this many
+    int r = 65536 / (maxt * minb);
+    r = r / 8 * 8;
+    return std::min(255, std::max(16, r));
+}
+
+// Resident blocks of `tpr` threads per SM for an instantiation.
+int blocks_per_sm(int tpr, int maxt, int minb)
+{
+    const int by_threads = kMaxThreadsPerSm / tpr;
+    const int by_regs = 65536 / (tpr * reg_cap(maxt, minb));
+    return std::max(1, std::min({by_threads, by_regs, 32}));
+}
+
+// ---- warp-per-row: a group of TPR lanes (<= 32) per row
+int plan_warp_exact(const Shape &s, int tpr, int nv, int minb, int64_t grid_cap,
+                    rmsnorm_plan_t *p)
+{
+    clear(p);
+    const int idx = find_rowreg(RMSNORM_VARIANT_WARP_PER_ROW, s.dtype, 16, tpr, nv, 256, minb, 0);
+    if (idx < 0)
         return RMSNORM_ERR_VARIANT;
-    const KernelDesc &d = t[best];
     p->variant = RMSNORM_VARIANT_WARP_PER_ROW;
-    p->vec_bytes = vb;
-    p->threads_per_row = d.tpr;
-    p->vecs_per_thread = d.nv;
-    p->block_threads = d.block;
-    p->rows_per_block = d.block / d.tpr;
+    p->vec_bytes = 16;
+    p->threads_per_row = tpr;
+    p->vecs_per_thread = nv;
+    p->block_threads = 256;
+    p->rows_per_block = 256 / tpr;
     const int64_t blocks = (s.rows + p->rows_per_block - 1) / p->rows_per_block;
-    p->grid = grid_for(blocks, INT_MAX);
-    p->smem_bytes = 0;
-    p->kernel_index = best;
+    p->grid = grid_for(blocks, grid_cap);
+    p->kernel_index = idx;
     return RMSNORM_OK;
 }
 
-// ---- block-per-row: blockDim = tpr threads x NV vectors per thread
-int plan_cta(const Shape &s, int vb, bool persistent, rmsnorm_plan_t *p)
-{
-    clear(p);
-    if (vb == 16 ? !s.a16 : !s.a32)
-        return RMSNORM_ERR_MISALIGNED;
-    const int64_t nvec = s.row_bytes / vb;
-    int n = 0;
-    const KernelDesc *t = kernel_table(&n);
-    int best = -1, best_tpr = 0;
-    double best_score = 1e30;
-    for (int i = 0; i < n; ++i) {
-        const KernelDesc &d = t[i];
-        if (d.variant != RMSNORM_VARIANT_CTA_PER_ROW || d.dtype != s.dtype || d.vec_bytes != vb ||
-            d.minb != 0 || d.cache != 0 || d.tpr != 0)
-            continue;
-        const int64_t need = (nvec + d.nv - 1) / d.nv;
-        const int64_t tpr = std::max<int64_t>(32, (need + 31) / 32 * 32);
-        if (tpr > d.block)
-            continue;
-        const double waste = double(tpr * d.nv - nvec) / double(tpr * d.nv);
-        double score;
-        if (persistent) {
-            // Decode: fewest serial vectors per thread (latency), then waste.
-            score = d.nv + waste;
-        } else {
-            // Prefill: little waste, and a block of 128..512 threads.
-            const double dev = tpr < 128 ? (128.0 / tpr) : (tpr > 512 ? tpr / 512.0 : 1.0);
-            score = waste * 4.0 + dev;
-        }
-        if (score < best_score) {
-            best_score = score;
-            best = i;
-            best_tpr = static_cast<int>(tpr);
-        }
-    }
-    if (best < 0)
-        return RMSNORM_ERR_VARIANT;
-    const KernelDesc &d = t[best];
-    p->variant = persistent ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW;
-    p->vec_bytes = vb;
-    p->threads_per_row = best_tpr;
-    p->vecs_per_thread = d.nv;
-    p->block_threads = best_tpr;
-    p->rows_per_block = 1;
-    if (persistent)
-        p->grid = grid_for(s.rows, int64_t(s.sm_count) * std::max(1, kMaxThreadsPerSm / best_tpr));
-    else
-        p->grid = grid_for(s.rows, INT_MAX);
-    p->smem_bytes = 0;
-    p->kernel_index = best;
-    return RMSNORM_OK;
-}
-
-// ---- staged: persistent blocks, rows streamed into shared-memory slots
-int plan_staged(const Shape &s, int blocks_per_sm, int consumers_wanted, rmsnorm_plan_t *p)
+// Forced warp-per-row: the narrowest group whose registers cover the row.
+int plan_warp(const Shape &s, rmsnorm_plan_t *p)
 {
     clear(p);
     if (!s.a16)
         return RMSNORM_ERR_MISALIGNED;
-    if (s.row_bytes > INT_MAX / 4)
+    const int64_t nvec = s.row_bytes / 16;
+    static const int kOptions[][3] = {{4, 1, 0},  {8, 1, 0},  {8, 2, 0},  {16, 1, 0},
+                                      {16, 2, 0}, {32, 1, 0}, {32, 2, 8}, {32, 4, 8}};
+    for (const auto &o : kOptions)
+        if (int64_t(o[0]) * o[1] >= nvec)
+            return plan_warp_exact(s, o[0], o[1], o[2], INT_MAX, p);
+    return RMSNORM_ERR_VARIANT;
+}
+
+// ---- block-per-row with a given instantiation and block size
+int plan_cta_exact(const Shape &s, int vb, int nv, int maxt, int minb, int cache, int tpr_fixed,
+                   int tpr, int64_t grid_cap, int variant, rmsnorm_plan_t *p)
+{
+    clear(p);
+    const int idx = find_rowreg(RMSNORM_VARIANT_CTA_PER_ROW, s.dtype, vb, tpr_fixed, nv, maxt,
+                                minb, cache);
+    if (idx < 0 || tpr > maxt || tpr < 32)
+        return RMSNORM_ERR_VARIANT;
+    p->variant = variant;
+    p->vec_bytes = vb;
+    p->threads_per_row = tpr;
+    p->vecs_per_thread = nv;
+    p->block_threads = tpr;
+    p->rows_per_block = 1;
+    p->grid = grid_for(s.rows, grid_cap);
+    p->kernel_index = idx;
+    return RMSNORM_OK;
+}
+
+int tpr_for(int64_t nvec, int nv)
+{
+    const int64_t need = (nvec + nv - 1) / nv;
+    return static_cast<int>(std::max<int64_t>(32, (need + 31) / 32 * 32));
+}
+
+// Decode (no more rows than SMs): one block per row on its own SM, as few
+// vectors per thread as the block allows (latency: one round trip).
+// 32-byte vectors once a row is 640 16-byte vectors or more.
+int plan_decode(const Shape &s, int variant, rmsnorm_plan_t *p)
+{
+    const int64_t nvec16 = s.row_bytes / 16;
+    const bool vb32 = s.a32 && nvec16 >= 640;
+    const int vb = vb32 ? 32 : 16;
+    const int64_t nvec = s.row_bytes / vb;
+    struct Opt { int nv, maxt, minb; };
+    static const Opt k16[] = {{1, 1024, 2}, {2, 1024, 2}, {4, 1024, 0}, {8, 512, 0}};
+    static const Opt k32[] = {{1, 1024, 2}, {2, 1024, 0}, {4, 512, 0}};
+    const Opt *opts = vb32 ? k32 : k16;
+    const int nopt = vb32 ? 3 : 4;
+    for (int i = 0; i < nopt; ++i) {
+        const int tpr = tpr_for(nvec, opts[i].nv);
+        if (tpr > opts[i].maxt)
+            continue;
+        if (!vb32 && opts[i].nv == 1 && tpr == 512)
+            return plan_cta_exact(s, 16, 1, 512, 0, 0, 512, 512, INT_MAX, variant, p);
+        const int64_t cap = int64_t(s.sm_count) * blocks_per_sm(tpr, opts[i].maxt, opts[i].minb);
+        return plan_cta_exact(s, vb, opts[i].nv, opts[i].maxt, opts[i].minb, 1, 0, tpr, cap,
+                              variant, p);
+    }
+    return RMSNORM_ERR_VARIANT;
+}
+
+// Prefill, rows of 97..1024 16-byte vectors: lean blocks of <= 256 threads
+// with 2, 3 or 4 vectors each (least idle lanes, then fewest vectors), the
+// register cap keeping 6-8 blocks (rows) resident per SM.
+int plan_prefill_mid(const Shape &s, int variant, bool persistent, rmsnorm_plan_t *p)
+{
+    const int64_t nvec = s.row_bytes / 16;
+    struct Opt { int nv, maxt, minb; };
+    static const Opt opts[] = {{2, 256, 8}, {3, 512, 3}, {4, 256, 6}};
+    int best = -1, best_tpr = 0;
+    int64_t best_waste = INT64_MAX;
+    for (int i = 0; i < 3; ++i) {
+        const int tpr = tpr_for(nvec, opts[i].nv);
+        if (tpr > 256)
+            continue;
+        const int64_t waste = int64_t(tpr) * opts[i].nv - nvec;
+        if (waste < best_waste) {
+            best_waste = waste;
+            best = i;
+            best_tpr = tpr;
+        }
+    }
+    if (best < 0)
+        return RMSNORM_ERR_VARIANT;
+    const Opt &o = opts[best];
+    const int64_t cap =
+        persistent ? int64_t(s.sm_count) * blocks_per_sm(best_tpr, o.maxt, o.minb) : INT_MAX;
+    return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap, variant, p);
+}
+
+// Prefill, rows of more than 1024 16-byte vectors: the fewest vectors per
+// thread that keep the block at <= 640 threads, on a persistent grid sized
+// to the blocks that fit on an SM.
+int plan_prefill_wide(const Shape &s, int variant, bool persistent, rmsnorm_plan_t *p)
+{
+    const int64_t nvec = s.row_bytes / 16;
+    struct Opt { int nv, maxt, minb; };
+    static const Opt opts[] = {{2, 1024, 2}, {3, 512, 3}, {4, 512, 2}, {8, 512, 0}};
+    for (const Opt &o : opts) {
+        const int tpr = tpr_for(nvec, o.nv);
+        if (tpr > std::min(640, o.maxt))
+            continue;
+        const int64_t cap =
+            persistent ? int64_t(s.sm_count) * blocks_per_sm(tpr, o.maxt, o.minb) : INT_MAX;
+        return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, tpr, cap, variant, p);
+    }
+    // Larger rows: the widest register body at its largest block.
+    const int tpr = tpr_for(nvec, 8);
+    if (tpr <= 512)
+        return plan_cta_exact(s, 16, 8, 512, 0, 1, 0, tpr,
+                              persistent ? int64_t(s.sm_count) : INT_MAX, variant, p);
+    return RMSNORM_ERR_VARIANT;
+}
+
+// Forced block-per-row / persistent.
+int plan_cta(const Shape &s, bool persistent, rmsnorm_plan_t *p)
+{
+    clear(p);
+    if (!s.a16)
+        return RMSNORM_ERR_MISALIGNED;
+    const int variant = persistent ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW;
+    const int64_t nvec = s.row_bytes / 16;
+    if (persistent && s.rows <= s.sm_count)
+        return plan_decode(s, variant, p);
+    if (nvec <= 1024 && plan_prefill_mid(s, variant, persistent, p) == RMSNORM_OK)
+        return RMSNORM_OK;
+    if (nvec > 1024)
+        return plan_prefill_wide(s, variant, persistent, p);
+    return plan_decode(s, variant, p); // short rows: one block of >= 32 threads per row
+}
+
+// ---- staged: persistent blocks, rows streamed into shared-memory slots.
+// `wpr` warps consume each row; `groups` rows are consumed at once per block.
+int plan_staged(const Shape &s, int blocks_per_sm, int groups_wanted, int wpr, bool tma_store,
+                rmsnorm_plan_t *p)
+{
+    clear(p);
+    if (!s.a16)
+        return RMSNORM_ERR_MISALIGNED;
+    if (s.row_bytes > INT_MAX / 4 || wpr < 1 || wpr > kStagedMaxConsumers)
         return RMSNORM_ERR_VARIANT;
     const int row_bytes = static_cast<int>(s.row_bytes);
     const int budget = std::min(s.smem_optin, kSmemPerSm / blocks_per_sm - kSmemReservedPerBlock);
@@ -217,21 +315,32 @@ int plan_staged(const Shape &s, int blocks_per_sm, int consumers_wanted, rmsnorm
             break;
         }
     }
-    if (stages < 2)
+    int groups = std::min({groups_wanted, kStagedMaxConsumers / wpr, tma_store ? stages / 2 : stages});
+    if (wpr > 1)
+        groups = std::min(groups, kStagedMaxNamedGroups);
+    if (groups < 1 || stages < 2)
         return RMSNORM_ERR_VARIANT;
-    int consumers = std::min({consumers_wanted, kStagedMaxConsumers, stages});
-    stages = stages / consumers * consumers;
+    stages = stages / groups * groups;
     p->variant = RMSNORM_VARIANT_STAGED;
     p->vec_bytes = 16;
-    p->threads_per_row = 32;
+    p->threads_per_row = 32 * wpr;
     p->vecs_per_thread = 0;
-    p->block_threads = 32 * (consumers + 1);
-    p->rows_per_block = consumers;
+    p->block_threads = 32 * (groups * wpr + 1);
+    p->rows_per_block = groups;
     p->stages = stages;
     p->grid = grid_for(s.rows, int64_t(s.sm_count) * blocks_per_sm);
     p->smem_bytes = staged_layout(row_bytes, stages).smem_bytes;
-    p->kernel_index = find_kernel(RMSNORM_VARIANT_STAGED, s.dtype, 16, 32, 0);
+    p->kernel_index = find_kernel(RMSNORM_VARIANT_STAGED, s.dtype, 16, 32, 0, tma_store ? 3 : 0);
     return p->kernel_index >= 0 ? RMSNORM_OK : RMSNORM_ERR_VARIANT;
+}
+
+// Forced staged: one warp per row up to 8 KiB rows, wider groups beyond.
+int plan_staged_auto(const Shape &s, rmsnorm_plan_t *p)
+{
+    int wpr = 1;
+    while (wpr < 8 && int64_t(wpr) * 8192 < s.row_bytes)
+        wpr *= 2;
+    return plan_staged(s, 1, std::max(1, 8 / wpr), wpr, false, p);
 }
 
 int check_common(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
@@ -268,13 +377,13 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return rc;
     switch (variant) {
     case RMSNORM_VARIANT_WARP_PER_ROW:
-        return plan_warp(s, 16, out);
+        return plan_warp(s, out);
     case RMSNORM_VARIANT_CTA_PER_ROW:
-        return plan_cta(s, 16, false, out);
+        return plan_cta(s, false, out);
     case RMSNORM_VARIANT_PERSISTENT:
-        return plan_cta(s, 16, true, out);
+        return plan_cta(s, true, out);
     case RMSNORM_VARIANT_STAGED:
-        return plan_staged(s, 1, 8, out);
+        return plan_staged_auto(s, out);
     case RMSNORM_VARIANT_GENERIC:
         return plan_generic(s, out);
     case RMSNORM_VARIANT_AUTO:
@@ -283,20 +392,43 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return RMSNORM_ERR_INVALID_ARG;
     }
 
-    // ---- automatic choice
+    // ---- automatic choice (rules fitted to a sweep of every plan over row
+    // sizes 128 B .. 64 KiB and 1 .. 2M rows on GB300; they depend on the
+    // row's byte length, not on the element type)
     if (!s.a16)
         return plan_generic(s, out);
     const int64_t nvec = s.row_bytes / 16;
-    // Decode: no more rows than SMs -> one block per row, one SM each.
-    if (s.rows <= s.sm_count && nvec > 32 && plan_cta(s, 16, true, out) == RMSNORM_OK)
+    if (s.rows <= s.sm_count) {
+        // Decode: rows of <= 32 vectors share a warp; longer rows get a block.
+        if (nvec <= 32) {
+            int tpr = 4;
+            while (tpr < nvec)
+                tpr *= 2;
+            return plan_warp_exact(s, tpr, 1, 0, INT_MAX, out);
+        }
+        if (plan_decode(s, RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
+            return RMSNORM_OK;
+        // Rows too long for one block's registers: as for prefill below.
+    }
+    // Prefill.  Short rows: lane groups of one warp, several rows per warp.
+    if (nvec > 1024)
+        goto wide;
+    if (nvec <= 8)
+        return plan_warp_exact(s, 8, 1, 0, int64_t(s.sm_count) * 16, out);
+    if (nvec <= 16)
+        return plan_warp_exact(s, 8, 2, 0, INT_MAX, out);
+    if (nvec <= 32)
+        return plan_warp_exact(s, 16, 2, 0, INT_MAX, out);
+    if (nvec <= 64)
+        return plan_warp_exact(s, 32, 2, 8, INT_MAX, out);
+    if (nvec <= 96)
+        return plan_warp_exact(s, 32, 4, 8, INT_MAX, out);
+    if (plan_prefill_mid(s, RMSNORM_VARIANT_CTA_PER_ROW, false, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    // Rows of at most 128 vectors (1024 x bf16, 512 x f32): a warp (or part
-    // of one) per row, everything in registers.
-    if (nvec <= 128 && plan_warp(s, 16, out) == RMSNORM_OK)
+wide:
+    if (plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    if (plan_cta(s, 16, false, out) == RMSNORM_OK)
-        return RMSNORM_OK;
-    if (plan_staged(s, 1, 8, out) == RMSNORM_OK)
+    if (plan_staged_auto(s, out) == RMSNORM_OK)
         return RMSNORM_OK;
     return plan_generic(s, out);
 }
@@ -339,11 +471,17 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
         break;
     case RMSNORM_VARIANT_STAGED: {
         const int consumers = p.block_threads / 32 - 1;
-        if (consumers < 1 || consumers > kStagedMaxConsumers || p.stages < 1 ||
-            p.stages > kStagedMaxStages || p.stages % consumers != 0 || s.row_bytes > INT_MAX / 4)
+        const int wpr = p.threads_per_row / 32;
+        if (consumers < 1 || consumers > kStagedMaxConsumers || wpr < 1 ||
+            p.threads_per_row % 32 != 0 || consumers % wpr != 0 || s.row_bytes > INT_MAX / 4)
             return RMSNORM_ERR_VARIANT;
-        // Bulk-store mode releases a slot one row later: each consumer needs two.
-        if (d.cache == 3 && p.stages < 2 * consumers)
+        const int groups = consumers / wpr;
+        if (wpr > 1 && groups > kStagedMaxNamedGroups)
+            return RMSNORM_ERR_VARIANT;
+        if (p.stages < 1 || p.stages > kStagedMaxStages || p.stages % groups != 0)
+            return RMSNORM_ERR_VARIANT;
+        // Bulk-store mode releases a slot one row later: each group needs two.
+        if (d.cache == 3 && p.stages < 2 * groups)
             return RMSNORM_ERR_VARIANT;
         const int need = staged_layout(static_cast<int>(s.row_bytes), p.stages).smem_bytes;
         if (p.smem_bytes != need || need > smem_optin || p.grid > rows)

@@ -13,9 +13,11 @@
 // per block; the row statistic stays in registers ("Build a GPU compiler
 // from scratch ... (Emmy)", sections "Tensor IR" and "Loop IR").
 //
-// Slot s holds rows k = s, s + stages, ...; consumer c takes k = c, c + C,
-// ...; `stages` is a multiple of C so each slot always has the same consumer
-// and mbarrier parity waits are never ambiguous.
+// Slot s holds rows k = s, s + stages, ...; group g of G takes k = g, g + G,
+// ...; `stages` is a multiple of G so each slot always has the same group and
+// mbarrier parity waits are never ambiguous.  The warps of a group agree on
+// every wait's outcome at their named barrier before anyone writes, so a
+// wait that runs out in one warp stops the whole group together.
 //
 // Every spin-wait is bounded by `limit_ns` of %globaltimer.  A wait that runs
 // out records RMSNORM_ERR_DEVICE_TIMEOUT in the status word, raises the
@@ -90,6 +92,12 @@ __device__ inline void bulk_wait_all()
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
+// Named barrier `id` over `threads` threads (whole warps).
+__device__ inline void group_sync(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 __device__ inline uint64_t globaltimer()
 {
     uint64_t t;
@@ -152,8 +160,8 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
 template <int DT, bool TMA_STORE>
 __global__ void __launch_bounds__(32 * 17)
 staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                   int32_t hidden, float eps, int32_t stages, int *status, uint64_t limit_ns,
-                   uint32_t flags)
+                   int32_t hidden, float eps, int32_t stages, int32_t wpr, int *status,
+                   uint64_t limit_ns, uint32_t flags)
 {
     using E = Elem<DT>;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -163,19 +171,22 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     // full[s] = bars[s], empty[s] = bars[stages + s], weight = bars[2 * stages]
     volatile int *abort_flag = reinterpret_cast<volatile int *>(bars + 2 * stages + 1);
+    float *red = reinterpret_cast<float *>(bars + 2 * stages + 2);  // [2][16] partial sums
+    int *agree = reinterpret_cast<int *>(red + 32);                  // [2][16] wait outcomes
     unsigned char *wsm = smem + L.bar_bytes;
     unsigned char *slots = wsm + L.slot_stride;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int consumers = (blockDim.x >> 5) - 1;
+    const int groups = consumers / wpr;
     const int64_t my_rows =
         rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&bars[s]), 1);
-            mbar_init(smem_u32(&bars[stages + s]), 1);
+            mbar_init(smem_u32(&bars[stages + s]), TMA_STORE ? 1 : wpr);
         }
         mbar_init(smem_u32(&bars[2 * stages]), 1);
         *abort_flag = 0;
@@ -230,43 +241,55 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
         return;
     }
 
-    // ---------------- consumers
+    // ---------------- consumers: warp c = wi-th warp of group g
     const int c = warp - 1;
-    if (!wait_warp(wbar, 0, limit_ns, abort_flag, lane)) {
-        if (lane == 0) {
-            if (!*abort_flag)
-                record_timeout(status);
-            *abort_flag = 1;
-        }
-        return;
-    }
+    const int g = c / wpr;
+    const int wi = c % wpr;
+    const int gsize = 32 * wpr;
+    const int gl = wi * 32 + lane; // thread index within the group
+    const bool issuer = wi == 0 && lane == 0;
     const int nvec = row_bytes / 16;
     const float n = static_cast<float>(hidden);
     char *yb = static_cast<char *>(y);
-    int prev_slot = -1; // TMA_STORE: slot whose bulk store may still be reading
+    int prev_slot = -1; // TMA_STORE: slot whose bulk store may still be reading it
 
-    for (int64_t k = c; k < my_rows; k += consumers) {
+    const bool have_weight = wait_warp(wbar, 0, limit_ns, abort_flag, lane);
+    int it = 0;
+    for (int64_t k = g; k < my_rows; k += groups, ++it) {
         const int s = static_cast<int>(k % stages);
         const uint32_t par = static_cast<uint32_t>((k / stages) & 1);
-        if (!wait_warp(smem_u32(&bars[s]), par, limit_ns, abort_flag, lane)) {
+        bool ok = have_weight && wait_warp(smem_u32(&bars[s]), par, limit_ns, abort_flag, lane);
+        const unsigned char *src = slots + static_cast<int64_t>(s) * L.slot_stride;
+
+        float acc = 0.f;
+        if (ok) {
+#pragma unroll 4
+            for (int v = gl; v < nvec; v += gsize) {
+                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                acc = sumsq<DT, 16>(xv, acc);
+            }
+        }
+        acc = group_allreduce<32>(acc);
+        if (wpr > 1) {
+            if (lane == 0) {
+                red[(it & 1) * 16 + c] = acc;
+                agree[(it & 1) * 16 + c] = ok ? 1 : 0;
+            }
+            group_sync(1 + g, gsize);
+            const int base = (it & 1) * 16 + g * wpr;
+            acc = lane < wpr ? red[base + lane] : 0.f;
+            const int bad = lane < wpr ? (agree[base + lane] == 0) : 0;
+            acc = group_allreduce<32>(acc);
+            ok = !__any_sync(0xFFFFFFFFu, bad);
+        }
+        if (!ok) { // the whole group leaves together, before writing anything
             if (lane == 0) {
                 if (!*abort_flag)
                     record_timeout(status);
                 *abort_flag = 1;
-                if (TMA_STORE)
-                    bulk_wait_all(); // own stores still read the slots
             }
-            return;
+            break;
         }
-        const unsigned char *src = slots + static_cast<int64_t>(s) * L.slot_stride;
-
-        float acc = 0.f;
-#pragma unroll 4
-        for (int v = lane; v < nvec; v += 32) {
-            const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
-            acc = sumsq<DT, 16>(xv, acc);
-        }
-        acc = group_allreduce<32>(acc);
         const float r = row_factor(acc, n, eps);
 
         const int64_t row = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
@@ -274,7 +297,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
         if (TMA_STORE) {
             unsigned char *dst = slots + static_cast<int64_t>(s) * L.slot_stride;
 #pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) {
+            for (int v = gl; v < nvec; v += gsize) {
                 const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
                 Vec<16> o;
@@ -283,10 +306,13 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
             }
             // The slot's new contents must be visible to the bulk copy (async proxy).
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (lane == 0) {
+            if (wpr > 1)
+                group_sync(1 + g, gsize);
+            else
+                __syncwarp();
+            if (issuer) {
                 bulk_copy_s2g(yr, smem_u32(dst), static_cast<uint32_t>(row_bytes));
-                // The previous row's copy has finished reading its slot: release it.
+                // The group's previous copy has finished reading its slot: release it.
                 bulk_wait_read<1>();
                 if (prev_slot >= 0)
                     mbar_arrive(smem_u32(&bars[stages + prev_slot]));
@@ -294,20 +320,20 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
             prev_slot = s;
         } else {
 #pragma unroll 4
-            for (int v = lane; v < nvec; v += 32) {
+            for (int v = gl; v < nvec; v += gsize) {
                 const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
                 Vec<16> o;
                 scale<DT, 16>(o, xv, wv, r);
-                st_stream<0>(yr + static_cast<int64_t>(v) * 16, o);
+                st_stream<1>(yr + static_cast<int64_t>(v) * 16, o);
             }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(smem_u32(&bars[stages + s]));
         }
     }
-    if (TMA_STORE && lane == 0) {
-        bulk_wait_all(); // every y row written before the block exits
+    if (TMA_STORE && issuer) {
+        bulk_wait_all(); // every y row of this group written before the block exits
         if (prev_slot >= 0)
             mbar_arrive(smem_u32(&bars[stages + prev_slot]));
     }
@@ -317,7 +343,8 @@ template <int DT, bool TS>
 cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
     staged_rows_kernel<DT, TS><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
-        a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, a.status, a.wait_limit_ns, a.flags);
+        a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32, a.status,
+        a.wait_limit_ns, a.flags);
     return cudaGetLastError();
 }
 

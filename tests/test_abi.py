@@ -111,7 +111,8 @@ def plan(rows, hidden, dtype, variant=rn.VARIANT_AUTO, xoff=0, sms=SMS):
 def test_selector_on_the_workloads():
     expect = {
         "f32_64x128": rn.VARIANT_WARP_PER_ROW,
-        "embed_bf16_8192x1024": rn.VARIANT_WARP_PER_ROW,
+        "embed_bf16_8192x1024": rn.VARIANT_CTA_PER_ROW,
+        "prefill_bf16_16384x4096": rn.VARIANT_CTA_PER_ROW,
         "decode_bf16_1x4096": rn.VARIANT_PERSISTENT,
         "decode_bf16_8x4096": rn.VARIANT_PERSISTENT,
         "decode_bf16_32x4096": rn.VARIANT_PERSISTENT,
@@ -181,9 +182,30 @@ def test_staged_plan_fits_and_is_consistent():
                 continue
             assert rc == rn.OK, (hidden, dt)
             consumers = p.block_threads // 32 - 1
-            assert p.stages % consumers == 0 and p.stages >= 2
+            wpr = p.threads_per_row // 32
+            assert consumers % wpr == 0
+            assert p.stages % (consumers // wpr) == 0 and p.stages >= 2
             assert p.smem_bytes <= OPTIN
             assert p.grid <= SMS
+
+
+def test_prefill_rules():
+    """The automatic plan for prefill shapes: lane groups for short rows,
+    lean blocks of <= 256 threads with 2-4 vectors each up to 16 KiB rows,
+    a persistent grid beyond."""
+    for hidden, variant in ((64, rn.VARIANT_WARP_PER_ROW), (512, rn.VARIANT_WARP_PER_ROW),
+                            (768, rn.VARIANT_WARP_PER_ROW), (1024, rn.VARIANT_CTA_PER_ROW),
+                            (4096, rn.VARIANT_CTA_PER_ROW), (8192, rn.VARIANT_CTA_PER_ROW),
+                            (16384, rn.VARIANT_PERSISTENT)):
+        rc, p = plan(100000, hidden, rn.BF16)
+        assert rc == rn.OK and p.variant == variant, (hidden, p.as_dict())
+        if variant == rn.VARIANT_CTA_PER_ROW:
+            assert p.block_threads <= 256 and 2 <= p.vecs_per_thread <= 4
+    rc, p = plan(16384, 4096, rn.BF16)
+    assert (p.block_threads, p.vecs_per_thread, p.grid) == (256, 2, 16384)
+    # the same row bytes give the same shape for f32
+    rc2, p2 = plan(16384, 2048, rn.F32)
+    assert (p2.block_threads, p2.vecs_per_thread, p2.vec_bytes) == (256, 2, 16)
 
 
 def test_huge_row_still_planned():

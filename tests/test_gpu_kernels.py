@@ -28,7 +28,7 @@ def ctx():
 
 def layout_bytes(row_bytes, stages):
     slot = (row_bytes + 127) // 128 * 128
-    bar = ((2 * stages + 2) * 8 + 127) // 128 * 128
+    bar = ((2 * stages + 2) * 8 + 256 + 127) // 128 * 128
     return bar + slot * (stages + 1)
 
 
@@ -62,18 +62,20 @@ def plans_for(k, rows, sms, optin):
                                                  rows_per_block=1, stages=0, grid=grid,
                                                  smem_bytes=0, kernel_index=k["index"])))
     elif v == rn.VARIANT_STAGED:
-        for hidden in (8 * 16 // es * 3, 4096 if es == 2 else 2048, 7168 if es == 2 else 3584):
+        for hidden in (8 * 16 // es * 3, 4096 if es == 2 else 2048, 7168 if es == 2 else 3584,
+                       20000 if es == 2 else 10000):
             rb = hidden * es
-            for c in (1, 2, 4):
-                stages = 2 * c if k["cache_policy"] == 3 else c
+            for wpr, groups in ((1, 1), (1, 2), (1, 4), (2, 2), (4, 1), (4, 3), (8, 2)):
+                stages = 2 * groups if k["cache_policy"] == 3 else groups
                 for st in (stages, 2 * stages):
                     smem = layout_bytes(rb, st)
                     if smem > optin:
                         continue
                     for grid in sorted({min(rows, sms), max(1, rows // 5)}):
-                        out.append((hidden, dict(variant=v, vec_bytes=16, threads_per_row=32,
-                                                 vecs_per_thread=0, block_threads=32 * (c + 1),
-                                                 rows_per_block=c, stages=st, grid=grid,
+                        out.append((hidden, dict(variant=v, vec_bytes=16,
+                                                 threads_per_row=32 * wpr, vecs_per_thread=0,
+                                                 block_threads=32 * (groups * wpr + 1),
+                                                 rows_per_block=groups, stages=st, grid=grid,
                                                  smem_bytes=smem, kernel_index=k["index"])))
     elif v == rn.VARIANT_GENERIC:
         for hidden in (1, 33, 1000, 4097):
