@@ -66,7 +66,8 @@ typedef enum {
     RMSNORM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device status word) */
     RMSNORM_ERR_MISALIGNED = 7,         /* a forced vector variant got pointers it cannot load */
     RMSNORM_ERR_UNSUPPORTED_DEVICE = 8, /* current device is not compute capability 10.x */
-    RMSNORM_ERR_VARIANT = 9             /* forced variant cannot take this shape */
+    RMSNORM_ERR_VARIANT = 9,            /* forced variant cannot take this shape */
+    RMSNORM_ERR_TOO_LARGE = 10          /* beyond the static scratch of rmsnorm_fwd_staged_noalloc */
 } rmsnorm_status_t;
 
 /* Kernel variants.  AUTO lets the selector choose from (rows, hidden, dtype,
@@ -202,6 +203,40 @@ int rmsnorm_set_wait_limit_ns(uint64_t limit_ns);
  * without touching y.  No fault, trap or hang is involved. */
 int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int64_t rows,
                                 int64_t hidden, int dtype, uint64_t limit_ns, void *stream);
+
+/* rmsnorm_fwd for callers that cannot allocate device memory.
+ *
+ * Some callers may not call cudaMalloc or anything that allocates: code
+ * running inside a caller-managed memory pool or arena that must stay the
+ * only owner of device memory, code that runs under a fixed memory budget
+ * where an allocation mid-stream is not allowed, or a library embedded in a
+ * host process whose allocator policy forbids it.  rmsnorm_create allocates
+ * a device status word, so those callers cannot use rmsnorm_fwd.  This entry
+ * point needs no rmsnorm_create and allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine): it runs the shared-memory-staged
+ * kernel (RMSNORM_VARIANT_STAGED; same arithmetic as rmsnorm_fwd) and keeps
+ * that kernel's status words in a static device array of 1024 ints (4 KiB,
+ * one word per block of the launch), which every device that loads the
+ * library holds until the process exits.  (The method's pages have no
+ * counterpart of this entry point; it is a property of this library.)
+ *
+ * Arguments, layout, aliasing and asynchrony are those of rmsnorm_fwd; the
+ * caller owns x, weight and y.  The first call on a device does a one-time
+ * set-up with that device current (it looks up the static array's device
+ * address and the device's limits); make that first call before any stream
+ * capture.  Returns RMSNORM_OK, an argument error as rmsnorm_fwd does,
+ * RMSNORM_ERR_UNSUPPORTED_DEVICE, RMSNORM_ERR_CUDA, or RMSNORM_ERR_TOO_LARGE
+ * when the row does not fit the staged kernel's shared memory or the launch
+ * would need more than 1024 blocks.
+ *
+ * Every call shares the static array and it keeps the last call's contents;
+ * each block clears its own word when it starts.  Calls that overlap on the
+ * GPU (different streams, no ordering between them) race on the array.  A
+ * bounded wait that runs out inside the kernel is not reported through
+ * rmsnorm_get_device_status: the block's word records it and the rows that
+ * block could not compute are written as NaN. */
+int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, void *y, int64_t rows,
+                               int64_t hidden, float eps, int dtype, void *stream);
 
 /* Static text for a status code. */
 const char *rmsnorm_status_string(int status);

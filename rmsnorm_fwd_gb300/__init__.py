@@ -33,6 +33,7 @@ ERR_DEVICE_TIMEOUT = 6
 ERR_MISALIGNED = 7
 ERR_UNSUPPORTED_DEVICE = 8
 ERR_VARIANT = 9
+ERR_TOO_LARGE = 10
 
 # variants (rmsnorm_variant_t)
 VARIANT_AUTO = 0
@@ -107,6 +108,7 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_get_device_status": ([ctypes.POINTER(ctypes.c_int)], i32),
             "rmsnorm_set_wait_limit_ns": ([u64], i32),
             "rmsnorm_test_staged_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
+            "rmsnorm_fwd_staged_noalloc": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
             "rmsnorm_status_string": ([i32], ctypes.c_char_p),
             "rmsnorm_version": ([], i32),
         }
@@ -214,6 +216,14 @@ def rmsnorm_test_staged_timeout(x: int, weight: int, y: int, rows: int, hidden: 
                                 limit_ns: int, stream: int | None) -> None:
     _check(_load().rmsnorm_test_staged_timeout(x, weight, y, rows, hidden, dtype, limit_ns,
                                                stream or None), "rmsnorm_test_staged_timeout")
+
+
+def rmsnorm_fwd_staged_noalloc(x: int, weight: int, y: int, rows: int, hidden: int, eps: float,
+                               dtype: int, stream: int | None) -> None:
+    """The allocation-free entry point (no context, no device allocation):
+    device pointers as integers, stream as a cudaStream_t integer."""
+    _check(_load().rmsnorm_fwd_staged_noalloc(x, weight, y, rows, hidden, eps, dtype,
+                                              stream or None), "rmsnorm_fwd_staged_noalloc")
 
 
 def rmsnorm_status_string(status: int) -> str:

@@ -161,6 +161,13 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
 }
 
 } // namespace
+
+int check_call_args(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
+                    float eps, int dtype)
+{
+    return check_args(x, w, const_cast<void *>(y), rows, hidden, eps, dtype);
+}
+
 } // namespace rmsnorm
 
 using namespace rmsnorm;
@@ -363,6 +370,8 @@ const char *rmsnorm_status_string(int status)
         return "device is not compute capability 10.3 (sm_103a)";
     case RMSNORM_ERR_VARIANT:
         return "the forced variant or plan cannot take this shape";
+    case RMSNORM_ERR_TOO_LARGE:
+        return "beyond the static scratch of the allocation-free entry point";
     default:
         return "unknown status";
     }

@@ -81,6 +81,10 @@ RMSNORM_HD inline StagedLayout staged_layout(int32_t row_bytes, int32_t stages)
 int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
                 int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out);
 
+// Argument checks shared by every launching entry point (api.cpp).
+int check_call_args(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
+                    float eps, int dtype);
+
 // Checks a caller-supplied plan against the shape and the kernel table.
 int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const void *y,
                   int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin);

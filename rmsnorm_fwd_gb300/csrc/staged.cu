@@ -24,6 +24,8 @@
 // block's abort flag, and the producer then waits (again bounded) for every
 // copy it issued before the block exits, so no copy lands in shared memory
 // that has been handed to another block.  Nothing here traps.
+#include <mutex>
+
 #include "internal.h"
 #include "device_common.cuh"
 
@@ -157,7 +159,12 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
 // the row to global memory with a bulk copy; the slot is handed back to the
 // producer once that copy has finished reading it.  Otherwise y is stored
 // from registers with 16-byte vector stores.
-template <int DT, bool TMA_STORE>
+//
+// BLOCK_STATUS: `status` points at one word per block instead of one word
+// per call; each block zeroes its own word when it starts, and a group whose
+// wait ran out writes its remaining rows of y as NaN so the failure is
+// visible in the output.
+template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false>
 __global__ void __launch_bounds__(32 * 17)
 staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                    int32_t hidden, float eps, int32_t stages, int32_t wpr, int *status,
@@ -183,6 +190,11 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
     const int64_t my_rows =
         rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
+    if (BLOCK_STATUS) {
+        status += blockIdx.x;
+        if (threadIdx.x == 0)
+            *status = 0;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) {
             mbar_init(smem_u32(&bars[s]), 1);
@@ -255,6 +267,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
 
     const bool have_weight = wait_warp(wbar, 0, limit_ns, abort_flag, lane);
     int it = 0;
+    int64_t failed_at = -1; // BLOCK_STATUS: first of this group's rows left uncomputed
     for (int64_t k = g; k < my_rows; k += groups, ++it) {
         const int s = static_cast<int>(k % stages);
         const uint32_t par = static_cast<uint32_t>((k / stages) & 1);
@@ -288,6 +301,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                     record_timeout(status);
                 *abort_flag = 1;
             }
+            failed_at = k;
             break;
         }
         const float r = row_factor(acc, n, eps);
@@ -337,6 +351,19 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
         if (prev_slot >= 0)
             mbar_arrive(smem_u32(&bars[stages + prev_slot]));
     }
+    if (BLOCK_STATUS && failed_at >= 0) {
+        Vec<16> nan;
+        const uint32_t q = E::kSize == 4 ? 0x7FC00000u
+                                         : (DT == RMSNORM_BF16 ? 0x7FC07FC0u : 0x7E007E00u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            nan.w[i] = q;
+        for (int64_t k = failed_at; k < my_rows; k += groups) {
+            char *yr = yb + (blockIdx.x + k * static_cast<int64_t>(gridDim.x)) * row_bytes;
+            for (int v = gl; v < nvec; v += gsize)
+                st_stream<0>(yr + static_cast<int64_t>(v) * 16, nan);
+        }
+    }
 }
 
 template <int DT, bool TS>
@@ -356,6 +383,88 @@ const KernelDesc kTable[] = {STAGED_ENTRY(RMSNORM_F32, false), STAGED_ENTRY(RMSN
                              STAGED_ENTRY(RMSNORM_F16, false), STAGED_ENTRY(RMSNORM_F32, true),
                              STAGED_ENTRY(RMSNORM_BF16, true), STAGED_ENTRY(RMSNORM_F16, true)};
 
+// ---------------------------------------------------------------- no allocation
+
+// Status words of rmsnorm_fwd_staged_noalloc: one per block of a launch,
+// 4 KiB per device, held by every device that loads the library until the
+// process exits.
+constexpr int kNoAllocMaxBlocks = 1024;
+static __device__ __align__(256) int g_noalloc_status[kNoAllocMaxBlocks];
+
+struct NoAllocDevice {
+    bool ready = false;
+    int *status = nullptr; // device address of g_noalloc_status on this device
+    int sm_count = 0;
+    int smem_optin = 0;
+};
+
+constexpr int kNoAllocMaxDevices = 64;
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+template <int DT>
+cudaError_t launch_staged_noalloc(const rmsnorm_plan_t &p, const LaunchArgs &a)
+{
+    staged_rows_kernel<DT, false, true><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
+        a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32, a.status,
+        a.wait_limit_ns, a.flags);
+    return cudaGetLastError();
+}
+
+const void *noalloc_kernel(int dtype)
+{
+    switch (dtype) {
+    case RMSNORM_F32:
+        return reinterpret_cast<const void *>(&staged_rows_kernel<RMSNORM_F32, false, true>);
+    case RMSNORM_BF16:
+        return reinterpret_cast<const void *>(&staged_rows_kernel<RMSNORM_BF16, false, true>);
+    default:
+        return reinterpret_cast<const void *>(&staged_rows_kernel<RMSNORM_F16, false, true>);
+    }
+}
+
+// One-time set-up of the current device, with that device current: the
+// status array's device address (the array's name in host code is only a
+// stand-in), the device limits, and the kernels' shared-memory opt-in.
+// Makes no allocation.
+int noalloc_setup(NoAllocDevice *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return RMSNORM_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, sms = 0, optin = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        if (major != 10 || minor != 3)
+            return RMSNORM_ERR_UNSUPPORTED_DEVICE;
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_status) != cudaSuccess || ptr == nullptr)
+            return RMSNORM_ERR_CUDA;
+        for (int dt = RMSNORM_F32; dt <= RMSNORM_F16; ++dt)
+            if (cudaFuncSetAttribute(noalloc_kernel(dt),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin) != cudaSuccess)
+                return RMSNORM_ERR_CUDA;
+        d.status = static_cast<int *>(ptr);
+        d.sm_count = sms;
+        d.smem_optin = optin;
+        d.ready = true;
+    }
+    *out = d;
+    return RMSNORM_OK;
+}
+
 } // namespace
 
 const KernelDesc *staged_kernels(int *n)
@@ -365,3 +474,50 @@ const KernelDesc *staged_kernels(int *n)
 }
 
 } // namespace rmsnorm
+
+extern "C" int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, void *y,
+                                          int64_t rows, int64_t hidden, float eps, int dtype,
+                                          void *stream)
+{
+    using namespace rmsnorm;
+    int rc = check_call_args(x, weight, y, rows, hidden, eps, dtype);
+    if (rc != RMSNORM_OK)
+        return rc;
+    NoAllocDevice d;
+    rc = noalloc_setup(&d);
+    if (rc != RMSNORM_OK)
+        return rc;
+    if (rows == 0)
+        return RMSNORM_OK;
+    rmsnorm_plan_t p;
+    rc = plan_launch(x, weight, y, rows, hidden, dtype, d.sm_count, d.smem_optin,
+                     RMSNORM_VARIANT_STAGED, &p);
+    if (rc != RMSNORM_OK)
+        return rc == RMSNORM_ERR_VARIANT ? RMSNORM_ERR_TOO_LARGE : rc;
+    if (p.grid > kNoAllocMaxBlocks)
+        return RMSNORM_ERR_TOO_LARGE;
+    LaunchArgs a;
+    a.x = x;
+    a.w = weight;
+    a.y = y;
+    a.rows = rows;
+    a.hidden = static_cast<int32_t>(hidden);
+    a.eps = eps;
+    a.status = d.status;
+    a.wait_limit_ns = 1000000000ull;
+    a.flags = 0u;
+    a.stream = static_cast<cudaStream_t>(stream);
+    cudaError_t err;
+    switch (dtype) {
+    case RMSNORM_F32:
+        err = launch_staged_noalloc<RMSNORM_F32>(p, a);
+        break;
+    case RMSNORM_BF16:
+        err = launch_staged_noalloc<RMSNORM_BF16>(p, a);
+        break;
+    default:
+        err = launch_staged_noalloc<RMSNORM_F16>(p, a);
+        break;
+    }
+    return err == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
