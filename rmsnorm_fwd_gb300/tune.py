@@ -1,0 +1,211 @@
+"""Plan sweep for the RMSNorm kernels (the offline tuning behind the selector).
+
+    python -m rmsnorm_fwd_gb300.tune --rows 16384 --hidden 4096 [--dtype bf16]
+    python -m rmsnorm_fwd_gb300.tune --grid [--classes bulk,mid,decode]
+
+For one shape, every feasible explicit plan (each compiled instantiation
+with the block sizes, grid sizes and staged-ring shapes that make sense for
+the row) is launched through rmsnorm_fwd_ex and timed with CUDA events over
+back-to-back launches on rotating input/output sets larger than L2 (decode
+shapes: replayed from a CUDA graph so host launch cost is excluded).  One
+JSON line per plan, then the best plans.  --grid walks row sizes 128 B ..
+64 KiB (bf16 hidden 64 .. 32768) for bulk (>= 256 MiB of input), mid (8192
+rows) and decode (1, 8, 32, 128 rows) classes and prints, per point, the
+best plans and the automatic plan's time.  Inputs are drawn on the device
+(values do not affect timing).  Performance depends on row bytes, not on the
+element type, so the grid runs bf16.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import sys
+
+L2 = 129 * 1024 * 1024
+GRID_HIDDEN = [64, 128, 256, 512, 768, 1024, 1536, 2048, 2560, 2880, 3072, 3584, 4096, 5120,
+               6144, 7168, 8192, 10240, 12288, 16384, 24576, 32768]
+ES = {"f32": 4, "bf16": 2, "f16": 2}
+
+
+def staged_smem(row_bytes: int, stages: int) -> int:
+    slot = (row_bytes + 127) // 128 * 128
+    bar = ((2 * stages + 2) * 8 + 256 + 127) // 128 * 128
+    return bar + slot * (stages + 1)
+
+
+def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int) -> list[dict]:
+    """Explicit plans worth timing for this shape (the library validates each)."""
+    import rmsnorm_fwd_gb300 as rn
+    es = ES[dtype]
+    dt = rn.DTYPE_CODES[dtype]
+    out = []
+    for k in rn.kernels():
+        if k["dtype"] != dt:
+            continue
+        v = k["variant"]
+        if v == rn.VARIANT_WARP_PER_ROW:
+            vb = k["vec_bytes"]
+            nvec = hidden * es // vb
+            if hidden * es % vb or k["tpr"] * k["nv"] < nvec or k["tpr"] * k["nv"] >= 2 * nvec + 32:
+                continue
+            gpb = k["block"] // k["tpr"]
+            full = -(-rows // gpb)
+            for g in sorted({full, min(full, sms * 4), min(full, sms * 8), min(full, sms * 16)}):
+                out.append(dict(variant=v, vec_bytes=vb, threads_per_row=k["tpr"],
+                                vecs_per_thread=k["nv"], block_threads=k["block"],
+                                rows_per_block=gpb, stages=0, grid=g, smem_bytes=0,
+                                kernel_index=k["index"]))
+        elif v == rn.VARIANT_CTA_PER_ROW:
+            vb = k["vec_bytes"]
+            if hidden * es % vb:
+                continue
+            nvec = hidden * es // vb
+            tpr = max(32, -(-(-(-nvec // k["nv"])) // 32) * 32)
+            if k["tpr"]:
+                if k["tpr"] * k["nv"] < nvec or k["tpr"] * k["nv"] >= 2 * nvec + 32:
+                    continue
+                tpr = k["tpr"]
+            if tpr > k["block"]:
+                continue
+            grids = {rows}
+            for m in (1, 2, 3, 4, 6, 8, 16):
+                if tpr * m <= 2048:
+                    grids.add(min(rows, sms * m))
+            for g in sorted(grids):
+                out.append(dict(variant=v if g == rows else rn.VARIANT_PERSISTENT, vec_bytes=vb,
+                                threads_per_row=tpr, vecs_per_thread=k["nv"], block_threads=tpr,
+                                rows_per_block=1, stages=0, grid=g, smem_bytes=0,
+                                kernel_index=k["index"]))
+        elif v == rn.VARIANT_STAGED:
+            rb = hidden * es
+            if rb % 16:
+                continue
+            for bps in (1, 2):
+                budget = min(optin, 233472 // bps - 1024)
+                smax = 0
+                for st in range(32, 0, -1):
+                    if staged_smem(rb, st) <= budget:
+                        smax = st
+                        break
+                for wpr, c in ((1, 2), (1, 4), (1, 6), (1, 8), (1, 12), (2, 2), (2, 4), (2, 6),
+                               (4, 1), (4, 2), (4, 3), (8, 1), (8, 2), (16, 1)):
+                    if c > smax:
+                        continue
+                    for st in sorted({smax // c * c, min(smax // c * c, 2 * c), c}):
+                        if st < 2 or st % c:
+                            continue
+                        out.append(dict(variant=v, vec_bytes=16, threads_per_row=32 * wpr,
+                                        vecs_per_thread=0, block_threads=32 * (c * wpr + 1),
+                                        rows_per_block=c, stages=st, grid=min(rows, sms * bps),
+                                        smem_bytes=staged_smem(rb, st), kernel_index=k["index"]))
+        elif v == rn.VARIANT_GENERIC:
+            for b in (256, 512, 1024):
+                out.append(dict(variant=v, vec_bytes=0, threads_per_row=b, vecs_per_thread=0,
+                                block_threads=b, rows_per_block=1, stages=0,
+                                grid=min(rows, sms * (2048 // b)), smem_bytes=0,
+                                kernel_index=k["index"]))
+    return out
+
+
+def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> list[dict]:
+    """Time the automatic plan and every candidate; sorted fastest first."""
+    import torch
+
+    import rmsnorm_fwd_gb300 as rn
+    dev = torch.device("cuda", 0)
+    rn.ensure_context(0)
+    sms, optin = rn.rmsnorm_device_limits()
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
+    es = ES[dtype]
+    set_bytes = 2 * rows * hidden * es
+    nsets = min(64, max(2, -(-3 * L2 // set_bytes)))
+    base = [torch.randn(rows, hidden, device=dev).to(tdt) for _ in range(min(nsets, 4))]
+    xs = [base[i % len(base)] if i < len(base) else base[i % len(base)].clone()
+          for i in range(nsets)]
+    ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    w = (1 + 0.1 * torch.randn(hidden, device=dev)).to(tdt)
+    fwd = rn._load().rmsnorm_fwd_ex
+    s = torch.cuda.current_stream().cuda_stream
+    dt = rn.DTYPE_CODES[dtype]
+    xp = [t.data_ptr() for t in xs]
+    yp = [t.data_ptr() for t in ys]
+    auto = rn.Plan()
+    rn.rmsnorm_fwd_ex(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, auto)
+    cands = [auto.as_dict()] + candidates(rows, hidden, dtype, sms, optin)
+    out = []
+    for ci, c in enumerate(cands):
+        p = rn.Plan(**c)
+        ref = rn.ctypes.byref(p)
+        if fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, ref) != 0:
+            continue
+        for i in range(5):
+            fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if graph:
+            g_ = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            with torch.cuda.graph(g_, stream=cs):
+                for i in range(iters):
+                    fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt,
+                        cs.cuda_stream, 0, ref)
+            g_.replay()
+            torch.cuda.synchronize()
+            e0.record()
+            g_.replay()
+            e1.record()
+        else:
+            e0.record()
+            for i in range(iters):
+                fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref)
+            e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / iters * 1e3
+        gbs = (2 * rows * hidden * es + hidden * es) / (us * 1e-6) / 1e9
+        out.append({"us": round(us, 3), "GBps": round(gbs, 1), "auto": ci == 0, "plan": c})
+    del xs, ys, base
+    torch.cuda.empty_cache()
+    if rn.rmsnorm_get_device_status() != rn.OK:
+        raise RuntimeError("a timed plan recorded a device-side error")
+    out.sort(key=lambda r: r["us"])
+    return out
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--rows", type=int, default=16384)
+    ap.add_argument("--hidden", type=int, default=4096)
+    ap.add_argument("--dtype", default="bf16", choices=sorted(ES))
+    ap.add_argument("--iters", type=int, default=100)
+    ap.add_argument("--graph", action="store_true", help="replay launches from a CUDA graph")
+    ap.add_argument("--grid", action="store_true", help="walk the row-size grid")
+    ap.add_argument("--classes", default="bulk,mid,decode")
+    ap.add_argument("--grid-hidden", default="", help="comma-separated bf16 hidden sizes")
+    ap.add_argument("--keep", type=int, default=5)
+    args = ap.parse_args(argv)
+    if not args.grid:
+        res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph)
+        for r in res:
+            print(json.dumps(r), flush=True)
+        return 0
+    hidden = [int(h) for h in args.grid_hidden.split(",")] if args.grid_hidden else GRID_HIDDEN
+    classes = args.classes.split(",")
+    for h in hidden:
+        points = []
+        if "bulk" in classes:
+            points.append(("bulk", max(4096, (256 << 20) // (2 * h)), 30, False))
+        if "mid" in classes:
+            points.append(("mid", 8192, 100, False))
+        if "decode" in classes:
+            points += [(f"decode{r}", r, 200, True) for r in (1, 8, 32, 128)]
+        for cls, rows, iters, graph in points:
+            res = time_plans(rows, h, "bf16", iters, graph)
+            auto = next((r for r in res if r["auto"]), None)
+            print(json.dumps({"hidden_bf16": h, "row_bytes": 2 * h, "rows": rows, "class": cls,
+                              "top": res[:args.keep], "auto": auto}), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
