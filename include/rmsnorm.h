@@ -197,6 +197,19 @@ int rmsnorm_get_device_status(int *status);
  * copies in flight, and returns.  0 restores the default. */
 int rmsnorm_set_wait_limit_ns(uint64_t limit_ns);
 
+/* Programmatic dependent launch ("CuTeDSL at Perplexity", section "Grid
+ * synchronization", names it as the way to cut launch overhead between
+ * kernels).  When on, every launch carries the programmatic stream
+ * serialization attribute: the kernel may be scheduled while the previous
+ * kernel on the stream is still finishing, and waits (griddepcontrol.wait)
+ * for that kernel's completion and memory before its first global access,
+ * so results are unchanged.  Process-wide; the initial value is on unless
+ * the environment variable RMSNORM_PDL is "0".  rmsnorm_set_pdl returns
+ * RMSNORM_OK or RMSNORM_ERR_INVALID_ARG (enable not 0 or 1);
+ * rmsnorm_get_pdl returns the current setting (0 or 1). */
+int rmsnorm_set_pdl(int enable);
+int rmsnorm_get_pdl(void);
+
 /* Failure-detection test hook: launch the staged kernel on a valid shape
  * with its row copies withheld, so every consumer wait runs out after
  * `limit_ns`; the kernel then records RMSNORM_ERR_DEVICE_TIMEOUT and returns

@@ -107,6 +107,8 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_kernel_info": ([i32, ctypes.POINTER(KernelInfo)], i32),
             "rmsnorm_get_device_status": ([ctypes.POINTER(ctypes.c_int)], i32),
             "rmsnorm_set_wait_limit_ns": ([u64], i32),
+            "rmsnorm_set_pdl": ([i32], i32),
+            "rmsnorm_get_pdl": ([], i32),
             "rmsnorm_test_staged_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
             "rmsnorm_fwd_staged_noalloc": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
             "rmsnorm_status_string": ([i32], ctypes.c_char_p),
@@ -210,6 +212,14 @@ def rmsnorm_get_device_status() -> int:
 
 def rmsnorm_set_wait_limit_ns(limit_ns: int) -> None:
     _check(_load().rmsnorm_set_wait_limit_ns(limit_ns), "rmsnorm_set_wait_limit_ns")
+
+
+def rmsnorm_set_pdl(enable: bool) -> None:
+    _check(_load().rmsnorm_set_pdl(1 if enable else 0), "rmsnorm_set_pdl")
+
+
+def rmsnorm_get_pdl() -> bool:
+    return bool(_load().rmsnorm_get_pdl())
 
 
 def rmsnorm_test_staged_timeout(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int,

@@ -48,6 +48,20 @@ struct DeviceCtx {
 std::mutex g_mu;
 DeviceCtx g_ctx[kMaxDevices];
 std::atomic<uint64_t> g_wait_limit{kDefaultWaitLimitNs};
+std::atomic<int> g_pdl{-1}; // -1: not set yet (RMSNORM_PDL decides), 0 off, 1 on
+
+bool pdl_enabled()
+{
+    int v = g_pdl.load();
+    if (v < 0) {
+        const char *e = std::getenv("RMSNORM_PDL");
+        v = (e && e[0] == '0') ? 0 : 1;
+        int expected = -1;
+        g_pdl.compare_exchange_strong(expected, v);
+        v = g_pdl.load();
+    }
+    return v == 1;
+}
 thread_local int t_last_variant = 0;
 
 bool log_enabled()
@@ -145,6 +159,7 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     a.wait_limit_ns = limit_ns;
     a.flags = flags;
     a.stream = static_cast<cudaStream_t>(stream);
+    a.pdl = pdl_enabled();
     if (log_enabled())
         std::fprintf(stderr,
                      "rmsnorm: rows=%lld hidden=%lld dtype=%d -> variant=%d vec=%d tpr=%d nv=%d "
@@ -336,6 +351,19 @@ int rmsnorm_set_wait_limit_ns(uint64_t limit_ns)
 {
     g_wait_limit.store(limit_ns ? limit_ns : kDefaultWaitLimitNs);
     return RMSNORM_OK;
+}
+
+int rmsnorm_set_pdl(int enable)
+{
+    if (enable != 0 && enable != 1)
+        return RMSNORM_ERR_INVALID_ARG;
+    g_pdl.store(enable);
+    return RMSNORM_OK;
+}
+
+int rmsnorm_get_pdl(void)
+{
+    return pdl_enabled() ? 1 : 0;
 }
 
 int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int64_t rows,

@@ -211,6 +211,20 @@ __device__ inline void scale(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB> &wv,
     }
 }
 
+// ---------------------------------------------------------------- launch order
+
+// Programmatic dependent launch.  Every kernel calls pdl_begin() before its
+// first global-memory access: the wait returns once the grid this launch
+// depends on has completed and its writes are visible (immediately when the
+// launch carries no programmatic dependency), and the trigger lets the next
+// dependent launch be scheduled as soon as every block of this grid has
+// started, so its blocks take SM slots while this grid's last blocks finish.
+__device__ inline void pdl_begin()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- reductions
 
 // Butterfly sum over aligned groups of WIDTH lanes (WIDTH a power of two

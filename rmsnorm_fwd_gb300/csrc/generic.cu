@@ -22,6 +22,7 @@ generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
 {
     using E = Elem<DT>;
     __shared__ float part[2][32];
+    pdl_begin();
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int warp = t >> 5;
@@ -55,9 +56,8 @@ generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
 template <int DT>
 cudaError_t launch_generic(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    generic_rows_kernel<DT><<<p.grid, p.block_threads, 0, a.stream>>>(a.x, a.w, a.y, a.rows,
-                                                                       a.hidden, a.eps);
-    return cudaGetLastError();
+    return launch_kernel(generic_rows_kernel<DT>, p.grid, p.block_threads, 0, a, a.x, a.w, a.y,
+                         a.rows, a.hidden, a.eps);
 }
 
 #define GENERIC_ENTRY(DT)                                                                      \

@@ -28,7 +28,33 @@ struct LaunchArgs {
     uint64_t wait_limit_ns; // bound on every spin-wait, %globaltimer ns
     uint32_t flags;         // kFlagWithholdCopies: failure-detection test only
     cudaStream_t stream;
+    bool pdl = false;       // launch with a programmatic dependency on the stream's last kernel
 };
+
+#if defined(__CUDACC__)
+// Launches `kernel` on a.stream, with the programmatic-stream-serialization
+// attribute when a.pdl is set (the kernels wait for their predecessor before
+// touching memory, so the attribute only lets launches overlap).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), int grid, int block, int smem,
+                          const LaunchArgs &a, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    if (a.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    const cudaError_t err = cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
+#endif
 
 constexpr uint32_t kFlagWithholdCopies = 1u;
 

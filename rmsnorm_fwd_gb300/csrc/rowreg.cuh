@@ -53,6 +53,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     constexpr int GROUPS = BLOCK / TPR;                    // rows per block per iteration
     constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;    // weight slice kept in registers
 
+    pdl_begin();
     const int nvec = hidden / VPE;
     const int t = threadIdx.x % TPR;
     const int g = threadIdx.x / TPR;
@@ -130,6 +131,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;
     __shared__ float part[2][32];
 
+    pdl_begin();
     const int nvec = hidden / VPE;
     const int t = threadIdx.x;
     const int tpr = TPRC > 0 ? TPRC : blockDim.x;
@@ -204,17 +206,15 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
 cudaError_t launch_warp(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP><<<p.grid, BLOCK, 0, a.stream>>>(
-        a.x, a.w, a.y, a.rows, a.hidden, a.eps);
-    return cudaGetLastError();
+    return launch_kernel(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP>, p.grid, BLOCK, 0, a,
+                         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
 }
 
 template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC>
 cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC><<<p.grid, p.block_threads, 0, a.stream>>>(
-        a.x, a.w, a.y, a.rows, a.hidden, a.eps);
-    return cudaGetLastError();
+    return launch_kernel(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC>, p.grid,
+                         p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps);
 }
 
 constexpr int kWarpBlock = 256;

@@ -190,6 +190,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
     const int64_t my_rows =
         rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
+    pdl_begin();
     if (BLOCK_STATUS) {
         status += blockIdx.x;
         if (threadIdx.x == 0)
@@ -369,10 +370,9 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
 template <int DT, bool TS>
 cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    staged_rows_kernel<DT, TS><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
-        a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32, a.status,
-        a.wait_limit_ns, a.flags);
-    return cudaGetLastError();
+    return launch_kernel(staged_rows_kernel<DT, TS>, p.grid, p.block_threads, p.smem_bytes, a,
+                         a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32,
+                         a.status, a.wait_limit_ns, a.flags);
 }
 
 #define STAGED_ENTRY(DT, TS)                                                                   \

@@ -22,6 +22,7 @@ import json
 import sys
 
 L2 = 129 * 1024 * 1024
+_AUTO_ONLY = False
 GRID_HIDDEN = [64, 128, 256, 512, 768, 1024, 1536, 2048, 2560, 2880, 3072, 3584, 4096, 5120,
                6144, 7168, 8192, 10240, 12288, 16384, 24576, 32768]
 ES = {"f32": 4, "bf16": 2, "f16": 2}
@@ -131,7 +132,7 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
     yp = [t.data_ptr() for t in ys]
     auto = rn.Plan()
     rn.rmsnorm_fwd_ex(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, auto)
-    cands = [auto.as_dict()] + candidates(rows, hidden, dtype, sms, optin)
+    cands = [auto.as_dict()] + ([] if _AUTO_ONLY else candidates(rows, hidden, dtype, sms, optin))
     out = []
     for ci, c in enumerate(cands):
         p = rn.Plan(**c)
@@ -183,7 +184,15 @@ def main(argv=None) -> int:
     ap.add_argument("--classes", default="bulk,mid,decode")
     ap.add_argument("--grid-hidden", default="", help="comma-separated bf16 hidden sizes")
     ap.add_argument("--keep", type=int, default=5)
+    ap.add_argument("--pdl", type=int, choices=[0, 1], default=None,
+                    help="programmatic dependent launch off/on (default: library setting)")
+    ap.add_argument("--auto-only", action="store_true", help="time only the automatic plan")
     args = ap.parse_args(argv)
+    if args.pdl is not None:
+        import rmsnorm_fwd_gb300 as rn
+        rn.rmsnorm_set_pdl(bool(args.pdl))
+    global _AUTO_ONLY
+    _AUTO_ONLY = args.auto_only
     if not args.grid:
         res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph)
         for r in res:
