@@ -201,6 +201,85 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     }
 }
 
+// ---------------------------------------------------------------- looped rows
+
+// Rows of any length (16-byte multiple): a block per row, grid-stride, the
+// row streamed twice in chunks of 4 vectors per thread -- the first pass sums
+// the squares, the second re-reads the row (an L2 hit: the resident blocks'
+// rows are a few tens of MB against a 129 MB L2), scales and stores.  DRAM
+// sees x once and y once.  For rows longer than the register bodies hold.
+template <int DT, int VB, int MAXT, int MINB, int CP>
+__global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
+cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+                int32_t hidden, float eps)
+{
+    using E = Elem<DT>;
+    constexpr int VPE = VB / E::kSize;
+    constexpr int U = 4; // vectors in flight per thread per step
+    __shared__ float part[2][32];
+
+    pdl_begin();
+    const int nvec = hidden / VPE;
+    const int t = threadIdx.x;
+    const int tpr = blockDim.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
+    const int nwarps = tpr >> 5;
+    const float n = static_cast<float>(hidden);
+    const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
+    const char *wb = static_cast<const char *>(w);
+
+    int it = 0;
+    for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
+        const char *xr = static_cast<const char *>(x) + row * row_bytes;
+        char *yr = static_cast<char *>(y) + row * row_bytes;
+        float s = 0.f;
+        for (int v0 = t; v0 < nvec; v0 += U * tpr) {
+            Vec<VB> xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * tpr;
+                if (v < nvec)
+                    ld_stream<CP>(xv[u], xr + static_cast<int64_t>(v) * VB);
+                else
+                    vzero(xv[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                s = sumsq<DT, VB>(xv[u], s);
+        }
+        s = group_allreduce<32>(s);
+        if (lane == 0)
+            part[it & 1][warp] = s;
+        // Also orders every first-pass read of this row before any write of
+        // it (in-place calls).
+        __syncthreads();
+        const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
+        const float r = row_factor(group_allreduce<32>(tot), n, eps);
+
+        for (int v0 = t; v0 < nvec; v0 += U * tpr) {
+            Vec<VB> xv[U], wv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * tpr;
+                if (v < nvec) {
+                    ld_stream<0>(xv[u], xr + static_cast<int64_t>(v) * VB);
+                    ld_weight(wv[u], wb + static_cast<int64_t>(v) * VB);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int v = v0 + u * tpr;
+                if (v < nvec) {
+                    Vec<VB> o;
+                    scale<DT, VB>(o, xv[u], wv[u], r);
+                    st_stream<CP>(yr + static_cast<int64_t>(v) * VB, o);
+                }
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- launchers
 
 template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
@@ -217,6 +296,13 @@ cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
                          p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps);
 }
 
+template <int DT, int VB, int MAXT, int MINB, int CP>
+cudaError_t launch_loop(const rmsnorm_plan_t &p, const LaunchArgs &a)
+{
+    return launch_kernel(cta_loop_kernel<DT, VB, MAXT, MINB, CP>, p.grid, p.block_threads, 0, a,
+                         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
+}
+
 constexpr int kWarpBlock = 256;
 
 #define WARP_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
@@ -229,6 +315,12 @@ constexpr int kWarpBlock = 256;
     KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, NV, MAXT, MINB, CP,                    \
                &launch_cta<DT, VB, NV, MAXT, MINB, CP, 0>,                                     \
                reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, 0>)}
+
+// Looped block-per-row (vectors per thread 0 = "any row length").
+#define LOOP_ENTRY(DT, VB, MAXT, MINB, CP)                                                     \
+    KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, 0, MAXT, MINB, CP,                     \
+               &launch_loop<DT, VB, MAXT, MINB, CP>,                                           \
+               reinterpret_cast<const void *>(&cta_loop_kernel<DT, VB, MAXT, MINB, CP>)}
 
 // Block of exactly TPR threads (compile time).
 #define CTAF_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
@@ -255,7 +347,8 @@ constexpr int kWarpBlock = 256;
         CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
         CTA_ENTRY(DT, 16, 2, 256, 8, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                     \
         CTA_ENTRY(DT, 16, 4, 256, 6, 1), CTA_ENTRY(DT, 16, 4, 512, 2, 1),                     \
-        CTA_ENTRY(DT, 16, 8, 512, 0, 1), CTAF_ENTRY(DT, 16, 512, 1, 0, 0)
+        CTA_ENTRY(DT, 16, 8, 512, 0, 1), CTAF_ENTRY(DT, 16, 512, 1, 0, 0),                    \
+        LOOP_ENTRY(DT, 16, 512, 2, 1)
 
 } // namespace rowreg
 } // namespace rmsnorm

@@ -254,6 +254,13 @@ int plan_prefill_mid(const Shape &s, int variant, bool persistent, rmsnorm_plan_
     return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap, variant, p);
 }
 
+// Rows of any length: the looped two-pass body, 512 threads, two blocks per SM.
+int plan_looped(const Shape &s, int variant, bool persistent, rmsnorm_plan_t *p)
+{
+    const int64_t cap = persistent ? int64_t(s.sm_count) * blocks_per_sm(512, 512, 2) : INT_MAX;
+    return plan_cta_exact(s, 16, 0, 512, 2, 1, 0, 512, cap, variant, p);
+}
+
 // Prefill, rows of more than 1024 16-byte vectors: the fewest vectors per
 // thread that keep the block at <= 640 threads, on a persistent grid sized
 // to the blocks that fit on an SM.
@@ -275,7 +282,7 @@ int plan_prefill_wide(const Shape &s, int variant, bool persistent, rmsnorm_plan
     if (tpr <= 512)
         return plan_cta_exact(s, 16, 8, 512, 0, 1, 0, tpr,
                               persistent ? int64_t(s.sm_count) : INT_MAX, variant, p);
-    return RMSNORM_ERR_VARIANT;
+    return plan_looped(s, variant, persistent, p);
 }
 
 // Forced block-per-row / persistent.
@@ -286,8 +293,11 @@ int plan_cta(const Shape &s, bool persistent, rmsnorm_plan_t *p)
         return RMSNORM_ERR_MISALIGNED;
     const int variant = persistent ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW;
     const int64_t nvec = s.row_bytes / 16;
-    if (persistent && s.rows <= s.sm_count)
-        return plan_decode(s, variant, p);
+    if (persistent && s.rows <= s.sm_count) {
+        if (plan_decode(s, variant, p) == RMSNORM_OK)
+            return RMSNORM_OK;
+        return plan_looped(s, variant, false, p);
+    }
     if (nvec <= 1024 && plan_prefill_mid(s, variant, persistent, p) == RMSNORM_OK)
         return RMSNORM_OK;
     if (nvec > 1024)
@@ -464,7 +474,8 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
             return RMSNORM_ERR_VARIANT;
         break;
     case RMSNORM_VARIANT_CTA_PER_ROW:
-        if (p.block_threads > d.block || int64_t(p.block_threads) * d.nv < nvec)
+        // nv == 0: the looped body takes any row length.
+        if (p.block_threads > d.block || (d.nv > 0 && int64_t(p.block_threads) * d.nv < nvec))
             return RMSNORM_ERR_VARIANT;
         if (d.tpr != 0 && p.block_threads != d.tpr) // block size fixed at compile time
             return RMSNORM_ERR_VARIANT;

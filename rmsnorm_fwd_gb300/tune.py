@@ -61,6 +61,14 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int) -> list
             if hidden * es % vb:
                 continue
             nvec = hidden * es // vb
+            if k["nv"] == 0:  # looped body: any row length
+                for tpr in (256, 512):
+                    for g in sorted({rows, min(rows, sms), min(rows, 2 * sms)}):
+                        out.append(dict(variant=v if g == rows else rn.VARIANT_PERSISTENT,
+                                        vec_bytes=vb, threads_per_row=tpr, vecs_per_thread=0,
+                                        block_threads=tpr, rows_per_block=1, stages=0, grid=g,
+                                        smem_bytes=0, kernel_index=k["index"]))
+                continue
             tpr = max(32, -(-(-(-nvec // k["nv"])) // 32) * 32)
             if k["tpr"]:
                 if k["tpr"] * k["nv"] < nvec or k["tpr"] * k["nv"] >= 2 * nvec + 32:

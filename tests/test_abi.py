@@ -146,7 +146,7 @@ def test_capacity_covers_row():
                 continue
             for v in (rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT):
                 rc, p = plan(4096, hidden, dt, v)
-                if rc == rn.OK:
+                if rc == rn.OK and p.vecs_per_thread > 0:  # 0: looped, any length
                     cap = p.threads_per_row * p.vecs_per_thread * p.vec_bytes // es
                     assert cap >= hidden, (dt, hidden, v, p.as_dict())
 
@@ -209,7 +209,12 @@ def test_prefill_rules():
 
 
 def test_huge_row_still_planned():
-    rc, p = plan(4, 1 << 22, rn.BF16)
+    # 8 MiB rows: the looped vector body, for decode and prefill row counts
+    for rows in (4, 100000):
+        rc, p = plan(rows, 1 << 22, rn.BF16)
+        assert rc == rn.OK and p.vecs_per_thread == 0 and p.vec_bytes == 16, p.as_dict()
+    # misaligned: the scalar body
+    rc, p = plan(4, 1 << 22, rn.BF16, xoff=2)
     assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC
 
 

@@ -49,6 +49,17 @@ def plans_for(k, rows, sms, optin):
                                              block_threads=k["block"], rows_per_block=gpb,
                                              stages=0, grid=grid, smem_bytes=0,
                                              kernel_index=k["index"])))
+    elif v == rn.VARIANT_CTA_PER_ROW and k["nv"] == 0:  # looped: any row length
+        vpe = k["vec_bytes"] // es
+        for tpr in (32, 96, k["block"]):
+            for nvec in (1, tpr - 1, 4 * tpr + 3, 9 * tpr + 5):
+                for grid in sorted({rows, max(1, rows // 4)}):
+                    out.append((nvec * vpe, dict(variant=v if grid == rows else
+                                                 rn.VARIANT_PERSISTENT,
+                                                 vec_bytes=k["vec_bytes"], threads_per_row=tpr,
+                                                 vecs_per_thread=0, block_threads=tpr,
+                                                 rows_per_block=1, stages=0, grid=grid,
+                                                 smem_bytes=0, kernel_index=k["index"])))
     elif v == rn.VARIANT_CTA_PER_ROW:
         vpe = k["vec_bytes"] // es
         tprs = [k["tpr"]] if k["tpr"] else sorted({32, 96, min(k["block"], 256), k["block"]})
