@@ -178,11 +178,14 @@ def hbm_peak():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device-code sources (kernels, their headers, the launch
+    helper); host-only files such as the selector do not change a kernel."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rmsnorm_fwd_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        if f.endswith((".cu", ".cuh")) or f == "internal.h":
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 

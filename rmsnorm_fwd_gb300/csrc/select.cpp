@@ -249,9 +249,16 @@ int plan_prefill_mid(const Shape &s, int variant, bool persistent, rmsnorm_plan_
     if (best < 0)
         return RMSNORM_ERR_VARIANT;
     const Opt &o = opts[best];
-    const int64_t cap =
-        persistent ? int64_t(s.sm_count) * blocks_per_sm(best_tpr, o.maxt, o.minb) : INT_MAX;
-    return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap, variant, p);
+    // Blocks of <= 96 threads are launched on a capped grid (16 per SM,
+    // grid-stride): tens of thousands of tiny blocks cost more to schedule
+    // than the rows they carry.
+    int64_t cap = INT_MAX;
+    if (persistent)
+        cap = int64_t(s.sm_count) * blocks_per_sm(best_tpr, o.maxt, o.minb);
+    else if (best_tpr <= 96)
+        cap = int64_t(s.sm_count) * 16;
+    return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap,
+                          cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : variant, p);
 }
 
 // Rows of any length: the looped two-pass body, 512 threads, two blocks per SM.
@@ -344,6 +351,25 @@ int plan_staged(const Shape &s, int blocks_per_sm, int groups_wanted, int wpr, b
     return p->kernel_index >= 0 ? RMSNORM_OK : RMSNORM_ERR_VARIANT;
 }
 
+// Rows of 32..72 KiB: the staged ring with 8 warps per row (one group) up to
+// 48 KiB rows and 4 warps x 2 groups beyond; 4 slots up to 40 KiB rows, 2
+// above (the sweep's best shapes for 40, 48 and 64 KiB rows).
+int plan_staged_wide(const Shape &s, rmsnorm_plan_t *p)
+{
+    const bool small = s.row_bytes <= 48 * 1024;
+    const int rc = plan_staged(s, 1, small ? 1 : 2, small ? 8 : 4, false, p);
+    if (rc != RMSNORM_OK)
+        return rc;
+    const int max_stages = s.row_bytes <= 40 * 1024 ? 4 : 2;
+    const int groups = p->rows_per_block;
+    int stages = std::min(p->stages, max_stages) / groups * groups;
+    if (stages < groups || stages < 2)
+        return RMSNORM_ERR_VARIANT;
+    p->stages = stages;
+    p->smem_bytes = staged_layout(static_cast<int>(s.row_bytes), stages).smem_bytes;
+    return RMSNORM_OK;
+}
+
 // Forced staged: one warp per row up to 8 KiB rows, wider groups beyond.
 int plan_staged_auto(const Shape &s, rmsnorm_plan_t *p)
 {
@@ -431,14 +457,20 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return plan_warp_exact(s, 16, 2, 0, INT_MAX, out);
     if (nvec <= 64)
         return plan_warp_exact(s, 32, 2, 8, INT_MAX, out);
-    if (nvec <= 96)
+    if (nvec <= 128)
         return plan_warp_exact(s, 32, 4, 8, INT_MAX, out);
     if (plan_prefill_mid(s, RMSNORM_VARIANT_CTA_PER_ROW, false, out) == RMSNORM_OK)
         return RMSNORM_OK;
 wide:
-    if (plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)
+    // 16..32 KiB rows: the register bodies on a persistent grid.
+    if (nvec <= 2048 && plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    if (plan_staged_auto(s, out) == RMSNORM_OK)
+    // 32..72 KiB rows: the shared-memory ring.
+    if (nvec <= 4608 && plan_staged_wide(s, out) == RMSNORM_OK)
+        return RMSNORM_OK;
+    // Longer rows: the looped body, one block per row.
+    if (plan_cta_exact(s, 16, 0, 512, 2, 1, 0, nvec <= 5120 ? 256 : 512, INT_MAX,
+                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
         return RMSNORM_OK;
     return plan_generic(s, out);
 }

@@ -111,7 +111,7 @@ def plan(rows, hidden, dtype, variant=rn.VARIANT_AUTO, xoff=0, sms=SMS):
 def test_selector_on_the_workloads():
     expect = {
         "f32_64x128": rn.VARIANT_WARP_PER_ROW,
-        "embed_bf16_8192x1024": rn.VARIANT_CTA_PER_ROW,
+        "embed_bf16_8192x1024": rn.VARIANT_WARP_PER_ROW,
         "prefill_bf16_16384x4096": rn.VARIANT_CTA_PER_ROW,
         "decode_bf16_1x4096": rn.VARIANT_PERSISTENT,
         "decode_bf16_8x4096": rn.VARIANT_PERSISTENT,
@@ -194,13 +194,17 @@ def test_prefill_rules():
     lean blocks of <= 256 threads with 2-4 vectors each up to 16 KiB rows,
     a persistent grid beyond."""
     for hidden, variant in ((64, rn.VARIANT_WARP_PER_ROW), (512, rn.VARIANT_WARP_PER_ROW),
-                            (768, rn.VARIANT_WARP_PER_ROW), (1024, rn.VARIANT_CTA_PER_ROW),
-                            (4096, rn.VARIANT_CTA_PER_ROW), (8192, rn.VARIANT_CTA_PER_ROW),
-                            (16384, rn.VARIANT_PERSISTENT)):
+                            (768, rn.VARIANT_WARP_PER_ROW), (1024, rn.VARIANT_WARP_PER_ROW),
+                            (1536, rn.VARIANT_PERSISTENT), (4096, rn.VARIANT_CTA_PER_ROW),
+                            (8192, rn.VARIANT_CTA_PER_ROW), (16384, rn.VARIANT_PERSISTENT),
+                            (24576, rn.VARIANT_STAGED), (32768, rn.VARIANT_STAGED),
+                            (65536, rn.VARIANT_CTA_PER_ROW)):
         rc, p = plan(100000, hidden, rn.BF16)
         assert rc == rn.OK and p.variant == variant, (hidden, p.as_dict())
-        if variant == rn.VARIANT_CTA_PER_ROW:
+        if variant == rn.VARIANT_CTA_PER_ROW and hidden <= 8192:
             assert p.block_threads <= 256 and 2 <= p.vecs_per_thread <= 4
+        if variant == rn.VARIANT_STAGED:
+            assert p.stages >= 2 and p.threads_per_row >= 128
     rc, p = plan(16384, 4096, rn.BF16)
     assert (p.block_threads, p.vecs_per_thread, p.grid) == (256, 2, 16384)
     # the same row bytes give the same shape for f32
