@@ -43,6 +43,7 @@
 #ifndef RMSNORM_H
 #define RMSNORM_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -137,6 +138,30 @@ int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_
  * AUTO, the chosen plan is written back into it. */
 int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
                    float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan);
+
+/* y = RMSNorm(x) * weight for x and y in HOST memory: rows are processed in
+ * chunks through a device workspace the caller provides, with the upload of
+ * one chunk, the kernel on the previous one and the download of the one
+ * before that overlapped (two internal streams of this context plus
+ * `stream` for the kernels; up to three buffers carved from the workspace).
+ *   x_host, y_host  host pointers, [rows, hidden] of `dtype`; pinned
+ *                   (page-locked) memory lets the copies overlap, pageable
+ *                   memory works but serialises; y_host may equal x_host
+ *   weight          DEVICE pointer, [hidden] of `dtype`
+ *   workspace       DEVICE pointer to workspace_bytes the caller owns; it
+ *                   must hold at least one row (256-byte aligned slices)
+ *   chunk_rows      rows per chunk; 0 = about rows / 16, within the buffers
+ *   stream          cudaStream_t (as void*): work already on it is ordered
+ *                   before the first upload, and it waits for the last
+ *                   download, so synchronising it makes y_host readable
+ * Asynchronous like rmsnorm_fwd: x_host must stay valid and unmodified, and
+ * y_host and the workspace untouched, until `stream` has passed this call.
+ * Calls on one device enqueue one at a time (a mutex); their pipelines
+ * share the context's two streams.  Returns the statuses of rmsnorm_fwd, or
+ * RMSNORM_ERR_INVALID_ARG when the workspace cannot hold a row. */
+int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64_t rows,
+                     int64_t hidden, float eps, int dtype, void *workspace,
+                     size_t workspace_bytes, int64_t chunk_rows, void *stream);
 
 /* The selector, host only (touches no memory behind the pointers and no
  * GPU): the plan rmsnorm_fwd_ex would launch for these arguments on a device

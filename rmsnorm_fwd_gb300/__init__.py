@@ -99,6 +99,8 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_fwd": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
             "rmsnorm_fwd_ex": ([vp, vp, vp, i64, i64, f32, i32, vp, i32, pp], i32),
             "rmsnorm_plan": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, pp], i32),
+            "rmsnorm_fwd_host": ([vp, vp, vp, i64, i64, f32, i32, vp, ctypes.c_size_t, i64, vp],
+                                 i32),
             "rmsnorm_last_variant": ([], i32),
             "rmsnorm_kernel_count": ([], i32),
             "rmsnorm_validate_plan": ([pp, vp, vp, vp, i64, i64, i32, i32, i32], i32),
@@ -151,6 +153,16 @@ def rmsnorm_fwd_ex(x: int, weight: int, y: int, rows: int, hidden: int, eps: flo
     _check(_load().rmsnorm_fwd_ex(x, weight, y, rows, hidden, eps, dtype, stream or None,
                                   variant, ref), "rmsnorm_fwd_ex")
     return plan
+
+
+def rmsnorm_fwd_host(x_host: int, weight: int, y_host: int, rows: int, hidden: int, eps: float,
+                     dtype: int, workspace: int, workspace_bytes: int, chunk_rows: int,
+                     stream: int | None) -> None:
+    """Host-buffer call: host x/y (pinned for overlap), device weight and
+    workspace, chunked upload / kernel / download pipeline."""
+    _check(_load().rmsnorm_fwd_host(x_host, weight, y_host, rows, hidden, eps, dtype, workspace,
+                                    workspace_bytes, chunk_rows, stream or None),
+           "rmsnorm_fwd_host")
 
 
 def rmsnorm_plan(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int, sm_count: int,

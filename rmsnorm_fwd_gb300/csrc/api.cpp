@@ -1,5 +1,6 @@
 // api.cpp -- the C ABI (include/rmsnorm.h): per-device contexts, argument
 // validation, plan selection and the launch.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -38,15 +39,61 @@ namespace {
 constexpr int kMaxDevices = 64;
 constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull; // one second
 
+// Host-buffer pipeline resources of one device (created on first use).
+constexpr int kPipeBuffers = 3;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t in = nullptr, out = nullptr; // upload / download streams
+    cudaEvent_t entry = nullptr;              // caller stream at entry
+    cudaEvent_t loaded[kPipeBuffers] = {};    // upload of a buffer done
+    cudaEvent_t computed[kPipeBuffers] = {};  // kernel on a buffer done
+    cudaEvent_t drained[kPipeBuffers] = {};   // download of a buffer done (buffer free)
+};
+
 struct DeviceCtx {
     int refs = 0;
     int sm_count = 0;
     int smem_optin = 0;
     int *status = nullptr; // device word
+    HostPipe *pipe = nullptr;
 };
 
 std::mutex g_mu;
 DeviceCtx g_ctx[kMaxDevices];
+std::mutex g_pipe_mu[kMaxDevices]; // one host-buffer call enqueues at a time per device
+
+void destroy_pipe(HostPipe *hp)
+{
+    if (!hp)
+        return;
+    if (hp->ready) {
+        cudaStreamDestroy(hp->in);
+        cudaStreamDestroy(hp->out);
+        cudaEventDestroy(hp->entry);
+        for (int b = 0; b < kPipeBuffers; ++b) {
+            cudaEventDestroy(hp->loaded[b]);
+            cudaEventDestroy(hp->computed[b]);
+            cudaEventDestroy(hp->drained[b]);
+        }
+    }
+    delete hp;
+}
+
+int make_pipe(HostPipe *hp)
+{
+    const unsigned ef = cudaEventDisableTiming;
+    if (cudaStreamCreateWithFlags(&hp->in, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&hp->out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&hp->entry, ef) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    for (int b = 0; b < kPipeBuffers; ++b)
+        if (cudaEventCreateWithFlags(&hp->loaded[b], ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp->computed[b], ef) != cudaSuccess ||
+            cudaEventCreateWithFlags(&hp->drained[b], ef) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+    hp->ready = true;
+    return RMSNORM_OK;
+}
 std::atomic<uint64_t> g_wait_limit{kDefaultWaitLimitNs};
 std::atomic<int> g_pdl{-1}; // -1: not set yet (RMSNORM_PDL decides), 0 off, 1 on
 
@@ -248,7 +295,9 @@ int rmsnorm_destroy(void)
     if (c.refs <= 0)
         return RMSNORM_ERR_NOT_INITIALIZED;
     if (--c.refs == 0) {
+        std::lock_guard<std::mutex> plk(g_pipe_mu[dev]);
         cudaFree(c.status);
+        destroy_pipe(c.pipe);
         c = DeviceCtx{};
     }
     return RMSNORM_OK;
@@ -266,6 +315,110 @@ int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int
 {
     return launch(x, weight, y, rows, hidden, eps, dtype, stream, variant, plan, 0u,
                   g_wait_limit.load());
+}
+
+int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64_t rows,
+                     int64_t hidden, float eps, int dtype, void *workspace,
+                     size_t workspace_bytes, int64_t chunk_rows, void *stream)
+{
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
+        return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+    if (rows < 0 || hidden <= 0 || !(eps >= 0.f) || !std::isfinite(eps) || chunk_rows < 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    if (!weight || (rows > 0 && (!x_host || !y_host || !workspace)))
+        return RMSNORM_ERR_INVALID_ARG;
+    const int64_t es = dtype == RMSNORM_F32 ? 4 : 2;
+    if (rows > INT64_MAX / 4 / hidden)
+        return RMSNORM_ERR_INVALID_ARG;
+    const int64_t row_bytes = hidden * es;
+    if (rows > 0 && ranges_overlap(x_host, rows * row_bytes, y_host, rows * row_bytes) &&
+        x_host != y_host)
+        return RMSNORM_ERR_ALIASING;
+    int dev = 0;
+    DeviceCtx ctx;
+    int rc = current_ctx(&ctx, &dev);
+    if (rc != RMSNORM_OK)
+        return rc;
+    if (rows == 0)
+        return RMSNORM_OK;
+
+    // Buffers: up to three slices of the workspace, 256-byte aligned.
+    const int64_t ws = static_cast<int64_t>(workspace_bytes);
+    int nbuf = kPipeBuffers;
+    int64_t per = 0;
+    for (; nbuf >= 1; --nbuf) {
+        per = (ws / nbuf) / 256 * 256;
+        if (per >= row_bytes)
+            break;
+    }
+    if (nbuf < 1)
+        return RMSNORM_ERR_INVALID_ARG; // the workspace holds less than one row
+    int64_t chunk = per / row_bytes;
+    if (chunk_rows > 0)
+        chunk = std::min(chunk, chunk_rows);
+    else // about 16 chunks, so filling and draining the pipeline stay small
+        chunk = std::min(chunk, std::max<int64_t>(1, (rows + 15) / 16));
+
+    std::lock_guard<std::mutex> plk(g_pipe_mu[dev]);
+    HostPipe *hp = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        DeviceCtx &c = g_ctx[dev];
+        if (c.refs <= 0)
+            return RMSNORM_ERR_NOT_INITIALIZED;
+        if (!c.pipe) {
+            c.pipe = new HostPipe;
+            if (make_pipe(c.pipe) != RMSNORM_OK) {
+                destroy_pipe(c.pipe);
+                c.pipe = nullptr;
+                return RMSNORM_ERR_CUDA;
+            }
+        }
+        hp = c.pipe;
+    }
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    // Everything already on the caller's stream (the workspace's last users,
+    // the weight's producer) happens first.
+    if (cudaEventRecord(hp->entry, cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->in, hp->entry, 0) != cudaSuccess ||
+        cudaStreamWaitEvent(hp->out, hp->entry, 0) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    const char *xh = static_cast<const char *>(x_host);
+    char *yh = static_cast<char *>(y_host);
+    char *wsb = static_cast<char *>(workspace);
+    int64_t i = 0;
+    for (int64_t r0 = 0; r0 < rows; r0 += chunk, ++i) {
+        const int b = static_cast<int>(i % nbuf);
+        const int64_t n = std::min(chunk, rows - r0);
+        const size_t bytes = static_cast<size_t>(n * row_bytes);
+        char *buf = wsb + b * per;
+        // upload (after the buffer's previous download)
+        if ((i >= nbuf && cudaStreamWaitEvent(hp->in, hp->drained[b], 0) != cudaSuccess) ||
+            cudaMemcpyAsync(buf, xh + r0 * row_bytes, bytes, cudaMemcpyHostToDevice, hp->in) !=
+                cudaSuccess ||
+            cudaEventRecord(hp->loaded[b], hp->in) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        // normalise in place on the caller's stream
+        if (cudaStreamWaitEvent(cs, hp->loaded[b], 0) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        rc = launch(buf, weight, buf, n, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                    0u, g_wait_limit.load());
+        if (rc != RMSNORM_OK)
+            return rc;
+        if (cudaEventRecord(hp->computed[b], cs) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        // download
+        if (cudaStreamWaitEvent(hp->out, hp->computed[b], 0) != cudaSuccess ||
+            cudaMemcpyAsync(yh + r0 * row_bytes, buf, bytes, cudaMemcpyDeviceToHost, hp->out) !=
+                cudaSuccess ||
+            cudaEventRecord(hp->drained[b], hp->out) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+    }
+    // The caller's stream resumes after the last download.
+    const int last = static_cast<int>((i - 1) % nbuf);
+    if (cudaStreamWaitEvent(cs, hp->drained[last], 0) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
 }
 
 int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows, int64_t hidden,

@@ -204,7 +204,9 @@ int tpr_for(int64_t nvec, int nv)
 int plan_decode(const Shape &s, int variant, rmsnorm_plan_t *p)
 {
     const int64_t nvec16 = s.row_bytes / 16;
-    const bool vb32 = s.a32 && nvec16 >= 640;
+    // 32-byte vectors (half the threads) for long rows, and for 64+ rows,
+    // where the row count is close to the SM count.
+    const bool vb32 = s.a32 && (nvec16 >= 640 || (s.rows >= 64 && nvec16 >= 128));
     const int vb = vb32 ? 32 : 16;
     const int64_t nvec = s.row_bytes / vb;
     struct Opt { int nv, maxt, minb; };
@@ -248,15 +250,18 @@ int plan_prefill_mid(const Shape &s, int variant, bool persistent, rmsnorm_plan_
     }
     if (best < 0)
         return RMSNORM_ERR_VARIANT;
-    const Opt &o = opts[best];
-    // Blocks of <= 96 threads are launched on a capped grid (16 per SM,
-    // grid-stride): tens of thousands of tiny blocks cost more to schedule
-    // than the rows they carry.
+    // Many rows on blocks of <= 96 threads: 64-thread blocks with 4 vectors
+    // each on a capped grid (16 per SM, grid-stride) -- tens of thousands of
+    // tiny blocks cost more to schedule than the rows they carry.
     int64_t cap = INT_MAX;
+    if (!persistent && best_tpr <= 96 && s.rows > 32768 && tpr_for(nvec, 4) <= 64) {
+        best = 2;
+        best_tpr = tpr_for(nvec, 4);
+        cap = int64_t(s.sm_count) * 16;
+    }
+    const Opt &o = opts[best];
     if (persistent)
         cap = int64_t(s.sm_count) * blocks_per_sm(best_tpr, o.maxt, o.minb);
-    else if (best_tpr <= 96)
-        cap = int64_t(s.sm_count) * 16;
     return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap,
                           cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : variant, p);
 }
@@ -444,7 +449,10 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         }
         if (plan_decode(s, RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
             return RMSNORM_OK;
-        // Rows too long for one block's registers: as for prefill below.
+        // Rows too long for one block's registers: the looped body, one
+        // 512-thread block per row.
+        if (plan_looped(s, RMSNORM_VARIANT_PERSISTENT, false, out) == RMSNORM_OK)
+            return RMSNORM_OK;
     }
     // Prefill.  Short rows: lane groups of one warp, several rows per warp.
     if (nvec > 1024)

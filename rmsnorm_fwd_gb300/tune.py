@@ -181,6 +181,35 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
     return out
 
 
+def plan_label(p: dict, kinfo: dict) -> str:
+    """Short text for a plan: variant, vector bytes, threads/row, vectors/thread,
+    block, grid, stages, register floor, cache policy."""
+    v = {1: "warp", 2: "block", 3: "staged", 4: "persistent", 5: "generic"}[p["variant"]]
+    k = kinfo[p["kernel_index"]]
+    nv = p["vecs_per_thread"] if p["variant"] != 3 else 0
+    extra = f" W{p['threads_per_row'] // 32}" if p["variant"] == 3 else f" {nv}v"
+    return (f"{v} {p['vec_bytes']}B{extra} t{p['threads_per_row']} b{p['block_threads']} "
+            f"g{p['grid']}" + (f" st{p['stages']}" if p["stages"] else "")
+            + (f" mb{k['min_blocks']}" if k["min_blocks"] else "")
+            + (f" cp{k['cache_policy']}" if k["cache_policy"] else ""))
+
+
+def summarize(path: str) -> str:
+    """Markdown table of a --grid run: per point the best plan and the
+    automatic plan."""
+    import rmsnorm_fwd_gb300 as rn
+    kinfo = {k["index"]: k for k in rn.kernels()}
+    lines = ["| bf16 hidden (row bytes) | class | rows | best us | best GB/s | best plan | "
+             "auto us | auto GB/s | auto / best |", "|" + "---|" * 9]
+    for line in open(path):
+        r = json.loads(line)
+        b, a = r["top"][0], r["auto"]
+        lines.append(f"| {r['hidden_bf16']} ({r['row_bytes']}) | {r['class']} | {r['rows']} | "
+                     f"{b['us']:.2f} | {b['GBps']:.0f} | {plan_label(b['plan'], kinfo)} | "
+                     f"{a['us']:.2f} | {a['GBps']:.0f} | {a['us'] / b['us']:.3f} |")
+    return "\n".join(lines)
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--rows", type=int, default=16384)
@@ -195,7 +224,11 @@ def main(argv=None) -> int:
     ap.add_argument("--pdl", type=int, choices=[0, 1], default=None,
                     help="programmatic dependent launch off/on (default: library setting)")
     ap.add_argument("--auto-only", action="store_true", help="time only the automatic plan")
+    ap.add_argument("--summarize", default="", help="print a markdown table of a --grid output")
     args = ap.parse_args(argv)
+    if args.summarize:
+        print(summarize(args.summarize))
+        return 0
     if args.pdl is not None:
         import rmsnorm_fwd_gb300 as rn
         rn.rmsnorm_set_pdl(bool(args.pdl))

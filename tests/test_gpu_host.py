@@ -1,0 +1,88 @@
+"""rmsnorm_fwd_host: host x / y, chunked through a caller-provided device
+workspace with upload, kernel and download overlapped; checked against the
+oracle for chunk sizes that leave ragged last chunks, one to three buffers,
+pinned and pageable host memory, in place, and zero rows."""
+import numpy as np
+import pytest
+
+import rmsnorm_fwd_gb300 as rn
+from rmsnorm_fwd_gb300 import inputs
+
+from _parity import compare, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rn.ensure_context(0)
+    yield
+    torch.cuda.synchronize()
+    assert rn.rmsnorm_get_device_status() == rn.OK
+
+
+def host_tensor(a: np.ndarray, dtype: str, pinned: bool):
+    t = torch.from_numpy(np.ascontiguousarray(a).copy())
+    if dtype != "f32":
+        t = t.view(torch.int16).view(torch.bfloat16 if dtype == "bf16" else torch.float16)
+    return t.pin_memory() if pinned else t
+
+
+def to_numpy(t, dtype: str) -> np.ndarray:
+    if dtype == "f32":
+        return t.numpy()
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+@pytest.mark.parametrize("dtype,rows,hidden,chunk,ws_rows,pinned", [
+    ("bf16", 1000, 4096, 0, 300, True),     # default chunking, three buffers
+    ("bf16", 1000, 4096, 7, 3, True),       # ragged chunks, one row per buffer
+    ("f16", 513, 2880, 64, 200, True),
+    ("f32", 77, 1000, 10, 20, True),        # two buffers
+    ("bf16", 50, 7168, 16, 1, True),        # a single buffer of one row
+    ("bf16", 333, 1025, 0, 50, True),       # ragged hidden (scalar kernel)
+    ("bf16", 200, 4096, 32, 100, False),    # pageable host memory
+])
+def test_host_pipeline_matches_oracle(dtype, rows, hidden, chunk, ws_rows, pinned):
+    es = 4 if dtype == "f32" else 2
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=rows)
+    xh = host_tensor(x_np, dtype, pinned)
+    yh = host_tensor(np.zeros_like(x_np), dtype, pinned)
+    w = to_device(w_np, dtype)
+    ws_bytes = ws_rows * hidden * es + 1024
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), yh.data_ptr(), rows, hidden, 1e-6,
+                        rn.DTYPE_CODES[dtype], ws.data_ptr(), ws_bytes, chunk, s.cuda_stream)
+    s.synchronize()
+    compare(to_numpy(yh, dtype), x_np, w_np, 1e-6, dtype)
+
+
+def test_host_pipeline_in_place_and_repeated():
+    dtype, rows, hidden = "bf16", 600, 4096
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=1)
+    w = to_device(w_np, dtype)
+    ws_bytes = 64 << 20
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(3):  # the pipeline's streams and events are reused across calls
+        xh = host_tensor(x_np, dtype, True)
+        rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), rows, hidden, 1e-6,
+                            rn.BF16, ws.data_ptr(), ws_bytes, 0, s.cuda_stream)
+        s.synchronize()
+        compare(to_numpy(xh, dtype), x_np, w_np, 1e-6, dtype)
+
+
+def test_host_pipeline_rejects_small_workspace_and_handles_zero_rows():
+    w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
+    xh = torch.zeros(4, 4096, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(rn.RmsnormError) as e:
+        rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), 4, 4096, 1e-6, rn.BF16,
+                            ws.data_ptr(), 1024, 0, torch.cuda.current_stream().cuda_stream)
+    assert e.value.status == rn.ERR_INVALID_ARG
+    rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), 0, 4096, 1e-6, rn.BF16,
+                        ws.data_ptr(), 1024, 0, torch.cuda.current_stream().cuda_stream)
