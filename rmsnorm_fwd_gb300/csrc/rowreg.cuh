@@ -20,8 +20,9 @@
 // Occupancy is what sets the bandwidth of an HBM-bound row kernel: a block
 // cannot store a row before all of it has arrived, so the bytes in flight per
 // SM are (resident rows) x (row bytes).  MINB > 0 asks the compiler for at
-// least MINB resident blocks per SM (a register cap) and loads the weight
-// after the reduction instead of holding it in registers across rows.
+// least MINB resident blocks per SM (a register cap) and, with more than one
+// vector per thread, loads the weight after the reduction instead of holding
+// it in registers across rows.
 #pragma once
 
 #include "internal.h"
@@ -51,7 +52,10 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;                     // elements per vector
     constexpr int GROUPS = BLOCK / TPR;                    // rows per block per iteration
-    constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;    // weight slice kept in registers
+    // Weight slice kept in registers (loaded before the row, off the
+    // reduction's critical path): always for one vector per thread, else
+    // only without a register cap.
+    constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0);
 
     pdl_begin();
     const int nvec = hidden / VPE;
@@ -128,7 +132,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
-    constexpr bool W_HELD = MINB == 0 && NV * VB <= 64;
+    constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0); // as above
     __shared__ float part[2][32];
 
     pdl_begin();
@@ -342,7 +346,7 @@ constexpr int kWarpBlock = 256;
         WARP_ENTRY(DT, 16, 32, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 4, 0, 0),                     \
         WARP_ENTRY(DT, 16, 32, 2, 8, 0), WARP_ENTRY(DT, 16, 32, 4, 8, 0),                     \
         WARP_ENTRY(DT, 32, 32, 1, 0, 0), WARP_ENTRY(DT, 32, 32, 2, 0, 0),                     \
-        CTA_ENTRY(DT, 16, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 1, 1024, 2, 1),                   \
+        CTA_ENTRY(DT, 16, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 1, 1024, 1, 1),                   \
         CTA_ENTRY(DT, 16, 2, 1024, 2, 1), CTA_ENTRY(DT, 32, 2, 1024, 0, 1),                   \
         CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
         CTA_ENTRY(DT, 16, 2, 256, 8, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                     \

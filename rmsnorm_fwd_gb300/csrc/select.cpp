@@ -211,7 +211,7 @@ int plan_decode(const Shape &s, int variant, rmsnorm_plan_t *p)
     const int64_t nvec = s.row_bytes / vb;
     struct Opt { int nv, maxt, minb; };
     static const Opt k16[] = {{1, 1024, 2}, {2, 1024, 2}, {4, 1024, 0}, {8, 512, 0}};
-    static const Opt k32[] = {{1, 1024, 2}, {2, 1024, 0}, {4, 512, 0}};
+    static const Opt k32[] = {{1, 1024, 1}, {2, 1024, 0}, {4, 512, 0}};
     const Opt *opts = vb32 ? k32 : k16;
     const int nopt = vb32 ? 3 : 4;
     for (int i = 0; i < nopt; ++i) {
@@ -254,12 +254,12 @@ int plan_prefill_mid(const Shape &s, int variant, bool persistent, rmsnorm_plan_
     // each on a capped grid (16 per SM, grid-stride) -- tens of thousands of
     // tiny blocks cost more to schedule than the rows they carry.
     int64_t cap = INT_MAX;
+    Opt o = opts[best];
     if (!persistent && best_tpr <= 96 && s.rows > 32768 && tpr_for(nvec, 4) <= 64) {
-        best = 2;
+        o = Opt{4, 512, 2}; // the 64-register body: measured faster here
         best_tpr = tpr_for(nvec, 4);
         cap = int64_t(s.sm_count) * 16;
     }
-    const Opt &o = opts[best];
     if (persistent)
         cap = int64_t(s.sm_count) * blocks_per_sm(best_tpr, o.maxt, o.minb);
     return plan_cta_exact(s, 16, o.nv, o.maxt, o.minb, 1, 0, best_tpr, cap,
