@@ -355,9 +355,9 @@ def run_ours(args, world, rank, local):
     status = rn.rmsnorm_get_device_status()
 
     # ---- e2e through the public API: x from pinned host memory, y back to
-    # pinned host memory, every step (rmsnorm_fwd_host: chunked upload /
-    # kernel / download pipeline through a device workspace; the weight is a
-    # resident parameter)
+    # pinned host memory, every step (rmsnorm_fwd_host: with page-locked
+    # buffers the kernel reads and writes host memory directly; the weight is
+    # a resident parameter)
     E = args.e2e_steps
     xh = x_host.pin_memory()
     yh = torch.empty_like(xh).pin_memory()
@@ -413,7 +413,8 @@ def run_ours(args, world, rank, local):
                      "kernel_ms_avg": round(max_kernel_ms, 6),
                      "kernel_ms_basis": "timed region / launches (gaps included)"},
         "e2e": {"value": round(e2e_gbs, 2) if e2e_gbs is not None else None, "unit": UNIT,
-                "steps": E, "api": "rmsnorm_fwd_host (pinned host x/y, resident weight)",
+                "steps": E, "api": "rmsnorm_fwd_host: pinned host x/y read and written by the "
+                "kernel over NVLink-C2C; weight resident on the device",
                 "h2d_bytes_per_step": int(xh.numel() * xh.element_size()),
                 "d2h_bytes_per_step": int(yh.numel() * yh.element_size())},
         "clocks": clocks,

@@ -139,14 +139,17 @@ int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_
 int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
                    float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan);
 
-/* y = RMSNorm(x) * weight for x and y in HOST memory: rows are processed in
+/* y = RMSNorm(x) * weight for x and y in HOST memory.  When both buffers
+ * are page-locked host memory mapped into the device's address space (for
+ * example from cudaHostAlloc or cudaHostRegister), the kernel reads x and
+ * writes y there directly over the CPU-GPU link (NVLink-C2C on GB300), with
+ * no staging and no use of the workspace.  Otherwise rows are processed in
  * chunks through a device workspace the caller provides, with the upload of
  * one chunk, the kernel on the previous one and the download of the one
  * before that overlapped (two internal streams of this context plus
  * `stream` for the kernels; up to three buffers carved from the workspace).
- *   x_host, y_host  host pointers, [rows, hidden] of `dtype`; pinned
- *                   (page-locked) memory lets the copies overlap, pageable
- *                   memory works but serialises; y_host may equal x_host
+ *   x_host, y_host  host pointers, [rows, hidden] of `dtype`; y_host may
+ *                   equal x_host
  *   weight          DEVICE pointer, [hidden] of `dtype`
  *   workspace       DEVICE pointer to workspace_bytes the caller owns; it
  *                   must hold at least one row (256-byte aligned slices)

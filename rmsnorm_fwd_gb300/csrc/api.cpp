@@ -79,6 +79,23 @@ void destroy_pipe(HostPipe *hp)
     delete hp;
 }
 
+// True when [p, p + bytes) is page-locked host memory that the current
+// device reaches at the same addresses.
+bool host_mapped(const void *p, int64_t bytes)
+{
+    const char *c = static_cast<const char *>(p);
+    for (const char *q : {c, c + bytes - 1}) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, q) != cudaSuccess) {
+            cudaGetLastError(); // clear the error this query may leave behind
+            return false;
+        }
+        if (a.type != cudaMemoryTypeHost || a.devicePointer != q)
+            return false;
+    }
+    return true;
+}
+
 int make_pipe(HostPipe *hp)
 {
     const unsigned ef = cudaEventDisableTiming;
@@ -358,6 +375,12 @@ int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64
         chunk = std::min(chunk, chunk_rows);
     else // about 16 chunks, so filling and draining the pipeline stay small
         chunk = std::min(chunk, std::max<int64_t>(1, (rows + 15) / 16));
+
+    // Page-locked, device-mapped host buffers: the kernel reads x and writes
+    // y in host memory directly (over the CPU-GPU link), no staging.
+    if (host_mapped(x_host, rows * row_bytes) && host_mapped(y_host, rows * row_bytes))
+        return launch(x_host, weight, y_host, rows, hidden, eps, dtype, stream,
+                      RMSNORM_VARIANT_AUTO, nullptr, 0u, g_wait_limit.load());
 
     std::lock_guard<std::mutex> plk(g_pipe_mu[dev]);
     HostPipe *hp = nullptr;

@@ -204,6 +204,10 @@ int tpr_for(int64_t nvec, int nv)
 int plan_decode(const Shape &s, int variant, rmsnorm_plan_t *p)
 {
     const int64_t nvec16 = s.row_bytes / 16;
+    // 2..8 KiB rows: the compile-time 512-thread body (idle threads beyond
+    // the row), measured 3-13% faster than a block sized to the row.
+    if (nvec16 > (s.rows >= 64 ? 256 : 128) && nvec16 <= 512)
+        return plan_cta_exact(s, 16, 1, 512, 0, 0, 512, 512, INT_MAX, variant, p);
     // 32-byte vectors (half the threads) for long rows, and for 64+ rows,
     // where the row count is close to the SM count.
     const bool vb32 = s.a32 && (nvec16 >= 640 || (s.rows >= 64 && nvec16 >= 128));

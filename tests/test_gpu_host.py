@@ -1,7 +1,9 @@
-"""rmsnorm_fwd_host: host x / y, chunked through a caller-provided device
-workspace with upload, kernel and download overlapped; checked against the
-oracle for chunk sizes that leave ragged last chunks, one to three buffers,
-pinned and pageable host memory, in place, and zero rows."""
+"""rmsnorm_fwd_host: host x / y.  Pinned (device-mapped) buffers are read and
+written by the kernel directly; pageable ones go through the chunked
+upload / kernel / download pipeline over a caller-provided device workspace.
+Checked against the oracle for both paths, chunk sizes that leave ragged
+last chunks, one to three buffers, one pinned and one pageable buffer (the
+pipeline), in place, and zero rows."""
 import numpy as np
 import pytest
 
@@ -45,6 +47,8 @@ def to_numpy(t, dtype: str) -> np.ndarray:
     ("bf16", 50, 7168, 16, 1, True),        # a single buffer of one row
     ("bf16", 333, 1025, 0, 50, True),       # ragged hidden (scalar kernel)
     ("bf16", 200, 4096, 32, 100, False),    # pageable host memory
+    ("f16", 1000, 5120, 0, 100, False),
+    ("bf16", 77, 1025, 8, 10, False),       # pageable, ragged hidden
 ])
 def test_host_pipeline_matches_oracle(dtype, rows, hidden, chunk, ws_rows, pinned):
     es = 4 if dtype == "f32" else 2
@@ -61,6 +65,20 @@ def test_host_pipeline_matches_oracle(dtype, rows, hidden, chunk, ws_rows, pinne
     compare(to_numpy(yh, dtype), x_np, w_np, 1e-6, dtype)
 
 
+def test_host_mixed_pinned_and_pageable_uses_the_pipeline():
+    dtype, rows, hidden = "bf16", 300, 2880
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=3)
+    xh = host_tensor(x_np, dtype, True)
+    yh = host_tensor(np.zeros_like(x_np), dtype, False)
+    w = to_device(w_np, dtype)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), yh.data_ptr(), rows, hidden, 1e-6, rn.BF16,
+                        ws.data_ptr(), 1 << 20, 16, s.cuda_stream)
+    s.synchronize()
+    compare(to_numpy(yh, dtype), x_np, w_np, 1e-6, dtype)
+
+
 def test_host_pipeline_in_place_and_repeated():
     dtype, rows, hidden = "bf16", 600, 4096
     x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=1)
@@ -68,8 +86,8 @@ def test_host_pipeline_in_place_and_repeated():
     ws_bytes = 64 << 20
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream()
-    for _ in range(3):  # the pipeline's streams and events are reused across calls
-        xh = host_tensor(x_np, dtype, True)
+    for pinned in (True, False, False):  # direct, then the pipeline twice (reused streams)
+        xh = host_tensor(x_np, dtype, pinned)
         rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), rows, hidden, 1e-6,
                             rn.BF16, ws.data_ptr(), ws_bytes, 0, s.cuda_stream)
         s.synchronize()
@@ -79,7 +97,7 @@ def test_host_pipeline_in_place_and_repeated():
 def test_host_pipeline_rejects_small_workspace_and_handles_zero_rows():
     w = torch.ones(4096, dtype=torch.bfloat16, device="cuda")
     ws = torch.empty(1024, dtype=torch.uint8, device="cuda")
-    xh = torch.zeros(4, 4096, dtype=torch.bfloat16).pin_memory()
+    xh = torch.zeros(4, 4096, dtype=torch.bfloat16)  # pageable: needs the workspace
     with pytest.raises(rn.RmsnormError) as e:
         rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), 4, 4096, 1e-6, rn.BF16,
                             ws.data_ptr(), 1024, 0, torch.cuda.current_stream().cuda_stream)
