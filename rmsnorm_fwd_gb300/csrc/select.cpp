@@ -208,9 +208,10 @@ int plan_decode(const Shape &s, int variant, rmsnorm_plan_t *p)
     // the row), measured 3-13% faster than a block sized to the row.
     if (nvec16 > (s.rows >= 64 ? 256 : 128) && nvec16 <= 512)
         return plan_cta_exact(s, 16, 1, 512, 0, 0, 512, 512, INT_MAX, variant, p);
-    // 32-byte vectors (half the threads) for long rows, and for 64+ rows,
-    // where the row count is close to the SM count.
-    const bool vb32 = s.a32 && (nvec16 >= 640 || (s.rows >= 64 && nvec16 >= 128));
+    // 32-byte vectors (half the threads) for 10..16 KiB rows, and for 2..4 KiB
+    // rows when there are 64+ of them (row count close to the SM count).
+    const bool vb32 = s.a32 && ((nvec16 >= 640 && nvec16 <= 1024) ||
+                                (s.rows >= 64 && nvec16 > 128 && nvec16 <= 256));
     const int vb = vb32 ? 32 : 16;
     const int64_t nvec = s.row_bytes / vb;
     struct Opt { int nv, maxt, minb; };
@@ -444,13 +445,12 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return plan_generic(s, out);
     const int64_t nvec = s.row_bytes / 16;
     if (s.rows <= s.sm_count) {
-        // Decode: rows of <= 32 vectors share a warp; longer rows get a block.
-        if (nvec <= 32) {
-            int tpr = 4;
-            while (tpr < nvec)
-                tpr *= 2;
-            return plan_warp_exact(s, tpr, 1, 0, INT_MAX, out);
-        }
+        // Decode: a whole warp per row up to 1 KiB rows (idle lanes cost less
+        // than shorter shuffle trees save); longer rows get a block.
+        if (nvec <= 32)
+            return plan_warp_exact(s, 32, 1, 0, INT_MAX, out);
+        if (nvec <= 64)
+            return plan_warp_exact(s, 32, 2, 0, INT_MAX, out);
         if (plan_decode(s, RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
             return RMSNORM_OK;
         // Rows too long for one block's registers: the looped body, one

@@ -110,7 +110,7 @@ def plan(rows, hidden, dtype, variant=rn.VARIANT_AUTO, xoff=0, sms=SMS):
 
 def test_selector_on_the_workloads():
     expect = {
-        "f32_64x128": rn.VARIANT_WARP_PER_ROW,
+        "f32_64x128": rn.VARIANT_WARP_PER_ROW,  # 512 B rows, decode-sized row count
         "embed_bf16_8192x1024": rn.VARIANT_WARP_PER_ROW,
         "prefill_bf16_16384x4096": rn.VARIANT_CTA_PER_ROW,
         "decode_bf16_1x4096": rn.VARIANT_PERSISTENT,
