@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
         for name in ("oracle_widen_array", "oracle_round_array"):
             getattr(l, name).argtypes = [vp, vp, i64, i32]
             getattr(l, name).restype = i32
+        l.oracle_qk_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32]
+        l.oracle_qk_norm.restype = i32
         l.oracle_round_value.argtypes = [ctypes.c_double, i32]
         l.oracle_round_value.restype = ctypes.c_double
         _lib = l
@@ -131,3 +133,26 @@ def round_to(v: np.ndarray, dtype) -> np.ndarray:
     out = np.empty(v.shape, dtype=_STORAGE[fmt])
     lib().oracle_round_array(_ptr(v), _ptr(out), v.size, fmt)
     return out
+
+
+def qk_norm(q: np.ndarray, k: np.ndarray, q_weight: np.ndarray, k_weight: np.ndarray,
+            tokens: int, q_heads: int, k_heads: int, head_dim: int, q_token_stride: int,
+            k_token_stride: int, weight_bias: float, eps: float, dtype) -> tuple:
+    """Per-head QK norm ("CuTeDSL at Perplexity", section "QK Norm") on copies
+    of q and k (flat storage arrays); returns the normalised copies."""
+    fmt = fmt_code(dtype)
+    qo = np.array(_check_storage(q, fmt), copy=True)
+    ko = np.array(_check_storage(k, fmt), copy=True)
+    qw = _check_storage(q_weight, fmt)
+    kw = _check_storage(k_weight, fmt)
+    if qw.size < head_dim or kw.size < head_dim:
+        raise ValueError("weights need head_dim elements")
+    if tokens > 0 and (qo.size < (tokens - 1) * q_token_stride + q_heads * head_dim
+                       or ko.size < (tokens - 1) * k_token_stride + k_heads * head_dim):
+        raise ValueError("q/k storage too small for tokens x stride")
+    rc = lib().oracle_qk_norm(_ptr(qo), _ptr(ko), _ptr(qw), _ptr(kw), tokens, q_heads, k_heads,
+                              head_dim, q_token_stride, k_token_stride, float(weight_bias),
+                              float(eps), fmt)
+    if rc != 0:
+        raise ValueError("oracle_qk_norm rejected its arguments")
+    return qo, ko

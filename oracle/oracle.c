@@ -240,3 +240,53 @@ int oracle_widen_array(const void *in, double *out, int64_t n, int fmt)
         out[i] = oracle_widen(in, i, fmt);
     return 0;
 }
+
+/* ---- per-head QK norm ----------------------------------------------------- */
+
+/*
+ * "CuTeDSL at Perplexity", section "QK Norm": every attention head of q
+ * (q_heads per token) and of k (k_heads per token) is normalised on its own,
+ * over head_dim elements, with the q or the k weight plus WEIGHT_BIAS, and
+ * the result replaces the head in place:
+ *
+ *     S = sum_d x[d]^2,  r = 1 / sqrt(S / head_dim + eps),
+ *     x[d] <- x[d] * r * (w[d] + weight_bias)
+ *
+ * Token t's heads start at element t * token_stride of q (resp. k); heads are
+ * contiguous within a token.  In binary64, rounded back nearest-even.
+ */
+static void norm_heads(void *base, const void *w, int64_t tokens, int64_t heads,
+                       int64_t head_dim, int64_t stride, double bias, double eps, int fmt)
+{
+    for (int64_t t = 0; t < tokens; ++t) {
+        for (int64_t h = 0; h < heads; ++h) {
+            const int64_t off = t * stride + h * head_dim;
+            double S = 0.0;
+            for (int64_t d = 0; d < head_dim; ++d) {
+                double xv = oracle_widen(base, off + d, fmt);
+                S += xv * xv;
+            }
+            double r = 1.0 / sqrt(S / (double)head_dim + eps);
+            for (int64_t d = 0; d < head_dim; ++d) {
+                double xv = oracle_widen(base, off + d, fmt);
+                double wv = oracle_widen(w, d, fmt) + bias;
+                oracle_store(xv * r * wv, base, off + d, fmt);
+            }
+        }
+    }
+}
+
+int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
+                   int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
+                   int64_t k_token_stride, float weight_bias, float eps, int fmt)
+{
+    if (tokens < 0 || q_heads < 0 || k_heads < 0 || head_dim <= 0 || fmt < 0 || fmt > 2)
+        return -1;
+    if (q_token_stride < q_heads * head_dim || k_token_stride < k_heads * head_dim)
+        return -1;
+    norm_heads(q, q_weight, tokens, q_heads, head_dim, q_token_stride, (double)weight_bias,
+               (double)eps, fmt);
+    norm_heads(k, k_weight, tokens, k_heads, head_dim, k_token_stride, (double)weight_bias,
+               (double)eps, fmt);
+    return 0;
+}

@@ -35,6 +35,14 @@ int oracle_widen_array(const void *in, double *out, int64_t n, int fmt);
 /* Round n binary64 values to the format (nearest-even, overflow to inf). */
 int oracle_round_array(const double *v, void *out, int64_t n, int fmt);
 
+/* Per-head QK norm, in place: each head of q and of k (head_dim contiguous
+ * elements; token t's heads start at t * token_stride) becomes
+ * x * (1 / sqrt(sum x^2 / head_dim + eps)) * (w + weight_bias), rounded
+ * nearest-even to the element format. */
+int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
+                   int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
+                   int64_t k_token_stride, float weight_bias, float eps, int fmt);
+
 /* Single-element helpers behind the array functions. */
 double oracle_widen(const void *base, int64_t index, int fmt);
 double oracle_round_value(double v, int fmt);
