@@ -166,6 +166,32 @@ int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64
                      int64_t hidden, float eps, int dtype, void *workspace,
                      size_t workspace_bytes, int64_t chunk_rows, void *stream);
 
+/* Per-head QK norm, in place ("CuTeDSL at Perplexity", section "QK Norm"):
+ * every head of q and of k is RMS-normalised over its head_dim elements,
+ *   x[d] <- (x[d] * rsqrt(sum_e x[e]^2 / head_dim + eps)) * (w[d] + weight_bias)
+ * with q_weight for q heads and k_weight for k heads, fp32 inside, rounded to
+ * the element type; q and k in one launch.
+ *   q, k            DEVICE pointers; token t's q heads are the q_heads *
+ *                   head_dim contiguous elements starting at element
+ *                   t * q_token_stride (0 = q_heads * head_dim, i.e.
+ *                   contiguous [tokens, q_heads, head_dim]); likewise k.
+ *                   Strides let q and k be views into one fused QKV buffer.
+ *   q_weight, k_weight  DEVICE pointers, [head_dim] each; may be equal
+ *   q_heads, k_heads    >= 0 (either may be 0; its pointers may then be NULL)
+ *   weight_bias     added to every weight element (0 for plain weights,
+ *                   1 for "1 + w" parameterisations)
+ *   eps             >= 0, finite
+ * Heads whose bytes start on 16-byte boundaries (pointers, head_dim and
+ * strides) take the vector kernel (a group of lanes per head); others a
+ * scalar warp-per-head kernel.  Returns RMSNORM_OK, RMSNORM_ERR_INVALID_ARG
+ * (bad sizes, a stride shorter than its heads, a missing pointer),
+ * RMSNORM_ERR_UNSUPPORTED_DTYPE, RMSNORM_ERR_ALIASING (a q head and a k head
+ * share bytes, or a weight lies inside a head), RMSNORM_ERR_NOT_INITIALIZED
+ * or RMSNORM_ERR_CUDA.  Asynchronous on `stream`. */
+int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
+                    int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
+                    int64_t k_token_stride, float weight_bias, float eps, int dtype, void *stream);
+
 /* The selector, host only (touches no memory behind the pointers and no
  * GPU): the plan rmsnorm_fwd_ex would launch for these arguments on a device
  * with `sm_count` SMs and `smem_optin` bytes of opt-in shared memory per

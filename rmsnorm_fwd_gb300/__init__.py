@@ -101,6 +101,8 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_plan": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, pp], i32),
             "rmsnorm_fwd_host": ([vp, vp, vp, i64, i64, f32, i32, vp, ctypes.c_size_t, i64, vp],
                                  i32),
+            "rmsnorm_qk_norm": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32, vp],
+                                i32),
             "rmsnorm_last_variant": ([], i32),
             "rmsnorm_kernel_count": ([], i32),
             "rmsnorm_validate_plan": ([pp, vp, vp, vp, i64, i64, i32, i32, i32], i32),
@@ -163,6 +165,38 @@ def rmsnorm_fwd_host(x_host: int, weight: int, y_host: int, rows: int, hidden: i
     _check(_load().rmsnorm_fwd_host(x_host, weight, y_host, rows, hidden, eps, dtype, workspace,
                                     workspace_bytes, chunk_rows, stream or None),
            "rmsnorm_fwd_host")
+
+
+def rmsnorm_qk_norm(q: int, k: int, q_weight: int, k_weight: int, tokens: int, q_heads: int,
+                    k_heads: int, head_dim: int, q_token_stride: int, k_token_stride: int,
+                    weight_bias: float, eps: float, dtype: int, stream: int | None) -> None:
+    """Per-head QK norm in place (device pointers as integers)."""
+    _check(_load().rmsnorm_qk_norm(q or None, k or None, q_weight or None, k_weight or None,
+                                   tokens, q_heads, k_heads, head_dim, q_token_stride,
+                                   k_token_stride, weight_bias, eps, dtype, stream or None),
+           "rmsnorm_qk_norm")
+
+
+def qk_norm(q, k, q_weight, k_weight, head_dim: int, eps: float, weight_bias: float = 0.0,
+            stream=None) -> None:
+    """In-place per-head norm of PyTorch CUDA tensors q [..., q_heads * head_dim]
+    and k [..., k_heads * head_dim] (the last dimension holds a token's heads;
+    the token dimension may be strided, e.g. views into a fused QKV tensor)."""
+    import torch
+    for t in (q, k):
+        if not t.is_cuda or t.stride(-1) != 1:
+            raise ValueError("q and k must be CUDA tensors with a contiguous last dimension")
+    tokens = q.numel() // q.shape[-1]
+    if k.numel() // k.shape[-1] != tokens:
+        raise ValueError("q and k must hold the same number of tokens")
+    qs = q.stride(-2) if q.dim() > 1 else q.shape[-1]
+    ks = k.stride(-2) if k.dim() > 1 else k.shape[-1]
+    ensure_context(q.device.index)
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device.index):
+        rmsnorm_qk_norm(q.data_ptr(), k.data_ptr(), q_weight.data_ptr(), k_weight.data_ptr(),
+                        tokens, q.shape[-1] // head_dim, k.shape[-1] // head_dim, head_dim, qs, ks,
+                        float(weight_bias), float(eps), torch_dtype_code(q.dtype), s.cuda_stream)
 
 
 def rmsnorm_plan(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int, sm_count: int,

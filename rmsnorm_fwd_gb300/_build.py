@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librmsnorm.so")
 
-SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu",
+SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu",
            "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "rowreg.cuh"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]

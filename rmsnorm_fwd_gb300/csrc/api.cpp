@@ -334,6 +334,48 @@ int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int
                   g_wait_limit.load());
 }
 
+// Whether two strided head sets can share a byte: set A is
+// {a + t * sa + [0, la)} and set B {b + t * sb + [0, lb)} for t < tokens (bytes).
+bool strided_overlap(uintptr_t a, int64_t sa, int64_t la, uintptr_t b, int64_t sb, int64_t lb,
+                     int64_t tokens)
+{
+    if (tokens <= 0 || la <= 0 || lb <= 0)
+        return false;
+    const int64_t ea = (tokens - 1) * sa + la, eb = (tokens - 1) * sb + lb;
+    if (!ranges_overlap(reinterpret_cast<const void *>(a), ea, reinterpret_cast<const void *>(b),
+                        eb))
+        return false; // the whole extents are apart
+    if (sa != sb || sa <= 0)
+        return true; // interleaved with different strides: refuse
+    // Equal strides P: some pair of tokens collides iff d + m P lies in
+    // (-lb, la) for an integer |m| < tokens, with d = b - a.
+    const int64_t d = static_cast<int64_t>(b - a), P = sa;
+    auto floor_div = [](int64_t x, int64_t y) { return x >= 0 ? x / y : -((-x + y - 1) / y); };
+    int64_t m_lo = floor_div(-lb - d, P) + 1;           // smallest m with d + mP > -lb
+    int64_t m_hi = -floor_div(-(la - d), P) - 1;        // largest m with d + mP < la
+    m_lo = std::max(m_lo, -(tokens - 1));
+    m_hi = std::min(m_hi, tokens - 1);
+    return m_lo <= m_hi;
+}
+
+// Whether the interval [w, w + wb) meets {a + t * P + [0, la)}, t < tokens.
+bool interval_hits_strided(uintptr_t a, int64_t P, int64_t la, int64_t tokens, uintptr_t w,
+                           int64_t wb)
+{
+    if (tokens <= 0 || la <= 0 || wb <= 0)
+        return false;
+    const int64_t d = static_cast<int64_t>(w - a);
+    if (P <= 0) // a single interval
+        return d < la && -d < wb;
+    // t P < d + wb and d < t P + la, for an integer t in [0, tokens)
+    auto floor_div = [](int64_t x, int64_t y) { return x >= 0 ? x / y : -((-x + y - 1) / y); };
+    int64_t t_lo = floor_div(d - la, P) + 1;   // smallest t with t P > d - la
+    int64_t t_hi = -floor_div(-(d + wb), P) - 1; // largest t with t P < d + wb
+    t_lo = std::max<int64_t>(t_lo, 0);
+    t_hi = std::min<int64_t>(t_hi, tokens - 1);
+    return t_lo <= t_hi;
+}
+
 int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64_t rows,
                      int64_t hidden, float eps, int dtype, void *workspace,
                      size_t workspace_bytes, int64_t chunk_rows, void *stream)
@@ -440,6 +482,100 @@ int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64
     // The caller's stream resumes after the last download.
     const int last = static_cast<int>((i - 1) % nbuf);
     if (cudaStreamWaitEvent(cs, hp->drained[last], 0) != cudaSuccess)
+        return RMSNORM_ERR_CUDA;
+    return RMSNORM_OK;
+}
+
+int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
+                    int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
+                    int64_t k_token_stride, float weight_bias, float eps, int dtype, void *stream)
+{
+    if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
+        return RMSNORM_ERR_UNSUPPORTED_DTYPE;
+    if (tokens < 0 || q_heads < 0 || k_heads < 0 || head_dim <= 0 || head_dim > (1 << 20) ||
+        q_heads > (1 << 20) || k_heads > (1 << 20) || !(eps >= 0.f) || !std::isfinite(eps) ||
+        !std::isfinite(weight_bias) || q_token_stride < 0 || k_token_stride < 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    const int64_t qs = q_token_stride ? q_token_stride : q_heads * head_dim;
+    const int64_t ks = k_token_stride ? k_token_stride : k_heads * head_dim;
+    if (qs < q_heads * head_dim || ks < k_heads * head_dim)
+        return RMSNORM_ERR_INVALID_ARG;
+    if ((q_heads > 0 && (!q || !q_weight)) || (k_heads > 0 && (!k || !k_weight)))
+        return RMSNORM_ERR_INVALID_ARG;
+    if (tokens > 0 && (tokens > INT64_MAX / 8 / std::max<int64_t>(qs, 1) ||
+                       tokens > INT64_MAX / 8 / std::max<int64_t>(ks, 1)))
+        return RMSNORM_ERR_INVALID_ARG;
+    const int64_t es = dtype == RMSNORM_F32 ? 4 : 2;
+    const uintptr_t qa = reinterpret_cast<uintptr_t>(q), ka = reinterpret_cast<uintptr_t>(k);
+    if (q_heads > 0 && k_heads > 0 &&
+        strided_overlap(qa, qs * es, q_heads * head_dim * es, ka, ks * es, k_heads * head_dim * es,
+                        tokens))
+        return RMSNORM_ERR_ALIASING;
+    // The weights are read-only inputs: they may not sit inside a head q or k
+    // writes.
+    const int64_t wbytes = head_dim * es;
+    for (const void *wp : {q_weight, k_weight}) {
+        if (!wp)
+            continue;
+        const uintptr_t wa = reinterpret_cast<uintptr_t>(wp);
+        if ((q_heads > 0 && interval_hits_strided(qa, qs * es, q_heads * head_dim * es, tokens, wa,
+                                                  wbytes)) ||
+            (k_heads > 0 && interval_hits_strided(ka, ks * es, k_heads * head_dim * es, tokens, wa,
+                                                  wbytes)))
+            return RMSNORM_ERR_ALIASING;
+    }
+    DeviceCtx ctx;
+    int rc = current_ctx(&ctx, nullptr);
+    if (rc != RMSNORM_OK)
+        return rc;
+    const int64_t heads = q_heads + k_heads;
+    if (tokens == 0 || heads == 0)
+        return RMSNORM_OK;
+
+    // Vector body when every head starts on a 16-byte boundary.
+    auto al = [](const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    const bool vec = (head_dim * es) % 16 == 0 && (qs * es) % 16 == 0 && (ks * es) % 16 == 0 &&
+                     (q_heads == 0 || (al(q) && al(q_weight))) &&
+                     (k_heads == 0 || (al(k) && al(k_weight)));
+    int tpr = 0, nv = 0;
+    if (vec) {
+        const int64_t nvec = head_dim * es / 16;
+        static const int kOpt[][2] = {{4, 1}, {8, 1}, {16, 1}, {32, 1}, {32, 2}, {32, 4}};
+        for (const auto &o : kOpt)
+            if (int64_t(o[0]) * o[1] >= nvec) {
+                tpr = o[0];
+                nv = o[1];
+                break;
+            }
+    }
+    int n = 0;
+    const QkKernel *t = qk_kernels(&n);
+    const QkKernel *kern = nullptr;
+    for (int i = 0; i < n; ++i)
+        if (t[i].dtype == dtype && t[i].tpr == tpr && t[i].nv == nv)
+            kern = &t[i];
+    if (!kern)
+        return RMSNORM_ERR_VARIANT;
+    QkArgs a;
+    a.base = LaunchArgs{};
+    a.base.stream = static_cast<cudaStream_t>(stream);
+    a.base.pdl = pdl_enabled();
+    a.q = q;
+    a.k = k;
+    a.qw = q_weight;
+    a.kw = k_weight;
+    a.tokens = tokens;
+    a.q_heads = static_cast<int32_t>(q_heads);
+    a.k_heads = static_cast<int32_t>(k_heads);
+    a.head_dim = static_cast<int32_t>(head_dim);
+    a.q_stride = qs;
+    a.k_stride = ks;
+    a.bias = weight_bias;
+    a.eps = eps;
+    const int64_t per_block = tpr ? 256 / tpr : 8;
+    const int64_t blocks = (tokens * heads + per_block - 1) / per_block;
+    a.grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(ctx.sm_count) * 16));
+    if (kern->launch(a) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
 }

@@ -103,6 +103,32 @@ RMSNORM_HD inline StagedLayout staged_layout(int32_t row_bytes, int32_t stages)
     return L;
 }
 
+// Per-head QK norm (qknorm.cu).
+struct QkArgs {
+    LaunchArgs base; // stream and launch attributes
+    void *q;
+    void *k;
+    const void *qw;
+    const void *kw;
+    int64_t tokens;
+    int32_t q_heads;
+    int32_t k_heads;
+    int32_t head_dim;
+    int64_t q_stride; // elements between tokens
+    int64_t k_stride;
+    float bias;
+    float eps;
+    int grid;
+};
+using QkLaunchFn = cudaError_t (*)(const QkArgs &);
+struct QkKernel {
+    int32_t dtype;
+    int32_t tpr; // lanes per head; 0 = scalar warp-per-head body
+    int32_t nv;  // 16-byte vectors per lane
+    QkLaunchFn launch;
+};
+const QkKernel *qk_kernels(int *n);
+
 // Host-side selector (select.cpp).
 int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
                 int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out);

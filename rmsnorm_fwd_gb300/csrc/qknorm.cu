@@ -1,0 +1,178 @@
+// qknorm.cu -- per-head QK norm ("CuTeDSL at Perplexity", section "QK
+// Norm"): every head of q and of k is RMS-normalised over head_dim with the q
+// or k weight plus WEIGHT_BIAS, in place, in one launch for both tensors.
+//
+// A head is a short row (64..256 elements), so TPR lanes of one warp own it
+// (TPR = 16 for a 128-element bf16 head, the page's half warp), NV 16-byte
+// vectors per lane, and 256 / TPR heads share a block.  Head h of token t:
+// h < q_heads -> q + t * q_token_stride + h * head_dim, else k (strides let q
+// and k be views into a fused QKV buffer).  Each lane always touches the
+// same vector positions of a head, so both weight slices stay in registers.
+// The reduction is the butterfly shuffle over the TPR lanes; the statistic
+// never leaves registers.
+#include "internal.h"
+#include "device_common.cuh"
+
+namespace rmsnorm {
+namespace {
+
+template <int DT>
+__device__ inline void scale_bias(Vec<16> &out, const Vec<16> &xv, const Vec<16> &wv, float r,
+                                  float bias)
+{
+#pragma unroll
+    for (int k = 0; k < Vec<16>::kWords; ++k) {
+        float xa, xb = 0.f, wa, wb = 0.f;
+        Elem<DT>::widen(xv.w[k], xa, xb);
+        Elem<DT>::widen(wv.w[k], wa, wb);
+        out.w[k] = Elem<DT>::narrow((xa * r) * (wa + bias), (xb * r) * (wb + bias));
+    }
+}
+
+__device__ inline void vzero16(Vec<16> &v)
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        v.w[k] = 0u;
+}
+
+template <int DT, int TPR, int NV>
+__global__ void __launch_bounds__(256)
+qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__restrict__ kw,
+               int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
+               int64_t q_stride, int64_t k_stride, float bias, float eps)
+{
+    using E = Elem<DT>;
+    constexpr int VPE = 16 / E::kSize;
+    constexpr int GROUPS = 256 / TPR;
+
+    pdl_begin();
+    const int nvec = head_dim / VPE;
+    const int t = threadIdx.x % TPR;
+    const int g = threadIdx.x / TPR;
+    const int heads = q_heads + k_heads;
+    const int64_t total = tokens * heads;
+    const float n = static_cast<float>(head_dim);
+
+    Vec<16> wq[NV], wk[NV];
+#pragma unroll
+    for (int j = 0; j < NV; ++j) {
+        const int v = t + j * TPR;
+        if (v < nvec && q_heads > 0)
+            ld_weight(wq[j], static_cast<const char *>(qw) + v * 16);
+        else
+            vzero16(wq[j]);
+        if (v < nvec && k_heads > 0)
+            ld_weight(wk[j], static_cast<const char *>(kw) + v * 16);
+        else
+            vzero16(wk[j]);
+    }
+
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * GROUPS; base < total;
+         base += static_cast<int64_t>(gridDim.x) * GROUPS) {
+        const int64_t row = base + g;
+        const bool active = row < total;
+        const int64_t tok = active ? row / heads : 0;
+        const int h = active ? static_cast<int>(row - tok * heads) : 0;
+        const bool isq = h < q_heads;
+        char *head = isq ? static_cast<char *>(q) + (tok * q_stride + int64_t(h) * head_dim) *
+                               E::kSize
+                         : static_cast<char *>(k) +
+                               (tok * k_stride + int64_t(h - q_heads) * head_dim) * E::kSize;
+        char *ht = head + t * 16;
+
+        Vec<16> xv[NV];
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (active && t + j * TPR < nvec)
+                ld_stream<0>(xv[j], ht + j * TPR * 16);
+            else
+                vzero16(xv[j]);
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int j = 0; j < NV; ++j)
+            s = sumsq<DT, 16>(xv[j], s);
+        s = group_allreduce<TPR>(s);
+        const float r = row_factor(s, n, eps);
+#pragma unroll
+        for (int j = 0; j < NV; ++j) {
+            if (active && t + j * TPR < nvec) {
+                Vec<16> o;
+                scale_bias<DT>(o, xv[j], isq ? wq[j] : wk[j], r, bias);
+                st_stream<0>(ht + j * TPR * 16, o);
+            }
+        }
+    }
+}
+
+// Any alignment / head size: a warp per head, scalar accesses, two passes
+// (the second re-reads the head from L1).
+template <int DT>
+__global__ void __launch_bounds__(256)
+qk_norm_scalar_kernel(void *q, void *k, const void *__restrict__ qw, const void *__restrict__ kw,
+                      int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
+                      int64_t q_stride, int64_t k_stride, float bias, float eps)
+{
+    using E = Elem<DT>;
+    pdl_begin();
+    const int lane = threadIdx.x & 31;
+    const int warps = blockDim.x >> 5;
+    const int heads = q_heads + k_heads;
+    const int64_t total = tokens * heads;
+    const float n = static_cast<float>(head_dim);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * warps + (threadIdx.x >> 5); row < total;
+         row += static_cast<int64_t>(gridDim.x) * warps) {
+        const int64_t tok = row / heads;
+        const int h = static_cast<int>(row - tok * heads);
+        const bool isq = h < q_heads;
+        void *base = isq ? q : k;
+        const void *w = isq ? qw : kw;
+        const int64_t off =
+            isq ? tok * q_stride + int64_t(h) * head_dim : tok * k_stride + int64_t(h - q_heads) * head_dim;
+        float s = 0.f;
+        for (int d = lane; d < head_dim; d += 32) {
+            const float v = E::widen1(base, off + d);
+            s = fmaf(v, v, s);
+        }
+        s = group_allreduce<32>(s);
+        const float r = row_factor(s, n, eps);
+        for (int d = lane; d < head_dim; d += 32) {
+            const float v = E::widen1(base, off + d);
+            E::store1(base, off + d, (v * r) * (E::widen1(w, d) + bias));
+        }
+    }
+}
+
+template <int DT, int TPR, int NV>
+cudaError_t launch_qk(const QkArgs &a)
+{
+    return launch_kernel(qk_norm_kernel<DT, TPR, NV>, a.grid, 256, 0, a.base, a.q, a.k, a.qw,
+                         a.kw, a.tokens, a.q_heads, a.k_heads, a.head_dim, a.q_stride,
+                         a.k_stride, a.bias, a.eps);
+}
+
+template <int DT>
+cudaError_t launch_qk_scalar(const QkArgs &a)
+{
+    return launch_kernel(qk_norm_scalar_kernel<DT>, a.grid, 256, 0, a.base, a.q, a.k, a.qw, a.kw,
+                         a.tokens, a.q_heads, a.k_heads, a.head_dim, a.q_stride, a.k_stride,
+                         a.bias, a.eps);
+}
+
+#define QK_ENTRY(DT, TPR, NV) QkKernel{DT, TPR, NV, &launch_qk<DT, TPR, NV>}
+#define QK_SET(DT)                                                                             \
+    QK_ENTRY(DT, 4, 1), QK_ENTRY(DT, 8, 1), QK_ENTRY(DT, 16, 1), QK_ENTRY(DT, 32, 1),         \
+        QK_ENTRY(DT, 32, 2), QK_ENTRY(DT, 32, 4), QkKernel{DT, 0, 0, &launch_qk_scalar<DT>}
+
+const QkKernel kTable[] = {QK_SET(RMSNORM_F32), QK_SET(RMSNORM_BF16), QK_SET(RMSNORM_F16)};
+
+} // namespace
+
+const QkKernel *qk_kernels(int *n)
+{
+    *n = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
+    return kTable;
+}
+
+} // namespace rmsnorm

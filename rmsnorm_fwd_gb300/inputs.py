@@ -166,3 +166,55 @@ def random_case(rows: int, hidden: int, dtype: str, seed: int, scale: float = 1.
     zr = _rng(seed, wl.key, rows)
     z = zr.standard_normal((rows, hidden), dtype=np.float32) * np.float32(scale)
     return to_storage(z, dtype), _draw_weight(wl, _rng(seed, wl.key, 10**6 + rows))
+
+
+@dataclass(frozen=True)
+class QkWorkload:
+    """Per-head QK norm shapes: q and k heads of a fused [q | k | v] buffer per
+    token (v as wide as k), x ~ N(0,1), weights ~ N(1,0.1)."""
+    name: str
+    dtype: str
+    tokens: int
+    q_heads: int
+    k_heads: int
+    head_dim: int
+    eps: float
+    key: int
+
+    @property
+    def width(self) -> int:
+        return (self.q_heads + 2 * self.k_heads) * self.head_dim
+
+    @property
+    def bytes_per_call(self) -> int:
+        s = ITEMSIZE[self.dtype]
+        return 2 * self.tokens * (self.q_heads + self.k_heads) * self.head_dim * s \
+            + 2 * self.head_dim * s
+
+
+QK_WORKLOADS: dict[str, QkWorkload] = {
+    w.name: w for w in (
+        QkWorkload("qk_bf16_16384tok_32q8k_128", "bf16", 16384, 32, 8, 128, 1e-6, 70),
+        QkWorkload("qk_bf16_32tok_32q8k_128", "bf16", 32, 32, 8, 128, 1e-6, 71),
+        QkWorkload("qk_bf16_16384tok_64q4k_128", "bf16", 16384, 64, 4, 128, 1e-6, 72),
+        QkWorkload("qk_bf16_8192tok_16q8k_256", "bf16", 8192, 16, 8, 256, 1e-6, 73),
+    )
+}
+
+
+def make_qk_inputs(wl: QkWorkload, seed: int = 0):
+    """(qkv [tokens * width] storage, q weight [head_dim], k weight [head_dim])."""
+    zr = _rng(seed, wl.key, 0)
+    buf = np.empty(wl.tokens * wl.width, dtype=STORAGE[wl.dtype])
+    step = _BLOCK_ROWS * wl.width
+    for o in range(0, buf.size, step):
+        n = min(step, buf.size - o)
+        buf[o:o + n] = to_storage(zr.standard_normal(n, dtype=np.float32), wl.dtype)
+    wr = _rng(seed, wl.key, 1)
+    qw = to_storage(np.float32(1) + np.float32(0.1) * wr.standard_normal(wl.head_dim,
+                                                                           dtype=np.float32),
+                    wl.dtype)
+    kw = to_storage(np.float32(1) + np.float32(0.1) * wr.standard_normal(wl.head_dim,
+                                                                           dtype=np.float32),
+                    wl.dtype)
+    return buf, qw, kw

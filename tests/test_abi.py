@@ -265,3 +265,64 @@ def test_validation_rejects_bad_plans():
     bad = rn.Plan(**sp.as_dict())
     bad.stages += 1  # no longer a multiple of the consumer count
     assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, 4096, 4096, rn.BF16, SMS, OPTIN) != rn.OK
+
+
+# ------------------------------------------------------------- QK norm validation (host only)
+
+def qk(q, k, qw, kw, tokens, hq, hk, d, qs, ks, bias=0.0, eps=1e-6, dtype=rn.BF16):
+    return rn._load().rmsnorm_qk_norm(q, k, qw, kw, tokens, hq, hk, d, qs, ks, bias, eps, dtype,
+                                      None)
+
+
+VALIDATED = (rn.ERR_CUDA, rn.ERR_NOT_INITIALIZED, rn.OK)  # got past argument checks
+
+
+def test_qk_norm_argument_checks():
+    Q, K, W = 1 << 40, 1 << 41, 1 << 42
+    assert qk(Q, K, W, W, 4, 8, 2, 128, 0, 0) in VALIDATED
+    assert qk(Q, K, W, W, 4, 8, 2, 128, 0, 0, dtype=9) == rn.ERR_UNSUPPORTED_DTYPE
+    assert qk(Q, K, W, W, -1, 8, 2, 128, 0, 0) == rn.ERR_INVALID_ARG
+    assert qk(Q, K, W, W, 4, 8, 2, 0, 0, 0) == rn.ERR_INVALID_ARG
+    assert qk(Q, K, W, W, 4, 8, 2, 128, 8 * 128 - 1, 0) == rn.ERR_INVALID_ARG  # stride < heads
+    assert qk(Q, K, W, W, 4, 8, 2, 128, 0, 0, eps=-1.0) == rn.ERR_INVALID_ARG
+    assert qk(Q, K, W, W, 4, 8, 2, 128, 0, 0, bias=float("inf")) == rn.ERR_INVALID_ARG
+    assert qk(0, K, W, W, 4, 8, 2, 128, 0, 0) == rn.ERR_INVALID_ARG
+    assert qk(0, K, 0, W, 4, 0, 2, 128, 0, 0) in VALIDATED  # no q heads: q may be NULL
+
+
+def test_qk_norm_fused_qkv_layout_accepted_overlaps_refused():
+    B, W = 1 << 40, 1 << 42
+    d, hq, hk, T = 128, 8, 2, 1000
+    width = (hq + 2 * hk) * d
+    es = 2
+    # q at the token's start, k right after q, v after k: disjoint, accepted
+    assert qk(B, B + hq * d * es, W, W, T, hq, hk, d, width, width) in VALIDATED
+    # k starting inside the q heads: refused
+    assert qk(B, B + (hq - 1) * d * es, W, W, T, hq, hk, d, width, width) == rn.ERR_ALIASING
+    # k one token later but overlapping the next token's q heads: refused
+    assert qk(B, B + width * es, W, W, T, hq, hk, d, width, width) == rn.ERR_ALIASING
+    # a weight inside a q head: refused
+    assert qk(B, B + hq * d * es, B + 5 * width * es + 64, W, T, hq, hk, d, width, width) == \
+        rn.ERR_ALIASING
+    # a weight in the v slot (not written): accepted
+    assert qk(B, B + hq * d * es, B + (hq + hk) * d * es, W, T, hq, hk, d, width, width) in \
+        VALIDATED
+
+
+def test_qk_norm_overlap_rule_matches_brute_force():
+    """The strided-overlap test inside rmsnorm_qk_norm against an explicit
+    byte-set intersection on small random layouts (equal strides)."""
+    import random
+    rnd = random.Random(0)
+    B, W = 1 << 40, 1 << 44
+    for _ in range(400):
+        d = rnd.choice([1, 2, 3, 8])
+        hq, hk = rnd.randint(1, 3), rnd.randint(1, 3)
+        T = rnd.randint(1, 5)
+        stride = (hq + hk) * d + rnd.randint(0, 6)
+        off = rnd.randint(-3 * stride, 3 * stride)
+        qset = {t * stride + e for t in range(T) for e in range(hq * d)}
+        kset = {off + t * stride + e for t in range(T) for e in range(hk * d)}
+        collide = bool(qset & kset)
+        rc = qk(B, B + 2 * off, W, W, T, hq, hk, d, stride, stride)
+        assert (rc == rn.ERR_ALIASING) == collide, (d, hq, hk, T, stride, off, rc)
