@@ -141,10 +141,10 @@ def test_qk_workloads_sampled_tokens(name):
     d, hq, hk, T, width = wl.head_dim, wl.q_heads, wl.k_heads, wl.tokens, wl.width
     dbuf = to_device(buf, wl.dtype)
     es = dbuf.element_size()
-    rn.rmsnorm_qk_norm(dbuf.data_ptr(), dbuf.data_ptr() + hq * d * es,
-                       to_device(qw, wl.dtype).data_ptr(), to_device(kw, wl.dtype).data_ptr(), T,
-                       hq, hk, d, width, width, 0.0, wl.eps, rn.DTYPE_CODES[wl.dtype],
-                       torch.cuda.current_stream().cuda_stream)
+    dqw, dkw = to_device(qw, wl.dtype), to_device(kw, wl.dtype)  # kept alive over the launch
+    rn.rmsnorm_qk_norm(dbuf.data_ptr(), dbuf.data_ptr() + hq * d * es, dqw.data_ptr(),
+                       dkw.data_ptr(), T, hq, hk, d, width, width, 0.0, wl.eps,
+                       rn.DTYPE_CODES[wl.dtype], torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     got = from_device(dbuf, wl.dtype).reshape(T, width)
     rows = buf.reshape(T, width)
