@@ -192,6 +192,26 @@ int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight
                     int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
                     int64_t k_token_stride, float weight_bias, float eps, int dtype, void *stream);
 
+/* Launch shape of rmsnorm_qk_norm_ex: lanes_per_head lanes of a warp own a
+ * head (-1: the scalar warp-per-head body), each with vecs_per_lane 16-byte
+ * vectors; a lane group takes heads_per_group heads per iteration of a
+ * grid-stride loop over grid blocks of 256 threads. */
+typedef struct {
+    int32_t lanes_per_head;
+    int32_t vecs_per_lane;
+    int32_t heads_per_group;
+    int32_t grid;
+} rmsnorm_qk_plan_t;
+
+/* rmsnorm_qk_norm with a launch shape: plan == NULL or
+ * plan->lanes_per_head == 0 chooses automatically (and, with a plan, writes
+ * the choice back); otherwise the given shape is launched if a compiled body
+ * matches it and its vectors cover the head (else RMSNORM_ERR_VARIANT). */
+int rmsnorm_qk_norm_ex(void *q, void *k, const void *q_weight, const void *k_weight,
+                       int64_t tokens, int64_t q_heads, int64_t k_heads, int64_t head_dim,
+                       int64_t q_token_stride, int64_t k_token_stride, float weight_bias,
+                       float eps, int dtype, void *stream, rmsnorm_qk_plan_t *plan);
+
 /* The selector, host only (touches no memory behind the pointers and no
  * GPU): the plan rmsnorm_fwd_ex would launch for these arguments on a device
  * with `sm_count` SMs and `smem_optin` bytes of opt-in shared memory per

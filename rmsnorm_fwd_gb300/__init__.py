@@ -62,6 +62,15 @@ class Plan(ctypes.Structure):
         return {name: getattr(self, name) for name, _ in self._fields_}
 
 
+class QkPlan(ctypes.Structure):
+    """rmsnorm_qk_plan_t."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "lanes_per_head", "vecs_per_lane", "heads_per_group", "grid")]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
 class KernelInfo(ctypes.Structure):
     """rmsnorm_kernel_info_t."""
     _fields_ = [(name, ctypes.c_int32) for name in (
@@ -103,6 +112,8 @@ def _load() -> ctypes.CDLL:
                                  i32),
             "rmsnorm_qk_norm": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32, vp],
                                 i32),
+            "rmsnorm_qk_norm_ex": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32, vp,
+                                    ctypes.POINTER(QkPlan)], i32),
             "rmsnorm_last_variant": ([], i32),
             "rmsnorm_kernel_count": ([], i32),
             "rmsnorm_validate_plan": ([pp, vp, vp, vp, i64, i64, i32, i32, i32], i32),
@@ -175,6 +186,18 @@ def rmsnorm_qk_norm(q: int, k: int, q_weight: int, k_weight: int, tokens: int, q
                                    tokens, q_heads, k_heads, head_dim, q_token_stride,
                                    k_token_stride, weight_bias, eps, dtype, stream or None),
            "rmsnorm_qk_norm")
+
+
+def rmsnorm_qk_norm_ex(q: int, k: int, q_weight: int, k_weight: int, tokens: int, q_heads: int,
+                       k_heads: int, head_dim: int, q_token_stride: int, k_token_stride: int,
+                       weight_bias: float, eps: float, dtype: int, stream: int | None,
+                       plan: QkPlan | None = None) -> QkPlan | None:
+    _check(_load().rmsnorm_qk_norm_ex(q or None, k or None, q_weight or None, k_weight or None,
+                                      tokens, q_heads, k_heads, head_dim, q_token_stride,
+                                      k_token_stride, weight_bias, eps, dtype, stream or None,
+                                      ctypes.byref(plan) if plan is not None else None),
+           "rmsnorm_qk_norm_ex")
+    return plan
 
 
 def qk_norm(q, k, q_weight, k_weight, head_dim: int, eps: float, weight_bias: float = 0.0,

@@ -2,6 +2,7 @@
 // validation, plan selection and the launch.
 #include <algorithm>
 #include <atomic>
+#include <climits>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -486,9 +487,10 @@ int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64
     return RMSNORM_OK;
 }
 
-int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
-                    int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
-                    int64_t k_token_stride, float weight_bias, float eps, int dtype, void *stream)
+int rmsnorm_qk_norm_ex(void *q, void *k, const void *q_weight, const void *k_weight,
+                       int64_t tokens, int64_t q_heads, int64_t k_heads, int64_t head_dim,
+                       int64_t q_token_stride, int64_t k_token_stride, float weight_bias,
+                       float eps, int dtype, void *stream, rmsnorm_qk_plan_t *plan)
 {
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
         return RMSNORM_ERR_UNSUPPORTED_DTYPE;
@@ -537,25 +539,58 @@ int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight
     const bool vec = (head_dim * es) % 16 == 0 && (qs * es) % 16 == 0 && (ks * es) % 16 == 0 &&
                      (q_heads == 0 || (al(q) && al(q_weight))) &&
                      (k_heads == 0 || (al(k) && al(k_weight)));
-    int tpr = 0, nv = 0;
-    if (vec) {
-        const int64_t nvec = head_dim * es / 16;
-        static const int kOpt[][2] = {{4, 1}, {8, 1}, {16, 1}, {32, 1}, {32, 2}, {32, 4}};
-        for (const auto &o : kOpt)
-            if (int64_t(o[0]) * o[1] >= nvec) {
-                tpr = o[0];
-                nv = o[1];
-                break;
-            }
-    }
+    const int64_t total = tokens * heads;
     int n = 0;
     const QkKernel *t = qk_kernels(&n);
     const QkKernel *kern = nullptr;
-    for (int i = 0; i < n; ++i)
-        if (t[i].dtype == dtype && t[i].tpr == tpr && t[i].nv == nv)
-            kern = &t[i];
-    if (!kern)
-        return RMSNORM_ERR_VARIANT;
+    int64_t grid = 0;
+    const bool explicit_plan = plan && plan->lanes_per_head != 0;
+    if (explicit_plan) {
+        // A caller's plan (tuning sweeps): the vector body it names must cover
+        // the head and the heads must be 16-byte aligned; -1 lanes = scalar.
+        const int lanes = plan->lanes_per_head < 0 ? 0 : plan->lanes_per_head;
+        for (int i = 0; i < n; ++i)
+            if (t[i].dtype == dtype && t[i].tpr == lanes && t[i].nv == plan->vecs_per_lane &&
+                t[i].rpg == plan->heads_per_group)
+                kern = &t[i];
+        if (!kern || plan->grid < 1)
+            return RMSNORM_ERR_VARIANT;
+        if (kern->tpr > 0 && (!vec || int64_t(kern->tpr) * kern->nv * 16 < head_dim * es))
+            return RMSNORM_ERR_VARIANT;
+        grid = plan->grid;
+    } else {
+        // Automatic (from a sweep of every compiled shape on GB300): two
+        // 16-byte vectors per lane (8 lanes for a 128-element bf16 head, 16
+        // for 256), one head per group per iteration, and for many heads a
+        // grid of 8 blocks per SM looping over them.
+        int tpr = 0, nv = 0, rpg = 1;
+        if (vec) {
+            const int64_t nvec = head_dim * es / 16;
+            static const int kOpt[][3] = {{4, 1, 1}, {4, 2, 1}, {8, 2, 1}, {16, 2, 1},
+                                          {32, 2, 1}, {32, 4, 1}};
+            for (const auto &o : kOpt)
+                if (int64_t(o[0]) * o[1] >= nvec) {
+                    tpr = o[0];
+                    nv = o[1];
+                    rpg = o[2];
+                    break;
+                }
+        }
+        for (int i = 0; i < n; ++i)
+            if (t[i].dtype == dtype && t[i].tpr == tpr && t[i].nv == (tpr ? nv : 0) &&
+                t[i].rpg == (tpr ? rpg : 1))
+                kern = &t[i];
+        if (!kern)
+            return RMSNORM_ERR_VARIANT;
+        const int64_t per_block = kern->tpr ? int64_t(256 / kern->tpr) * kern->rpg : 8;
+        grid = std::min<int64_t>((total + per_block - 1) / per_block, int64_t(ctx.sm_count) * 8);
+        if (plan) {
+            plan->lanes_per_head = kern->tpr ? kern->tpr : -1;
+            plan->vecs_per_lane = kern->nv;
+            plan->heads_per_group = kern->rpg;
+            plan->grid = static_cast<int32_t>(grid);
+        }
+    }
     QkArgs a;
     a.base = LaunchArgs{};
     a.base.stream = static_cast<cudaStream_t>(stream);
@@ -572,12 +607,19 @@ int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight
     a.k_stride = ks;
     a.bias = weight_bias;
     a.eps = eps;
-    const int64_t per_block = tpr ? 256 / tpr : 8;
-    const int64_t blocks = (tokens * heads + per_block - 1) / per_block;
-    a.grid = static_cast<int>(std::min<int64_t>(blocks, int64_t(ctx.sm_count) * 16));
+    a.grid = static_cast<int>(grid);
     if (kern->launch(a) != cudaSuccess)
         return RMSNORM_ERR_CUDA;
     return RMSNORM_OK;
+}
+
+int rmsnorm_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight, int64_t tokens,
+                    int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
+                    int64_t k_token_stride, float weight_bias, float eps, int dtype, void *stream)
+{
+    return rmsnorm_qk_norm_ex(q, k, q_weight, k_weight, tokens, q_heads, k_heads, head_dim,
+                              q_token_stride, k_token_stride, weight_bias, eps, dtype, stream,
+                              nullptr);
 }
 
 int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows, int64_t hidden,

@@ -125,6 +125,7 @@ struct QkKernel {
     int32_t dtype;
     int32_t tpr; // lanes per head; 0 = scalar warp-per-head body
     int32_t nv;  // 16-byte vectors per lane
+    int32_t rpg; // heads a lane group takes per iteration
     QkLaunchFn launch;
 };
 const QkKernel *qk_kernels(int *n);

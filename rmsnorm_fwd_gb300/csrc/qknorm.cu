@@ -3,8 +3,9 @@
 // or k weight plus WEIGHT_BIAS, in place, in one launch for both tensors.
 //
 // A head is a short row (64..256 elements), so TPR lanes of one warp own it
-// (TPR = 16 for a 128-element bf16 head, the page's half warp), NV 16-byte
-// vectors per lane, and 256 / TPR heads share a block.  Head h of token t:
+// (the page uses a half warp with one 16-byte vector per lane for a
+// 128-element bf16 head; on GB300 8 lanes with two vectors each measure
+// faster), NV 16-byte vectors per lane, and 256 / TPR heads share a block.  Head h of token t:
 // h < q_heads -> q + t * q_token_stride + h * head_dim, else k (strides let q
 // and k be views into a fused QKV buffer).  Each lane always touches the
 // same vector positions of a head, so both weight slices stay in registers.
@@ -36,7 +37,7 @@ __device__ inline void vzero16(Vec<16> &v)
         v.w[k] = 0u;
 }
 
-template <int DT, int TPR, int NV>
+template <int DT, int TPR, int NV, int RPG>
 __global__ void __launch_bounds__(256)
 qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__restrict__ kw,
                int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
@@ -52,6 +53,7 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
     const int g = threadIdx.x / TPR;
     const int heads = q_heads + k_heads;
     const int64_t total = tokens * heads;
+    const bool small = total < (int64_t(1) << 31); // 32-bit head index arithmetic
     const float n = static_cast<float>(head_dim);
 
     Vec<16> wq[NV], wk[NV];
@@ -68,39 +70,57 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
             vzero16(wk[j]);
     }
 
-    for (int64_t base = static_cast<int64_t>(blockIdx.x) * GROUPS; base < total;
-         base += static_cast<int64_t>(gridDim.x) * GROUPS) {
-        const int64_t row = base + g;
-        const bool active = row < total;
-        const int64_t tok = active ? row / heads : 0;
-        const int h = active ? static_cast<int>(row - tok * heads) : 0;
-        const bool isq = h < q_heads;
-        char *head = isq ? static_cast<char *>(q) + (tok * q_stride + int64_t(h) * head_dim) *
-                               E::kSize
-                         : static_cast<char *>(k) +
-                               (tok * k_stride + int64_t(h - q_heads) * head_dim) * E::kSize;
-        char *ht = head + t * 16;
-
-        Vec<16> xv[NV];
+    // Each group takes RPG heads per iteration (heads g, g + GROUPS, ... of
+    // the block's window), so a lane has RPG * NV loads in flight.
+    for (int64_t base = static_cast<int64_t>(blockIdx.x) * GROUPS * RPG; base < total;
+         base += static_cast<int64_t>(gridDim.x) * GROUPS * RPG) {
+        char *ht[RPG];
+        bool isq[RPG], active[RPG];
+        Vec<16> xv[RPG][NV];
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if (active && t + j * TPR < nvec)
-                ld_stream<0>(xv[j], ht + j * TPR * 16);
-            else
-                vzero16(xv[j]);
+        for (int r = 0; r < RPG; ++r) {
+            const int64_t row = base + g + r * GROUPS;
+            active[r] = row < total;
+            int64_t tok;
+            int h;
+            if (small) {
+                const uint32_t rr = active[r] ? static_cast<uint32_t>(row) : 0u;
+                const uint32_t tt = rr / static_cast<uint32_t>(heads);
+                tok = tt;
+                h = static_cast<int>(rr - tt * static_cast<uint32_t>(heads));
+            } else {
+                tok = active[r] ? row / heads : 0;
+                h = active[r] ? static_cast<int>(row - tok * heads) : 0;
+            }
+            isq[r] = h < q_heads;
+            char *head = isq[r] ? static_cast<char *>(q) +
+                                      (tok * q_stride + int64_t(h) * head_dim) * E::kSize
+                                : static_cast<char *>(k) +
+                                      (tok * k_stride + int64_t(h - q_heads) * head_dim) * E::kSize;
+            ht[r] = head + t * 16;
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (active[r] && t + j * TPR < nvec)
+                    ld_stream<0>(xv[r][j], ht[r] + j * TPR * 16);
+                else
+                    vzero16(xv[r][j]);
+            }
         }
-        float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < NV; ++j)
-            s = sumsq<DT, 16>(xv[j], s);
-        s = group_allreduce<TPR>(s);
-        const float r = row_factor(s, n, eps);
+        for (int r = 0; r < RPG; ++r) {
+            float s = 0.f;
 #pragma unroll
-        for (int j = 0; j < NV; ++j) {
-            if (active && t + j * TPR < nvec) {
-                Vec<16> o;
-                scale_bias<DT>(o, xv[j], isq ? wq[j] : wk[j], r, bias);
-                st_stream<0>(ht + j * TPR * 16, o);
+            for (int j = 0; j < NV; ++j)
+                s = sumsq<DT, 16>(xv[r][j], s);
+            s = group_allreduce<TPR>(s);
+            const float rf = row_factor(s, n, eps);
+#pragma unroll
+            for (int j = 0; j < NV; ++j) {
+                if (active[r] && t + j * TPR < nvec) {
+                    Vec<16> o;
+                    scale_bias<DT>(o, xv[r][j], isq[r] ? wq[j] : wk[j], rf, bias);
+                    st_stream<0>(ht[r] + j * TPR * 16, o);
+                }
             }
         }
     }
@@ -144,10 +164,10 @@ qk_norm_scalar_kernel(void *q, void *k, const void *__restrict__ qw, const void 
     }
 }
 
-template <int DT, int TPR, int NV>
+template <int DT, int TPR, int NV, int RPG>
 cudaError_t launch_qk(const QkArgs &a)
 {
-    return launch_kernel(qk_norm_kernel<DT, TPR, NV>, a.grid, 256, 0, a.base, a.q, a.k, a.qw,
+    return launch_kernel(qk_norm_kernel<DT, TPR, NV, RPG>, a.grid, 256, 0, a.base, a.q, a.k, a.qw,
                          a.kw, a.tokens, a.q_heads, a.k_heads, a.head_dim, a.q_stride,
                          a.k_stride, a.bias, a.eps);
 }
@@ -160,10 +180,14 @@ cudaError_t launch_qk_scalar(const QkArgs &a)
                          a.bias, a.eps);
 }
 
-#define QK_ENTRY(DT, TPR, NV) QkKernel{DT, TPR, NV, &launch_qk<DT, TPR, NV>}
+#define QK_ENTRY(DT, TPR, NV, RPG) QkKernel{DT, TPR, NV, RPG, &launch_qk<DT, TPR, NV, RPG>}
 #define QK_SET(DT)                                                                             \
-    QK_ENTRY(DT, 4, 1), QK_ENTRY(DT, 8, 1), QK_ENTRY(DT, 16, 1), QK_ENTRY(DT, 32, 1),         \
-        QK_ENTRY(DT, 32, 2), QK_ENTRY(DT, 32, 4), QkKernel{DT, 0, 0, &launch_qk_scalar<DT>}
+    QK_ENTRY(DT, 4, 1, 1), QK_ENTRY(DT, 4, 1, 4), QK_ENTRY(DT, 4, 2, 1), QK_ENTRY(DT, 4, 2, 2), \
+        QK_ENTRY(DT, 8, 1, 1), QK_ENTRY(DT, 8, 1, 2), QK_ENTRY(DT, 8, 1, 4),                  \
+        QK_ENTRY(DT, 8, 2, 1), QK_ENTRY(DT, 8, 2, 2), QK_ENTRY(DT, 16, 1, 1),                 \
+        QK_ENTRY(DT, 16, 1, 2), QK_ENTRY(DT, 16, 1, 4), QK_ENTRY(DT, 16, 2, 1),               \
+        QK_ENTRY(DT, 16, 2, 2), QK_ENTRY(DT, 32, 1, 1), QK_ENTRY(DT, 32, 1, 2),               \
+        QK_ENTRY(DT, 32, 2, 1), QK_ENTRY(DT, 32, 4, 1), QkKernel{DT, 0, 0, 1, &launch_qk_scalar<DT>}
 
 const QkKernel kTable[] = {QK_SET(RMSNORM_F32), QK_SET(RMSNORM_BF16), QK_SET(RMSNORM_F16)};
 

@@ -181,6 +181,84 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
     return out
 
 
+def time_qk_plans(name: str, iters: int, graph: bool) -> list[dict]:
+    """Every compiled QK-norm launch shape (lanes per head, vectors per lane,
+    heads per group) x grid sizes on a QK workload (fused layout, rotating
+    buffers larger than L2); sorted fastest first, the automatic plan marked."""
+    import torch
+
+    import rmsnorm_fwd_gb300 as rn
+    from rmsnorm_fwd_gb300 import inputs
+    wl = inputs.QK_WORKLOADS[name]
+    rn.ensure_context(0)
+    sms, _ = rn.rmsnorm_device_limits()
+    dev = torch.device("cuda", 0)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[wl.dtype]
+    es = ES[wl.dtype]
+    nbytes = wl.tokens * wl.width * es
+    nsets = min(64, max(2, -(-3 * L2 // nbytes)))
+    bufs = [torch.randn(wl.tokens * wl.width, device=dev).to(tdt) for _ in range(nsets)]
+    qw = torch.ones(wl.head_dim, device=dev, dtype=tdt)
+    d, hq, hk, T = wl.head_dim, wl.q_heads, wl.k_heads, wl.tokens
+    fn = rn._load().rmsnorm_qk_norm_ex
+    s = torch.cuda.current_stream().cuda_stream
+    dt = rn.DTYPE_CODES[wl.dtype]
+    ptr = [b.data_ptr() for b in bufs]
+    auto = rn.QkPlan()
+    rn.rmsnorm_qk_norm_ex(ptr[0], ptr[0] + hq * d * es, qw.data_ptr(), qw.data_ptr(), T, hq, hk,
+                          d, wl.width, wl.width, 0.0, wl.eps, dt, s, auto)
+    total = T * (hq + hk)
+    cands = [auto.as_dict()]
+    for lanes in (4, 8, 16, 32):
+        for nv in (1, 2, 4):
+            for rpg in (1, 2, 4):
+                per = (256 // lanes) * rpg
+                full = -(-total // per)
+                for g in sorted({full, min(full, sms * 16), min(full, sms * 8), min(full, sms * 4)}):
+                    cands.append(dict(lanes_per_head=lanes, vecs_per_lane=nv, heads_per_group=rpg,
+                                      grid=g))
+    out = []
+    for ci, c in enumerate(cands):
+        p = rn.QkPlan(**c)
+        ref = rn.ctypes.byref(p)
+
+        def call(i):
+            return fn(ptr[i % nsets], ptr[i % nsets] + hq * d * es, qw.data_ptr(), qw.data_ptr(),
+                      T, hq, hk, d, wl.width, wl.width, 0.0, wl.eps, dt, s, ref)
+        if call(0) != 0:
+            continue
+        for i in range(5):
+            call(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        if graph:
+            g_ = torch.cuda.CUDAGraph()
+            cs = torch.cuda.Stream()
+            with torch.cuda.graph(g_, stream=cs):
+                for i in range(iters):
+                    fn(ptr[i % nsets], ptr[i % nsets] + hq * d * es, qw.data_ptr(), qw.data_ptr(),
+                       T, hq, hk, d, wl.width, wl.width, 0.0, wl.eps, dt, cs.cuda_stream, ref)
+            g_.replay()
+            torch.cuda.synchronize()
+            e0.record()
+            g_.replay()
+            e1.record()
+        else:
+            e0.record()
+            for i in range(iters):
+                call(i)
+            e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / iters * 1e3
+        out.append({"us": round(us, 3), "GBps": round(wl.bytes_per_call / (us * 1e-6) / 1e9, 1),
+                    "auto": ci == 0, "plan": c})
+    if rn.rmsnorm_get_device_status() != rn.OK:
+        raise RuntimeError("a timed plan recorded a device-side error")
+    out.sort(key=lambda r: r["us"])
+    return out
+
+
 def plan_label(p: dict, kinfo: dict) -> str:
     """Short text for a plan: variant, vector bytes, threads/row, vectors/thread,
     block, grid, stages, register floor, cache policy."""
@@ -225,7 +303,15 @@ def main(argv=None) -> int:
                     help="programmatic dependent launch off/on (default: library setting)")
     ap.add_argument("--auto-only", action="store_true", help="time only the automatic plan")
     ap.add_argument("--summarize", default="", help="print a markdown table of a --grid output")
+    ap.add_argument("--qk-workload", default="", help="sweep the QK-norm launch shapes instead")
     args = ap.parse_args(argv)
+    if args.qk_workload:
+        if args.pdl is not None:
+            import rmsnorm_fwd_gb300 as rn
+            rn.rmsnorm_set_pdl(bool(args.pdl))
+        for r in time_qk_plans(args.qk_workload, args.iters, args.graph)[:args.keep]:
+            print(json.dumps(r), flush=True)
+        return 0
     if args.summarize:
         print(summarize(args.summarize))
         return 0
