@@ -5,12 +5,11 @@
 // A head is a short row (64..256 elements), so TPR lanes of one warp own it
 // (the page uses a half warp with one 16-byte vector per lane for a
 // 128-element bf16 head; on GB300 8 lanes with two vectors each measure
-// faster), NV 16-byte vectors per lane, and 256 / TPR heads share a block.  Head h of token t:
-// h < q_heads -> q + t * q_token_stride + h * head_dim, else k (strides let q
-// and k be views into a fused QKV buffer).  Each lane always touches the
-// same vector positions of a head, so both weight slices stay in registers.
-// The reduction is the butterfly shuffle over the TPR lanes; the statistic
-// never leaves registers.
+// faster), NV 16-byte vectors per lane, and 256 / TPR heads share a block.
+// Head h of token t: h < q_heads -> q + t * q_token_stride + h * head_dim,
+// else k (strides let q and k be views into a fused QKV buffer).  The
+// reduction is the butterfly shuffle over the TPR lanes; the statistic never
+// leaves registers.
 #include "internal.h"
 #include "device_common.cuh"
 
@@ -38,7 +37,7 @@ __device__ inline void vzero16(Vec<16> &v)
 }
 
 template <int DT, int TPR, int NV, int RPG>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 6) // <= 40 registers: 6 resident blocks
 qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__restrict__ kw,
                int64_t tokens, int32_t q_heads, int32_t k_heads, int32_t head_dim,
                int64_t q_stride, int64_t k_stride, float bias, float eps)
@@ -56,27 +55,13 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
     const bool small = total < (int64_t(1) << 31); // 32-bit head index arithmetic
     const float n = static_cast<float>(head_dim);
 
-    Vec<16> wq[NV], wk[NV];
-#pragma unroll
-    for (int j = 0; j < NV; ++j) {
-        const int v = t + j * TPR;
-        if (v < nvec && q_heads > 0)
-            ld_weight(wq[j], static_cast<const char *>(qw) + v * 16);
-        else
-            vzero16(wq[j]);
-        if (v < nvec && k_heads > 0)
-            ld_weight(wk[j], static_cast<const char *>(kw) + v * 16);
-        else
-            vzero16(wk[j]);
-    }
-
     // Each group takes RPG heads per iteration (heads g, g + GROUPS, ... of
     // the block's window), so a lane has RPG * NV loads in flight.
     for (int64_t base = static_cast<int64_t>(blockIdx.x) * GROUPS * RPG; base < total;
          base += static_cast<int64_t>(gridDim.x) * GROUPS * RPG) {
         char *ht[RPG];
-        bool isq[RPG], active[RPG];
-        Vec<16> xv[RPG][NV];
+        bool active[RPG];
+        Vec<16> xv[RPG][NV], wv[RPG][NV];
 #pragma unroll
         for (int r = 0; r < RPG; ++r) {
             const int64_t row = base + g + r * GROUPS;
@@ -92,18 +77,25 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
                 tok = active[r] ? row / heads : 0;
                 h = active[r] ? static_cast<int>(row - tok * heads) : 0;
             }
-            isq[r] = h < q_heads;
-            char *head = isq[r] ? static_cast<char *>(q) +
-                                      (tok * q_stride + int64_t(h) * head_dim) * E::kSize
-                                : static_cast<char *>(k) +
-                                      (tok * k_stride + int64_t(h - q_heads) * head_dim) * E::kSize;
+            const bool isq = h < q_heads;
+            char *head = isq ? static_cast<char *>(q) +
+                                   (tok * q_stride + int64_t(h) * head_dim) * E::kSize
+                             : static_cast<char *>(k) +
+                                   (tok * k_stride + int64_t(h - q_heads) * head_dim) * E::kSize;
             ht[r] = head + t * 16;
+            // The head's weight slice comes with it (an L1 hit after the
+            // first heads), instead of holding both q and k slices in
+            // registers across the loop.
+            const char *wt = static_cast<const char *>(isq ? qw : kw) + t * 16;
 #pragma unroll
             for (int j = 0; j < NV; ++j) {
-                if (active[r] && t + j * TPR < nvec)
+                if (active[r] && t + j * TPR < nvec) {
                     ld_stream<0>(xv[r][j], ht[r] + j * TPR * 16);
-                else
+                    ld_weight(wv[r][j], wt + j * TPR * 16);
+                } else {
                     vzero16(xv[r][j]);
+                    vzero16(wv[r][j]);
+                }
             }
         }
 #pragma unroll
@@ -115,10 +107,13 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
             s = group_allreduce<TPR>(s);
             const float rf = row_factor(s, n, eps);
 #pragma unroll
+            for (int j = 0; j < NV; ++j)
+                reuse_barrier(xv[r][j]);
+#pragma unroll
             for (int j = 0; j < NV; ++j) {
                 if (active[r] && t + j * TPR < nvec) {
                     Vec<16> o;
-                    scale_bias<DT>(o, xv[r][j], isq[r] ? wq[j] : wk[j], rf, bias);
+                    scale_bias<DT>(o, xv[r][j], wv[r][j], rf, bias);
                     st_stream<0>(ht[r] + j * TPR * 16, o);
                 }
             }
