@@ -561,8 +561,7 @@ int rmsnorm_qk_norm_ex(void *q, void *k, const void *q_weight, const void *k_wei
     } else {
         // Automatic (from a sweep of every compiled shape on GB300): two
         // 16-byte vectors per lane (8 lanes for a 128-element bf16 head, 16
-        // for 256), one head per group per iteration, and for many heads a
-        // grid of 8 blocks per SM looping over them.
+        // for 256), one head per group, one pass over all heads.
         int tpr = 0, nv = 0, rpg = 1;
         if (vec) {
             const int64_t nvec = head_dim * es / 16;
@@ -583,7 +582,7 @@ int rmsnorm_qk_norm_ex(void *q, void *k, const void *q_weight, const void *k_wei
         if (!kern)
             return RMSNORM_ERR_VARIANT;
         const int64_t per_block = kern->tpr ? int64_t(256 / kern->tpr) * kern->rpg : 8;
-        grid = std::min<int64_t>((total + per_block - 1) / per_block, int64_t(ctx.sm_count) * 8);
+        grid = std::min<int64_t>((total + per_block - 1) / per_block, INT_MAX);
         if (plan) {
             plan->lanes_per_head = kern->tpr ? kern->tpr : -1;
             plan->vecs_per_lane = kern->nv;
