@@ -10,7 +10,9 @@ What it computes is the RMSNorm of "Build a GPU compiler from scratch: from
 PyTorch to CUDA via multi-level IR (Emmy)" (introduction and section "Tensor
 IR": square, sum, divide by the count, add epsilon, rsqrt, two multiplies)
 and "CuTeDSL at Perplexity", section "QK Norm" (rsqrt of the mean square plus
-EPS, times the element, times the weight, cast back to the element type).
+EPS, times the element, times the weight plus WEIGHT_BIAS, cast back to the
+element type), with the MXFP8 output the same page's section "Blackwell
+support" names, in the OCP Microscaling v1.0 definition.
 """
 from __future__ import annotations
 
@@ -64,6 +66,15 @@ def lib() -> ctypes.CDLL:
         for name in ("oracle_widen_array", "oracle_round_array"):
             getattr(l, name).argtypes = [vp, vp, i64, i32]
             getattr(l, name).restype = i32
+        for name in ("oracle_rmsnorm_bias_f64", "oracle_rmsnorm_bias"):
+            getattr(l, name).argtypes = [vp, vp, vp, i64, i64, f32, f32, i32]
+            getattr(l, name).restype = i32
+        l.oracle_mxfp8_quantize.argtypes = [vp, i64, i64, vp, vp]
+        l.oracle_mxfp8_quantize.restype = i32
+        l.oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+        l.oracle_e4m3_value.restype = ctypes.c_double
+        l.oracle_e4m3_encode.argtypes = [ctypes.c_double]
+        l.oracle_e4m3_encode.restype = ctypes.c_uint8
         l.oracle_qk_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32]
         l.oracle_qk_norm.restype = i32
         l.oracle_round_value.argtypes = [ctypes.c_double, i32]
@@ -115,6 +126,77 @@ def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float, dtype) -> np.ndarray:
     if rc != 0:
         raise ValueError("oracle_rmsnorm rejected its arguments")
     return y
+
+
+def rmsnorm_bias_f64(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float,
+                     dtype) -> np.ndarray:
+    """y = x * rsqrt(mean(x^2) + eps) * (w + weight_bias) per row, binary64."""
+    fmt = fmt_code(dtype)
+    x = _check_storage(x, fmt)
+    w = _check_storage(w, fmt)
+    rows, hidden = x.shape
+    if w.shape != (hidden,):
+        raise ValueError("weight must have shape [hidden]")
+    y = np.empty((rows, hidden), dtype=np.float64)
+    rc = lib().oracle_rmsnorm_bias_f64(_ptr(x), _ptr(w), _ptr(y), rows, hidden,
+                                       float(weight_bias), float(eps), fmt)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_bias_f64 rejected its arguments")
+    return y
+
+
+def rmsnorm_bias(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float,
+                 dtype) -> np.ndarray:
+    """rmsnorm_bias_f64 rounded nearest-even to the element format."""
+    fmt = fmt_code(dtype)
+    x = _check_storage(x, fmt)
+    w = _check_storage(w, fmt)
+    rows, hidden = x.shape
+    if w.shape != (hidden,):
+        raise ValueError("weight must have shape [hidden]")
+    y = np.empty((rows, hidden), dtype=_STORAGE[fmt])
+    rc = lib().oracle_rmsnorm_bias(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(weight_bias),
+                                   float(eps), fmt)
+    if rc != 0:
+        raise ValueError("oracle_rmsnorm_bias rejected its arguments")
+    return y
+
+
+def mxfp8_quantize(v: np.ndarray) -> tuple:
+    """MXFP8 of a [rows, cols] array of values (cols a multiple of 32):
+    (E4M3 codes uint8 [rows, cols], E8M0 scales uint8 [rows, cols / 32])."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    rows, cols = v.shape
+    codes = np.empty((rows, cols), dtype=np.uint8)
+    scales = np.empty((rows, max(cols // 32, 0)), dtype=np.uint8)
+    rc = lib().oracle_mxfp8_quantize(_ptr(v), rows, cols, _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("oracle_mxfp8_quantize rejected its arguments")
+    return codes, scales
+
+
+def rmsnorm_mxfp8(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float, dtype,
+                  rel: float = 0.0) -> tuple:
+    """The normalised rows quantised to MXFP8.
+
+    The value that decides each code is the row result in binary32 (the
+    binary64 result rounded nearest-even to binary32), as a kernel holding
+    fp32 values decides it; ``rel`` scales those values by (1 + rel) first,
+    which brackets the codes any result within that relative distance may
+    take."""
+    y = rmsnorm_bias_f64(x, w, weight_bias, eps, dtype)
+    y32 = round_to(y, "f32").astype(np.float64)
+    if rel:
+        y32 = y32 * (1.0 + rel)
+    return mxfp8_quantize(y32)
+
+
+def e4m3_value(code: int) -> float:
+    return lib().oracle_e4m3_value(int(code))
+
+
+def e4m3_encode(v: float) -> int:
+    return int(lib().oracle_e4m3_encode(float(v)))
 
 
 def widen(a: np.ndarray, dtype) -> np.ndarray:

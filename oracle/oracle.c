@@ -20,7 +20,15 @@
  *
  *   "CuTeDSL at Perplexity", section "QK Norm": the same statistic taken as
  *   rsqrt(sum / head_dim + EPS), each element scaled by that factor and by
- *   its weight, the result cast back to the input's element type.
+ *   its weight plus WEIGHT_BIAS, the result cast back to the input's element
+ *   type.
+ *
+ *   Same page, section "Blackwell support" (MXFP8 / MXFP4 / NVFP4, absolute
+ *   maxima over blocks of 16 or 32 elements): the normalised row may instead
+ *   leave as MXFP8 -- E4M3 elements with one power-of-two E8M0 scale per 32
+ *   consecutive elements.  The pages name the format but do not define it;
+ *   the definition used is the one the OCP Microscaling (MX) v1.0
+ *   specification publishes (see the MXFP8 section below).
  *
  * Every value is widened exactly to IEEE binary64 and every operation runs in
  * binary64, left to right, with no blocking, fusion or reordering.  The final
@@ -288,5 +296,149 @@ int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight,
                (double)eps, fmt);
     norm_heads(k, k_weight, tokens, k_heads, head_dim, k_token_stride, (double)weight_bias,
                (double)eps, fmt);
+    return 0;
+}
+
+/* ---- weight bias ---------------------------------------------------------- */
+
+/*
+ * The row normalisation with the weight offset of "CuTeDSL at Perplexity",
+ * section "QK Norm" (w + WEIGHT_BIAS) applied to whole rows:
+ *     y[i,j] = x[i,j] * r_i * (w[j] + weight_bias)
+ * in binary64, unrounded.
+ */
+int oracle_rmsnorm_bias_f64(const void *x, const void *w, double *y, int64_t rows,
+                            int64_t hidden, float weight_bias, float eps, int fmt)
+{
+    if (rows < 0 || hidden <= 0 || fmt < 0 || fmt > 2)
+        return -1;
+    double e = (double)eps;
+    double b = (double)weight_bias;
+    for (int64_t i = 0; i < rows; ++i) {
+        double r = row_factor(x, i, hidden, e, fmt);
+        for (int64_t j = 0; j < hidden; ++j) {
+            double xv = oracle_widen(x, i * hidden + j, fmt);
+            double wv = oracle_widen(w, j, fmt) + b;
+            y[i * hidden + j] = xv * r * wv;
+        }
+    }
+    return 0;
+}
+
+/* The same, rounded nearest-even to the element format. */
+int oracle_rmsnorm_bias(const void *x, const void *w, void *y, int64_t rows, int64_t hidden,
+                        float weight_bias, float eps, int fmt)
+{
+    if (rows < 0 || hidden <= 0 || fmt < 0 || fmt > 2)
+        return -1;
+    double e = (double)eps;
+    double b = (double)weight_bias;
+    for (int64_t i = 0; i < rows; ++i) {
+        double r = row_factor(x, i, hidden, e, fmt);
+        for (int64_t j = 0; j < hidden; ++j) {
+            double xv = oracle_widen(x, i * hidden + j, fmt);
+            double wv = oracle_widen(w, j, fmt) + b;
+            oracle_store(xv * r * wv, y, i * hidden + j, fmt);
+        }
+    }
+    return 0;
+}
+
+/* ---- MXFP8: E4M3 elements, one E8M0 scale per 32 elements ----------------- */
+
+/*
+ * E4M3 (the OCP 8-bit floating-point format "E4M3"): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 fraction bits; no infinities; exponent field 15 with
+ * fraction 7 is NaN, so the largest finite magnitude is 1.75 * 2^8 = 448;
+ * exponent field 0 holds the subnormals f * 2^-9.
+ */
+double oracle_e4m3_value(uint8_t code)
+{
+    int sign = (code >> 7) & 1;
+    int expo = (code >> 3) & 0xF;
+    int frac = code & 0x7;
+    double mag;
+    if (expo == 0xF && frac == 0x7)
+        mag = NAN;
+    else if (expo == 0)
+        mag = ldexp((double)frac, -9);
+    else
+        mag = ldexp((double)(8 + frac), expo - 7 - 3);
+    return sign ? -mag : mag;
+}
+
+/*
+ * Round to E4M3, nearest with ties to even, saturating: a magnitude that
+ * rounds above 448 becomes 448 (the format has no infinity; the MX
+ * specification leaves overflow to the implementation, and clamping is the
+ * plainest choice).  NaN becomes the NaN code with the input's sign.
+ */
+uint8_t oracle_e4m3_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7F);
+    double a = fabs(v);
+    /* p = 4 significand bits, minimum normal exponent -6; the generic
+     * rounding's overflow to infinity is replaced by the clamp. */
+    double r = isinf(a) ? 448.0 : round_to_format(a, 4, -6, 8);
+    if (isinf(r) || r > 448.0)
+        r = 448.0;
+    if (r == 0.0)
+        return sign;
+    if (r < ldexp(1.0, -6))
+        return (uint8_t)(sign | (uint8_t)ldexp(r, 9)); /* subnormal: r = f * 2^-9 */
+    int k;
+    frexp(r, &k);
+    int e = k - 1; /* r in [2^e, 2^(e+1)) */
+    uint8_t frac = (uint8_t)(ldexp(r, 3 - e) - 8.0);
+    return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | frac);
+}
+
+/*
+ * One MX block (OCP Microscaling v1.0, conversion of a vector of scalars to
+ * an MX block): the shared exponent is floor(log2(max |v|)) minus the
+ * largest exponent of the element format (8 for E4M3), clamped to the E8M0
+ * range [-127, 127]; the scale is X = 2^shared; every element is v / X
+ * rounded to E4M3 as above.  E8M0 stores shared + 127; 0xFF (NaN) when the
+ * block holds a NaN or an infinity.  An all-zero block takes the smallest
+ * scale, 2^-127 (code 0).
+ */
+static void mx_block(const double *v, int n, uint8_t *codes, uint8_t *scale)
+{
+    double amax = 0.0;
+    int special = 0;
+    for (int i = 0; i < n; ++i) {
+        if (isnan(v[i]) || isinf(v[i]))
+            special = 1;
+        else if (fabs(v[i]) > amax)
+            amax = fabs(v[i]);
+    }
+    int shared;
+    if (amax == 0.0) {
+        shared = -127;
+    } else {
+        int k;
+        frexp(amax, &k); /* amax in [2^(k-1), 2^k): floor(log2 amax) = k - 1 */
+        shared = (k - 1) - 8;
+        if (shared < -127)
+            shared = -127;
+        if (shared > 127)
+            shared = 127;
+    }
+    *scale = special ? 0xFF : (uint8_t)(shared + 127);
+    for (int i = 0; i < n; ++i)
+        codes[i] = oracle_e4m3_encode(ldexp(v[i], -shared)); /* v / X, exact */
+}
+
+int oracle_mxfp8_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *codes,
+                          uint8_t *scales)
+{
+    if (rows < 0 || cols <= 0 || cols % 32 != 0)
+        return -1;
+    const int64_t nb = cols / 32;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t b = 0; b < nb; ++b)
+            mx_block(v + i * cols + b * 32, 32, codes + i * cols + b * 32, scales + i * nb + b);
     return 0;
 }

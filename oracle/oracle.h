@@ -43,6 +43,21 @@ int oracle_qk_norm(void *q, void *k, const void *q_weight, const void *k_weight,
                    int64_t q_heads, int64_t k_heads, int64_t head_dim, int64_t q_token_stride,
                    int64_t k_token_stride, float weight_bias, float eps, int fmt);
 
+/* Row normalisation with a weight offset: y = x * r * (w + weight_bias),
+ * binary64 (the _f64 form) or rounded nearest-even to the element format. */
+int oracle_rmsnorm_bias_f64(const void *x, const void *w, double *y, int64_t rows,
+                            int64_t hidden, float weight_bias, float eps, int fmt);
+int oracle_rmsnorm_bias(const void *x, const void *w, void *y, int64_t rows, int64_t hidden,
+                        float weight_bias, float eps, int fmt);
+
+/* MXFP8: rows x cols binary64 values (cols a multiple of 32) to E4M3 codes
+ * [rows, cols] and E8M0 scales [rows, cols / 32], one scale per 32
+ * consecutive elements of a row. */
+int oracle_mxfp8_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *codes,
+                          uint8_t *scales);
+double oracle_e4m3_value(uint8_t code);
+uint8_t oracle_e4m3_encode(double v);
+
 /* Single-element helpers behind the array functions. */
 double oracle_widen(const void *base, int64_t index, int fmt);
 double oracle_round_value(double v, int fmt);
