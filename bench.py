@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
+                    [--op rmsnorm|qk_norm|bias|mxfp8]
 
 A step is one RMSNorm forward over one batch: the headline workload is the
 prefill-shaped batch, 16384 rows x 4096 hidden, bf16 in/out, fp32
@@ -179,15 +180,24 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the device-code sources (kernels, their headers, the launch
-    helper); host-only files such as the selector do not change a kernel."""
+# The translation unit that holds the register-resident row kernels of each
+# element type, and every file it includes from the tree.
+ROWREG_SOURCES = ("rowreg.cuh", "device_common.cuh", "internal.h")
+
+
+def kernel_source_hash(dtype: str = "bf16") -> str:
+    """Hash of the sources of the plain row kernels of `dtype` (the unit that
+    compiles them and the headers it includes, plus the build flags); other
+    kernels and host-only files such as the selector do not change them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rmsnorm_fwd_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")) or f == "internal.h":
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    paths = [os.path.join(csrc, f) for f in (f"rowreg_{dtype}.cu",) + ROWREG_SOURCES]
+    paths.append(os.path.join(ROOT, "include", "rmsnorm.h"))
+    for p in paths:
+        with open(p, "rb") as fh:
+            h.update(os.path.basename(p).encode() + fh.read())
+    from rmsnorm_fwd_gb300 import _build
+    h.update(repr((_build.GENCODE, _build.CFLAGS, _build.CUDA_FLAGS)).encode())
     return h.hexdigest()[:16]
 
 
@@ -199,7 +209,7 @@ def ncu_traffic(workload: str, variant: str):
         text = open(path).read()
     except OSError:
         return None
-    src = kernel_source_hash()
+    src = kernel_source_hash(inputs.WORKLOADS[workload].dtype)
     for m in re.finditer(r"^workload=(\S+) variant=(\S+) src=(\S+) dram_bytes_per_launch=(\d+)",
                          text, flags=re.M):
         if m.group(1) == workload and m.group(2) == variant and m.group(3) == src:
@@ -520,6 +530,113 @@ def run_qk(args, world, rank, local):
     return 0
 
 
+def run_epi(args, world, rank, local):
+    """--op bias | mxfp8: the row norm with the weight offset, or with the
+    fused MXFP8 output (E4M3 codes + one E8M0 scale per 32 elements), on the
+    chosen workload; the plain kernel on the same inputs is timed beside it
+    for context."""
+    import torch
+
+    import rmsnorm_fwd_gb300 as rn
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = inputs.WORKLOADS[args.workload]
+    es = inputs.ITEMSIZE[wl.dtype]
+    x_np, w_np = inputs.make_inputs(wl, seed=rank)
+    x_host = to_torch(x_np, wl.dtype, torch)
+    w = to_torch(w_np, wl.dtype, torch).to(device)
+    mx = args.op == "mxfp8"
+    n = wl.rows * wl.hidden
+    out_bytes = (n + n // 32) if mx else n * es
+    step_bytes = n * es + wl.hidden * es + out_bytes
+    set_bytes = n * es + out_bytes
+    nsets = max(2, -(-3 * L2_BYTES // set_bytes))
+    xs = [x_host.to(device) for _ in range(nsets)]
+    if mx:
+        ys = [torch.empty(n, dtype=torch.uint8, device=device) for _ in range(nsets)]
+        ss = [torch.empty(n // 32, dtype=torch.uint8, device=device) for _ in range(nsets)]
+    else:
+        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+        ss = [None] * nsets
+    rn.ensure_context(local)
+    stream = torch.cuda.current_stream(device)
+    sptr = stream.cuda_stream
+    dt = rn.DTYPE_CODES[wl.dtype]
+    epi = rn.EPI_MXFP8 if mx else rn.EPI_BIAS
+    bias = 1.0
+    plan = rn.Plan()
+    rn.rmsnorm_fwd_epilogue_ex(xs[0].data_ptr(), w.data_ptr(), ys[0].data_ptr(),
+                               ss[0].data_ptr() if mx else None, wl.rows, wl.hidden, epi, bias,
+                               wl.eps, dt, sptr, rn.VARIANT_AUTO, plan)
+    fn = rn._load().rmsnorm_fwd_epilogue_ex
+    pref = rn.ctypes.byref(plan)
+    xp = [t.data_ptr() for t in xs]
+    yp = [t.data_ptr() for t in ys]
+    sp = [t.data_ptr() if t is not None else None for t in ss]
+
+    def step(i):
+        j = i % nsets
+        rc = fn(xp[j], w.data_ptr(), yp[j], sp[j], wl.rows, wl.hidden, epi, bias, wl.eps, dt,
+                sptr, 0, pref)
+        if rc != rn.OK:
+            raise rn.RmsnormError(rc, "rmsnorm_fwd_epilogue_ex")
+
+    ys_plain = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    gen = rn._load().rmsnorm_fwd
+
+    def step_plain(i):
+        j = i % nsets
+        gen(xp[j], w.data_ptr(), ys_plain[j].data_ptr(), wl.rows, wl.hidden, wl.eps, dt, sptr)
+
+    def timed(fn_step, K):
+        for i in range(max(3, args.warmup)):
+            fn_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(K):
+            fn_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K
+
+    K = args.steps
+    sampler = ClockSampler(local)
+    sampler.start()
+    t0 = time.time()
+    ms = timed(step, K)
+    t1 = time.time()
+    sampler.stop()
+    ms_plain = timed(step_plain, K)
+    value = step_bytes / (ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    plain_bytes = wl.bytes_per_call
+    line = {
+        "metric": ("RMSNorm + MXFP8 output achieved HBM GB/s" if mx else
+                   "RMSNorm with weight offset achieved HBM GB/s"),
+        "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "ms_per_step": round(ms, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden,
+                   "io_dtype": wl.dtype, "epilogue": rn.EPI_NAMES[epi], "weight_bias": bias,
+                   "variant": rn.VARIANT_NAMES[plan.variant], "plan": plan.as_dict(),
+                   "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.0f} MB"},
+        "rows_per_s": round(wl.rows / (ms / 1e3), 1),
+        "gpu_launches": K,
+        "roofline": {"bound": "hbm", "achieved": round(value, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(value / peak, 4), "peak_source": peak_kind,
+                     "algorithmic_bytes_per_launch": step_bytes},
+        "plain_output_same_rows": {"ms_per_step": round(ms_plain, 6),
+                                   "GBps": round(plain_bytes / (ms_plain / 1e3) / 1e9, 2),
+                                   "time_ratio": round(ms / ms_plain, 4)},
+        "clocks": sampler.summary(t0, t1),
+        "device_status": rn.rmsnorm_get_device_status(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -530,13 +647,15 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=60.0)
-    ap.add_argument("--op", choices=["rmsnorm", "qk_norm"], default="rmsnorm")
+    ap.add_argument("--op", choices=["rmsnorm", "qk_norm", "bias", "mxfp8"], default="rmsnorm")
     ap.add_argument("--qk-workload", default="qk_bf16_16384tok_32q8k_128",
                     choices=sorted(inputs.QK_WORKLOADS))
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     if args.op == "qk_norm":
         return run_qk(args, world, rank, local)
+    if args.op in ("bias", "mxfp8"):
+        return run_epi(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)

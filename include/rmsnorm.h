@@ -71,6 +71,13 @@ typedef enum {
     RMSNORM_ERR_TOO_LARGE = 10          /* beyond the static scratch of rmsnorm_fwd_staged_noalloc */
 } rmsnorm_status_t;
 
+/* What a row kernel writes (see rmsnorm_fwd_bias and rmsnorm_fwd_mxfp8). */
+typedef enum {
+    RMSNORM_EPI_PLAIN = 0, /* y = round((x * r) * w) in the element type */
+    RMSNORM_EPI_BIAS = 1,  /* y = round((x * r) * (w + weight_bias)) in the element type */
+    RMSNORM_EPI_MXFP8 = 2  /* (x * r) * (w + weight_bias) as MXFP8: E4M3 codes + E8M0 scales */
+} rmsnorm_epilogue_t;
+
 /* Kernel variants.  AUTO lets the selector choose from (rows, hidden, dtype,
  * pointer alignment, SM count). */
 typedef enum {
@@ -138,6 +145,66 @@ int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_
  * AUTO, the chosen plan is written back into it. */
 int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
                    float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan);
+
+/* ---- epilogues ("CuTeDSL at Perplexity": section "QK Norm" for the weight
+ * offset WEIGHT_BIAS; section "Blackwell support" for the MXFP8 / MXFP4 /
+ * NVFP4 block formats whose absolute maxima are taken over 16 or 32
+ * elements) ---------------------------------------------------------------- */
+
+/* Row normalisation with a weight offset, as the per-head kernel applies it:
+ *
+ *   y[i, j] = round( (x[i, j] * r_i) * (w[j] + weight_bias) )
+ *
+ * with w[j] + weight_bias formed in fp32 (weight_bias = -0.0f gives exactly
+ * rmsnorm_fwd's result; +0.0f may differ from it only in the sign of zero
+ * outputs of zero weights).  Arguments, layout, aliasing (y == x allowed),
+ * errors and asynchrony as rmsnorm_fwd.  weight_bias must be finite. */
+int rmsnorm_fwd_bias(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                     float weight_bias, float eps, int dtype, void *stream);
+
+/* Fused RMSNorm -> MXFP8.  The normalised values v[i, j] = (x[i, j] * r_i) *
+ * (w[j] + weight_bias), held in fp32, leave as the OCP Microscaling (MX)
+ * v1.0 format MXFP8 with E4M3 elements (the pages name the format; its
+ * definition is the MX specification's):
+ *
+ *   for every 32 consecutive elements of a row (block b = j / 32):
+ *     s = floor(log2(max |v|)) - 8, clamped to [-127, 127]  (8 = E4M3's largest exponent)
+ *     scales[i, b] = s + 127        (E8M0; 0xFF when the block holds a NaN or an infinity;
+ *                                    an all-zero block gets s = -127)
+ *     q[i, j] = E4M3( v[i, j] / 2^s )   (nearest-even, saturating at +-448)
+ *
+ *   x      [rows, hidden] of `dtype` (device), 16-byte aligned
+ *   weight [hidden] of `dtype` (device), 16-byte aligned
+ *   q      [rows, hidden] bytes (device, E4M3 codes), 16-byte aligned
+ *   scales [rows, hidden / 32] bytes (device, E8M0 codes), row-major, any alignment
+ *
+ * hidden must be a multiple of 32 (RMSNORM_ERR_INVALID_ARG otherwise);
+ * misaligned x / weight / q give RMSNORM_ERR_MISALIGNED (there is no scalar
+ * MX body).  q and scales may not overlap each other, x or weight
+ * (RMSNORM_ERR_ALIASING).  Otherwise as rmsnorm_fwd. */
+int rmsnorm_fwd_mxfp8(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float weight_bias, float eps, int dtype, void *stream);
+
+/* Any epilogue with a forced variant or an explicit plan (as rmsnorm_fwd_ex;
+ * `scales` is used by RMSNORM_EPI_MXFP8 only, `weight_bias` by BIAS and
+ * MXFP8).  The bulk-copy staged variant exists for RMSNORM_EPI_PLAIN only:
+ * the automatic choice uses the register or looped bodies instead, and a
+ * forced STAGED returns RMSNORM_ERR_VARIANT. */
+int rmsnorm_fwd_epilogue_ex(const void *x, const void *weight, void *y, void *scales,
+                            int64_t rows, int64_t hidden, int epilogue, float weight_bias,
+                            float eps, int dtype, void *stream, int variant,
+                            rmsnorm_plan_t *plan);
+
+/* The selector for an epilogue (host only, as rmsnorm_plan). */
+int rmsnorm_plan_epilogue(const void *x, const void *weight, const void *y, int64_t rows,
+                          int64_t hidden, int dtype, int epilogue, int sm_count, int smem_optin,
+                          int variant, rmsnorm_plan_t *out);
+
+/* Host-only check of an explicit plan for an epilogue (as rmsnorm_validate_plan). */
+int rmsnorm_validate_plan_epilogue(const rmsnorm_plan_t *plan, const void *x,
+                                   const void *weight, const void *y, int64_t rows,
+                                   int64_t hidden, int dtype, int epilogue, int sm_count,
+                                   int smem_optin);
 
 /* y = RMSNorm(x) * weight for x and y in HOST memory.  When both buffers
  * are page-locked host memory mapped into the device's address space (for
@@ -233,6 +300,7 @@ typedef struct {
     int32_t min_blocks;   /* resident blocks per SM the build was register-capped for; 0 = none */
     int32_t cache_policy; /* 0 plain, 1 L2 256-byte prefetch hint, 2 streaming (.cs) loads and
                            * stores, 3 staged rows written back by bulk copies */
+    int32_t epilogue;     /* rmsnorm_epilogue_t the instantiation writes */
 } rmsnorm_kernel_info_t;
 
 /* SM count and opt-in shared memory per block of the current device, as

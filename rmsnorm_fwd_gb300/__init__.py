@@ -45,6 +45,10 @@ VARIANT_GENERIC = 5
 VARIANT_NAMES = {0: "auto", 1: "warp_per_row", 2: "cta_per_row", 3: "staged", 4: "persistent",
                  5: "generic"}
 
+# epilogues (rmsnorm_epilogue_t)
+EPI_PLAIN, EPI_BIAS, EPI_MXFP8 = 0, 1, 2
+EPI_NAMES = {EPI_PLAIN: "plain", EPI_BIAS: "bias", EPI_MXFP8: "mxfp8"}
+
 
 class RmsnormError(RuntimeError):
     def __init__(self, status: int, where: str):
@@ -74,7 +78,8 @@ class QkPlan(ctypes.Structure):
 class KernelInfo(ctypes.Structure):
     """rmsnorm_kernel_info_t."""
     _fields_ = [(name, ctypes.c_int32) for name in (
-        "variant", "dtype", "vec_bytes", "tpr", "nv", "block", "min_blocks", "cache_policy")]
+        "variant", "dtype", "vec_bytes", "tpr", "nv", "block", "min_blocks", "cache_policy",
+        "epilogue")]
 
     def as_dict(self) -> dict:
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -114,6 +119,13 @@ def _load() -> ctypes.CDLL:
                                 i32),
             "rmsnorm_qk_norm_ex": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32, vp,
                                     ctypes.POINTER(QkPlan)], i32),
+            "rmsnorm_fwd_bias": ([vp, vp, vp, i64, i64, f32, f32, i32, vp], i32),
+            "rmsnorm_fwd_mxfp8": ([vp, vp, vp, vp, i64, i64, f32, f32, i32, vp], i32),
+            "rmsnorm_fwd_epilogue_ex": ([vp, vp, vp, vp, i64, i64, i32, f32, f32, i32, vp, i32, pp],
+                                        i32),
+            "rmsnorm_plan_epilogue": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, pp], i32),
+            "rmsnorm_validate_plan_epilogue": ([pp, vp, vp, vp, i64, i64, i32, i32, i32, i32],
+                                               i32),
             "rmsnorm_last_variant": ([], i32),
             "rmsnorm_kernel_count": ([], i32),
             "rmsnorm_validate_plan": ([pp, vp, vp, vp, i64, i64, i32, i32, i32], i32),
@@ -220,6 +232,45 @@ def qk_norm(q, k, q_weight, k_weight, head_dim: int, eps: float, weight_bias: fl
         rmsnorm_qk_norm(q.data_ptr(), k.data_ptr(), q_weight.data_ptr(), k_weight.data_ptr(),
                         tokens, q.shape[-1] // head_dim, k.shape[-1] // head_dim, head_dim, qs, ks,
                         float(weight_bias), float(eps), torch_dtype_code(q.dtype), s.cuda_stream)
+
+
+def rmsnorm_fwd_bias(x: int, weight: int, y: int, rows: int, hidden: int, weight_bias: float,
+                     eps: float, dtype: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_fwd_bias(x, weight, y, rows, hidden, weight_bias, eps, dtype,
+                                    stream or None), "rmsnorm_fwd_bias")
+
+
+def rmsnorm_fwd_mxfp8(x: int, weight: int, q: int, scales: int, rows: int, hidden: int,
+                      weight_bias: float, eps: float, dtype: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_fwd_mxfp8(x, weight, q, scales, rows, hidden, weight_bias, eps, dtype,
+                                     stream or None), "rmsnorm_fwd_mxfp8")
+
+
+def rmsnorm_fwd_epilogue_ex(x: int, weight: int, y: int, scales: int | None, rows: int,
+                            hidden: int, epilogue: int, weight_bias: float, eps: float,
+                            dtype: int, stream: int | None, variant: int = VARIANT_AUTO,
+                            plan: Plan | None = None) -> None:
+    _check(_load().rmsnorm_fwd_epilogue_ex(x, weight, y, scales or None, rows, hidden, epilogue,
+                                           weight_bias, eps, dtype, stream or None, variant,
+                                           ctypes.byref(plan) if plan is not None else None),
+           "rmsnorm_fwd_epilogue_ex")
+
+
+def rmsnorm_plan_epilogue_status(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int,
+                                 epilogue: int, sm_count: int, smem_optin: int,
+                                 variant: int = VARIANT_AUTO):
+    """(status, plan) of the selector for an epilogue, without raising."""
+    p = Plan()
+    rc = _load().rmsnorm_plan_epilogue(x, weight, y, rows, hidden, dtype, epilogue, sm_count,
+                                       smem_optin, variant, ctypes.byref(p))
+    return rc, p
+
+
+def rmsnorm_validate_plan_epilogue(plan: Plan, x: int, weight: int, y: int, rows: int,
+                                   hidden: int, dtype: int, epilogue: int, sm_count: int,
+                                   smem_optin: int) -> int:
+    return _load().rmsnorm_validate_plan_epilogue(ctypes.byref(plan), x, weight, y, rows, hidden,
+                                                  dtype, epilogue, sm_count, smem_optin)
 
 
 def rmsnorm_plan(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int, sm_count: int,
@@ -364,3 +415,63 @@ def rms_norm(x, weight, eps: float, out=None, variant: int = VARIANT_AUTO, plan:
         rmsnorm_fwd_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), rows, hidden, float(eps),
                        torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
     return out
+
+
+def rms_norm_bias(x, weight, weight_bias: float, eps: float, out=None, variant: int = VARIANT_AUTO,
+                  plan: Plan | None = None, stream=None):
+    """y = x * rsqrt(mean(x^2, -1) + eps) * (weight + weight_bias) through
+    rmsnorm_fwd_epilogue_ex (tensors as for ``rms_norm``)."""
+    import torch
+    _check_rows(x, weight)
+    if out is None:
+        out = torch.empty_like(x)
+    elif out.shape != x.shape or out.dtype != x.dtype or not out.is_contiguous():
+        raise ValueError("out must match x (shape, dtype, contiguous)")
+    ensure_context(x.device.index)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    hidden = x.shape[-1]
+    rows = x.numel() // hidden if hidden else 0
+    with torch.cuda.device(x.device.index):
+        rmsnorm_fwd_epilogue_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), None, rows, hidden,
+                                EPI_BIAS, float(weight_bias), float(eps),
+                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
+    return out
+
+
+def rms_norm_mxfp8(x, weight, eps: float, weight_bias: float = -0.0, out=None, scales=None,
+                   variant: int = VARIANT_AUTO, plan: Plan | None = None, stream=None):
+    """RMSNorm with an MXFP8 output: (codes uint8 [..., hidden] holding E4M3
+    bit patterns, scales uint8 [..., hidden / 32] holding E8M0 exponents)."""
+    import torch
+    _check_rows(x, weight)
+    hidden = x.shape[-1]
+    if hidden % 32:
+        raise ValueError("hidden must be a multiple of 32 for MXFP8")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(tuple(x.shape[:-1]) + (hidden // 32,), dtype=torch.uint8,
+                             device=x.device)
+    if out.dtype != torch.uint8 or out.shape != x.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous uint8 tensor shaped like x")
+    if scales.dtype != torch.uint8 or scales.numel() * 32 != x.numel() or not scales.is_contiguous():
+        raise ValueError("scales must be a contiguous uint8 tensor of x.numel() / 32 bytes")
+    ensure_context(x.device.index)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    rows = x.numel() // hidden if hidden else 0
+    with torch.cuda.device(x.device.index):
+        rmsnorm_fwd_epilogue_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), scales.data_ptr(),
+                                rows, hidden, EPI_MXFP8, float(weight_bias), float(eps),
+                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
+    return out, scales
+
+
+def _check_rows(x, weight):
+    if not (x.is_cuda and weight.is_cuda):
+        raise ValueError("CUDA tensors required (there is no CPU path)")
+    if x.dtype != weight.dtype:
+        raise TypeError("x and weight must share a dtype")
+    if not x.is_contiguous() or not weight.is_contiguous():
+        raise ValueError("x and weight must be contiguous")
+    if weight.numel() != x.shape[-1]:
+        raise ValueError("weight must have hidden elements")

@@ -20,9 +20,12 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librmsnorm.so")
 
 SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu",
-           "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu"]
+           "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu",
+           "rowreg_epi_f32.cu", "rowreg_epi_bf16.cu", "rowreg_epi_f16.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "rowreg.cuh"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
+CFLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC"]
+CUDA_FLAGS = ["-lineinfo"]
 
 
 def _nvcc() -> str:
@@ -48,13 +51,13 @@ def build(force: bool = False, verbose: bool = False) -> str:
         return LIB
     nvcc = _nvcc()
     os.makedirs(OUT, exist_ok=True)
-    common = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
+    common = [*CFLAGS, "-I", INCLUDE, "-I", CSRC]
 
     def compile_one(src: str) -> str:
         obj = os.path.join(OUT, src + ".o")
         cmd = [nvcc, *common, "-c", os.path.join(CSRC, src), "-o", obj]
         if src.endswith(".cu"):
-            cmd[1:1] = [*GENCODE, "-lineinfo"]
+            cmd[1:1] = [*GENCODE, *CUDA_FLAGS]
             if verbose:
                 cmd.append("-Xptxas=-v")
         res = subprocess.run(cmd, capture_output=True, text=True)

@@ -17,16 +17,18 @@ namespace rmsnorm {
 
 const KernelDesc *kernel_table(int *n)
 {
-    static KernelDesc table[256];
+    constexpr int kCap = 512;
+    static KernelDesc table[kCap];
     static int count = [] {
         int c = 0;
-        const KernelDesc *(*parts[])(int *) = {rowreg_kernels_f32, rowreg_kernels_bf16,
-                                                rowreg_kernels_f16, staged_kernels,
-                                                generic_kernels};
+        const KernelDesc *(*parts[])(int *) = {
+            rowreg_kernels_f32,     rowreg_kernels_bf16,     rowreg_kernels_f16,
+            staged_kernels,         generic_kernels,         rowreg_epi_kernels_f32,
+            rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16};
         for (auto part : parts) {
             int m = 0;
             const KernelDesc *t = part(&m);
-            for (int i = 0; i < m && c < 256; ++i)
+            for (int i = 0; i < m && c < kCap; ++i)
                 table[c++] = t[i];
         }
         return c;
@@ -162,19 +164,33 @@ bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes
 }
 
 int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
-               int dtype)
+               int dtype, int epi = RMSNORM_EPI_PLAIN, float bias = -0.0f,
+               const void *scales = nullptr)
 {
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
         return RMSNORM_ERR_UNSUPPORTED_DTYPE;
-    if (rows < 0 || hidden <= 0 || !(eps >= 0.f) || !std::isfinite(eps))
+    if (rows < 0 || hidden <= 0 || !(eps >= 0.f) || !std::isfinite(eps) || !std::isfinite(bias))
         return RMSNORM_ERR_INVALID_ARG;
-    if (!w || (rows > 0 && (!x || !y)))
+    if (epi != RMSNORM_EPI_PLAIN && epi != RMSNORM_EPI_BIAS && epi != RMSNORM_EPI_MXFP8)
+        return RMSNORM_ERR_INVALID_ARG;
+    const bool mx = epi == RMSNORM_EPI_MXFP8;
+    if (mx && hidden % 32 != 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    if (!w || (rows > 0 && (!x || !y || (mx && !scales))))
         return RMSNORM_ERR_INVALID_ARG;
     if (rows > 0) {
         const int64_t es = dtype == RMSNORM_F32 ? 4 : 2;
         if (rows > INT64_MAX / 4 / hidden)
             return RMSNORM_ERR_INVALID_ARG;
         const int64_t bytes = rows * hidden * es;
+        if (mx) { // codes and scales are new buffers: no overlap with anything
+            const int64_t qb = rows * hidden, sb = rows * (hidden / 32);
+            if (ranges_overlap(x, bytes, y, qb) || ranges_overlap(w, hidden * es, y, qb) ||
+                ranges_overlap(x, bytes, scales, sb) ||
+                ranges_overlap(w, hidden * es, scales, sb) || ranges_overlap(y, qb, scales, sb))
+                return RMSNORM_ERR_ALIASING;
+            return RMSNORM_OK;
+        }
         if (y != x && ranges_overlap(x, bytes, y, bytes))
             return RMSNORM_ERR_ALIASING;
         if (ranges_overlap(w, hidden * es, y, bytes))
@@ -185,9 +201,10 @@ int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidd
 
 int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
            int dtype, void *stream, int variant, rmsnorm_plan_t *plan, uint32_t flags,
-           uint64_t limit_ns)
+           uint64_t limit_ns, int epi = RMSNORM_EPI_PLAIN, float bias = -0.0f,
+           void *scales = nullptr)
 {
-    int rc = check_args(x, w, y, rows, hidden, eps, dtype);
+    int rc = check_args(x, w, y, rows, hidden, eps, dtype, epi, bias, scales);
     if (rc != RMSNORM_OK)
         return rc;
     DeviceCtx ctx;
@@ -203,9 +220,10 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     rmsnorm_plan_t p;
     if (plan && plan->variant != RMSNORM_VARIANT_AUTO) {
         p = *plan;
-        rc = validate_plan(p, x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin);
+        rc = validate_plan(p, x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, epi);
     } else {
-        rc = plan_launch(x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, variant, &p);
+        rc = plan_launch(x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, variant, &p,
+                         epi);
     }
     if (rc != RMSNORM_OK)
         return rc;
@@ -225,11 +243,13 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     a.flags = flags;
     a.stream = static_cast<cudaStream_t>(stream);
     a.pdl = pdl_enabled();
+    a.bias = bias;
+    a.scales = scales;
     if (log_enabled())
         std::fprintf(stderr,
-                     "rmsnorm: rows=%lld hidden=%lld dtype=%d -> variant=%d vec=%d tpr=%d nv=%d "
-                     "block=%d grid=%d stages=%d smem=%d kernel=%d\n",
-                     static_cast<long long>(rows), static_cast<long long>(hidden), dtype,
+                     "rmsnorm: rows=%lld hidden=%lld dtype=%d epi=%d -> variant=%d vec=%d tpr=%d "
+                     "nv=%d block=%d grid=%d stages=%d smem=%d kernel=%d\n",
+                     static_cast<long long>(rows), static_cast<long long>(hidden), dtype, epi,
                      p.variant, p.vec_bytes, p.threads_per_row, p.vecs_per_thread,
                      p.block_threads, p.grid, p.stages, p.smem_bytes, p.kernel_index);
     if (d.launch(p, a) != cudaSuccess)
@@ -333,6 +353,31 @@ int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int
 {
     return launch(x, weight, y, rows, hidden, eps, dtype, stream, variant, plan, 0u,
                   g_wait_limit.load());
+}
+
+int rmsnorm_fwd_bias(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                     float weight_bias, float eps, int dtype, void *stream)
+{
+    return launch(x, weight, y, rows, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                  0u, g_wait_limit.load(), RMSNORM_EPI_BIAS, weight_bias, nullptr);
+}
+
+int rmsnorm_fwd_mxfp8(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float weight_bias, float eps, int dtype, void *stream)
+{
+    return launch(x, weight, q, rows, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                  0u, g_wait_limit.load(), RMSNORM_EPI_MXFP8, weight_bias, scales);
+}
+
+int rmsnorm_fwd_epilogue_ex(const void *x, const void *weight, void *y, void *scales,
+                            int64_t rows, int64_t hidden, int epilogue, float weight_bias,
+                            float eps, int dtype, void *stream, int variant,
+                            rmsnorm_plan_t *plan)
+{
+    return launch(x, weight, y, rows, hidden, eps, dtype, stream, variant, plan, 0u,
+                  g_wait_limit.load(), epilogue,
+                  epilogue == RMSNORM_EPI_PLAIN ? -0.0f : weight_bias,
+                  epilogue == RMSNORM_EPI_MXFP8 ? scales : nullptr);
 }
 
 // Whether two strided head sets can share a byte: set A is
@@ -636,6 +681,25 @@ int rmsnorm_validate_plan(const rmsnorm_plan_t *plan, const void *x, const void 
     return validate_plan(*plan, x, weight, y, rows, hidden, dtype, sm_count, smem_optin);
 }
 
+int rmsnorm_plan_epilogue(const void *x, const void *weight, const void *y, int64_t rows,
+                          int64_t hidden, int dtype, int epilogue, int sm_count, int smem_optin,
+                          int variant, rmsnorm_plan_t *out)
+{
+    return plan_launch(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant, out,
+                       epilogue);
+}
+
+int rmsnorm_validate_plan_epilogue(const rmsnorm_plan_t *plan, const void *x,
+                                   const void *weight, const void *y, int64_t rows,
+                                   int64_t hidden, int dtype, int epilogue, int sm_count,
+                                   int smem_optin)
+{
+    if (!plan)
+        return RMSNORM_ERR_INVALID_ARG;
+    return validate_plan(*plan, x, weight, y, rows, hidden, dtype, sm_count, smem_optin,
+                         epilogue);
+}
+
 int rmsnorm_device_limits(int *sm_count, int *smem_optin)
 {
     if (!sm_count || !smem_optin)
@@ -671,6 +735,7 @@ int rmsnorm_kernel_info(int index, rmsnorm_kernel_info_t *out)
     out->block = d.block;
     out->min_blocks = d.minb;
     out->cache_policy = d.cache;
+    out->epilogue = d.epi;
     return RMSNORM_OK;
 }
 

@@ -211,6 +211,118 @@ __device__ inline void scale(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB> &wv,
     }
 }
 
+// ---------------------------------------------------------------- epilogues
+
+// out = (x * r) * (w + bias) per element -- the weight offset WEIGHT_BIAS of
+// "CuTeDSL at Perplexity", section "QK Norm" -- rounded to the element type.
+template <int DT, int VB>
+__device__ inline void scale_bias(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB> &wv, float r,
+                                  float bias)
+{
+#pragma unroll
+    for (int k = 0; k < Vec<VB>::kWords; ++k) {
+        float xa, xb = 0.f, wa, wb = 0.f;
+        Elem<DT>::widen(xv.w[k], xa, xb);
+        Elem<DT>::widen(wv.w[k], wa, wb);
+        out.w[k] = Elem<DT>::narrow((xa * r) * (wa + bias), (xb * r) * (wb + bias));
+    }
+}
+
+// MXFP8 output geometry of one vector: its elements become that many E4M3
+// code bytes, and a 32-element scale block spans kLanes consecutive vectors
+// (held by kLanes consecutive lanes).
+template <int DT, int VB> struct Mx {
+    static constexpr int kElems = VB / Elem<DT>::kSize;
+    static constexpr int kLanes = 32 / kElems;
+};
+
+// Four fp32 values to four E4M3 codes, value i in byte i.  The conversion
+// instruction rounds to nearest-even and saturates finite overflow to +-448
+// (.satfinite); a NaN stays NaN.  The instruction puts its first source in
+// the upper byte of each 16-bit pair.
+__device__ inline uint32_t e4m3x4(float a0, float a1, float a2, float a3)
+{
+    uint32_t r;
+    asm("{\n\t.reg .b16 lo, hi;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+        "mov.b32 %0, {lo, hi};\n\t}"
+        : "=r"(r)
+        : "f"(a0), "f"(a1), "f"(a2), "f"(a3));
+    return r;
+}
+
+// Stores NB = 4, 8 or 16 code bytes (not allocated in L1).
+template <int NB>
+__device__ inline void st_codes(void *p, const uint32_t (&w)[NB / 4])
+{
+    if constexpr (NB == 4)
+        asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
+    else if constexpr (NB == 8)
+        asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]),
+                     "r"(w[1])
+                     : "memory");
+    else
+        asm volatile("st.global.L1::no_allocate.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p),
+                     "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3])
+                     : "memory");
+}
+
+// One vector of the MXFP8 epilogue (OCP Microscaling v1.0 with E4M3
+// elements; "CuTeDSL at Perplexity", section "Blackwell support", for the
+// absolute maximum taken over the lanes that share a 32-element block).
+//
+// v = (x * r) * (w + bias) in fp32; the block maximum of |v| is taken on the
+// bit patterns (for non-negative floats the integer order is the numeric
+// order, and Inf / NaN patterns sort above every finite value, so they
+// reach the scale instead of being dropped as fmaxf would drop a NaN) with
+// butterfly shuffles over the block's kLanes lanes.  Its biased exponent e
+// gives the shared exponent floor(log2 max) - 8 = e - 135, clamped at -127:
+// E8M0 code max(e - 8, 0), or 0xFF for Inf / NaN.  Scaling by 2^(127 - code)
+// is exact, and the conversion rounds each scaled value to E4M3.
+//
+// Every lane of the warp must call this (the shuffles span the full warp);
+// `live` says whether this lane's vector is part of the row.  The lane
+// holding the first vector of a block (`leader`) stores the scale byte.
+template <int DT, int VB>
+__device__ inline void mx_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, float bias,
+                                bool live, bool leader, void *q, uint8_t *scale)
+{
+    constexpr int NE = Mx<DT, VB>::kElems;
+    constexpr int LPB = Mx<DT, VB>::kLanes;
+    constexpr int PW = Elem<DT>::kPerWord;
+    float f[NE];
+#pragma unroll
+    for (int k = 0; k < Vec<VB>::kWords; ++k) {
+        float xa, xb = 0.f, wa, wb = 0.f;
+        Elem<DT>::widen(xv.w[k], xa, xb);
+        Elem<DT>::widen(wv.w[k], wa, wb);
+        f[k * PW] = (xa * r) * (wa + bias);
+        if (PW == 2)
+            f[k * PW + PW - 1] = (xb * r) * (wb + bias);
+    }
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < NE; ++i)
+        m = max(m, __float_as_uint(f[i]) & 0x7FFFFFFFu);
+#pragma unroll
+    for (int off = 1; off < LPB; off <<= 1)
+        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off, 32));
+    const uint32_t e = m >> 23;
+    const uint32_t code = e == 255u ? 255u : (e > 8u ? e - 8u : 0u);
+    const float inv = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
+    uint32_t words[NE / 4];
+#pragma unroll
+    for (int j = 0; j < NE / 4; ++j)
+        words[j] = e4m3x4(f[4 * j] * inv, f[4 * j + 1] * inv, f[4 * j + 2] * inv,
+                          f[4 * j + 3] * inv);
+    if (live) {
+        st_codes<NE>(q, words);
+        if (leader)
+            *scale = static_cast<uint8_t>(code);
+    }
+}
+
 // ---------------------------------------------------------------- launch order
 
 // Programmatic dependent launch.  Every kernel calls pdl_begin() before its

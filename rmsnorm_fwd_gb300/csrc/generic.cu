@@ -15,10 +15,11 @@
 namespace rmsnorm {
 namespace {
 
-template <int DT>
+// EPI: RMSNORM_EPI_PLAIN, or RMSNORM_EPI_BIAS (the weight plus `bias`).
+template <int DT, int EPI>
 __global__ void __launch_bounds__(1024)
 generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                    int32_t hidden, float eps)
+                    int32_t hidden, float eps, float bias)
 {
     using E = Elem<DT>;
     __shared__ float part[2][32];
@@ -48,24 +49,29 @@ generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
         const float r = row_factor(tot, n, eps);
         for (int j = t; j < hidden; j += blockDim.x) {
             const float v = E::widen1(x, base + j);
-            E::store1(y, base + j, (v * r) * E::widen1(w, j));
+            if constexpr (EPI == RMSNORM_EPI_BIAS)
+                E::store1(y, base + j, (v * r) * (E::widen1(w, j) + bias));
+            else
+                E::store1(y, base + j, (v * r) * E::widen1(w, j));
         }
     }
 }
 
-template <int DT>
+template <int DT, int EPI>
 cudaError_t launch_generic(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(generic_rows_kernel<DT>, p.grid, p.block_threads, 0, a, a.x, a.w, a.y,
-                         a.rows, a.hidden, a.eps);
+    return launch_kernel(generic_rows_kernel<DT, EPI>, p.grid, p.block_threads, 0, a, a.x, a.w,
+                         a.y, a.rows, a.hidden, a.eps, a.bias);
 }
 
-#define GENERIC_ENTRY(DT)                                                                      \
-    KernelDesc{RMSNORM_VARIANT_GENERIC, DT, 0, 0, 0, 0, 0, 0, &launch_generic<DT>,                  \
-               reinterpret_cast<const void *>(&generic_rows_kernel<DT>)}
+#define GENERIC_ENTRY(DT, EPI)                                                                 \
+    KernelDesc{RMSNORM_VARIANT_GENERIC, DT, 0, 0, 0, 0, 0, 0, &launch_generic<DT, EPI>,        \
+               reinterpret_cast<const void *>(&generic_rows_kernel<DT, EPI>), EPI}
 
-const KernelDesc kTable[] = {GENERIC_ENTRY(RMSNORM_F32), GENERIC_ENTRY(RMSNORM_BF16),
-                             GENERIC_ENTRY(RMSNORM_F16)};
+const KernelDesc kTable[] = {
+    GENERIC_ENTRY(RMSNORM_F32, RMSNORM_EPI_PLAIN), GENERIC_ENTRY(RMSNORM_BF16, RMSNORM_EPI_PLAIN),
+    GENERIC_ENTRY(RMSNORM_F16, RMSNORM_EPI_PLAIN), GENERIC_ENTRY(RMSNORM_F32, RMSNORM_EPI_BIAS),
+    GENERIC_ENTRY(RMSNORM_BF16, RMSNORM_EPI_BIAS), GENERIC_ENTRY(RMSNORM_F16, RMSNORM_EPI_BIAS)};
 
 } // namespace
 

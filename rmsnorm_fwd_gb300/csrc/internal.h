@@ -29,6 +29,8 @@ struct LaunchArgs {
     uint32_t flags;         // kFlagWithholdCopies: failure-detection test only
     cudaStream_t stream;
     bool pdl = false;       // launch with a programmatic dependency on the stream's last kernel
+    float bias = -0.0f;     // weight offset (BIAS / MXFP8 epilogues); -0 adds nothing
+    void *scales = nullptr; // MXFP8 epilogue: E8M0 scales [rows, hidden / 32]; y holds the codes
 };
 
 #if defined(__CUDACC__)
@@ -73,12 +75,16 @@ struct KernelDesc {
                          // 3 staged rows stored by bulk copies
     LaunchFn launch;
     const void *func;    // the __global__ function (attributes)
+    int32_t epi = RMSNORM_EPI_PLAIN; // what it writes (rmsnorm_epilogue_t)
 };
 
 // Per translation unit tables, concatenated by kernel_table().
 const KernelDesc *rowreg_kernels_f32(int *n);
 const KernelDesc *rowreg_kernels_bf16(int *n);
 const KernelDesc *rowreg_kernels_f16(int *n);
+const KernelDesc *rowreg_epi_kernels_f32(int *n); // BIAS and MXFP8 epilogues
+const KernelDesc *rowreg_epi_kernels_bf16(int *n);
+const KernelDesc *rowreg_epi_kernels_f16(int *n);
 const KernelDesc *staged_kernels(int *n);
 const KernelDesc *generic_kernels(int *n);
 
@@ -132,7 +138,8 @@ const QkKernel *qk_kernels(int *n);
 
 // Host-side selector (select.cpp).
 int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
-                int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out);
+                int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out,
+                int epi = RMSNORM_EPI_PLAIN);
 
 // Argument checks shared by every launching entry point (api.cpp).
 int check_call_args(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
@@ -140,6 +147,7 @@ int check_call_args(const void *x, const void *w, const void *y, int64_t rows, i
 
 // Checks a caller-supplied plan against the shape and the kernel table.
 int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const void *y,
-                  int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin);
+                  int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin,
+                  int epi = RMSNORM_EPI_PLAIN);
 
 } // namespace rmsnorm

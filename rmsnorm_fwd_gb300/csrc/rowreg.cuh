@@ -44,14 +44,18 @@ __device__ inline void vzero(Vec<VB> &v)
 // TPR lanes (4..32, power of two) per row, BLOCK/TPR rows per block per
 // iteration, grid-stride over rows.  The loop bound is block-uniform so every
 // lane takes part in every shuffle.
-template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
+template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI>
 __global__ void __launch_bounds__(BLOCK, MINB > 0 ? MINB : 1)
 warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                 int32_t hidden, float eps)
+                 int32_t hidden, float eps, float bias, uint8_t *scales)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;                     // elements per vector
     constexpr int GROUPS = BLOCK / TPR;                    // rows per block per iteration
+    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
+    constexpr int LPB = Mx<DT, VB>::kLanes;                // MX: lanes per 32-element block
+    constexpr int OB = MX ? Mx<DT, VB>::kElems : VB;       // output bytes per vector
+    static_assert(!MX || TPR % LPB == 0, "an MX block must not straddle two rows");
     // Weight slice kept in registers (loaded before the row, off the
     // reduction's critical path): always for one vector per thread, else
     // only without a register cap.
@@ -63,6 +67,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     const int g = threadIdx.x / TPR;
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
+    const int64_t out_row = MX ? hidden : row_bytes; // output bytes per row
     const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
@@ -80,9 +85,8 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
          base += static_cast<int64_t>(gridDim.x) * GROUPS) {
         const int64_t row = base + g;
         const bool active = row < rows;
-        const int64_t off = row * row_bytes + t * VB;
-        const char *xr = static_cast<const char *>(x) + off;
-        char *yr = static_cast<char *>(y) + off;
+        const char *xr = static_cast<const char *>(x) + row * row_bytes + t * VB;
+        char *yr = static_cast<char *>(y) + row * out_row + t * OB;
 
         Vec<VB> xv[NV];
 #pragma unroll
@@ -104,15 +108,28 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            if (active && t + k * TPR < nvec) {
-                Vec<VB> o;
-                if (W_HELD) {
-                    scale<DT, VB>(o, xv[k], wv[W_HELD ? k : 0], r);
-                } else {
-                    Vec<VB> wk;
+            if constexpr (MX) {
+                const bool live = active && t + k * TPR < nvec;
+                Vec<VB> wk;
+                if (W_HELD)
+                    wk = wv[W_HELD ? k : 0];
+                else if (live)
                     ld_weight(wk, wt + k * TPR * VB);
+                else
+                    vzero(wk);
+                mx_store<DT, VB>(xv[k], wk, r, bias, live, t % LPB == 0, yr + k * TPR * OB,
+                                 scales + row * (hidden / 32) + (t + k * TPR) / LPB);
+            } else if (active && t + k * TPR < nvec) {
+                Vec<VB> o;
+                Vec<VB> wk;
+                if (W_HELD)
+                    wk = wv[W_HELD ? k : 0];
+                else
+                    ld_weight(wk, wt + k * TPR * VB);
+                if constexpr (EPI == RMSNORM_EPI_BIAS)
+                    scale_bias<DT, VB>(o, xv[k], wk, r, bias);
+                else
                     scale<DT, VB>(o, xv[k], wk, r);
-                }
                 st_stream<CP>(yr + k * TPR * VB, o);
             }
         }
@@ -125,13 +142,16 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 // rows.  Warp totals go through a double-buffered shared array so one
 // __syncthreads per row suffices.  TPRC > 0 fixes blockDim.x = TPRC at
 // compile time (vector offsets become immediates).
-template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC>
+template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                int32_t hidden, float eps)
+                int32_t hidden, float eps, float bias, uint8_t *scales)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
+    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
+    constexpr int LPB = Mx<DT, VB>::kLanes;
+    constexpr int OB = MX ? Mx<DT, VB>::kElems : VB;
     constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0); // as above
     __shared__ float part[2][32];
 
@@ -145,6 +165,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     const int stride = tpr * VB; // bytes between a thread's consecutive vectors
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
+    const int64_t out_row = MX ? hidden : row_bytes;
     const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
@@ -160,9 +181,8 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
     int it = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
-        const int64_t off = row * row_bytes + t * VB;
-        const char *xr = static_cast<const char *>(x) + off;
-        char *yr = static_cast<char *>(y) + off;
+        const char *xr = static_cast<const char *>(x) + row * row_bytes + t * VB;
+        char *yr = static_cast<char *>(y) + row * out_row + t * OB;
         Vec<VB> xv[NV];
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
@@ -190,15 +210,28 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
-            if (t + k * tpr < nvec) {
-                Vec<VB> o;
-                if (W_HELD) {
-                    scale<DT, VB>(o, xv[k], wv[W_HELD ? k : 0], r);
-                } else {
-                    Vec<VB> wk;
+            if constexpr (MX) {
+                const bool live = t + k * tpr < nvec;
+                Vec<VB> wk;
+                if (W_HELD)
+                    wk = wv[W_HELD ? k : 0];
+                else if (live)
                     ld_weight(wk, wt + k * stride);
+                else
+                    vzero(wk);
+                mx_store<DT, VB>(xv[k], wk, r, bias, live, t % LPB == 0, yr + k * tpr * OB,
+                                 scales + row * (hidden / 32) + (t + k * tpr) / LPB);
+            } else if (t + k * tpr < nvec) {
+                Vec<VB> o;
+                Vec<VB> wk;
+                if (W_HELD)
+                    wk = wv[W_HELD ? k : 0];
+                else
+                    ld_weight(wk, wt + k * stride);
+                if constexpr (EPI == RMSNORM_EPI_BIAS)
+                    scale_bias<DT, VB>(o, xv[k], wk, r, bias);
+                else
                     scale<DT, VB>(o, xv[k], wk, r);
-                }
                 st_stream<CP>(yr + k * stride, o);
             }
         }
@@ -212,14 +245,17 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 // the squares, the second re-reads the row (an L2 hit: the resident blocks'
 // rows are a few tens of MB against a 129 MB L2), scales and stores.  DRAM
 // sees x once and y once.  For rows longer than the register bodies hold.
-template <int DT, int VB, int MAXT, int MINB, int CP>
+template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                int32_t hidden, float eps)
+                int32_t hidden, float eps, float bias, uint8_t *scales)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
     constexpr int U = 4; // vectors in flight per thread per step
+    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
+    constexpr int LPB = Mx<DT, VB>::kLanes;
+    constexpr int OB = Mx<DT, VB>::kElems;
     __shared__ float part[2][32];
 
     pdl_begin();
@@ -236,7 +272,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     int it = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
         const char *xr = static_cast<const char *>(x) + row * row_bytes;
-        char *yr = static_cast<char *>(y) + row * row_bytes;
+        char *yr = static_cast<char *>(y) + row * (MX ? static_cast<int64_t>(hidden) : row_bytes);
         float s = 0.f;
         for (int v0 = t; v0 < nvec; v0 += U * tpr) {
             Vec<VB> xv[U];
@@ -261,6 +297,33 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
         const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
         const float r = row_factor(group_allreduce<32>(tot), n, eps);
 
+        if constexpr (MX) {
+            // Warp-uniform trip count (the block maximum is a shuffle over
+            // the whole warp): lane l of the warp starting at vector v0
+            // takes vector v0 + l, the same vectors as below.
+            uint8_t *sr = scales + row * (hidden / 32);
+            for (int v0 = t & ~31; v0 < nvec; v0 += U * tpr) {
+                Vec<VB> xv[U], wv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + lane + u * tpr;
+                    if (v < nvec) {
+                        ld_stream<0>(xv[u], xr + static_cast<int64_t>(v) * VB);
+                        ld_weight(wv[u], wb + static_cast<int64_t>(v) * VB);
+                    } else {
+                        vzero(xv[u]);
+                        vzero(wv[u]);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + lane + u * tpr;
+                    mx_store<DT, VB>(xv[u], wv[u], r, bias, v < nvec, lane % LPB == 0,
+                                     yr + static_cast<int64_t>(v) * OB, sr + v / LPB);
+                }
+            }
+            continue;
+        }
         for (int v0 = t; v0 < nvec; v0 += U * tpr) {
             Vec<VB> xv[U], wv[U];
 #pragma unroll
@@ -276,7 +339,10 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                 const int v = v0 + u * tpr;
                 if (v < nvec) {
                     Vec<VB> o;
-                    scale<DT, VB>(o, xv[u], wv[u], r);
+                    if constexpr (EPI == RMSNORM_EPI_BIAS)
+                        scale_bias<DT, VB>(o, xv[u], wv[u], r, bias);
+                    else
+                        scale<DT, VB>(o, xv[u], wv[u], r);
                     st_stream<CP>(yr + static_cast<int64_t>(v) * VB, o);
                 }
             }
@@ -286,73 +352,85 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
 // ---------------------------------------------------------------- launchers
 
-template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP>
+template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI>
 cudaError_t launch_warp(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP>, p.grid, BLOCK, 0, a,
-                         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
+    return launch_kernel(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP, EPI>, p.grid, BLOCK,
+                         0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
+                         static_cast<uint8_t *>(a.scales));
 }
 
-template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC>
+template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
 cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC>, p.grid,
-                         p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps);
+    return launch_kernel(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC, EPI>, p.grid,
+                         p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
+                         static_cast<uint8_t *>(a.scales));
 }
 
-template <int DT, int VB, int MAXT, int MINB, int CP>
+template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
 cudaError_t launch_loop(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(cta_loop_kernel<DT, VB, MAXT, MINB, CP>, p.grid, p.block_threads, 0, a,
-                         a.x, a.w, a.y, a.rows, a.hidden, a.eps);
+    return launch_kernel(cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI>, p.grid, p.block_threads, 0,
+                         a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
+                         static_cast<uint8_t *>(a.scales));
 }
 
 constexpr int kWarpBlock = 256;
 
-#define WARP_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
+#define WARP_ENTRY(DT, VB, TPR, NV, MINB, CP, EPI)                                             \
     KernelDesc{RMSNORM_VARIANT_WARP_PER_ROW, DT, VB, TPR, NV, kWarpBlock, MINB, CP,           \
-               &launch_warp<DT, VB, TPR, NV, kWarpBlock, MINB, CP>,                            \
+               &launch_warp<DT, VB, TPR, NV, kWarpBlock, MINB, CP, EPI>,                       \
                reinterpret_cast<const void *>(                                                 \
-                   &warp_rows_kernel<DT, VB, TPR, NV, kWarpBlock, MINB, CP>)}
+                   &warp_rows_kernel<DT, VB, TPR, NV, kWarpBlock, MINB, CP, EPI>),             \
+               EPI}
 
-#define CTA_ENTRY(DT, VB, NV, MAXT, MINB, CP)                                                  \
+#define CTA_ENTRY(DT, VB, NV, MAXT, MINB, CP, EPI)                                             \
     KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, NV, MAXT, MINB, CP,                    \
-               &launch_cta<DT, VB, NV, MAXT, MINB, CP, 0>,                                     \
-               reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, 0>)}
+               &launch_cta<DT, VB, NV, MAXT, MINB, CP, 0, EPI>,                                \
+               reinterpret_cast<const void *>(                                                 \
+                   &cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, 0, EPI>),                      \
+               EPI}
 
 // Looped block-per-row (vectors per thread 0 = "any row length").
-#define LOOP_ENTRY(DT, VB, MAXT, MINB, CP)                                                     \
+#define LOOP_ENTRY(DT, VB, MAXT, MINB, CP, EPI)                                                \
     KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, 0, 0, MAXT, MINB, CP,                     \
-               &launch_loop<DT, VB, MAXT, MINB, CP>,                                           \
-               reinterpret_cast<const void *>(&cta_loop_kernel<DT, VB, MAXT, MINB, CP>)}
+               &launch_loop<DT, VB, MAXT, MINB, CP, EPI>,                                      \
+               reinterpret_cast<const void *>(&cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI>),  \
+               EPI}
 
 // Block of exactly TPR threads (compile time).
-#define CTAF_ENTRY(DT, VB, TPR, NV, MINB, CP)                                                  \
+#define CTAF_ENTRY(DT, VB, TPR, NV, MINB, CP, EPI)                                             \
     KernelDesc{RMSNORM_VARIANT_CTA_PER_ROW, DT, VB, TPR, NV, TPR, MINB, CP,                   \
-               &launch_cta<DT, VB, NV, TPR, MINB, CP, TPR>,                                    \
-               reinterpret_cast<const void *>(&cta_rows_kernel<DT, VB, NV, TPR, MINB, CP, TPR>)}
+               &launch_cta<DT, VB, NV, TPR, MINB, CP, TPR, EPI>,                               \
+               reinterpret_cast<const void *>(                                                 \
+                   &cta_rows_kernel<DT, VB, NV, TPR, MINB, CP, TPR, EPI>),                     \
+               EPI}
 
-// The instantiations every element type gets.
+// The instantiations every element type gets, per epilogue.
 //   warp-per-row: (VB, TPR, NV, MINB, CP)
 //   block-per-row, runtime block size <= MAXT: (VB, NV, MAXT, MINB, CP)
 //   block-per-row, block size fixed at TPR: (VB, TPR, NV, MINB, CP)
 // MINB caps registers so at least MINB blocks of MAXT threads fit on an SM
 // (65536 registers): MAXT x MINB = 2048 -> 32 registers per thread.  The
-// selector (select.cpp) names these entries by their parameters.
-#define ROWREG_SET(DT)                                                                         \
-    WARP_ENTRY(DT, 16, 4, 1, 0, 0), WARP_ENTRY(DT, 16, 8, 1, 0, 0),                           \
-        WARP_ENTRY(DT, 16, 8, 2, 0, 0), WARP_ENTRY(DT, 16, 16, 1, 0, 0),                      \
-        WARP_ENTRY(DT, 16, 16, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 1, 0, 0),                     \
-        WARP_ENTRY(DT, 16, 32, 2, 0, 0), WARP_ENTRY(DT, 16, 32, 4, 0, 0),                     \
-        WARP_ENTRY(DT, 16, 32, 2, 8, 0), WARP_ENTRY(DT, 16, 32, 4, 8, 0),                     \
-        WARP_ENTRY(DT, 32, 32, 1, 0, 0), WARP_ENTRY(DT, 32, 32, 2, 0, 0),                     \
-        CTA_ENTRY(DT, 16, 1, 1024, 2, 1), CTA_ENTRY(DT, 32, 1, 1024, 1, 1),                   \
-        CTA_ENTRY(DT, 16, 2, 1024, 2, 1), CTA_ENTRY(DT, 32, 2, 1024, 0, 1),                   \
-        CTA_ENTRY(DT, 16, 4, 1024, 0, 1), CTA_ENTRY(DT, 32, 4, 512, 0, 1),                    \
-        CTA_ENTRY(DT, 16, 2, 256, 8, 1), CTA_ENTRY(DT, 16, 3, 512, 3, 1),                     \
-        CTA_ENTRY(DT, 16, 4, 256, 6, 1), CTA_ENTRY(DT, 16, 4, 512, 2, 1),                     \
-        CTA_ENTRY(DT, 16, 8, 512, 0, 1), CTAF_ENTRY(DT, 16, 512, 1, 0, 0),                    \
-        LOOP_ENTRY(DT, 16, 512, 2, 1)
+// selector (select.cpp) names these entries by their parameters.  The
+// 4-lane warp body is left out of the MXFP8 set (a 32-element f32 block
+// spans 8 lanes).
+#define ROWREG_SET_WIDE(DT, EPI)                                                               \
+    WARP_ENTRY(DT, 16, 8, 1, 0, 0, EPI), WARP_ENTRY(DT, 16, 8, 2, 0, 0, EPI),                  \
+        WARP_ENTRY(DT, 16, 16, 1, 0, 0, EPI), WARP_ENTRY(DT, 16, 16, 2, 0, 0, EPI),            \
+        WARP_ENTRY(DT, 16, 32, 1, 0, 0, EPI), WARP_ENTRY(DT, 16, 32, 2, 0, 0, EPI),            \
+        WARP_ENTRY(DT, 16, 32, 4, 0, 0, EPI), WARP_ENTRY(DT, 16, 32, 2, 8, 0, EPI),            \
+        WARP_ENTRY(DT, 16, 32, 4, 8, 0, EPI), WARP_ENTRY(DT, 32, 32, 1, 0, 0, EPI),            \
+        WARP_ENTRY(DT, 32, 32, 2, 0, 0, EPI), CTA_ENTRY(DT, 16, 1, 1024, 2, 1, EPI),           \
+        CTA_ENTRY(DT, 32, 1, 1024, 1, 1, EPI), CTA_ENTRY(DT, 16, 2, 1024, 2, 1, EPI),          \
+        CTA_ENTRY(DT, 32, 2, 1024, 0, 1, EPI), CTA_ENTRY(DT, 16, 4, 1024, 0, 1, EPI),          \
+        CTA_ENTRY(DT, 32, 4, 512, 0, 1, EPI), CTA_ENTRY(DT, 16, 2, 256, 8, 1, EPI),            \
+        CTA_ENTRY(DT, 16, 3, 512, 3, 1, EPI), CTA_ENTRY(DT, 16, 4, 256, 6, 1, EPI),            \
+        CTA_ENTRY(DT, 16, 4, 512, 2, 1, EPI), CTA_ENTRY(DT, 16, 8, 512, 0, 1, EPI),            \
+        CTAF_ENTRY(DT, 16, 512, 1, 0, 0, EPI), LOOP_ENTRY(DT, 16, 512, 2, 1, EPI)
+
+#define ROWREG_SET(DT, EPI) WARP_ENTRY(DT, 16, 4, 1, 0, 0, EPI), ROWREG_SET_WIDE(DT, EPI)
 
 } // namespace rowreg
 } // namespace rmsnorm

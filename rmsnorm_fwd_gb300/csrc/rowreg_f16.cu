@@ -5,7 +5,7 @@
 namespace rmsnorm {
 namespace rowreg {
 namespace {
-const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_F16)};
+const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_F16, RMSNORM_EPI_PLAIN)};
 } // namespace
 } // namespace rowreg
 

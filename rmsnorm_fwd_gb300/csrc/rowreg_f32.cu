@@ -5,7 +5,7 @@
 namespace rmsnorm {
 namespace rowreg {
 namespace {
-const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_F32)};
+const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_F32, RMSNORM_EPI_PLAIN)};
 } // namespace
 } // namespace rowreg
 

@@ -45,16 +45,16 @@ int round_up(int v, int m)
     return (v + m - 1) / m * m;
 }
 
-// Finds the table entry for (variant, dtype, vec_bytes, tpr, nv, cache) with
-// no occupancy cap; -1 if none.
-int find_kernel(int variant, int dtype, int vec_bytes, int tpr, int nv, int cache = 0)
+// Finds the table entry for (variant, dtype, vec_bytes, tpr, nv, cache,
+// epilogue) with no occupancy cap; -1 if none.
+int find_kernel(int variant, int dtype, int vec_bytes, int tpr, int nv, int cache, int epi)
 {
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
         if (d.variant == variant && d.dtype == dtype && d.vec_bytes == vec_bytes &&
-            d.tpr == tpr && d.nv == nv && d.cache == cache && d.minb == 0)
+            d.tpr == tpr && d.nv == nv && d.cache == cache && d.minb == 0 && d.epi == epi)
             return i;
     }
     return -1;
@@ -70,6 +70,7 @@ struct Shape {
     bool a32;
     int sm_count;
     int smem_optin;
+    int epi; // rmsnorm_epilogue_t
 };
 
 void clear(rmsnorm_plan_t *p)
@@ -100,19 +101,20 @@ int plan_generic(const Shape &s, rmsnorm_plan_t *p)
     p->rows_per_block = 1;
     p->grid = grid_for(s.rows, int64_t(s.sm_count) * (kMaxThreadsPerSm / block));
     p->smem_bytes = 0;
-    p->kernel_index = find_kernel(RMSNORM_VARIANT_GENERIC, s.dtype, 0, 0, 0);
+    p->kernel_index = find_kernel(RMSNORM_VARIANT_GENERIC, s.dtype, 0, 0, 0, 0, s.epi);
     return p->kernel_index >= 0 ? RMSNORM_OK : RMSNORM_ERR_VARIANT;
 }
 
 // Exact lookup of a register-resident instantiation by its parameters.
-int find_rowreg(int variant, int dtype, int vb, int tpr, int nv, int maxt, int minb, int cache)
+int find_rowreg(int variant, int dtype, int vb, int tpr, int nv, int maxt, int minb, int cache,
+                int epi)
 {
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
     for (int i = 0; i < n; ++i) {
         const KernelDesc &d = t[i];
         if (d.variant == variant && d.dtype == dtype && d.vec_bytes == vb && d.tpr == tpr &&
-            d.nv == nv && d.block == maxt && d.minb == minb && d.cache == cache)
+            d.nv == nv && d.block == maxt && d.minb == minb && d.cache == cache && d.epi == epi)
             return i;
     }
     return -1;
@@ -142,7 +144,8 @@ int plan_warp_exact(const Shape &s, int tpr, int nv, int minb, int64_t grid_cap,
                     rmsnorm_plan_t *p)
 {
     clear(p);
-    const int idx = find_rowreg(RMSNORM_VARIANT_WARP_PER_ROW, s.dtype, 16, tpr, nv, 256, minb, 0);
+    const int idx =
+        find_rowreg(RMSNORM_VARIANT_WARP_PER_ROW, s.dtype, 16, tpr, nv, 256, minb, 0, s.epi);
     if (idx < 0)
         return RMSNORM_ERR_VARIANT;
     p->variant = RMSNORM_VARIANT_WARP_PER_ROW;
@@ -166,9 +169,11 @@ int plan_warp(const Shape &s, rmsnorm_plan_t *p)
     const int64_t nvec = s.row_bytes / 16;
     static const int kOptions[][3] = {{4, 1, 0},  {8, 1, 0},  {8, 2, 0},  {16, 1, 0},
                                       {16, 2, 0}, {32, 1, 0}, {32, 2, 8}, {32, 4, 8}};
-    for (const auto &o : kOptions)
-        if (int64_t(o[0]) * o[1] >= nvec)
-            return plan_warp_exact(s, o[0], o[1], o[2], INT_MAX, p);
+    for (const auto &o : kOptions) // the narrowest group compiled for this epilogue
+        if (int64_t(o[0]) * o[1] >= nvec && plan_warp_exact(s, o[0], o[1], o[2], INT_MAX, p) ==
+                                                RMSNORM_OK)
+            return RMSNORM_OK;
+    clear(p);
     return RMSNORM_ERR_VARIANT;
 }
 
@@ -178,7 +183,7 @@ int plan_cta_exact(const Shape &s, int vb, int nv, int maxt, int minb, int cache
 {
     clear(p);
     const int idx = find_rowreg(RMSNORM_VARIANT_CTA_PER_ROW, s.dtype, vb, tpr_fixed, nv, maxt,
-                                minb, cache);
+                                minb, cache, s.epi);
     if (idx < 0 || tpr > maxt || tpr < 32)
         return RMSNORM_ERR_VARIANT;
     p->variant = variant;
@@ -357,7 +362,8 @@ int plan_staged(const Shape &s, int blocks_per_sm, int groups_wanted, int wpr, b
     p->stages = stages;
     p->grid = grid_for(s.rows, int64_t(s.sm_count) * blocks_per_sm);
     p->smem_bytes = staged_layout(row_bytes, stages).smem_bytes;
-    p->kernel_index = find_kernel(RMSNORM_VARIANT_STAGED, s.dtype, 16, 32, 0, tma_store ? 3 : 0);
+    p->kernel_index =
+        find_kernel(RMSNORM_VARIANT_STAGED, s.dtype, 16, 32, 0, tma_store ? 3 : 0, s.epi);
     return p->kernel_index >= 0 ? RMSNORM_OK : RMSNORM_ERR_VARIANT;
 }
 
@@ -390,11 +396,15 @@ int plan_staged_auto(const Shape &s, rmsnorm_plan_t *p)
 }
 
 int check_common(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
-                 int dtype, int sm_count, int smem_optin, Shape *s)
+                 int dtype, int sm_count, int smem_optin, int epi, Shape *s)
 {
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
         return RMSNORM_ERR_UNSUPPORTED_DTYPE;
     if (rows < 0 || hidden <= 0 || hidden > kMaxHidden || sm_count <= 0 || smem_optin < 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    if (epi != RMSNORM_EPI_PLAIN && epi != RMSNORM_EPI_BIAS && epi != RMSNORM_EPI_MXFP8)
+        return RMSNORM_ERR_INVALID_ARG;
+    if (epi == RMSNORM_EPI_MXFP8 && hidden % 32 != 0) // whole 32-element scale blocks
         return RMSNORM_ERR_INVALID_ARG;
     if (rows > 0 && rows > INT64_MAX / 4 / hidden)
         return RMSNORM_ERR_INVALID_ARG;
@@ -407,18 +417,20 @@ int check_common(const void *x, const void *w, const void *y, int64_t rows, int6
     s->a32 = aligned(x, 32) && aligned(y, 32) && aligned(w, 32) && s->row_bytes % 32 == 0;
     s->sm_count = sm_count;
     s->smem_optin = smem_optin;
+    s->epi = epi;
     return RMSNORM_OK;
 }
 
 } // namespace
 
 int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
-                int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out)
+                int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out,
+                int epi)
 {
     if (!out)
         return RMSNORM_ERR_INVALID_ARG;
     Shape s;
-    int rc = check_common(x, w, y, rows, hidden, dtype, sm_count, smem_optin, &s);
+    int rc = check_common(x, w, y, rows, hidden, dtype, sm_count, smem_optin, epi, &s);
     if (rc != RMSNORM_OK)
         return rc;
     switch (variant) {
@@ -431,6 +443,10 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     case RMSNORM_VARIANT_STAGED:
         return plan_staged_auto(s, out);
     case RMSNORM_VARIANT_GENERIC:
+        if (s.epi == RMSNORM_EPI_MXFP8) { // no scalar MX body
+            clear(out);
+            return RMSNORM_ERR_VARIANT;
+        }
         return plan_generic(s, out);
     case RMSNORM_VARIANT_AUTO:
         break;
@@ -441,8 +457,13 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // ---- automatic choice (rules fitted to a sweep of every plan over row
     // sizes 128 B .. 64 KiB and 1 .. 2M rows on GB300; they depend on the
     // row's byte length, not on the element type)
-    if (!s.a16)
+    if (!s.a16) {
+        if (s.epi == RMSNORM_EPI_MXFP8) { // the MX bodies need 16-byte vectors
+            clear(out);
+            return RMSNORM_ERR_MISALIGNED;
+        }
         return plan_generic(s, out);
+    }
     const int64_t nvec = s.row_bytes / 16;
     if (s.rows <= s.sm_count) {
         // Decode: a whole warp per row up to 1 KiB rows (idle lanes cost less
@@ -477,8 +498,9 @@ wide:
     // 16..32 KiB rows: the register bodies on a persistent grid.
     if (nvec <= 2048 && plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    // 32..72 KiB rows: the shared-memory ring.
-    if (nvec <= 4608 && plan_staged_wide(s, out) == RMSNORM_OK)
+    // 32..72 KiB rows: the shared-memory ring (plain output only; the
+    // epilogues take the looped body below).
+    if (nvec <= 4608 && s.epi == RMSNORM_EPI_PLAIN && plan_staged_wide(s, out) == RMSNORM_OK)
         return RMSNORM_OK;
     // Longer rows: the looped body, one block per row.
     if (plan_cta_exact(s, 16, 0, 512, 2, 1, 0, nvec <= 5120 ? 256 : 512, INT_MAX,
@@ -488,10 +510,10 @@ wide:
 }
 
 int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const void *y,
-                  int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin)
+                  int64_t rows, int64_t hidden, int dtype, int sm_count, int smem_optin, int epi)
 {
     Shape s;
-    int rc = check_common(x, w, y, rows, hidden, dtype, sm_count, smem_optin, &s);
+    int rc = check_common(x, w, y, rows, hidden, dtype, sm_count, smem_optin, epi, &s);
     if (rc != RMSNORM_OK)
         return rc;
     int n = 0;
@@ -499,7 +521,7 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
     if (p.kernel_index < 0 || p.kernel_index >= n)
         return RMSNORM_ERR_INVALID_ARG;
     const KernelDesc &d = t[p.kernel_index];
-    if (d.dtype != dtype)
+    if (d.dtype != dtype || d.epi != epi)
         return RMSNORM_ERR_INVALID_ARG;
     const int dv = d.variant;
     const bool cta_like = dv == RMSNORM_VARIANT_CTA_PER_ROW;

@@ -236,11 +236,11 @@ def test_per_kernel_parity_plans_are_valid():
     for k in rn.kernels():
         es = tk.ES[k["dtype"]]
         for hidden, pd in tk.plans_for(k, 37, SMS, OPTIN):
-            rc = rn.rmsnorm_validate_plan(rn.Plan(**pd), A, 3 * A, 5 * A, 37, hidden, k["dtype"],
-                                          SMS, OPTIN)
+            rc = rn.rmsnorm_validate_plan_epilogue(rn.Plan(**pd), A, 3 * A, 5 * A, 37, hidden,
+                                                   k["dtype"], k["epilogue"], SMS, OPTIN)
             assert rc == rn.OK, (k, hidden, pd, rc)
             n += 1
-    assert n > 500
+    assert n > 1000
 
 
 def test_validation_rejects_bad_plans():
@@ -326,3 +326,89 @@ def test_qk_norm_overlap_rule_matches_brute_force():
         collide = bool(qset & kset)
         rc = qk(B, B + 2 * off, W, W, T, hq, hk, d, stride, stride)
         assert (rc == rn.ERR_ALIASING) == collide, (d, hq, hk, T, stride, off, rc)
+
+
+# ------------------------------------------------------------------ epilogues
+
+def plan_epi(rows, hidden, dtype, epi, variant=rn.VARIANT_AUTO, x=None, w=None, y=None):
+    return rn.rmsnorm_plan_epilogue_status(x or A, w or 3 * A, y or 5 * A, rows, hidden, dtype,
+                                           epi, SMS, OPTIN, variant)
+
+
+def test_epilogue_kernel_sets():
+    ks = rn.kernels()
+    for dt in (rn.F32, rn.BF16, rn.F16):
+        plain = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_PLAIN]
+        bias = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_BIAS]
+        mx = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_MXFP8]
+        key = lambda k: (k["variant"], k["vec_bytes"], k["tpr"], k["nv"], k["block"],
+                         k["min_blocks"], k["cache_policy"])
+        # every register / looped / generic body has a bias twin; the staged one has none
+        assert {key(k) for k in bias} == {key(k) for k in plain
+                                          if k["variant"] != rn.VARIANT_STAGED}
+        # MXFP8: the register and looped bodies except the 4-lane group
+        assert {key(k) for k in mx} == {key(k) for k in plain
+                                        if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
+                                                            rn.VARIANT_CTA_PER_ROW)
+                                        and k["tpr"] != 4}
+
+
+@pytest.mark.parametrize("epi", [rn.EPI_BIAS, rn.EPI_MXFP8])
+def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
+    """The epilogues take the same body as the plain output wherever that is
+    not the staged ring, and a kernel of their own epilogue."""
+    ks = rn.kernels()
+    for rows in (1, 8, 100, 152, 4096, 65536):
+        for hidden in (128, 512, 1024, 2048, 4096, 8192, 16384, 20480, 36864, 65536, 131072):
+            for dt in (rn.BF16, rn.F32):
+                rc, p = plan_epi(rows, hidden, dt, epi)
+                assert rc == rn.OK, (rows, hidden, dt, rc)
+                assert ks[p.kernel_index]["epilogue"] == epi
+                assert p.variant != rn.VARIANT_STAGED
+                rc0, p0 = plan_epi(rows, hidden, dt, rn.EPI_PLAIN)
+                if p0.variant != rn.VARIANT_STAGED:
+                    k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
+                    strip = lambda k: {a: b for a, b in k.items() if a not in ("index", "epilogue")}
+                    assert strip(k) == strip(k0)
+                    d, d0 = p.as_dict(), p0.as_dict()
+                    d.pop("kernel_index"), d0.pop("kernel_index")
+                    assert d == d0, (rows, hidden, dt)
+
+
+def test_epilogue_argument_rules():
+    # MXFP8 wants whole 32-element blocks and 16-byte vectors
+    assert plan_epi(64, 4000, rn.BF16, rn.EPI_MXFP8)[0] == rn.OK      # 125 blocks
+    assert plan_epi(64, 4008, rn.BF16, rn.EPI_MXFP8)[0] == rn.ERR_INVALID_ARG
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_MXFP8, x=A + 2)[0] == rn.ERR_MISALIGNED
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_MXFP8, y=A + 8)[0] == rn.ERR_MISALIGNED
+    # the bias epilogue falls back to the scalar body like the plain one
+    rc, p = plan_epi(64, 4097, rn.BF16, rn.EPI_BIAS)
+    assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC
+    assert rn.kernels()[p.kernel_index]["epilogue"] == rn.EPI_BIAS
+    # forced variants the epilogues do not have
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_BIAS, rn.VARIANT_STAGED)[0] == rn.ERR_VARIANT
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_MXFP8, rn.VARIANT_GENERIC)[0] == rn.ERR_VARIANT
+    assert plan_epi(64, 4096, rn.BF16, 7)[0] == rn.ERR_INVALID_ARG
+    # a plan naming another epilogue's kernel is refused
+    rc, p = plan_epi(64, 4096, rn.BF16, rn.EPI_PLAIN)
+    for epi in (rn.EPI_BIAS, rn.EPI_MXFP8):
+        assert rn.rmsnorm_validate_plan_epilogue(p, A, 3 * A, 5 * A, 64, 4096, rn.BF16, epi,
+                                                 SMS, OPTIN) == rn.ERR_INVALID_ARG
+
+
+def test_epilogue_calls_validate_before_context():
+    """Argument errors come before the context check (no GPU here)."""
+    lib = rn._load()
+    # hidden not a multiple of 32
+    assert lib.rmsnorm_fwd_mxfp8(A, 3 * A, 5 * A, 7 * A, 4, 100, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_INVALID_ARG
+    # non-finite bias
+    assert lib.rmsnorm_fwd_bias(A, 3 * A, 5 * A, 4, 128, float("inf"), 1e-6, rn.BF16,
+                                None) == rn.ERR_INVALID_ARG
+    # scales overlapping the codes, codes overlapping x
+    assert lib.rmsnorm_fwd_mxfp8(A, 3 * A, 5 * A, 5 * A + 64, 4, 128, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_ALIASING
+    assert lib.rmsnorm_fwd_mxfp8(A, 3 * A, A + 256, 7 * A, 4, 128, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_ALIASING
+    assert lib.rmsnorm_fwd_mxfp8(A, 3 * A, 5 * A, None, 4, 128, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_INVALID_ARG

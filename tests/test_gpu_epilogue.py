@@ -1,0 +1,214 @@
+"""GPU parity of the epilogues against the fp64 oracle: the weight offset
+(w + WEIGHT_BIAS of "CuTeDSL at Perplexity", section "QK Norm") and the
+fused MXFP8 output (same page, section "Blackwell support"; the OCP MX v1.0
+definition).
+
+* every workload shape (full compare where the oracle is quick, sampled rows
+  at the 65536-row shapes), in the selector's automatic plan;
+* every shape class the selector distinguishes (decode, short, mid, wide,
+  staged-range, looped) for f32 / bf16 / f16;
+* bias -0 reproduces the plain kernel bit for bit; in place; ragged rows;
+* MXFP8 special blocks (zero rows, NaN / Inf inputs, extreme row scales),
+  argument errors, guard bytes around the codes and the scales.
+"""
+import numpy as np
+import pytest
+
+import rmsnorm_fwd_gb300 as rn
+from rmsnorm_fwd_gb300 import inputs
+
+from _parity import compare, compare_mx, from_device, sample_rows, to_device
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def ctx():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    rn.ensure_context(0)
+    yield
+    torch.cuda.synchronize()
+    assert rn.rmsnorm_get_device_status() == rn.OK
+
+
+def run_bias(x_np, w_np, bias, eps, dtype, out_is_x=False):
+    x = to_device(x_np, dtype)
+    w = to_device(w_np, dtype)
+    y = rn.rms_norm_bias(x, w, bias, eps, out=x if out_is_x else None)
+    torch.cuda.synchronize()
+    return from_device(y, dtype)
+
+
+def run_mx(x_np, w_np, bias, eps, dtype, variant=rn.VARIANT_AUTO):
+    x = to_device(x_np, dtype)
+    w = to_device(w_np, dtype)
+    q, s = rn.rms_norm_mxfp8(x, w, eps, weight_bias=bias, variant=variant)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+SMALL = ["f32_64x128", "embed_bf16_8192x1024", "decode_bf16_1x4096", "decode_bf16_8x4096",
+         "decode_bf16_32x4096", "prefill_bf16_16384x4096"]
+WIDE = [n for n in inputs.WORKLOADS if n.startswith("wide_")]
+# (rows, hidden): decode warp / block bodies, short and mid prefill rows,
+# 16-32 KiB persistent rows, the 32-72 KiB range (staged for the plain
+# output, looped here), and rows longer than the register bodies hold.
+SHAPES = [(1, 256), (7, 1024), (100, 4096), (152, 8192), (3, 65536), (513, 64), (2049, 512),
+          (1000, 1536), (333, 2048), (97, 5120), (160, 8192), (64, 12288), (40, 20480),
+          (33, 36864), (9, 65536), (5, 131072)]
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_bias_workloads(name):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    y = run_bias(x, w, 1.0, wl.eps, wl.dtype)
+    compare(y, x, w, wl.eps, wl.dtype, bias=1.0)
+
+
+@pytest.mark.parametrize("name", SMALL)
+def test_mx_workloads(name):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    q, s = run_mx(x, w, 0.0, wl.eps, wl.dtype)
+    r = compare_mx(q, s, x, w, 0.0, wl.eps, wl.dtype)
+    assert r["rows"] == wl.rows and r["exact_codes"] > 0.999
+
+
+@pytest.mark.parametrize("name", WIDE)
+def test_epilogues_wide_workloads_sampled(name):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    idx = sample_rows(wl.rows, 48, seed=wl.key)
+    compare(run_bias(x, w, 0.5, wl.eps, wl.dtype), x, w, wl.eps, wl.dtype, rows_idx=idx,
+            bias=0.5)
+    q, s = run_mx(x, w, 0.5, wl.eps, wl.dtype)
+    compare_mx(q, s, x, w, 0.5, wl.eps, wl.dtype, rows_idx=idx)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows,hidden", SHAPES)
+def test_epilogue_shape_classes(dtype, rows, hidden):
+    if dtype == "f32" and hidden > 65536:
+        hidden //= 2
+    x, w = inputs.random_case(rows, hidden, dtype, seed=rows + hidden)
+    idx = sample_rows(rows, 64, seed=hidden) if rows * hidden > (1 << 22) else None
+    compare(run_bias(x, w, -0.25, 1e-6, dtype), x, w, 1e-6, dtype, rows_idx=idx, bias=-0.25)
+    q, s = run_mx(x, w, 1.0, 1e-6, dtype)
+    compare_mx(q, s, x, w, 1.0, 1e-6, dtype, rows_idx=idx)
+
+
+def test_bias_minus_zero_is_the_plain_kernel_bit_for_bit():
+    for name in ("embed_bf16_8192x1024", "f32_64x128", "decode_bf16_8x4096"):
+        wl = inputs.WORKLOADS[name]
+        x_np, w_np = inputs.make_inputs(wl)
+        x = to_device(x_np, wl.dtype)
+        w = to_device(w_np, wl.dtype)
+        y0 = rn.rms_norm(x, w, wl.eps)
+        y1 = rn.rms_norm_bias(x, w, -0.0, wl.eps)
+        torch.cuda.synchronize()
+        assert np.array_equal(from_device(y0, wl.dtype), from_device(y1, wl.dtype))
+
+
+def test_bias_in_place_and_ragged():
+    wl = inputs.WORKLOADS["embed_bf16_8192x1024"]
+    x, w = inputs.make_inputs(wl)
+    compare(run_bias(x, w, 1.0, wl.eps, wl.dtype, out_is_x=True), x, w, wl.eps, wl.dtype,
+            bias=1.0)
+    for dtype, hidden in (("bf16", 1001), ("f16", 4097), ("f32", 33)):
+        x, w = inputs.random_case(65, hidden, dtype, seed=hidden)
+        y = run_bias(x, w, 0.75, 1e-6, dtype)
+        assert rn.rmsnorm_last_variant() == rn.VARIANT_GENERIC
+        compare(y, x, w, 1e-6, dtype, bias=0.75)
+
+
+def test_bias_every_forced_variant():
+    x, w = inputs.random_case(300, 4096, "bf16", seed=9)
+    xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
+    for v in (rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT,
+              rn.VARIANT_GENERIC):
+        try:
+            y = rn.rms_norm_bias(xd, wd, 2.0, 1e-6, variant=v)
+        except rn.RmsnormError as e:
+            assert e.status == rn.ERR_VARIANT and v == rn.VARIANT_WARP_PER_ROW
+            continue
+        torch.cuda.synchronize()
+        compare(from_device(y, "bf16"), x, w, 1e-6, "bf16", bias=2.0)
+    with pytest.raises(rn.RmsnormError) as e:
+        rn.rms_norm_bias(xd, wd, 2.0, 1e-6, variant=rn.VARIANT_STAGED)
+    assert e.value.status == rn.ERR_VARIANT
+
+
+def test_mx_special_blocks():
+    rows, hidden = 12, 1024
+    for dtype in ("bf16", "f16", "f32"):
+        z = np.random.default_rng(3).standard_normal((rows, hidden)).astype(np.float32)
+        z[0] = 0.0                                   # all-zero row: scale 2^-127, zero codes
+        z[1, 5] = np.nan                             # NaN: the sum and so the whole row is NaN
+        z[2, 700] = np.inf                           # Inf: r = 0, one NaN element (Inf * 0)
+        z[3, :32] = 0.0                              # one zero block in a live row
+        # tiny and huge rows, normalised anyway (squares stay inside the fp32
+        # range the pages' fp32 accumulator has)
+        z[4] *= 1e-15 if dtype == "f32" else 1e-3
+        z[5] *= 1e15 if dtype == "f32" else (1e4 if dtype == "f16" else 3e4)
+        z[6, ::2] = 0.0
+        z[6, 1] = 1e4 if dtype != "f16" else 6e4     # one outlier: others go subnormal in E4M3
+        x = inputs.to_storage(z, dtype)
+        _, w = inputs.random_case(1, hidden, dtype, seed=2)
+        for eps in (1e-6, 0.0):
+            q, s = run_mx(x, w, 0.0, eps, dtype)
+            compare_mx(q, s, x, w, 0.0, eps, dtype)
+            if eps == 0.0:                           # 0 * inf: NaN row, NaN scales
+                assert (s[0] == 0xFF).all()
+            else:
+                assert (s[0] == 0).all() and np.isin(q[0], (0x00, 0x80)).all()
+            assert (s[1] == 0xFF).all()
+            assert s[2, 700 // 32] == 0xFF and (np.delete(s[2], 700 // 32) == 0).all()
+
+
+def test_mx_every_forced_variant_and_guard_bytes():
+    rows, hidden = 161, 4096
+    x, w = inputs.random_case(rows, hidden, "bf16", seed=12)
+    xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
+    pad = 4096
+    for v in (rn.VARIANT_AUTO, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT):
+        qb = torch.full((rows * hidden + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
+        sb = torch.full((rows * hidden // 32 + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
+        q = qb[pad:pad + rows * hidden].view(rows, hidden)
+        s = sb[pad:pad + rows * hidden // 32].view(rows, hidden // 32)
+        rn.rms_norm_mxfp8(xd, wd, 1e-6, weight_bias=0.0, out=q, scales=s, variant=v)
+        torch.cuda.synchronize()
+        for b in (qb, sb):
+            assert (b[:pad] == 0x5A).all() and (b[-pad:] == 0x5A).all()
+        compare_mx(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.0, 1e-6, "bf16")
+    for v, st in ((rn.VARIANT_STAGED, rn.ERR_VARIANT), (rn.VARIANT_GENERIC, rn.ERR_VARIANT)):
+        with pytest.raises(rn.RmsnormError) as e:
+            rn.rms_norm_mxfp8(xd, wd, 1e-6, variant=v)
+        assert e.value.status == st
+
+
+def test_mx_argument_errors():
+    x, w = inputs.random_case(8, 4096, "bf16", seed=13)
+    xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
+    xfull = to_device(np.concatenate([np.zeros(8, np.uint16), x.ravel()]), "bf16")
+    lib = rn._load()
+    q = torch.empty(8, 4096, dtype=torch.uint8, device="cuda")
+    s = torch.empty(8, 128, dtype=torch.uint8, device="cuda")
+    # misaligned x (one element in): no scalar MX body
+    assert lib.rmsnorm_fwd_mxfp8(xfull.data_ptr() + 2, wd.data_ptr(), q.data_ptr(), s.data_ptr(),
+                                 8, 4096, 0.0, 1e-6, rn.BF16, None) == rn.ERR_MISALIGNED
+    # hidden not a multiple of 32 (4080 = 127.5 blocks)
+    assert lib.rmsnorm_fwd_mxfp8(xd.data_ptr(), wd.data_ptr(), q.data_ptr(), s.data_ptr(), 8, 4080,
+                                 0.0, 1e-6, rn.BF16, None) == rn.ERR_INVALID_ARG
+    # scales inside the codes, codes inside x
+    assert lib.rmsnorm_fwd_mxfp8(xd.data_ptr(), wd.data_ptr(), q.data_ptr(),
+                                 q.data_ptr() + 1024, 8, 4096, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_ALIASING
+    assert lib.rmsnorm_fwd_mxfp8(xd.data_ptr(), wd.data_ptr(), xd.data_ptr(), s.data_ptr(), 8,
+                                 4096, 0.0, 1e-6, rn.BF16, None) == rn.ERR_ALIASING
+    # the zero-row call launches nothing and succeeds
+    assert lib.rmsnorm_fwd_mxfp8(xd.data_ptr(), wd.data_ptr(), q.data_ptr(), s.data_ptr(), 0,
+                                 4096, 0.0, 1e-6, rn.BF16, None) == rn.OK
+    torch.cuda.synchronize()

@@ -1,13 +1,14 @@
 """Every compiled kernel instantiation, launched with explicit plans through
-rmsnorm_fwd_ex, against the fp64 oracle: full and partly filled rows, one
-row per block and grid-stride (fewer blocks than rows), odd row counts."""
+rmsnorm_fwd_ex (plain) or rmsnorm_fwd_epilogue_ex (weight bias, MXFP8),
+against the fp64 oracle: full and partly filled rows, one row per block and
+grid-stride (fewer blocks than rows), odd row counts."""
 import numpy as np
 import pytest
 
 import rmsnorm_fwd_gb300 as rn
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, from_device, to_device
+from _parity import compare, compare_mx, from_device, to_device
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -33,7 +34,24 @@ def layout_bytes(row_bytes, stages):
 
 
 def plans_for(k, rows, sms, optin):
-    """(hidden, plan dict) cases exercising kernel k."""
+    """(hidden, plan dict) cases exercising kernel k.  MXFP8 kernels get
+    row lengths of whole 32-element blocks."""
+    cases = _plans_for(k, rows, sms, optin)
+    if k["epilogue"] != rn.EPI_MXFP8:
+        return cases
+    out = []
+    for hidden, pd in cases:
+        h = hidden // 32 * 32
+        if h == 0:
+            h = 32
+        if pd["vecs_per_thread"] and h // (k["vec_bytes"] // ES[k["dtype"]]) > \
+                pd["threads_per_row"] * pd["vecs_per_thread"]:
+            continue
+        out.append((h, pd))
+    return list({(h, tuple(sorted(pd.items()))): (h, pd) for h, pd in out}.values())
+
+
+def _plans_for(k, rows, sms, optin):
     es = ES[k["dtype"]]
     v = k["variant"]
     out = []
@@ -116,11 +134,24 @@ def test_kernel_instantiation(index):
     dt = DT_NAME[k["dtype"]]
     cases = plans_for(k, rows, sms, optin)
     assert cases, k
+    epi = k["epilogue"]
     for hidden, pd in cases:
         x_np, w_np = inputs.random_case(rows, hidden, dt, seed=index)
         x = to_device(x_np, dt)
         w = to_device(w_np, dt)
+        if epi == rn.EPI_MXFP8:
+            q = torch.full((rows, hidden), 0xAA, dtype=torch.uint8, device="cuda")
+            sc = torch.full((rows, hidden // 32), 0xAA, dtype=torch.uint8, device="cuda")
+            rn.rms_norm_mxfp8(x, w, 1e-6, weight_bias=0.625, out=q, scales=sc,
+                              plan=rn.Plan(**pd))
+            torch.cuda.synchronize()
+            compare_mx(q.cpu().numpy(), sc.cpu().numpy(), x_np, w_np, 0.625, 1e-6, dt)
+            continue
         y = torch.full_like(x, 3.0)
-        rn.rms_norm(x, w, 1e-6, out=y, plan=rn.Plan(**pd))
+        if epi == rn.EPI_BIAS:
+            rn.rms_norm_bias(x, w, 0.625, 1e-6, out=y, plan=rn.Plan(**pd))
+        else:
+            rn.rms_norm(x, w, 1e-6, out=y, plan=rn.Plan(**pd))
         torch.cuda.synchronize()
-        compare(from_device(y, dt), x_np, w_np, 1e-6, dt)
+        compare(from_device(y, dt), x_np, w_np, 1e-6, dt,
+                bias=0.625 if epi == rn.EPI_BIAS else None)

@@ -1,0 +1,61 @@
+"""The GPU tests' comparison helpers, exercised on the CPU with results the
+oracle itself produced (must pass) and with planted mistakes (must fail)."""
+import numpy as np
+import pytest
+
+import oracle
+from rmsnorm_fwd_gb300 import inputs
+
+from _parity import compare, compare_mx
+
+
+def test_compare_accepts_oracle_and_rejects_one_ulp_plus():
+    x, w = inputs.random_case(8, 256, "bf16", seed=2)
+    y = oracle.rmsnorm_bias(x, w, 0.75, 1e-6, "bf16")
+    compare(y, x, w, 1e-6, "bf16", bias=0.75)
+    bad = y.copy()
+    bad[2, 9] += 2                       # two units in the last place
+    with pytest.raises(AssertionError):
+        compare(bad, x, w, 1e-6, "bf16", bias=0.75)
+    with pytest.raises(AssertionError):  # the plain norm is not the biased one
+        compare(oracle.rmsnorm(x, w, 1e-6, "bf16"), x, w, 1e-6, "bf16", bias=0.75)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_compare_mx_accepts_band_and_rejects_planted(dtype):
+    x, w = inputs.random_case(64, 512, dtype, seed=1)
+    c, s = oracle.rmsnorm_mxfp8(x, w, 0.5, 1e-6, dtype)
+    assert compare_mx(c, s, x, w, 0.5, 1e-6, dtype)["exact_codes"] == 1.0
+    # results within the band (a 3e-6 relative change of every value) pass
+    c3, s3 = oracle.rmsnorm_mxfp8(x, w, 0.5, 1e-6, dtype, rel=3e-6)
+    compare_mx(c3, s3, x, w, 0.5, 1e-6, dtype)
+    # a code one step off, a scale one binade off, a 1e-3 relative error: fail
+    c2 = c.copy()
+    c2[3, 17] ^= 1
+    with pytest.raises(AssertionError):
+        compare_mx(c2, s, x, w, 0.5, 1e-6, dtype)
+    s2 = s.copy()
+    s2[5, 2] += 1
+    with pytest.raises(AssertionError):
+        compare_mx(c, s2, x, w, 0.5, 1e-6, dtype)
+    c4, s4 = oracle.rmsnorm_mxfp8(x, w, 0.5, 1e-6, dtype, rel=1e-3)
+    with pytest.raises(AssertionError):
+        compare_mx(c4, s4, x, w, 0.5, 1e-6, dtype)
+
+
+def test_compare_mx_band_scale_block():
+    # A block whose maximum sits just below a power of two: a 1e-6 relative
+    # change moves its scale; both choices (with their own codes) pass.
+    x = np.zeros((1, 32), np.float32)
+    x[0, :] = 1.0
+    x[0, 0] = np.float32(np.sqrt(32.0))  # sets the row's RMS
+    w = np.ones(32, np.float32)
+    y = oracle.rmsnorm_bias_f64(x, w, 0.0, 0.0, "f32")
+    # scale the weight so the maximum lands at 2^3 * (1 - 2e-6)
+    k = (8.0 * (1 - 2e-6)) / y.max()
+    w = (w * np.float32(k)).astype(np.float32)
+    c, s = oracle.rmsnorm_mxfp8(x, w, 0.0, 0.0, "f32")
+    chi, shi = oracle.rmsnorm_mxfp8(x, w, 0.0, 0.0, "f32", rel=1e-5)
+    assert shi[0, 0] == s[0, 0] + 1
+    assert compare_mx(c, s, x, w, 0.0, 0.0, "f32")["band_blocks"] == 1
+    compare_mx(chi, shi, x, w, 0.0, 0.0, "f32")
