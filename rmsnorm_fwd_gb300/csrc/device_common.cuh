@@ -268,18 +268,87 @@ __device__ inline void st_codes(void *p, const uint32_t (&w)[NB / 4])
                      : "memory");
 }
 
+// Two fp32 lanes in one 64-bit register for the sm_100-family packed
+// arithmetic (add / mul / fma .rn.f32x2: one instruction for two IEEE
+// operations, each rounded exactly as its scalar form).
+__device__ inline uint64_t f2(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ inline void f2split(uint64_t v, float &a, float &b)
+{
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ inline uint64_t add2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ inline uint64_t mul2(uint64_t a, uint64_t b)
+{
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ inline uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
+// Element pair p of a vector (elements 2p and 2p + 1) widened to fp32.
+template <int DT, int VB>
+__device__ inline uint64_t widen_pair(const Vec<VB> &v, int p)
+{
+    float a, b = 0.f;
+    if (Elem<DT>::kPerWord == 2) {
+        Elem<DT>::widen(v.w[p], a, b);
+    } else {
+        float u;
+        Elem<DT>::widen(v.w[2 * p], a, u);
+        Elem<DT>::widen(v.w[2 * p + 1], b, u);
+    }
+    return f2(a, b);
+}
+
+// Sum of squares of one vector into two fp32 accumulators (even and odd
+// elements), one packed fma per element pair.
+template <int DT, int VB>
+__device__ inline uint64_t sumsq2(const Vec<VB> &v, uint64_t acc)
+{
+    constexpr int P = VB / Elem<DT>::kSize / 2;
+#pragma unroll
+    for (int p = 0; p < P; ++p) {
+        const uint64_t x = widen_pair<DT, VB>(v, p);
+        acc = fma2(x, x, acc);
+    }
+    return acc;
+}
+
+// max(|a|, m), a NaN in either giving NaN (max.NaN).
+__device__ inline float absmax_nan(float a, float m)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(m));
+    return r;
+}
+
 // One vector of the MXFP8 epilogue (OCP Microscaling v1.0 with E4M3
 // elements; "CuTeDSL at Perplexity", section "Blackwell support", for the
 // absolute maximum taken over the lanes that share a 32-element block).
 //
-// v = (x * r) * (w + bias) in fp32; the block maximum of |v| is taken on the
-// bit patterns (for non-negative floats the integer order is the numeric
-// order, and Inf / NaN patterns sort above every finite value, so they
-// reach the scale instead of being dropped as fmaxf would drop a NaN) with
-// butterfly shuffles over the block's kLanes lanes.  Its biased exponent e
-// gives the shared exponent floor(log2 max) - 8 = e - 135, clamped at -127:
-// E8M0 code max(e - 8, 0), or 0xFF for Inf / NaN.  Scaling by 2^(127 - code)
-// is exact, and the conversion rounds each scaled value to E4M3.
+// v = (x * r) * (w + bias) in fp32, two elements per packed instruction.
+// The block maximum of |v| is a NaN-propagating max (a NaN or an Inf in the
+// block must reach the scale; fmaxf would drop a NaN), reduced over the
+// block's kLanes lanes with butterfly shuffles.  Its biased exponent e gives
+// the shared exponent floor(log2 max) - 8 = e - 135, clamped at -127: E8M0
+// code max(e - 8, 0), or 0xFF when e = 255 (Inf / NaN).  Scaling by
+// 2^(127 - code) is exact, and the conversion rounds each scaled value to
+// E4M3.
 //
 // Every lane of the warp must call this (the shuffles span the full warp);
 // `live` says whether this lane's vector is part of the row.  The lane
@@ -290,32 +359,34 @@ __device__ inline void mx_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, f
 {
     constexpr int NE = Mx<DT, VB>::kElems;
     constexpr int LPB = Mx<DT, VB>::kLanes;
-    constexpr int PW = Elem<DT>::kPerWord;
-    float f[NE];
+    constexpr int P = NE / 2;
+    const uint64_t r2 = f2(r, r), b2 = f2(bias, bias);
+    uint64_t v[P];
+    float m = 0.f;
 #pragma unroll
-    for (int k = 0; k < Vec<VB>::kWords; ++k) {
-        float xa, xb = 0.f, wa, wb = 0.f;
-        Elem<DT>::widen(xv.w[k], xa, xb);
-        Elem<DT>::widen(wv.w[k], wa, wb);
-        f[k * PW] = (xa * r) * (wa + bias);
-        if (PW == 2)
-            f[k * PW + PW - 1] = (xb * r) * (wb + bias);
+    for (int p = 0; p < P; ++p) {
+        const uint64_t x = widen_pair<DT, VB>(xv, p);
+        const uint64_t w = widen_pair<DT, VB>(wv, p);
+        v[p] = mul2(mul2(x, r2), add2(w, b2));
+        float a, b;
+        f2split(v[p], a, b);
+        m = absmax_nan(a, absmax_nan(b, m));
     }
-    uint32_t m = 0u;
-#pragma unroll
-    for (int i = 0; i < NE; ++i)
-        m = max(m, __float_as_uint(f[i]) & 0x7FFFFFFFu);
 #pragma unroll
     for (int off = 1; off < LPB; off <<= 1)
-        m = max(m, __shfl_xor_sync(0xFFFFFFFFu, m, off, 32));
-    const uint32_t e = m >> 23;
+        m = absmax_nan(__shfl_xor_sync(0xFFFFFFFFu, m, off, 32), m);
+    const uint32_t e = __float_as_uint(m) >> 23;
     const uint32_t code = e == 255u ? 255u : (e > 8u ? e - 8u : 0u);
     const float inv = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
+    const uint64_t inv2 = f2(inv, inv);
     uint32_t words[NE / 4];
 #pragma unroll
-    for (int j = 0; j < NE / 4; ++j)
-        words[j] = e4m3x4(f[4 * j] * inv, f[4 * j + 1] * inv, f[4 * j + 2] * inv,
-                          f[4 * j + 3] * inv);
+    for (int j = 0; j < NE / 4; ++j) {
+        float a0, a1, a2, a3;
+        f2split(mul2(v[2 * j], inv2), a0, a1);
+        f2split(mul2(v[2 * j + 1], inv2), a2, a3);
+        words[j] = e4m3x4(a0, a1, a2, a3);
+    }
     if (live) {
         st_codes<NE>(q, words);
         if (leader)
