@@ -315,25 +315,47 @@ __device__ inline uint64_t widen_pair(const Vec<VB> &v, int p)
     return f2(a, b);
 }
 
-// Sum of squares of one vector into two fp32 accumulators (even and odd
-// elements), one packed fma per element pair.
+// Sum of squares of one vector, element by element in the order sumsq()
+// uses, so the total is bit-identical to it.  16-bit elements go straight
+// into the mixed-precision fma (bf16 / f16 operands, fp32 accumulator): the
+// product of two 16-bit values is exact in fp32 and the fma rounds once, as
+// the fp32 fma on the widened values does, without the widening.
 template <int DT, int VB>
-__device__ inline uint64_t sumsq2(const Vec<VB> &v, uint64_t acc)
+__device__ inline float sumsq_mixed(const Vec<VB> &v, float s)
 {
-    constexpr int P = VB / Elem<DT>::kSize / 2;
+    if constexpr (DT == RMSNORM_F32) {
+        return sumsq<DT, VB>(v, s);
+    } else {
 #pragma unroll
-    for (int p = 0; p < P; ++p) {
-        const uint64_t x = widen_pair<DT, VB>(v, p);
-        acc = fma2(x, x, acc);
+        for (int k = 0; k < Vec<VB>::kWords; ++k) {
+            if constexpr (DT == RMSNORM_BF16)
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                    "fma.rn.f32.bf16 %0, lo, lo, %0;\n\tfma.rn.f32.bf16 %0, hi, hi, %0;\n\t}"
+                    : "+f"(s)
+                    : "r"(v.w[k]));
+            else
+                asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\t"
+                    "fma.rn.f32.f16 %0, lo, lo, %0;\n\tfma.rn.f32.f16 %0, hi, hi, %0;\n\t}"
+                    : "+f"(s)
+                    : "r"(v.w[k]));
+        }
+        return s;
     }
-    return acc;
 }
 
-// max(|a|, m), a NaN in either giving NaN (max.NaN).
-__device__ inline float absmax_nan(float a, float m)
+// max(|a|, |b|, m), a NaN in any giving NaN (three-input max.NaN).
+__device__ inline float absmax3_nan(float a, float b, float m)
 {
     float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(fabsf(a)), "f"(m));
+    asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(fabsf(a)), "f"(fabsf(b)), "f"(m));
+    return r;
+}
+
+// max(a, m), a NaN in either giving NaN.
+__device__ inline float max_nan(float a, float m)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(m));
     return r;
 }
 
@@ -370,11 +392,11 @@ __device__ inline void mx_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, f
         v[p] = mul2(mul2(x, r2), add2(w, b2));
         float a, b;
         f2split(v[p], a, b);
-        m = absmax_nan(a, absmax_nan(b, m));
+        m = absmax3_nan(a, b, m);
     }
 #pragma unroll
     for (int off = 1; off < LPB; off <<= 1)
-        m = absmax_nan(__shfl_xor_sync(0xFFFFFFFFu, m, off, 32), m);
+        m = max_nan(__shfl_xor_sync(0xFFFFFFFFu, m, off, 32), m);
     const uint32_t e = __float_as_uint(m) >> 23;
     const uint32_t code = e == 255u ? 255u : (e > 8u ? e - 8u : 0u);
     const float inv = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);

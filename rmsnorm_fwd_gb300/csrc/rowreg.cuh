@@ -97,19 +97,9 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                 vzero(xv[k]);
         }
         float s = 0.f;
-        if constexpr (MX) { // packed: even and odd elements in two accumulators
-            uint64_t s2 = 0ull;
 #pragma unroll
-            for (int k = 0; k < NV; ++k)
-                s2 = sumsq2<DT, VB>(xv[k], s2);
-            float lo, hi;
-            f2split(s2, lo, hi);
-            s = lo + hi;
-        } else {
-#pragma unroll
-            for (int k = 0; k < NV; ++k)
-                s = sumsq<DT, VB>(xv[k], s);
-        }
+        for (int k = 0; k < NV; ++k)
+            s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<TPR>(s);
         const float r = row_factor(s, n, eps);
 #pragma unroll
@@ -202,19 +192,9 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                 vzero(xv[k]);
         }
         float s = 0.f;
-        if constexpr (MX) {
-            uint64_t s2 = 0ull;
 #pragma unroll
-            for (int k = 0; k < NV; ++k)
-                s2 = sumsq2<DT, VB>(xv[k], s2);
-            float lo, hi;
-            f2split(s2, lo, hi);
-            s = lo + hi;
-        } else {
-#pragma unroll
-            for (int k = 0; k < NV; ++k)
-                s = sumsq<DT, VB>(xv[k], s);
-        }
+        for (int k = 0; k < NV; ++k)
+            s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<32>(s);
         if (TPRC != 32) {
             if (lane == 0)
@@ -306,7 +286,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
             }
 #pragma unroll
             for (int u = 0; u < U; ++u)
-                s = sumsq<DT, VB>(xv[u], s);
+                s = MX ? sumsq_mixed<DT, VB>(xv[u], s) : sumsq<DT, VB>(xv[u], s);
         }
         s = group_allreduce<32>(s);
         if (lane == 0)

@@ -479,6 +479,24 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         if (plan_looped(s, RMSNORM_VARIANT_PERSISTENT, false, out) == RMSNORM_OK)
             return RMSNORM_OK;
     }
+    // Prefill with the MXFP8 output: its body issues about half again as many
+    // instructions per element as the plain one and is issue-bound at two
+    // vectors per thread, so it takes four (the per-row work spread over
+    // twice the elements): 2-16 KiB rows on blocks of nvec / 4 threads, 16-32
+    // KiB rows on 32-byte vectors with a persistent grid of 4 blocks per SM
+    // (the fastest plans of a sweep on GB300).
+    if (s.epi == RMSNORM_EPI_MXFP8 && s.a32 && nvec > 64 && nvec <= 128 &&
+        plan_cta_exact(s, 32, 1, 1024, 1, 1, 0, tpr_for(nvec / 2, 1), int64_t(s.sm_count) * 16,
+                       RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
+        return RMSNORM_OK; // 1-2 KiB rows: one 32-byte vector per thread, 16 blocks per SM
+    if (s.epi == RMSNORM_EPI_MXFP8 && nvec > 128 && nvec <= 1024 &&
+        plan_cta_exact(s, 16, 4, 256, 6, 1, 0, tpr_for(nvec, 4), INT_MAX,
+                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+        return RMSNORM_OK;
+    if (s.epi == RMSNORM_EPI_MXFP8 && s.a32 && nvec > 1024 && nvec <= 2048 &&
+        plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), int64_t(s.sm_count) * 4,
+                       RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
+        return RMSNORM_OK;
     // Prefill.  Short rows: lane groups of one warp, several rows per warp.
     if (nvec > 1024)
         goto wide;

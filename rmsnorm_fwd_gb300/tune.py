@@ -34,14 +34,16 @@ def staged_smem(row_bytes: int, stages: int) -> int:
     return bar + slot * (stages + 1)
 
 
-def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int) -> list[dict]:
-    """Explicit plans worth timing for this shape (the library validates each)."""
+def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
+               epi: int = 0) -> list[dict]:
+    """Explicit plans worth timing for this shape and epilogue (the library
+    validates each)."""
     import rmsnorm_fwd_gb300 as rn
     es = ES[dtype]
     dt = rn.DTYPE_CODES[dtype]
     out = []
     for k in rn.kernels():
-        if k["dtype"] != dt:
+        if k["dtype"] != dt or k["epilogue"] != epi:
             continue
         v = k["variant"]
         if v == rn.VARIANT_WARP_PER_ROW:
@@ -116,8 +118,10 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int) -> list
     return out
 
 
-def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> list[dict]:
-    """Time the automatic plan and every candidate; sorted fastest first."""
+def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
+               epi: int = 0) -> list[dict]:
+    """Time the automatic plan and every candidate; sorted fastest first.
+    epi: the epilogue (0 plain, 1 weight bias, 2 MXFP8 output)."""
     import torch
 
     import rmsnorm_fwd_gb300 as rn
@@ -131,16 +135,33 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
     base = [torch.randn(rows, hidden, device=dev).to(tdt) for _ in range(min(nsets, 4))]
     xs = [base[i % len(base)] if i < len(base) else base[i % len(base)].clone()
           for i in range(nsets)]
-    ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+    mx = epi == rn.EPI_MXFP8
+    if mx:
+        ys = [torch.empty(rows * hidden, dtype=torch.uint8, device=dev) for _ in range(nsets)]
+        ss = [torch.empty(rows * hidden // 32, dtype=torch.uint8, device=dev)
+              for _ in range(nsets)]
+        sp = [t.data_ptr() for t in ss]
+    else:
+        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+        sp = [None] * nsets
     w = (1 + 0.1 * torch.randn(hidden, device=dev)).to(tdt)
-    fwd = rn._load().rmsnorm_fwd_ex
+    lib = rn._load()
     s = torch.cuda.current_stream().cuda_stream
     dt = rn.DTYPE_CODES[dtype]
     xp = [t.data_ptr() for t in xs]
     yp = [t.data_ptr() for t in ys]
+
+    def fwd(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref, j=0):
+        if epi == 0:
+            return lib.rmsnorm_fwd_ex(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref)
+        return lib.rmsnorm_fwd_epilogue_ex(x, wp, y, sp[j], rows_, hidden_, epi, 1.0, eps, dt_,
+                                           stream, variant, ref)
+
     auto = rn.Plan()
-    rn.rmsnorm_fwd_ex(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, auto)
-    cands = [auto.as_dict()] + ([] if _AUTO_ONLY else candidates(rows, hidden, dtype, sms, optin))
+    fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, rn.ctypes.byref(auto))
+    cands = [auto.as_dict()] + ([] if _AUTO_ONLY else candidates(rows, hidden, dtype, sms, optin,
+                                                                  epi))
+    out_bytes = rows * hidden + rows * hidden // 32 if mx else rows * hidden * es
     out = []
     for ci, c in enumerate(cands):
         p = rn.Plan(**c)
@@ -148,7 +169,8 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
         if fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, ref) != 0:
             continue
         for i in range(5):
-            fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref)
+            fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref,
+                i % nsets)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -158,7 +180,7 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
             with torch.cuda.graph(g_, stream=cs):
                 for i in range(iters):
                     fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt,
-                        cs.cuda_stream, 0, ref)
+                        cs.cuda_stream, 0, ref, i % nsets)
             g_.replay()
             torch.cuda.synchronize()
             e0.record()
@@ -167,11 +189,12 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool) -> l
         else:
             e0.record()
             for i in range(iters):
-                fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref)
+                fwd(xp[i % nsets], w.data_ptr(), yp[i % nsets], rows, hidden, 1e-6, dt, s, 0, ref,
+                    i % nsets)
             e1.record()
         torch.cuda.synchronize()
         us = e0.elapsed_time(e1) / iters * 1e3
-        gbs = (2 * rows * hidden * es + hidden * es) / (us * 1e-6) / 1e9
+        gbs = (rows * hidden * es + hidden * es + out_bytes) / (us * 1e-6) / 1e9
         out.append({"us": round(us, 3), "GBps": round(gbs, 1), "auto": ci == 0, "plan": c})
     del xs, ys, base
     torch.cuda.empty_cache()
@@ -304,6 +327,7 @@ def main(argv=None) -> int:
     ap.add_argument("--auto-only", action="store_true", help="time only the automatic plan")
     ap.add_argument("--summarize", default="", help="print a markdown table of a --grid output")
     ap.add_argument("--qk-workload", default="", help="sweep the QK-norm launch shapes instead")
+    ap.add_argument("--epilogue", default="plain", choices=["plain", "bias", "mxfp8"])
     args = ap.parse_args(argv)
     if args.qk_workload:
         if args.pdl is not None:
@@ -320,8 +344,9 @@ def main(argv=None) -> int:
         rn.rmsnorm_set_pdl(bool(args.pdl))
     global _AUTO_ONLY
     _AUTO_ONLY = args.auto_only
+    epi = {"plain": 0, "bias": 1, "mxfp8": 2}[args.epilogue]
     if not args.grid:
-        res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph)
+        res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph, epi)
         for r in res:
             print(json.dumps(r), flush=True)
         return 0
@@ -336,7 +361,7 @@ def main(argv=None) -> int:
         if "decode" in classes:
             points += [(f"decode{r}", r, 200, True) for r in (1, 8, 32, 128)]
         for cls, rows, iters, graph in points:
-            res = time_plans(rows, h, "bf16", iters, graph)
+            res = time_plans(rows, h, "bf16", iters, graph, epi)
             auto = next((r for r in res if r["auto"]), None)
             print(json.dumps({"hidden_bf16": h, "row_bytes": 2 * h, "rows": rows, "class": cls,
                               "top": res[:args.keep], "auto": auto}), flush=True)
