@@ -97,7 +97,11 @@ typedef enum {
     RMSNORM_VARIANT_PERSISTENT = 4,
     /* Any hidden and any element alignment: scalar loads, two passes over
      * the row (the second from cache).  Fallback for ragged shapes. */
-    RMSNORM_VARIANT_GENERIC = 5
+    RMSNORM_VARIANT_GENERIC = 5,
+    /* Decode shapes with long rows: each row split over a thread-block
+     * cluster of 2, 4 or 8 blocks (on as many SMs); the blocks' partial sums
+     * meet through distributed shared memory.  Plain output only. */
+    RMSNORM_VARIANT_CLUSTER = 6
 } rmsnorm_variant_t;
 
 /* A launch plan: what the selector chose.  Filled by rmsnorm_plan. */
@@ -108,7 +112,8 @@ typedef struct {
     int32_t vecs_per_thread; /* register-resident vectors per thread per row */
     int32_t block_threads;   /* threads per block */
     int32_t rows_per_block;  /* rows a block works on at once */
-    int32_t stages;          /* staged: row slots in shared memory; else 0 */
+    int32_t stages;          /* staged: row slots in shared memory; cluster: blocks per row
+                              * (the cluster size, 2, 4 or 8); else 0 */
     int32_t grid;            /* blocks launched (0 when rows == 0) */
     int32_t smem_bytes;      /* dynamic shared memory per block */
     int32_t kernel_index;    /* internal instantiation index */

@@ -42,8 +42,9 @@ VARIANT_CTA_PER_ROW = 2
 VARIANT_STAGED = 3
 VARIANT_PERSISTENT = 4
 VARIANT_GENERIC = 5
+VARIANT_CLUSTER = 6
 VARIANT_NAMES = {0: "auto", 1: "warp_per_row", 2: "cta_per_row", 3: "staged", 4: "persistent",
-                 5: "generic"}
+                 5: "generic", 6: "cluster"}
 
 # epilogues (rmsnorm_epilogue_t)
 EPI_PLAIN, EPI_BIAS, EPI_MXFP8 = 0, 1, 2

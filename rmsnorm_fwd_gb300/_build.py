@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librmsnorm.so")
 
-SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu",
+SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu", "cluster.cu",
            "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu",
            "rowreg_epi_f32.cu", "rowreg_epi_bf16.cu", "rowreg_epi_f16.cu"]
 HEADERS = ["internal.h", "device_common.cuh", "rowreg.cuh"]

@@ -24,7 +24,7 @@ const KernelDesc *kernel_table(int *n)
         const KernelDesc *(*parts[])(int *) = {
             rowreg_kernels_f32,     rowreg_kernels_bf16,     rowreg_kernels_f16,
             staged_kernels,         generic_kernels,         rowreg_epi_kernels_f32,
-            rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16};
+            rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16, cluster_kernels};
         for (auto part : parts) {
             int m = 0;
             const KernelDesc *t = part(&m);

@@ -64,7 +64,7 @@ using LaunchFn = cudaError_t (*)(const rmsnorm_plan_t &, const LaunchArgs &);
 
 // One compiled kernel instantiation.
 struct KernelDesc {
-    int32_t variant;     // WARP_PER_ROW, CTA_PER_ROW (also PERSISTENT), STAGED, GENERIC
+    int32_t variant;     // WARP_PER_ROW, CTA_PER_ROW (also PERSISTENT), STAGED, GENERIC, CLUSTER
     int32_t dtype;       // rmsnorm_dtype_t
     int32_t vec_bytes;   // 16 / 32; 0 = scalar
     int32_t tpr;         // threads per row, compile time (warp kernels); 0 = runtime
@@ -86,6 +86,7 @@ const KernelDesc *rowreg_epi_kernels_f32(int *n); // BIAS and MXFP8 epilogues
 const KernelDesc *rowreg_epi_kernels_bf16(int *n);
 const KernelDesc *rowreg_epi_kernels_f16(int *n);
 const KernelDesc *staged_kernels(int *n);
+const KernelDesc *cluster_kernels(int *n);
 const KernelDesc *generic_kernels(int *n);
 
 const KernelDesc *kernel_table(int *n);

@@ -386,6 +386,51 @@ int plan_staged_wide(const Shape &s, rmsnorm_plan_t *p)
     return RMSNORM_OK;
 }
 
+// ---- cluster: a row over C blocks of one cluster (decode, long rows).
+// Slice S = ceil(nvec / C) vectors per block; the fewest vectors per thread
+// that keep the block at <= 512 threads (<= 1024 with 4 per thread).
+int plan_cluster_exact(const Shape &s, int C, int vb, rmsnorm_plan_t *p)
+{
+    clear(p);
+    if (s.epi != RMSNORM_EPI_PLAIN)
+        return RMSNORM_ERR_VARIANT;
+    if (!(vb == 32 ? s.a32 : s.a16))
+        return RMSNORM_ERR_MISALIGNED;
+    if ((C != 2 && C != 4 && C != 8) || s.rows > INT_MAX / C)
+        return RMSNORM_ERR_VARIANT;
+    const int64_t nvec = s.row_bytes / vb;
+    const int64_t S = (nvec + C - 1) / C;
+    for (int nv : {1, 2, 4}) {
+        const int tpr = tpr_for(S, nv);
+        if (tpr > (nv == 4 ? 1024 : 512))
+            continue;
+        const int idx = find_rowreg(RMSNORM_VARIANT_CLUSTER, s.dtype, vb, 0, nv, 1024, 0, 1, s.epi);
+        if (idx < 0)
+            continue;
+        p->variant = RMSNORM_VARIANT_CLUSTER;
+        p->vec_bytes = vb;
+        p->threads_per_row = tpr * C;
+        p->vecs_per_thread = nv;
+        p->block_threads = tpr;
+        p->rows_per_block = 1;
+        p->stages = C;
+        p->grid = static_cast<int>(s.rows * C);
+        p->kernel_index = idx;
+        return RMSNORM_OK;
+    }
+    return RMSNORM_ERR_VARIANT;
+}
+
+// Forced cluster: the smallest cluster whose slices are <= 8 KiB (at most 8
+// blocks), 16-byte vectors.
+int plan_cluster(const Shape &s, rmsnorm_plan_t *p)
+{
+    int C = 2;
+    while (C < 8 && s.row_bytes > int64_t(C) * 8192)
+        C *= 2;
+    return plan_cluster_exact(s, C, 16, p);
+}
+
 // Forced staged: one warp per row up to 8 KiB rows, wider groups beyond.
 int plan_staged_auto(const Shape &s, rmsnorm_plan_t *p)
 {
@@ -442,6 +487,8 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return plan_cta(s, true, out);
     case RMSNORM_VARIANT_STAGED:
         return plan_staged_auto(s, out);
+    case RMSNORM_VARIANT_CLUSTER:
+        return plan_cluster(s, out);
     case RMSNORM_VARIANT_GENERIC:
         if (s.epi == RMSNORM_EPI_MXFP8) { // no scalar MX body
             clear(out);
@@ -585,9 +632,22 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
     }
     case RMSNORM_VARIANT_GENERIC:
         break;
+    case RMSNORM_VARIANT_CLUSTER: {
+        const int C = p.stages;
+        if (C != 2 && C != 4 && C != 8)
+            return RMSNORM_ERR_VARIANT;
+        const int64_t S = (nvec + C - 1) / C;
+        if (p.block_threads > d.block || int64_t(p.block_threads) * d.nv < S)
+            return RMSNORM_ERR_VARIANT;
+        if (int64_t(p.grid) != rows * C) // one cluster per row, exactly
+            return RMSNORM_ERR_VARIANT;
+        break;
+    }
     default:
         return RMSNORM_ERR_INVALID_ARG;
     }
+    if (dv != RMSNORM_VARIANT_STAGED && dv != RMSNORM_VARIANT_CLUSTER && p.stages != 0)
+        return RMSNORM_ERR_INVALID_ARG;
     if (dv != RMSNORM_VARIANT_STAGED && p.smem_bytes != 0)
         return RMSNORM_ERR_INVALID_ARG;
     return RMSNORM_OK;

@@ -109,6 +109,19 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
                                         vecs_per_thread=0, block_threads=32 * (c * wpr + 1),
                                         rows_per_block=c, stages=st, grid=min(rows, sms * bps),
                                         smem_bytes=staged_smem(rb, st), kernel_index=k["index"]))
+        elif v == rn.VARIANT_CLUSTER:
+            vb = k["vec_bytes"]
+            if hidden * es % vb or rows > 4 * sms:
+                continue
+            nvec = hidden * es // vb
+            for C in (2, 4, 8):
+                S = -(-nvec // C)
+                tpr = max(32, -(-(-(-S // k["nv"])) // 32) * 32)
+                if tpr > 1024 or (k["nv"] > 1 and tpr < 64):
+                    continue
+                out.append(dict(variant=v, vec_bytes=vb, threads_per_row=tpr * C,
+                                vecs_per_thread=k["nv"], block_threads=tpr, rows_per_block=1,
+                                stages=C, grid=rows * C, smem_bytes=0, kernel_index=k["index"]))
         elif v == rn.VARIANT_GENERIC:
             for b in (256, 512, 1024):
                 out.append(dict(variant=v, vec_bytes=0, threads_per_row=b, vecs_per_thread=0,
@@ -285,7 +298,8 @@ def time_qk_plans(name: str, iters: int, graph: bool) -> list[dict]:
 def plan_label(p: dict, kinfo: dict) -> str:
     """Short text for a plan: variant, vector bytes, threads/row, vectors/thread,
     block, grid, stages, register floor, cache policy."""
-    v = {1: "warp", 2: "block", 3: "staged", 4: "persistent", 5: "generic"}[p["variant"]]
+    v = {1: "warp", 2: "block", 3: "staged", 4: "persistent", 5: "generic",
+         6: "cluster"}[p["variant"]]
     k = kinfo[p["kernel_index"]]
     nv = p["vecs_per_thread"] if p["variant"] != 3 else 0
     extra = f" W{p['threads_per_row'] // 32}" if p["variant"] == 3 else f" {nv}v"

@@ -343,9 +343,11 @@ def test_epilogue_kernel_sets():
         mx = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_MXFP8]
         key = lambda k: (k["variant"], k["vec_bytes"], k["tpr"], k["nv"], k["block"],
                          k["min_blocks"], k["cache_policy"])
-        # every register / looped / generic body has a bias twin; the staged one has none
+        # every register / looped / generic body has a bias twin; the staged and
+        # cluster ones have none
         assert {key(k) for k in bias} == {key(k) for k in plain
-                                          if k["variant"] != rn.VARIANT_STAGED}
+                                          if k["variant"] not in (rn.VARIANT_STAGED,
+                                                                  rn.VARIANT_CLUSTER)}
         # MXFP8: the register and looped bodies except the 4-lane group
         assert {key(k) for k in mx} == {key(k) for k in plain
                                         if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
@@ -422,3 +424,30 @@ def test_epilogue_calls_validate_before_context():
                                  None) == rn.ERR_ALIASING
     assert lib.rmsnorm_fwd_mxfp8(A, 3 * A, 5 * A, None, 4, 128, 0.0, 1e-6, rn.BF16,
                                  None) == rn.ERR_INVALID_ARG
+
+
+# ------------------------------------------------------------------ cluster split
+
+def test_cluster_plans():
+    for rows, hidden, C in ((1, 65536, 8), (8, 16384, 4), (1, 4096, 2), (32, 32768, 8)):
+        rc, p = plan(rows, hidden, rn.BF16, rn.VARIANT_CLUSTER)
+        assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == C
+        assert p.grid == rows * C and p.block_threads * p.vecs_per_thread * C * 16 >= hidden * 2
+        assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, rows, hidden, rn.BF16, SMS,
+                                        OPTIN) == rn.OK
+        bad = rn.Plan(**p.as_dict())
+        bad.grid += 1                       # one cluster per row, exactly
+        assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, rows, hidden, rn.BF16, SMS,
+                                        OPTIN) == rn.ERR_VARIANT
+        bad = rn.Plan(**p.as_dict())
+        bad.stages = 3                      # cluster sizes 2, 4, 8
+        assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, rows, hidden, rn.BF16, SMS,
+                                        OPTIN) == rn.ERR_VARIANT
+    # plain output only; vectors need alignment
+    assert plan_epi(1, 65536, rn.BF16, rn.EPI_BIAS, rn.VARIANT_CLUSTER)[0] == rn.ERR_VARIANT
+    assert plan(1, 65536, rn.BF16, rn.VARIANT_CLUSTER, xoff=2)[0] == rn.ERR_MISALIGNED
+    # a stages value on a non-staged, non-cluster plan is refused
+    rc, p = plan(64, 4096, rn.BF16, rn.VARIANT_CTA_PER_ROW)
+    p.stages = 2
+    assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, 64, 4096, rn.BF16, SMS,
+                                    OPTIN) == rn.ERR_INVALID_ARG

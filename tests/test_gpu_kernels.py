@@ -106,6 +106,17 @@ def _plans_for(k, rows, sms, optin):
                                                  block_threads=32 * (groups * wpr + 1),
                                                  rows_per_block=groups, stages=st, grid=grid,
                                                  smem_bytes=smem, kernel_index=k["index"])))
+    elif v == rn.VARIANT_CLUSTER:
+        vpe = k["vec_bytes"] // es
+        for C in (2, 4, 8):
+            for tpr in (32, 160, 512):
+                S = tpr * k["nv"]                       # a full slice per block
+                for nvec in sorted({S * C, S * (C - 1) + 1, max(1, S * C - tpr + 3), 3}):
+                    out.append((nvec * vpe, dict(variant=v, vec_bytes=k["vec_bytes"],
+                                                 threads_per_row=tpr * C,
+                                                 vecs_per_thread=k["nv"], block_threads=tpr,
+                                                 rows_per_block=1, stages=C, grid=rows * C,
+                                                 smem_bytes=0, kernel_index=k["index"])))
     elif v == rn.VARIANT_GENERIC:
         for hidden in (1, 33, 1000, 4097):
             for block in (32, 256):

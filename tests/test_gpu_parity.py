@@ -72,7 +72,7 @@ def test_wide_workload_sampled(name):
 
 @pytest.mark.parametrize("variant", [rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
                                      rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT,
-                                     rn.VARIANT_GENERIC])
+                                     rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER])
 def test_headline_shape_every_variant(variant):
     wl = inputs.WORKLOADS["prefill_bf16_16384x4096"]
     x, w = inputs.make_inputs(wl)
@@ -91,7 +91,7 @@ HIDDEN = [1, 2, 3, 7, 8, 9, 31, 33, 127, 128, 129, 1000, 1023, 1024, 1025, 2880,
           7168, 8191, 16384, 32768]
 ROWS = [0, 1, 2, 31, 160, 161]
 VARIANTS = [rn.VARIANT_AUTO, rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
-            rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT, rn.VARIANT_GENERIC]
+            rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT, rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER]
 
 
 def accepts(rows, hidden, dtype, variant):
