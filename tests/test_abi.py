@@ -358,8 +358,9 @@ def test_epilogue_kernel_sets():
 @pytest.mark.parametrize("epi", [rn.EPI_BIAS, rn.EPI_MXFP8])
 def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
     """The epilogues take the same body as the plain output wherever that is
-    not the staged ring (MXFP8: nor the 2-32 KiB prefill rows, where it takes
-    four vectors per thread), and a kernel of their own epilogue."""
+    not the staged ring or the cluster split (MXFP8: nor the 1-32 KiB prefill
+    rows, where it takes its own shapes), and a kernel of their own
+    epilogue."""
     ks = rn.kernels()
     for rows in (1, 8, 100, 152, 4096, 65536):
         for hidden in (128, 512, 1024, 2048, 4096, 8192, 16384, 20480, 36864, 65536, 131072):
@@ -378,7 +379,7 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                         p.threads_per_row * nv * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
-                if p0.variant != rn.VARIANT_STAGED:
+                if p0.variant not in (rn.VARIANT_STAGED, rn.VARIANT_CLUSTER):
                     k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
                     strip = lambda k: {a: b for a, b in k.items() if a not in ("index", "epilogue")}
                     assert strip(k) == strip(k0)
@@ -451,3 +452,19 @@ def test_cluster_plans():
     p.stages = 2
     assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, 64, 4096, rn.BF16, SMS,
                                     OPTIN) == rn.ERR_INVALID_ARG
+
+
+def test_cluster_split_chosen_for_long_decode_rows():
+    ks = rn.kernels()
+    for rows, hidden, C in ((1, 32768, 8), (1, 65536, 8), (8, 65536, 8), (19, 65536, 8),
+                            (20, 65536, 4), (32, 32768, 4), (64, 32768, 2), (76, 32768, 2)):
+        rc, p = plan(rows, hidden, rn.BF16)
+        assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == C, \
+            (rows, hidden, p.as_dict())
+        assert p.vec_bytes == 32 and p.block_threads <= 512
+        assert ks[p.kernel_index]["variant"] == rn.VARIANT_CLUSTER
+    # shorter rows, more rows than fit one block per SM, or an epilogue: no cluster
+    for rows, hidden, epi in ((1, 16384, 0), (32, 16384, 0), (77, 32768, 0), (153, 65536, 0),
+                              (1, 65536, rn.EPI_BIAS), (1, 65536, rn.EPI_MXFP8)):
+        rc, p = plan_epi(rows, hidden, rn.BF16, epi)
+        assert rc == rn.OK and p.variant != rn.VARIANT_CLUSTER, (rows, hidden, epi)
