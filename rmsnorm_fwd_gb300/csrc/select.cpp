@@ -522,7 +522,8 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
             while (C > 2 && s.rows * C > s.sm_count)
                 C /= 2;
             if (s.rows * C <= s.sm_count &&
-                plan_cluster_exact(s, C, s.a32 ? 32 : 16, out) == RMSNORM_OK)
+                ((s.a32 && plan_cluster_exact(s, C, 32, out) == RMSNORM_OK) ||
+                 plan_cluster_exact(s, C, 16, out) == RMSNORM_OK))
                 return RMSNORM_OK;
         }
         // Decode: a whole warp per row up to 1 KiB rows (idle lanes cost less

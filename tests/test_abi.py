@@ -463,6 +463,10 @@ def test_cluster_split_chosen_for_long_decode_rows():
             (rows, hidden, p.as_dict())
         assert p.vec_bytes == 32 and p.block_threads <= 512
         assert ks[p.kernel_index]["variant"] == rn.VARIANT_CLUSTER
+    # 512 KiB rows: 16-byte vectors, four per thread, 1024 threads per block
+    rc, p = plan(1, 131072, rn.F32)
+    assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == 8
+    assert p.vec_bytes == 16 and p.vecs_per_thread == 4 and p.block_threads == 1024
     # shorter rows, more rows than fit one block per SM, or an epilogue: no cluster
     for rows, hidden, epi in ((1, 16384, 0), (32, 16384, 0), (77, 32768, 0), (153, 65536, 0),
                               (1, 65536, rn.EPI_BIAS), (1, 65536, rn.EPI_MXFP8)):
