@@ -513,11 +513,13 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     }
     const int64_t nvec = s.row_bytes / 16;
     if (s.rows <= s.sm_count) {
-        // Decode rows of 64 KiB or more: one row over a cluster of blocks, as
-        // large a cluster (<= 8) as keeps every block on its own SM (measured
-        // on GB300: 1 x 64 Ki bf16 6.1 -> 2.6 us, 8 x 64 Ki 9.1 -> 3.3 us,
-        // 32 x 32 Ki 4.0 -> 3.6 us; shorter rows gain nothing).
-        if (s.epi == RMSNORM_EPI_PLAIN && s.row_bytes >= 64 * 1024) {
+        // Decode rows longer than 32 KiB (up to 8 of them; any number from 48
+        // KiB): one row over a cluster of blocks, as large a cluster (<= 8) as
+        // keeps every block on its own SM (measured on GB300: 1 x 64 Ki bf16
+        // 6.1 -> 2.6 us, 8 x 64 Ki 9.1 -> 3.3 us, 8 x 24 Ki 2.9 -> 2.4 us,
+        // 32 x 32 Ki 4.0 -> 3.6 us; 32 KiB rows and shorter gain nothing).
+        if (s.epi == RMSNORM_EPI_PLAIN && s.row_bytes > 32 * 1024 &&
+            (s.rows <= 8 || s.row_bytes >= 48 * 1024)) {
             int C = 8;
             while (C > 2 && s.rows * C > s.sm_count)
                 C /= 2;

@@ -457,7 +457,8 @@ def test_cluster_plans():
 def test_cluster_split_chosen_for_long_decode_rows():
     ks = rn.kernels()
     for rows, hidden, C in ((1, 32768, 8), (1, 65536, 8), (8, 65536, 8), (19, 65536, 8),
-                            (20, 65536, 4), (32, 32768, 4), (64, 32768, 2), (76, 32768, 2)):
+                            (20, 65536, 4), (32, 32768, 4), (64, 32768, 2), (76, 32768, 2),
+                            (1, 20480, 8), (8, 20480, 8), (32, 24576, 4)):
         rc, p = plan(rows, hidden, rn.BF16)
         assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == C, \
             (rows, hidden, p.as_dict())
@@ -469,6 +470,7 @@ def test_cluster_split_chosen_for_long_decode_rows():
     assert p.vec_bytes == 16 and p.vecs_per_thread == 4 and p.block_threads == 1024
     # shorter rows, more rows than fit one block per SM, or an epilogue: no cluster
     for rows, hidden, epi in ((1, 16384, 0), (32, 16384, 0), (77, 32768, 0), (153, 65536, 0),
+                              (9, 20480, 0), (32, 20480, 0),
                               (1, 65536, rn.EPI_BIAS), (1, 65536, rn.EPI_MXFP8)):
         rc, p = plan_epi(rows, hidden, rn.BF16, epi)
         assert rc == rn.OK and p.variant != rn.VARIANT_CLUSTER, (rows, hidden, epi)
