@@ -75,6 +75,14 @@ def lib() -> ctypes.CDLL:
         l.oracle_e4m3_value.restype = ctypes.c_double
         l.oracle_e4m3_encode.argtypes = [ctypes.c_double]
         l.oracle_e4m3_encode.restype = ctypes.c_uint8
+        l.oracle_mxfp4_quantize.argtypes = [vp, i64, i64, vp, vp]
+        l.oracle_mxfp4_quantize.restype = i32
+        l.oracle_nvfp4_quantize.argtypes = [vp, i64, i64, ctypes.c_double, vp, vp]
+        l.oracle_nvfp4_quantize.restype = i32
+        l.oracle_e2m1_value.argtypes = [ctypes.c_uint8]
+        l.oracle_e2m1_value.restype = ctypes.c_double
+        l.oracle_e2m1_encode.argtypes = [ctypes.c_double]
+        l.oracle_e2m1_encode.restype = ctypes.c_uint8
         l.oracle_qk_norm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32]
         l.oracle_qk_norm.restype = i32
         l.oracle_round_value.argtypes = [ctypes.c_double, i32]
@@ -189,6 +197,57 @@ def rmsnorm_mxfp8(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float, 
     if rel:
         y32 = y32 * (1.0 + rel)
     return mxfp8_quantize(y32)
+
+
+def mxfp4_quantize(v: np.ndarray) -> tuple:
+    """MXFP4 of a [rows, cols] array (cols a multiple of 32): (packed E2M1
+    codes uint8 [rows, cols / 2], even element in the low nibble; E8M0 scales
+    uint8 [rows, cols / 32])."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    rows, cols = v.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.empty((rows, max(cols // 32, 0)), dtype=np.uint8)
+    if lib().oracle_mxfp4_quantize(_ptr(v), rows, cols, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle_mxfp4_quantize rejected its arguments")
+    return codes, scales
+
+
+def nvfp4_quantize(v: np.ndarray, global_scale: float) -> tuple:
+    """NVFP4 of a [rows, cols] array (cols a multiple of 16) against the
+    per-tensor scale: (packed E2M1 codes uint8 [rows, cols / 2]; E4M3 scales
+    uint8 [rows, cols / 16])."""
+    v = np.ascontiguousarray(v, dtype=np.float64)
+    rows, cols = v.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.empty((rows, max(cols // 16, 0)), dtype=np.uint8)
+    if lib().oracle_nvfp4_quantize(_ptr(v), rows, cols, float(global_scale), _ptr(codes),
+                                   _ptr(scales)) != 0:
+        raise ValueError("oracle_nvfp4_quantize rejected its arguments")
+    return codes, scales
+
+
+def rmsnorm_fp4(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float, dtype, fmt: str,
+                global_scale: float = 1.0, rel: float = 0.0) -> tuple:
+    """The normalised rows quantised to "mxfp4" or "nvfp4"; the deciding
+    values are the binary32 row results, scaled by (1 + rel), as for
+    rmsnorm_mxfp8."""
+    y = rmsnorm_bias_f64(x, w, weight_bias, eps, dtype)
+    y32 = round_to(y, "f32").astype(np.float64)
+    if rel:
+        y32 = y32 * (1.0 + rel)
+    if fmt == "mxfp4":
+        return mxfp4_quantize(y32)
+    if fmt == "nvfp4":
+        return nvfp4_quantize(y32, global_scale)
+    raise ValueError(fmt)
+
+
+def e2m1_value(code: int) -> float:
+    return lib().oracle_e2m1_value(int(code))
+
+
+def e2m1_encode(v: float) -> int:
+    return int(lib().oracle_e2m1_encode(float(v)))
 
 
 def e4m3_value(code: int) -> float:

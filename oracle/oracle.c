@@ -25,10 +25,13 @@
  *
  *   Same page, section "Blackwell support" (MXFP8 / MXFP4 / NVFP4, absolute
  *   maxima over blocks of 16 or 32 elements): the normalised row may instead
- *   leave as MXFP8 -- E4M3 elements with one power-of-two E8M0 scale per 32
- *   consecutive elements.  The pages name the format but do not define it;
- *   the definition used is the one the OCP Microscaling (MX) v1.0
- *   specification publishes (see the MXFP8 section below).
+ *   leave as MXFP8 (E4M3 elements, one power-of-two E8M0 scale per 32
+ *   consecutive elements), MXFP4 (E2M1 elements, the same scales) or NVFP4
+ *   (E2M1 elements, one E4M3 scale per 16 elements times a per-tensor fp32
+ *   scale).  The pages name the formats but do not define them; the
+ *   definitions used are the OCP Microscaling (MX) v1.0 specification's for
+ *   the MX formats and NVIDIA's published description of NVFP4 (see the
+ *   sections below).
  *
  * Every value is widened exactly to IEEE binary64 and every operation runs in
  * binary64, left to right, with no blocking, fusion or reordering.  The final
@@ -440,5 +443,139 @@ int oracle_mxfp8_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *
     for (int64_t i = 0; i < rows; ++i)
         for (int64_t b = 0; b < nb; ++b)
             mx_block(v + i * cols + b * 32, 32, codes + i * cols + b * 32, scales + i * nb + b);
+    return 0;
+}
+
+/* ---- MXFP4 and NVFP4: E2M1 elements -------------------------------------- */
+
+/*
+ * E2M1 (the OCP 4-bit floating-point element format): 1 sign bit, 2 exponent
+ * bits with bias 1, 1 fraction bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; no
+ * infinity or NaN.  Codes are 4-bit values 0..15 (sign in bit 3).
+ */
+double oracle_e2m1_value(uint8_t code)
+{
+    int sign = (code >> 3) & 1;
+    int expo = (code >> 1) & 0x3;
+    int frac = code & 0x1;
+    double mag = expo == 0 ? 0.5 * frac : ldexp(1.0 + 0.5 * frac, expo - 1);
+    return sign ? -mag : mag;
+}
+
+/* Round to E2M1, nearest with ties to even, saturating at +-6 (the largest
+ * magnitude).  The format has no NaN: a NaN input gives the code of +-6
+ * (only inside a block whose scale is NaN, where element codes carry no
+ * value). */
+uint8_t oracle_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 0x8 : 0x0;
+    if (isnan(v))
+        return (uint8_t)(sign | 0x7);
+    double a = fabs(v);
+    /* p = 2 significand bits, minimum normal exponent 0, largest exponent 2 */
+    double r = isinf(a) ? 6.0 : round_to_format(a, 2, 0, 2);
+    if (isinf(r) || r > 6.0)
+        r = 6.0;
+    if (r == 0.0)
+        return sign;
+    if (r < 1.0)
+        return (uint8_t)(sign | 0x1); /* the subnormal 0.5 */
+    int k;
+    frexp(r, &k);
+    int e = k - 1; /* r in [2^e, 2^(e+1)), e in 0..2 */
+    uint8_t frac = (uint8_t)(ldexp(r, 1 - e) - 2.0);
+    return (uint8_t)(sign | (uint8_t)((e + 1) << 1) | frac);
+}
+
+/* Element j of a row goes to byte j / 2, low nibble for even j. */
+static void put_nibble(uint8_t *row, int64_t j, uint8_t code)
+{
+    if (j % 2 == 0)
+        row[j / 2] = (uint8_t)((row[j / 2] & 0xF0) | (code & 0xF));
+    else
+        row[j / 2] = (uint8_t)((row[j / 2] & 0x0F) | (uint8_t)((code & 0xF) << 4));
+}
+
+/*
+ * MXFP4 (OCP MX v1.0 with E2M1 elements): per 32 consecutive elements the
+ * shared exponent floor(log2(max |v|)) - 2 (2 = the largest E2M1 exponent),
+ * clamped to [-127, 127], stored as E8M0 (0xFF for a block holding a NaN or
+ * an infinity; an all-zero block takes -127); each element v / 2^shared
+ * rounded to E2M1.  Codes are packed two per byte, the even element in the
+ * low nibble: codes [rows, cols / 2], scales [rows, cols / 32].
+ */
+int oracle_mxfp4_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *codes,
+                          uint8_t *scales)
+{
+    if (rows < 0 || cols <= 0 || cols % 32 != 0)
+        return -1;
+    const int64_t nb = cols / 32;
+    for (int64_t i = 0; i < rows; ++i) {
+        uint8_t *crow = codes + i * (cols / 2);
+        for (int64_t b = 0; b < nb; ++b) {
+            const double *blk = v + i * cols + b * 32;
+            double amax = 0.0;
+            int special = 0;
+            for (int j = 0; j < 32; ++j) {
+                if (isnan(blk[j]) || isinf(blk[j]))
+                    special = 1;
+                else if (fabs(blk[j]) > amax)
+                    amax = fabs(blk[j]);
+            }
+            int shared = -127;
+            if (amax > 0.0) {
+                int k;
+                frexp(amax, &k);
+                shared = (k - 1) - 2;
+                if (shared < -127)
+                    shared = -127;
+                if (shared > 127)
+                    shared = 127;
+            }
+            scales[i * nb + b] = special ? 0xFF : (uint8_t)(shared + 127);
+            for (int j = 0; j < 32; ++j)
+                put_nibble(crow, b * 32 + j, oracle_e2m1_encode(ldexp(blk[j], -shared)));
+        }
+    }
+    return 0;
+}
+
+/*
+ * NVFP4 (NVIDIA's description of the format: E2M1 elements, an E4M3 scale
+ * per 16 consecutive elements, and a per-tensor fp32 scale g).  A value is
+ * represented as code * scale * g.  Per block:
+ *     s      = E4M3( max |v| / (6 * g) )        nearest-even, saturating at 448
+ *     code_j = E2M1( v_j / (value(s) * g) )     (every code zero when value(s) = 0)
+ * The division by 6 maps the block maximum onto the largest E2M1 magnitude.
+ * A NaN in the block gives the NaN scale code 0x7F.  g must be positive and
+ * finite.  Codes [rows, cols / 2] packed as for MXFP4, scales [rows, cols / 16].
+ */
+int oracle_nvfp4_quantize(const double *v, int64_t rows, int64_t cols, double g, uint8_t *codes,
+                          uint8_t *scales)
+{
+    if (rows < 0 || cols <= 0 || cols % 16 != 0 || !(g > 0.0) || isinf(g))
+        return -1;
+    const int64_t nb = cols / 16;
+    for (int64_t i = 0; i < rows; ++i) {
+        uint8_t *crow = codes + i * (cols / 2);
+        for (int64_t b = 0; b < nb; ++b) {
+            const double *blk = v + i * cols + b * 16;
+            double amax = 0.0;
+            int nan = 0;
+            for (int j = 0; j < 16; ++j) {
+                if (isnan(blk[j]))
+                    nan = 1;
+                else if (fabs(blk[j]) > amax)
+                    amax = fabs(blk[j]);
+            }
+            uint8_t s = nan ? 0x7F : oracle_e4m3_encode(amax / (6.0 * g));
+            scales[i * nb + b] = s;
+            double d = nan ? NAN : oracle_e4m3_value(s);
+            for (int j = 0; j < 16; ++j) {
+                double t = d == 0.0 ? blk[j] * 0.0 : blk[j] / (d * g);
+                put_nibble(crow, b * 16 + j, oracle_e2m1_encode(t));
+            }
+        }
+    }
     return 0;
 }

@@ -58,6 +58,17 @@ int oracle_mxfp8_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *
 double oracle_e4m3_value(uint8_t code);
 uint8_t oracle_e4m3_encode(double v);
 
+/* MXFP4: E2M1 codes packed two per byte (even element in the low nibble)
+ * [rows, cols / 2], E8M0 scales [rows, cols / 32]; cols a multiple of 32. */
+int oracle_mxfp4_quantize(const double *v, int64_t rows, int64_t cols, uint8_t *codes,
+                          uint8_t *scales);
+/* NVFP4: E2M1 codes as for MXFP4, E4M3 scales [rows, cols / 16] against the
+ * per-tensor scale g > 0; cols a multiple of 16. */
+int oracle_nvfp4_quantize(const double *v, int64_t rows, int64_t cols, double g, uint8_t *codes,
+                          uint8_t *scales);
+double oracle_e2m1_value(uint8_t code);
+uint8_t oracle_e2m1_encode(double v);
+
 /* Single-element helpers behind the array functions. */
 double oracle_widen(const void *base, int64_t index, int fmt);
 double oracle_round_value(double v, int fmt);

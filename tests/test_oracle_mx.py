@@ -210,3 +210,137 @@ def test_rmsnorm_mxfp8_reconstructs_rows():
     hi, _ = oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "bf16", rel=1e-5)
     # the bracket moves only codes near a rounding boundary
     assert np.mean(lo != hi) < 0.01
+
+
+# ------------------------------------------------------------------ E2M1, MXFP4, NVFP4
+
+E2M1_CODES = list(range(16))
+
+
+def _golden_fp4():
+    d = {}
+    with open(os.path.join(GOLDEN, "fp4_hand_example.txt")) as fh:
+        for line in fh:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                k, *v = line.split()
+                d[k] = [float(t) for t in v]
+    return d
+
+
+def _unpack(codes, cols):
+    """[rows, cols / 2] packed bytes -> [rows, cols] 4-bit codes (even element low)."""
+    lo = codes & 0xF
+    hi = codes >> 4
+    out = np.empty((codes.shape[0], cols), dtype=np.uint8)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out
+
+
+def _e2m1(codes):
+    return np.array([oracle.e2m1_value(int(c)) for c in np.ravel(codes)]).reshape(np.shape(codes))
+
+
+def test_e2m1_values_and_brute_force_rounding():
+    mags = [oracle.e2m1_value(c) for c in range(8)]
+    assert mags == [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert [oracle.e2m1_value(c + 8) for c in range(8)] == [-m for m in mags]
+    pos = sorted(set(mags))
+    mids = [(a + b) / 2 for a, b in zip(pos, pos[1:])]
+    rng = np.random.default_rng(9)
+    vals = list(rng.uniform(-8, 8, 500)) + mids + [-m for m in mids] + \
+        [m * (1 + 1e-9) for m in mids] + [m * (1 - 1e-9) for m in mids] + [7.0, -100.0, 1e30]
+    from fractions import Fraction
+    for v in vals:
+        best = None
+        for c in E2M1_CODES:
+            dd = abs(Fraction(oracle.e2m1_value(c)) - Fraction(v))   # exact distances
+            if best is None or dd < best[0] or (dd == best[0] and (c & 1) == 0 and (best[1] & 1)):
+                best = (dd, c)
+        got = oracle.e2m1_encode(v)
+        assert oracle.e2m1_value(got) == oracle.e2m1_value(best[1]), (v, got, best)
+    for c in E2M1_CODES:
+        if c != 8:   # -0 encodes as 8, +0 as 0
+            assert oracle.e2m1_encode(oracle.e2m1_value(c)) == c
+
+
+def test_fp4_hand_examples():
+    g = _golden_fp4()
+    v = np.arange(1, 33, dtype=np.float64)[None, :]
+    codes, scales = oracle.mxfp4_quantize(v)
+    assert scales[0, 0] == g["mx4_scale"][0]
+    assert codes[0, :4].tolist() == g["mx4_bytes0_3"]          # the nibble order
+    q = _e2m1(_unpack(codes, 32))[0]
+    assert q[:8].tolist() == g["mx4_first8"] and q[-2:].tolist() == g["mx4_last2"]
+    codes, scales = oracle.nvfp4_quantize(v, 1.0)
+    assert scales[0].tolist() == g["nv4_scales"]
+    q = _e2m1(_unpack(codes, 32))[0]
+    assert q[:4].tolist() == g["nv4_first4"] and q[15] == g["nv4_last_of_block0"][0]
+    assert [q[16], q[31]] == g["nv4_block1_first_last"]
+
+
+def test_mxfp4_invariant_and_error_bound():
+    rng = np.random.default_rng(10)
+    v = _blocks(rng, 2000, lo=-130, hi=120)
+    v[::89] = 0.0
+    codes, scales = oracle.mxfp4_quantize(v.reshape(-1, 64))
+    q = _e2m1(_unpack(codes, 64)).reshape(-1, 32)
+    scales = scales.reshape(-1)
+    for b in range(v.shape[0]):
+        amax = np.max(np.abs(v[b]))
+        s = int(scales[b]) - 127
+        X = 2.0 ** s
+        if amax == 0:
+            assert scales[b] == 0 and not q[b].any()
+            continue
+        if s > -127:
+            assert 4.0 <= amax / X < 8.0, (b, amax, s)   # the shared exponent's definition
+        t = np.abs(v[b]) / X
+        rec = q[b] * X
+        for i in range(32):
+            if t[i] >= 6:
+                assert abs(q[b, i]) == 6
+            else:
+                step = 0.5 if t[i] < 2 else 2.0 ** (np.floor(np.log2(t[i])) - 1)
+                assert abs(rec[i] - v[b, i]) <= step / 2 * X
+
+
+def test_nvfp4_scale_and_error_bound():
+    rng = np.random.default_rng(11)
+    for g in (1.0, 3.7e-3, 250.0):
+        v = _blocks(rng, 1500, lo=-20, hi=20) * g
+        v[::97] = 0.0
+        codes, scales = oracle.nvfp4_quantize(v.reshape(-1, 64), g)
+        q = _e2m1(_unpack(codes, 64)).reshape(-1, 16)
+        s = np.array([oracle.e4m3_value(c) for c in scales.reshape(-1)])
+        vb = v.reshape(-1, 16)
+        for b in range(vb.shape[0]):
+            amax = np.max(np.abs(vb[b]))
+            t = amax / (6 * g)
+            # the scale is E4M3's rounding of max / (6 g): within half a step
+            if 2.0 ** -6 <= t <= 448:
+                assert abs(s[b] - t) <= 2.0 ** (np.floor(np.log2(t)) - 4) * (1 + 1e-12)
+            if s[b] == 0:
+                assert not q[b].any()
+                continue
+            d = s[b] * g
+            tt = np.abs(vb[b]) / d
+            for i in range(16):
+                if tt[i] >= 6:
+                    assert abs(q[b, i]) == 6
+                else:
+                    step = 0.5 if tt[i] < 2 else 2.0 ** (np.floor(np.log2(tt[i])) - 1)
+                    assert abs(q[b, i] * d - vb[b, i]) <= step / 2 * d * (1 + 1e-12)
+    # special blocks and argument checks
+    v = np.zeros((3, 16))
+    v[1, 4] = np.nan
+    v[2, :] = 1e-30
+    codes, scales = oracle.nvfp4_quantize(v, 1.0)
+    assert scales[0, 0] == 0 and not codes[0].any()
+    assert scales[1, 0] == 0x7F
+    assert scales[2, 0] == 0 and not (codes[2] & 0x77).any()   # signed zeros only
+    with pytest.raises(ValueError):
+        oracle.nvfp4_quantize(np.zeros((1, 24)), 1.0)
+    with pytest.raises(ValueError):
+        oracle.nvfp4_quantize(np.zeros((1, 16)), 0.0)
