@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
-                    [--op rmsnorm|qk_norm|bias|mxfp8]
+                    [--op rmsnorm|qk_norm|bias|mxfp8|mxfp4|nvfp4]
 
 A step is one RMSNorm forward over one batch: the headline workload is the
 prefill-shaped batch, 16384 rows x 4096 hidden, bf16 in/out, fp32
@@ -545,16 +545,18 @@ def run_epi(args, world, rank, local):
     x_np, w_np = inputs.make_inputs(wl, seed=rank)
     x_host = to_torch(x_np, wl.dtype, torch)
     w = to_torch(w_np, wl.dtype, torch).to(device)
-    mx = args.op == "mxfp8"
+    epi = rn.EPI_CODES[args.op]
+    mx = epi in rn.QUANT_FORMATS
     n = wl.rows * wl.hidden
-    out_bytes = (n + n // 32) if mx else n * es
+    block, bits = rn.QUANT_FORMATS.get(epi, (1, 8 * es))
+    out_bytes = (n * bits // 8 + n // block) if mx else n * es
     step_bytes = n * es + wl.hidden * es + out_bytes
     set_bytes = n * es + out_bytes
     nsets = max(2, -(-3 * L2_BYTES // set_bytes))
     xs = [x_host.to(device) for _ in range(nsets)]
     if mx:
-        ys = [torch.empty(n, dtype=torch.uint8, device=device) for _ in range(nsets)]
-        ss = [torch.empty(n // 32, dtype=torch.uint8, device=device) for _ in range(nsets)]
+        ys = [torch.empty(n * bits // 8, dtype=torch.uint8, device=device) for _ in range(nsets)]
+        ss = [torch.empty(n // block, dtype=torch.uint8, device=device) for _ in range(nsets)]
     else:
         ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
         ss = [None] * nsets
@@ -562,12 +564,12 @@ def run_epi(args, world, rank, local):
     stream = torch.cuda.current_stream(device)
     sptr = stream.cuda_stream
     dt = rn.DTYPE_CODES[wl.dtype]
-    epi = rn.EPI_MXFP8 if mx else rn.EPI_BIAS
     bias = 1.0
+    gscale = 1.0 / (448 * 6) * 4.0  # a per-tensor NVFP4 scale for values of magnitude ~4
     plan = rn.Plan()
     rn.rmsnorm_fwd_epilogue_ex(xs[0].data_ptr(), w.data_ptr(), ys[0].data_ptr(),
                                ss[0].data_ptr() if mx else None, wl.rows, wl.hidden, epi, bias,
-                               wl.eps, dt, sptr, rn.VARIANT_AUTO, plan)
+                               wl.eps, dt, sptr, rn.VARIANT_AUTO, plan, gscale)
     fn = rn._load().rmsnorm_fwd_epilogue_ex
     pref = rn.ctypes.byref(plan)
     xp = [t.data_ptr() for t in xs]
@@ -576,8 +578,8 @@ def run_epi(args, world, rank, local):
 
     def step(i):
         j = i % nsets
-        rc = fn(xp[j], w.data_ptr(), yp[j], sp[j], wl.rows, wl.hidden, epi, bias, wl.eps, dt,
-                sptr, 0, pref)
+        rc = fn(xp[j], w.data_ptr(), yp[j], sp[j], wl.rows, wl.hidden, epi, bias, gscale, wl.eps,
+                dt, sptr, 0, pref)
         if rc != rn.OK:
             raise rn.RmsnormError(rc, "rmsnorm_fwd_epilogue_ex")
 
@@ -612,13 +614,14 @@ def run_epi(args, world, rank, local):
     peak, peak_kind = hbm_peak()
     plain_bytes = wl.bytes_per_call
     line = {
-        "metric": ("RMSNorm + MXFP8 output achieved HBM GB/s" if mx else
+        "metric": (f"RMSNorm + {args.op.upper()} output achieved HBM GB/s" if mx else
                    "RMSNorm with weight offset achieved HBM GB/s"),
         "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": max(3, args.warmup), "ms_per_step": round(ms, 6), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden,
                    "io_dtype": wl.dtype, "epilogue": rn.EPI_NAMES[epi], "weight_bias": bias,
+                   "global_scale": gscale if epi == rn.EPI_NVFP4 else None,
                    "variant": rn.VARIANT_NAMES[plan.variant], "plan": plan.as_dict(),
                    "l2": f"{nsets} rotating input/output sets of {set_bytes / 1e6:.0f} MB"},
         "rows_per_s": round(wl.rows / (ms / 1e3), 1),
@@ -647,14 +650,15 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=60.0)
-    ap.add_argument("--op", choices=["rmsnorm", "qk_norm", "bias", "mxfp8"], default="rmsnorm")
+    ap.add_argument("--op", choices=["rmsnorm", "qk_norm", "bias", "mxfp8", "mxfp4", "nvfp4"],
+                    default="rmsnorm")
     ap.add_argument("--qk-workload", default="qk_bf16_16384tok_32q8k_128",
                     choices=sorted(inputs.QK_WORKLOADS))
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     if args.op == "qk_norm":
         return run_qk(args, world, rank, local)
-    if args.op in ("bias", "mxfp8"):
+    if args.op in ("bias", "mxfp8", "mxfp4", "nvfp4"):
         return run_epi(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)

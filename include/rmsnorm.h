@@ -75,7 +75,9 @@ typedef enum {
 typedef enum {
     RMSNORM_EPI_PLAIN = 0, /* y = round((x * r) * w) in the element type */
     RMSNORM_EPI_BIAS = 1,  /* y = round((x * r) * (w + weight_bias)) in the element type */
-    RMSNORM_EPI_MXFP8 = 2  /* (x * r) * (w + weight_bias) as MXFP8: E4M3 codes + E8M0 scales */
+    RMSNORM_EPI_MXFP8 = 2, /* (x * r) * (w + weight_bias) as MXFP8: E4M3 codes + E8M0 scales */
+    RMSNORM_EPI_MXFP4 = 3, /* ... as MXFP4: packed E2M1 codes + E8M0 scales per 32 */
+    RMSNORM_EPI_NVFP4 = 4  /* ... as NVFP4: packed E2M1 codes + E4M3 scales per 16 */
 } rmsnorm_epilogue_t;
 
 /* Kernel variants.  AUTO lets the selector choose from (rows, hidden, dtype,
@@ -190,14 +192,44 @@ int rmsnorm_fwd_bias(const void *x, const void *weight, void *y, int64_t rows, i
 int rmsnorm_fwd_mxfp8(const void *x, const void *weight, void *q, void *scales, int64_t rows,
                       int64_t hidden, float weight_bias, float eps, int dtype, void *stream);
 
+/* Fused RMSNorm -> MXFP4: as rmsnorm_fwd_mxfp8 with E2M1 elements (OCP MX
+ * v1.0): per 32 elements s = floor(log2(max |v|)) - 2 (2 = E2M1's largest
+ * exponent), clamped to [-127, 127], scales[i, b] = s + 127 (0xFF for a
+ * NaN / Inf block, 0 for an all-zero block); each element v / 2^s rounded to
+ * E2M1 (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6; nearest-even, saturating at
+ * +-6).  q is [rows, hidden / 2] bytes, two 4-bit codes per byte, element
+ * 2k in the low nibble of byte k; scales [rows, hidden / 32].  hidden must
+ * be a multiple of 32.  Pointer, aliasing and error rules as
+ * rmsnorm_fwd_mxfp8. */
+int rmsnorm_fwd_mxfp4(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float weight_bias, float eps, int dtype, void *stream);
+
+/* Fused RMSNorm -> NVFP4 (NVIDIA's description of the format: E2M1
+ * elements, an E4M3 scale per 16 elements, a per-tensor fp32 scale g =
+ * global_scale, a value standing for code * scale * g):
+ *
+ *   per 16 consecutive elements of a row (block b = j / 16):
+ *     scales[i, b] = E4M3( max |v| / (6 * g) )     (nearest-even, saturating at 448;
+ *                                                    0x7F when the block holds a NaN)
+ *     q[i, j]      = E2M1( v[i, j] / (value(scales[i, b]) * g) )   (0 when the scale is 0)
+ *
+ * The device forms 1 / (6 g) and 1 / (value * g) once per block and
+ * multiplies.  q is [rows, hidden / 2] bytes packed as for MXFP4; scales
+ * [rows, hidden / 16] bytes.  hidden must be a multiple of 16, global_scale
+ * positive and finite (RMSNORM_ERR_INVALID_ARG otherwise). */
+int rmsnorm_fwd_nvfp4(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float global_scale, float weight_bias, float eps,
+                      int dtype, void *stream);
+
 /* Any epilogue with a forced variant or an explicit plan (as rmsnorm_fwd_ex;
- * `scales` is used by RMSNORM_EPI_MXFP8 only, `weight_bias` by BIAS and
- * MXFP8).  The bulk-copy staged variant exists for RMSNORM_EPI_PLAIN only:
- * the automatic choice uses the register or looped bodies instead, and a
- * forced STAGED returns RMSNORM_ERR_VARIANT. */
+ * `scales` is used by the block-scaled epilogues only, `weight_bias` by all
+ * but PLAIN, `global_scale` by NVFP4 only).  The bulk-copy staged and the
+ * cluster variants exist for RMSNORM_EPI_PLAIN only: the automatic choice
+ * uses the register or looped bodies instead, and forcing them returns
+ * RMSNORM_ERR_VARIANT. */
 int rmsnorm_fwd_epilogue_ex(const void *x, const void *weight, void *y, void *scales,
                             int64_t rows, int64_t hidden, int epilogue, float weight_bias,
-                            float eps, int dtype, void *stream, int variant,
+                            float global_scale, float eps, int dtype, void *stream, int variant,
                             rmsnorm_plan_t *plan);
 
 /* The selector for an epilogue (host only, as rmsnorm_plan). */

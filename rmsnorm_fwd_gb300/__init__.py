@@ -47,8 +47,12 @@ VARIANT_NAMES = {0: "auto", 1: "warp_per_row", 2: "cta_per_row", 3: "staged", 4:
                  5: "generic", 6: "cluster"}
 
 # epilogues (rmsnorm_epilogue_t)
-EPI_PLAIN, EPI_BIAS, EPI_MXFP8 = 0, 1, 2
-EPI_NAMES = {EPI_PLAIN: "plain", EPI_BIAS: "bias", EPI_MXFP8: "mxfp8"}
+EPI_PLAIN, EPI_BIAS, EPI_MXFP8, EPI_MXFP4, EPI_NVFP4 = 0, 1, 2, 3, 4
+EPI_NAMES = {EPI_PLAIN: "plain", EPI_BIAS: "bias", EPI_MXFP8: "mxfp8", EPI_MXFP4: "mxfp4",
+             EPI_NVFP4: "nvfp4"}
+EPI_CODES = {v: k for k, v in EPI_NAMES.items()}
+# block-scaled outputs: (elements per scale block, bits per element code)
+QUANT_FORMATS = {EPI_MXFP8: (32, 8), EPI_MXFP4: (32, 4), EPI_NVFP4: (16, 4)}
 
 
 class RmsnormError(RuntimeError):
@@ -122,8 +126,10 @@ def _load() -> ctypes.CDLL:
                                     ctypes.POINTER(QkPlan)], i32),
             "rmsnorm_fwd_bias": ([vp, vp, vp, i64, i64, f32, f32, i32, vp], i32),
             "rmsnorm_fwd_mxfp8": ([vp, vp, vp, vp, i64, i64, f32, f32, i32, vp], i32),
-            "rmsnorm_fwd_epilogue_ex": ([vp, vp, vp, vp, i64, i64, i32, f32, f32, i32, vp, i32, pp],
-                                        i32),
+            "rmsnorm_fwd_mxfp4": ([vp, vp, vp, vp, i64, i64, f32, f32, i32, vp], i32),
+            "rmsnorm_fwd_nvfp4": ([vp, vp, vp, vp, i64, i64, f32, f32, f32, i32, vp], i32),
+            "rmsnorm_fwd_epilogue_ex": ([vp, vp, vp, vp, i64, i64, i32, f32, f32, f32, i32, vp,
+                                         i32, pp], i32),
             "rmsnorm_plan_epilogue": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, i32, pp], i32),
             "rmsnorm_validate_plan_epilogue": ([pp, vp, vp, vp, i64, i64, i32, i32, i32, i32],
                                                i32),
@@ -247,12 +253,26 @@ def rmsnorm_fwd_mxfp8(x: int, weight: int, q: int, scales: int, rows: int, hidde
                                      stream or None), "rmsnorm_fwd_mxfp8")
 
 
+def rmsnorm_fwd_mxfp4(x: int, weight: int, q: int, scales: int, rows: int, hidden: int,
+                      weight_bias: float, eps: float, dtype: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_fwd_mxfp4(x, weight, q, scales, rows, hidden, weight_bias, eps, dtype,
+                                     stream or None), "rmsnorm_fwd_mxfp4")
+
+
+def rmsnorm_fwd_nvfp4(x: int, weight: int, q: int, scales: int, rows: int, hidden: int,
+                      global_scale: float, weight_bias: float, eps: float, dtype: int,
+                      stream: int | None) -> None:
+    _check(_load().rmsnorm_fwd_nvfp4(x, weight, q, scales, rows, hidden, global_scale,
+                                     weight_bias, eps, dtype, stream or None), "rmsnorm_fwd_nvfp4")
+
+
 def rmsnorm_fwd_epilogue_ex(x: int, weight: int, y: int, scales: int | None, rows: int,
                             hidden: int, epilogue: int, weight_bias: float, eps: float,
                             dtype: int, stream: int | None, variant: int = VARIANT_AUTO,
-                            plan: Plan | None = None) -> None:
+                            plan: Plan | None = None, global_scale: float = 1.0) -> None:
     _check(_load().rmsnorm_fwd_epilogue_ex(x, weight, y, scales or None, rows, hidden, epilogue,
-                                           weight_bias, eps, dtype, stream or None, variant,
+                                           weight_bias, global_scale, eps, dtype, stream or None,
+                                           variant,
                                            ctypes.byref(plan) if plan is not None else None),
            "rmsnorm_fwd_epilogue_ex")
 
@@ -435,36 +455,52 @@ def rms_norm_bias(x, weight, weight_bias: float, eps: float, out=None, variant: 
     with torch.cuda.device(x.device.index):
         rmsnorm_fwd_epilogue_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), None, rows, hidden,
                                 EPI_BIAS, float(weight_bias), float(eps),
-                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
+                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan, 1.0)
     return out
+
+
+def rms_norm_quant(x, weight, eps: float, fmt: str = "mxfp8", weight_bias: float = -0.0,
+                   global_scale: float = 1.0, out=None, scales=None,
+                   variant: int = VARIANT_AUTO, plan: Plan | None = None, stream=None):
+    """RMSNorm with a block-scaled output, fmt "mxfp8" | "mxfp4" | "nvfp4":
+    (codes uint8 [..., hidden * bits / 8] -- E4M3 bytes, or two E2M1 codes per
+    byte with the even element in the low nibble -- and scales uint8
+    [..., hidden / block] -- E8M0 exponents, or E4M3 values for NVFP4, which
+    stand for code * scale * global_scale)."""
+    import torch
+    _check_rows(x, weight)
+    epi = EPI_CODES[fmt]
+    block, bits = QUANT_FORMATS[epi]
+    hidden = x.shape[-1]
+    if hidden % block:
+        raise ValueError(f"hidden must be a multiple of {block} for {fmt}")
+    lead = tuple(x.shape[:-1])
+    if out is None:
+        out = torch.empty(lead + (hidden * bits // 8,), dtype=torch.uint8, device=x.device)
+    if scales is None:
+        scales = torch.empty(lead + (hidden // block,), dtype=torch.uint8, device=x.device)
+    if out.dtype != torch.uint8 or out.numel() * 8 != x.numel() * bits or not out.is_contiguous():
+        raise ValueError(f"out must be a contiguous uint8 tensor of x.numel() * {bits} / 8 bytes")
+    if scales.dtype != torch.uint8 or scales.numel() * block != x.numel() or \
+            not scales.is_contiguous():
+        raise ValueError(f"scales must be a contiguous uint8 tensor of x.numel() / {block} bytes")
+    ensure_context(x.device.index)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    rows = x.numel() // hidden if hidden else 0
+    with torch.cuda.device(x.device.index):
+        rmsnorm_fwd_epilogue_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), scales.data_ptr(),
+                                rows, hidden, epi, float(weight_bias), float(eps),
+                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan,
+                                float(global_scale))
+    return out, scales
 
 
 def rms_norm_mxfp8(x, weight, eps: float, weight_bias: float = -0.0, out=None, scales=None,
                    variant: int = VARIANT_AUTO, plan: Plan | None = None, stream=None):
     """RMSNorm with an MXFP8 output: (codes uint8 [..., hidden] holding E4M3
     bit patterns, scales uint8 [..., hidden / 32] holding E8M0 exponents)."""
-    import torch
-    _check_rows(x, weight)
-    hidden = x.shape[-1]
-    if hidden % 32:
-        raise ValueError("hidden must be a multiple of 32 for MXFP8")
-    if out is None:
-        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
-    if scales is None:
-        scales = torch.empty(tuple(x.shape[:-1]) + (hidden // 32,), dtype=torch.uint8,
-                             device=x.device)
-    if out.dtype != torch.uint8 or out.shape != x.shape or not out.is_contiguous():
-        raise ValueError("out must be a contiguous uint8 tensor shaped like x")
-    if scales.dtype != torch.uint8 or scales.numel() * 32 != x.numel() or not scales.is_contiguous():
-        raise ValueError("scales must be a contiguous uint8 tensor of x.numel() / 32 bytes")
-    ensure_context(x.device.index)
-    s = stream if stream is not None else torch.cuda.current_stream(x.device)
-    rows = x.numel() // hidden if hidden else 0
-    with torch.cuda.device(x.device.index):
-        rmsnorm_fwd_epilogue_ex(x.data_ptr(), weight.data_ptr(), out.data_ptr(), scales.data_ptr(),
-                                rows, hidden, EPI_MXFP8, float(weight_bias), float(eps),
-                                torch_dtype_code(x.dtype), s.cuda_stream, variant, plan)
-    return out, scales
+    return rms_norm_quant(x, weight, eps, "mxfp8", weight_bias, 1.0, out, scales, variant, plan,
+                          stream)
 
 
 def _check_rows(x, weight):

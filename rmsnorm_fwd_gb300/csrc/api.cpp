@@ -24,7 +24,8 @@ const KernelDesc *kernel_table(int *n)
         const KernelDesc *(*parts[])(int *) = {
             rowreg_kernels_f32,     rowreg_kernels_bf16,     rowreg_kernels_f16,
             staged_kernels,         generic_kernels,         rowreg_epi_kernels_f32,
-            rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16, cluster_kernels};
+            rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16, cluster_kernels,
+            rowreg_fp4_kernels_f32, rowreg_fp4_kernels_bf16, rowreg_fp4_kernels_f16};
         for (auto part : parts) {
             int m = 0;
             const KernelDesc *t = part(&m);
@@ -165,16 +166,20 @@ bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes
 
 int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
                int dtype, int epi = RMSNORM_EPI_PLAIN, float bias = -0.0f,
-               const void *scales = nullptr)
+               const void *scales = nullptr, float gscale = 1.0f)
 {
     if (dtype != RMSNORM_F32 && dtype != RMSNORM_BF16 && dtype != RMSNORM_F16)
         return RMSNORM_ERR_UNSUPPORTED_DTYPE;
     if (rows < 0 || hidden <= 0 || !(eps >= 0.f) || !std::isfinite(eps) || !std::isfinite(bias))
         return RMSNORM_ERR_INVALID_ARG;
-    if (epi != RMSNORM_EPI_PLAIN && epi != RMSNORM_EPI_BIAS && epi != RMSNORM_EPI_MXFP8)
+    if (epi < RMSNORM_EPI_PLAIN || epi > RMSNORM_EPI_NVFP4)
         return RMSNORM_ERR_INVALID_ARG;
-    const bool mx = epi == RMSNORM_EPI_MXFP8;
-    if (mx && hidden % 32 != 0)
+    const bool mx = epi >= RMSNORM_EPI_MXFP8; // a block-scaled output
+    const int block = epi == RMSNORM_EPI_NVFP4 ? 16 : 32;
+    const int bits = epi == RMSNORM_EPI_MXFP8 ? 8 : 4;
+    if (mx && hidden % block != 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    if (epi == RMSNORM_EPI_NVFP4 && !(gscale > 0.f && std::isfinite(gscale)))
         return RMSNORM_ERR_INVALID_ARG;
     if (!w || (rows > 0 && (!x || !y || (mx && !scales))))
         return RMSNORM_ERR_INVALID_ARG;
@@ -184,7 +189,7 @@ int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidd
             return RMSNORM_ERR_INVALID_ARG;
         const int64_t bytes = rows * hidden * es;
         if (mx) { // codes and scales are new buffers: no overlap with anything
-            const int64_t qb = rows * hidden, sb = rows * (hidden / 32);
+            const int64_t qb = rows * hidden * bits / 8, sb = rows * (hidden / block);
             if (ranges_overlap(x, bytes, y, qb) || ranges_overlap(w, hidden * es, y, qb) ||
                 ranges_overlap(x, bytes, scales, sb) ||
                 ranges_overlap(w, hidden * es, scales, sb) || ranges_overlap(y, qb, scales, sb))
@@ -202,9 +207,9 @@ int check_args(const void *x, const void *w, void *y, int64_t rows, int64_t hidd
 int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, float eps,
            int dtype, void *stream, int variant, rmsnorm_plan_t *plan, uint32_t flags,
            uint64_t limit_ns, int epi = RMSNORM_EPI_PLAIN, float bias = -0.0f,
-           void *scales = nullptr)
+           void *scales = nullptr, float gscale = 1.0f)
 {
-    int rc = check_args(x, w, y, rows, hidden, eps, dtype, epi, bias, scales);
+    int rc = check_args(x, w, y, rows, hidden, eps, dtype, epi, bias, scales, gscale);
     if (rc != RMSNORM_OK)
         return rc;
     DeviceCtx ctx;
@@ -245,6 +250,7 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     a.pdl = pdl_enabled();
     a.bias = bias;
     a.scales = scales;
+    a.gscale = gscale;
     if (log_enabled())
         std::fprintf(stderr,
                      "rmsnorm: rows=%lld hidden=%lld dtype=%d epi=%d -> variant=%d vec=%d tpr=%d "
@@ -369,15 +375,32 @@ int rmsnorm_fwd_mxfp8(const void *x, const void *weight, void *q, void *scales, 
                   0u, g_wait_limit.load(), RMSNORM_EPI_MXFP8, weight_bias, scales);
 }
 
+int rmsnorm_fwd_mxfp4(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float weight_bias, float eps, int dtype, void *stream)
+{
+    return launch(x, weight, q, rows, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                  0u, g_wait_limit.load(), RMSNORM_EPI_MXFP4, weight_bias, scales);
+}
+
+int rmsnorm_fwd_nvfp4(const void *x, const void *weight, void *q, void *scales, int64_t rows,
+                      int64_t hidden, float global_scale, float weight_bias, float eps,
+                      int dtype, void *stream)
+{
+    return launch(x, weight, q, rows, hidden, eps, dtype, stream, RMSNORM_VARIANT_AUTO, nullptr,
+                  0u, g_wait_limit.load(), RMSNORM_EPI_NVFP4, weight_bias, scales,
+                  global_scale);
+}
+
 int rmsnorm_fwd_epilogue_ex(const void *x, const void *weight, void *y, void *scales,
                             int64_t rows, int64_t hidden, int epilogue, float weight_bias,
-                            float eps, int dtype, void *stream, int variant,
+                            float global_scale, float eps, int dtype, void *stream, int variant,
                             rmsnorm_plan_t *plan)
 {
     return launch(x, weight, y, rows, hidden, eps, dtype, stream, variant, plan, 0u,
                   g_wait_limit.load(), epilogue,
                   epilogue == RMSNORM_EPI_PLAIN ? -0.0f : weight_bias,
-                  epilogue == RMSNORM_EPI_MXFP8 ? scales : nullptr);
+                  epilogue >= RMSNORM_EPI_MXFP8 ? scales : nullptr,
+                  epilogue == RMSNORM_EPI_NVFP4 ? global_scale : 1.0f);
 }
 
 // Whether two strided head sets can share a byte: set A is

@@ -228,12 +228,32 @@ __device__ inline void scale_bias(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB>
     }
 }
 
-// MXFP8 output geometry of one vector: its elements become that many E4M3
-// code bytes, and a 32-element scale block spans kLanes consecutive vectors
-// (held by kLanes consecutive lanes).
-template <int DT, int VB> struct Mx {
+// Block-scaled output formats ("CuTeDSL at Perplexity", section "Blackwell
+// support": MXFP8, MXFP4 and NVFP4, absolute maxima over blocks of 32 or 16
+// elements).  MX formats (OCP Microscaling v1.0): 32-element blocks, E8M0
+// power-of-two scale 2^(floor(log2 max) - kEmax), kEmax the element format's
+// largest exponent.  NVFP4 (NVIDIA's description): 16-element blocks, E4M3
+// scale E4M3(max / (6 g)) times a per-tensor fp32 scale g.
+enum { kQMxfp8 = 0, kQMxfp4 = 1, kQNvfp4 = 2 };
+template <int Q> struct QFmt;
+template <> struct QFmt<kQMxfp8> {
+    static constexpr int kBlock = 32, kBits = 8, kEmax = 8;
+};
+template <> struct QFmt<kQMxfp4> {
+    static constexpr int kBlock = 32, kBits = 4, kEmax = 2;
+};
+template <> struct QFmt<kQNvfp4> {
+    static constexpr int kBlock = 16, kBits = 4, kEmax = 0;
+};
+
+// Geometry of one vector's output: its kElems elements become kCodeBytes
+// code bytes, and one scale block spans kLanes consecutive vectors (held by
+// kLanes consecutive lanes).
+template <int DT, int VB, int Q> struct QGeo {
     static constexpr int kElems = VB / Elem<DT>::kSize;
-    static constexpr int kLanes = 32 / kElems;
+    static constexpr int kLanes = QFmt<Q>::kBlock / kElems;
+    static constexpr int kCodeBytes = kElems * QFmt<Q>::kBits / 8;
+    static_assert(kLanes >= 1, "a vector must not straddle two scale blocks");
 };
 
 // Four fp32 values to four E4M3 codes, value i in byte i.  The conversion
@@ -252,11 +272,67 @@ __device__ inline uint32_t e4m3x4(float a0, float a1, float a2, float a3)
     return r;
 }
 
-// Stores NB = 4, 8 or 16 code bytes (not allocated in L1).
-template <int NB>
-__device__ inline void st_codes(void *p, const uint32_t (&w)[NB / 4])
+// Eight fp32 values to eight E2M1 codes packed in a word, value i in
+// nibble i (the even element of each byte in its low nibble).  Nearest-even,
+// saturating at +-6 (.satfinite).  The instruction puts its first source in
+// the upper nibble of its byte.
+__device__ inline uint32_t e2m1x8(const float (&f)[8])
 {
-    if constexpr (NB == 4)
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]), "f"(f[4]), "f"(f[5]), "f"(f[6]),
+          "f"(f[7]));
+    return r;
+}
+
+// Four fp32 values to four E2M1 codes in the low 16 bits.
+__device__ inline uint32_t e2m1x4(const float (&f)[4])
+{
+    uint32_t r;
+    asm("{\n\t.reg .b8 b0, b1;\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b16 h, {b0, b1};\n\t"
+        "cvt.u32.u16 %0, h;\n\t}"
+        : "=r"(r)
+        : "f"(f[0]), "f"(f[1]), "f"(f[2]), "f"(f[3]));
+    return r;
+}
+
+// The E4M3 code of a non-negative value (nearest-even, saturating at 448, a
+// NaN giving 0x7F) and the value that code stands for.
+__device__ inline uint32_t e4m3_code(float t)
+{
+    uint16_t h;
+    asm("{\n\t.reg .b16 c;\n\tcvt.rn.satfinite.e4m3x2.f32 c, %1, %2;\n\tmov.b16 %0, c;\n\t}"
+        : "=h"(h)
+        : "f"(0.f), "f"(t));
+    return h & 0xFFu;
+}
+__device__ inline float e4m3_value(uint32_t code)
+{
+    uint32_t hh;
+    asm("{\n\t.reg .b16 c;\n\tcvt.u16.u32 c, %1;\n\tcvt.rn.f16x2.e4m3x2 %0, c;\n\t}"
+        : "=r"(hh)
+        : "r"(code));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(hh & 0xFFFFu)));
+}
+
+// Stores NB = 2, 4, 8 or 16 code bytes (not allocated in L1).
+template <int NB>
+__device__ inline void st_codes(void *p, const uint32_t (&w)[(NB + 3) / 4])
+{
+    if constexpr (NB == 2)
+        asm volatile("st.global.L1::no_allocate.u16 [%0], %1;" ::"l"(p),
+                     "h"(static_cast<unsigned short>(w[0]))
+                     : "memory");
+    else if constexpr (NB == 4)
         asm volatile("st.global.L1::no_allocate.u32 [%0], %1;" ::"l"(p), "r"(w[0]) : "memory");
     else if constexpr (NB == 8)
         asm volatile("st.global.L1::no_allocate.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(w[0]),
@@ -359,28 +435,29 @@ __device__ inline float max_nan(float a, float m)
     return r;
 }
 
-// One vector of the MXFP8 epilogue (OCP Microscaling v1.0 with E4M3
-// elements; "CuTeDSL at Perplexity", section "Blackwell support", for the
-// absolute maximum taken over the lanes that share a 32-element block).
+// One vector of a block-scaled epilogue (QFmt above).
 //
 // v = (x * r) * (w + bias) in fp32, two elements per packed instruction.
 // The block maximum of |v| is a NaN-propagating max (a NaN or an Inf in the
 // block must reach the scale; fmaxf would drop a NaN), reduced over the
-// block's kLanes lanes with butterfly shuffles.  Its biased exponent e gives
-// the shared exponent floor(log2 max) - 8 = e - 135, clamped at -127: E8M0
-// code max(e - 8, 0), or 0xFF when e = 255 (Inf / NaN).  Scaling by
-// 2^(127 - code) is exact, and the conversion rounds each scaled value to
-// E4M3.
+// block's kLanes lanes with butterfly shuffles.  MX formats: the biased
+// exponent e of the maximum gives the shared exponent floor(log2 max) - kEmax
+// = e - 127 - kEmax, clamped at -127: E8M0 code max(e - kEmax, 0), or 0xFF
+// when e = 255 (Inf / NaN); scaling by 2^(127 - code) is exact.  NVFP4: the
+// scale code is E4M3(max * (1 / (6 g))) and the values are multiplied by
+// 1 / (value(code) * g) (by 0 when the scale is 0).  The conversions round
+// each scaled value to the element format.
 //
 // Every lane of the warp must call this (the shuffles span the full warp);
 // `live` says whether this lane's vector is part of the row.  The lane
 // holding the first vector of a block (`leader`) stores the scale byte.
-template <int DT, int VB>
-__device__ inline void mx_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, float bias,
-                                bool live, bool leader, void *q, uint8_t *scale)
+template <int DT, int VB, int Q>
+__device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, float bias,
+                               float g, bool live, bool leader, void *q, uint8_t *scale)
 {
-    constexpr int NE = Mx<DT, VB>::kElems;
-    constexpr int LPB = Mx<DT, VB>::kLanes;
+    using G = QGeo<DT, VB, Q>;
+    constexpr int NE = G::kElems;
+    constexpr int LPB = G::kLanes;
     constexpr int P = NE / 2;
     const uint64_t r2 = f2(r, r), b2 = f2(bias, bias);
     uint64_t v[P];
@@ -397,20 +474,42 @@ __device__ inline void mx_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, f
 #pragma unroll
     for (int off = 1; off < LPB; off <<= 1)
         m = max_nan(__shfl_xor_sync(0xFFFFFFFFu, m, off, 32), m);
-    const uint32_t e = __float_as_uint(m) >> 23;
-    const uint32_t code = e == 255u ? 255u : (e > 8u ? e - 8u : 0u);
-    const float inv = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
-    const uint64_t inv2 = f2(inv, inv);
-    uint32_t words[NE / 4];
+    uint32_t code;
+    float mul;
+    if constexpr (Q == kQNvfp4) {
+        code = e4m3_code(m * __frcp_rn(6.f * g));
+        const float d = e4m3_value(code);
+        mul = d == 0.f ? 0.f : __frcp_rn(d * g);
+    } else {
+        constexpr uint32_t EM = QFmt<Q>::kEmax;
+        const uint32_t e = __float_as_uint(m) >> 23;
+        code = e == 255u ? 255u : (e > EM ? e - EM : 0u);
+        mul = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
+    }
+    const uint64_t mul2v = f2(mul, mul);
+    float sv[NE];
 #pragma unroll
-    for (int j = 0; j < NE / 4; ++j) {
-        float a0, a1, a2, a3;
-        f2split(mul2(v[2 * j], inv2), a0, a1);
-        f2split(mul2(v[2 * j + 1], inv2), a2, a3);
-        words[j] = e4m3x4(a0, a1, a2, a3);
+    for (int p = 0; p < P; ++p)
+        f2split(mul2(v[p], mul2v), sv[2 * p], sv[2 * p + 1]);
+    constexpr int NB = G::kCodeBytes;
+    uint32_t words[(NB + 3) / 4];
+    if constexpr (QFmt<Q>::kBits == 8) {
+#pragma unroll
+        for (int j = 0; j < NE / 4; ++j)
+            words[j] = e4m3x4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
+    } else if constexpr (NE == 4) {
+        const float f4[4] = {sv[0], sv[1], sv[2], sv[3]};
+        words[0] = e2m1x4(f4);
+    } else {
+#pragma unroll
+        for (int j = 0; j < NE / 8; ++j) {
+            const float f8[8] = {sv[8 * j], sv[8 * j + 1], sv[8 * j + 2], sv[8 * j + 3],
+                                 sv[8 * j + 4], sv[8 * j + 5], sv[8 * j + 6], sv[8 * j + 7]};
+            words[j] = e2m1x8(f8);
+        }
     }
     if (live) {
-        st_codes<NE>(q, words);
+        st_codes<NB>(q, words);
         if (leader)
             *scale = static_cast<uint8_t>(code);
     }

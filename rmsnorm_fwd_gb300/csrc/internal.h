@@ -30,7 +30,8 @@ struct LaunchArgs {
     cudaStream_t stream;
     bool pdl = false;       // launch with a programmatic dependency on the stream's last kernel
     float bias = -0.0f;     // weight offset (BIAS / MXFP8 epilogues); -0 adds nothing
-    void *scales = nullptr; // MXFP8 epilogue: E8M0 scales [rows, hidden / 32]; y holds the codes
+    void *scales = nullptr; // block-scaled epilogues: the scales; y holds the codes
+    float gscale = 1.0f;    // NVFP4: the per-tensor scale
 };
 
 #if defined(__CUDACC__)
@@ -85,6 +86,9 @@ const KernelDesc *rowreg_kernels_f16(int *n);
 const KernelDesc *rowreg_epi_kernels_f32(int *n); // BIAS and MXFP8 epilogues
 const KernelDesc *rowreg_epi_kernels_bf16(int *n);
 const KernelDesc *rowreg_epi_kernels_f16(int *n);
+const KernelDesc *rowreg_fp4_kernels_f32(int *n); // MXFP4 and NVFP4 epilogues
+const KernelDesc *rowreg_fp4_kernels_bf16(int *n);
+const KernelDesc *rowreg_fp4_kernels_f16(int *n);
 const KernelDesc *staged_kernels(int *n);
 const KernelDesc *cluster_kernels(int *n);
 const KernelDesc *generic_kernels(int *n);

@@ -47,15 +47,16 @@ __device__ inline void vzero(Vec<VB> &v)
 template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI>
 __global__ void __launch_bounds__(BLOCK, MINB > 0 ? MINB : 1)
 warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                 int32_t hidden, float eps, float bias, uint8_t *scales)
+                 int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;                     // elements per vector
     constexpr int GROUPS = BLOCK / TPR;                    // rows per block per iteration
-    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
-    constexpr int LPB = Mx<DT, VB>::kLanes;                // MX: lanes per 32-element block
-    constexpr int OB = MX ? Mx<DT, VB>::kElems : VB;       // output bytes per vector
-    static_assert(!MX || TPR % LPB == 0, "an MX block must not straddle two rows");
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;          // a block-scaled output
+    constexpr int Q = MX ? EPI - RMSNORM_EPI_MXFP8 : 0;    // its format (QFmt)
+    constexpr int LPB = QGeo<DT, VB, Q>::kLanes;           // lanes per scale block
+    constexpr int OB = MX ? QGeo<DT, VB, Q>::kCodeBytes : VB; // output bytes per vector
+    static_assert(!MX || TPR % LPB == 0, "a scale block must not straddle two rows");
     // Weight slice kept in registers (loaded before the row, off the
     // reduction's critical path): always for one vector per thread, else
     // only without a register cap.
@@ -67,7 +68,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     const int g = threadIdx.x / TPR;
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
-    const int64_t out_row = MX ? hidden : row_bytes; // output bytes per row
+    const int64_t out_row = MX ? int64_t(hidden) * QFmt<Q>::kBits / 8 : row_bytes; // per row
     const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
@@ -117,8 +118,9 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                     ld_weight(wk, wt + k * TPR * VB);
                 else
                     vzero(wk);
-                mx_store<DT, VB>(xv[k], wk, r, bias, live, t % LPB == 0, yr + k * TPR * OB,
-                                 scales + row * (hidden / 32) + (t + k * TPR) / LPB);
+                q_store<DT, VB, Q>(xv[k], wk, r, bias, gscale, live, t % LPB == 0,
+                                   yr + k * TPR * OB,
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
             } else if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -145,13 +147,14 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                int32_t hidden, float eps, float bias, uint8_t *scales)
+                int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
-    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
-    constexpr int LPB = Mx<DT, VB>::kLanes;
-    constexpr int OB = MX ? Mx<DT, VB>::kElems : VB;
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
+    constexpr int Q = MX ? EPI - RMSNORM_EPI_MXFP8 : 0;
+    constexpr int LPB = QGeo<DT, VB, Q>::kLanes;
+    constexpr int OB = MX ? QGeo<DT, VB, Q>::kCodeBytes : VB;
     constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0); // as above
     __shared__ float part[2][32];
 
@@ -165,7 +168,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     const int stride = tpr * VB; // bytes between a thread's consecutive vectors
     const float n = static_cast<float>(hidden);
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
-    const int64_t out_row = MX ? hidden : row_bytes;
+    const int64_t out_row = MX ? int64_t(hidden) * QFmt<Q>::kBits / 8 : row_bytes;
     const char *wt = static_cast<const char *>(w) + t * VB;
 
     Vec<VB> wv[W_HELD ? NV : 1];
@@ -219,8 +222,9 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                     ld_weight(wk, wt + k * stride);
                 else
                     vzero(wk);
-                mx_store<DT, VB>(xv[k], wk, r, bias, live, t % LPB == 0, yr + k * tpr * OB,
-                                 scales + row * (hidden / 32) + (t + k * tpr) / LPB);
+                q_store<DT, VB, Q>(xv[k], wk, r, bias, gscale, live, t % LPB == 0,
+                                   yr + k * tpr * OB,
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
             } else if (t + k * tpr < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -248,14 +252,15 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                int32_t hidden, float eps, float bias, uint8_t *scales)
+                int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
     constexpr int U = 4; // vectors in flight per thread per step
-    constexpr bool MX = EPI == RMSNORM_EPI_MXFP8;
-    constexpr int LPB = Mx<DT, VB>::kLanes;
-    constexpr int OB = Mx<DT, VB>::kElems;
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
+    constexpr int Q = MX ? EPI - RMSNORM_EPI_MXFP8 : 0;
+    constexpr int LPB = QGeo<DT, VB, Q>::kLanes;
+    constexpr int OB = QGeo<DT, VB, Q>::kCodeBytes;
     __shared__ float part[2][32];
 
     pdl_begin();
@@ -272,7 +277,8 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     int it = 0;
     for (int64_t row = blockIdx.x; row < rows; row += gridDim.x, ++it) {
         const char *xr = static_cast<const char *>(x) + row * row_bytes;
-        char *yr = static_cast<char *>(y) + row * (MX ? static_cast<int64_t>(hidden) : row_bytes);
+        char *yr = static_cast<char *>(y) +
+                   row * (MX ? int64_t(hidden) * QFmt<Q>::kBits / 8 : row_bytes);
         float s = 0.f;
         for (int v0 = t; v0 < nvec; v0 += U * tpr) {
             Vec<VB> xv[U];
@@ -301,7 +307,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
             // Warp-uniform trip count (the block maximum is a shuffle over
             // the whole warp): lane l of the warp starting at vector v0
             // takes vector v0 + l, the same vectors as below.
-            uint8_t *sr = scales + row * (hidden / 32);
+            uint8_t *sr = scales + row * (hidden / QFmt<Q>::kBlock);
             for (int v0 = t & ~31; v0 < nvec; v0 += U * tpr) {
                 Vec<VB> xv[U], wv[U];
 #pragma unroll
@@ -318,7 +324,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + lane + u * tpr;
-                    mx_store<DT, VB>(xv[u], wv[u], r, bias, v < nvec, lane % LPB == 0,
+                    q_store<DT, VB, Q>(xv[u], wv[u], r, bias, gscale, v < nvec, lane % LPB == 0,
                                      yr + static_cast<int64_t>(v) * OB, sr + v / LPB);
                 }
             }
@@ -357,7 +363,7 @@ cudaError_t launch_warp(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
     return launch_kernel(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP, EPI>, p.grid, BLOCK,
                          0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales));
+                         static_cast<uint8_t *>(a.scales), a.gscale);
 }
 
 template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
@@ -365,7 +371,7 @@ cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
     return launch_kernel(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC, EPI>, p.grid,
                          p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales));
+                         static_cast<uint8_t *>(a.scales), a.gscale);
 }
 
 template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
@@ -373,7 +379,7 @@ cudaError_t launch_loop(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
     return launch_kernel(cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI>, p.grid, p.block_threads, 0,
                          a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales));
+                         static_cast<uint8_t *>(a.scales), a.gscale);
 }
 
 constexpr int kWarpBlock = 256;

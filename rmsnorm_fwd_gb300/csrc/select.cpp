@@ -35,6 +35,14 @@ int elem_size(int dtype)
     return dtype == RMSNORM_F32 ? 4 : 2;
 }
 
+// Elements per scale block of an epilogue (1: not block-scaled).
+int epi_block(int epi)
+{
+    return epi == RMSNORM_EPI_MXFP8 || epi == RMSNORM_EPI_MXFP4 ? 32
+           : epi == RMSNORM_EPI_NVFP4                          ? 16
+                                                               : 1;
+}
+
 bool aligned(const void *p, int a)
 {
     return (reinterpret_cast<uintptr_t>(p) % static_cast<uintptr_t>(a)) == 0;
@@ -447,9 +455,9 @@ int check_common(const void *x, const void *w, const void *y, int64_t rows, int6
         return RMSNORM_ERR_UNSUPPORTED_DTYPE;
     if (rows < 0 || hidden <= 0 || hidden > kMaxHidden || sm_count <= 0 || smem_optin < 0)
         return RMSNORM_ERR_INVALID_ARG;
-    if (epi != RMSNORM_EPI_PLAIN && epi != RMSNORM_EPI_BIAS && epi != RMSNORM_EPI_MXFP8)
+    if (epi < RMSNORM_EPI_PLAIN || epi > RMSNORM_EPI_NVFP4)
         return RMSNORM_ERR_INVALID_ARG;
-    if (epi == RMSNORM_EPI_MXFP8 && hidden % 32 != 0) // whole 32-element scale blocks
+    if (hidden % epi_block(epi) != 0) // whole scale blocks
         return RMSNORM_ERR_INVALID_ARG;
     if (rows > 0 && rows > INT64_MAX / 4 / hidden)
         return RMSNORM_ERR_INVALID_ARG;
@@ -490,7 +498,7 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     case RMSNORM_VARIANT_CLUSTER:
         return plan_cluster(s, out);
     case RMSNORM_VARIANT_GENERIC:
-        if (s.epi == RMSNORM_EPI_MXFP8) { // no scalar MX body
+        if (s.epi >= RMSNORM_EPI_MXFP8) { // no scalar body for the block-scaled outputs
             clear(out);
             return RMSNORM_ERR_VARIANT;
         }
@@ -505,7 +513,7 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // sizes 128 B .. 64 KiB and 1 .. 2M rows on GB300; they depend on the
     // row's byte length, not on the element type)
     if (!s.a16) {
-        if (s.epi == RMSNORM_EPI_MXFP8) { // the MX bodies need 16-byte vectors
+        if (s.epi >= RMSNORM_EPI_MXFP8) { // the block-scaled bodies need 16-byte vectors
             clear(out);
             return RMSNORM_ERR_MISALIGNED;
         }
@@ -547,15 +555,16 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // twice the elements): 2-16 KiB rows on blocks of nvec / 4 threads, 16-32
     // KiB rows on 32-byte vectors with a persistent grid of 4 blocks per SM
     // (the fastest plans of a sweep on GB300).
-    if (s.epi == RMSNORM_EPI_MXFP8 && s.a32 && nvec > 64 && nvec <= 128 &&
+    const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
+    if (blockq && s.a32 && nvec > 64 && nvec <= 128 &&
         plan_cta_exact(s, 32, 1, 1024, 1, 1, 0, tpr_for(nvec / 2, 1), int64_t(s.sm_count) * 16,
                        RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
         return RMSNORM_OK; // 1-2 KiB rows: one 32-byte vector per thread, 16 blocks per SM
-    if (s.epi == RMSNORM_EPI_MXFP8 && nvec > 128 && nvec <= 1024 &&
+    if (blockq && nvec > 128 && nvec <= 1024 &&
         plan_cta_exact(s, 16, 4, 256, 6, 1, 0, tpr_for(nvec, 4), INT_MAX,
                        RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    if (s.epi == RMSNORM_EPI_MXFP8 && s.a32 && nvec > 1024 && nvec <= 2048 &&
+    if (blockq && s.a32 && nvec > 1024 && nvec <= 2048 &&
         plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), int64_t(s.sm_count) * 4,
                        RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
         return RMSNORM_OK;

@@ -148,10 +148,12 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
     base = [torch.randn(rows, hidden, device=dev).to(tdt) for _ in range(min(nsets, 4))]
     xs = [base[i % len(base)] if i < len(base) else base[i % len(base)].clone()
           for i in range(nsets)]
-    mx = epi == rn.EPI_MXFP8
+    mx = epi in rn.QUANT_FORMATS
+    block, bits = rn.QUANT_FORMATS.get(epi, (1, 8 * es))
     if mx:
-        ys = [torch.empty(rows * hidden, dtype=torch.uint8, device=dev) for _ in range(nsets)]
-        ss = [torch.empty(rows * hidden // 32, dtype=torch.uint8, device=dev)
+        ys = [torch.empty(rows * hidden * bits // 8, dtype=torch.uint8, device=dev)
+              for _ in range(nsets)]
+        ss = [torch.empty(rows * hidden // block, dtype=torch.uint8, device=dev)
               for _ in range(nsets)]
         sp = [t.data_ptr() for t in ss]
     else:
@@ -167,14 +169,14 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
     def fwd(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref, j=0):
         if epi == 0:
             return lib.rmsnorm_fwd_ex(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref)
-        return lib.rmsnorm_fwd_epilogue_ex(x, wp, y, sp[j], rows_, hidden_, epi, 1.0, eps, dt_,
-                                           stream, variant, ref)
+        return lib.rmsnorm_fwd_epilogue_ex(x, wp, y, sp[j], rows_, hidden_, epi, 1.0, 0.01, eps,
+                                           dt_, stream, variant, ref)
 
     auto = rn.Plan()
     fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, rn.ctypes.byref(auto))
     cands = [auto.as_dict()] + ([] if _AUTO_ONLY else candidates(rows, hidden, dtype, sms, optin,
                                                                   epi))
-    out_bytes = rows * hidden + rows * hidden // 32 if mx else rows * hidden * es
+    out_bytes = rows * hidden * bits // 8 + rows * hidden // block if mx else rows * hidden * es
     out = []
     for ci, c in enumerate(cands):
         p = rn.Plan(**c)
@@ -341,7 +343,8 @@ def main(argv=None) -> int:
     ap.add_argument("--auto-only", action="store_true", help="time only the automatic plan")
     ap.add_argument("--summarize", default="", help="print a markdown table of a --grid output")
     ap.add_argument("--qk-workload", default="", help="sweep the QK-norm launch shapes instead")
-    ap.add_argument("--epilogue", default="plain", choices=["plain", "bias", "mxfp8"])
+    ap.add_argument("--epilogue", default="plain",
+                    choices=["plain", "bias", "mxfp8", "mxfp4", "nvfp4"])
     args = ap.parse_args(argv)
     if args.qk_workload:
         if args.pdl is not None:
@@ -358,7 +361,7 @@ def main(argv=None) -> int:
         rn.rmsnorm_set_pdl(bool(args.pdl))
     global _AUTO_ONLY
     _AUTO_ONLY = args.auto_only
-    epi = {"plain": 0, "bias": 1, "mxfp8": 2}[args.epilogue]
+    epi = {"plain": 0, "bias": 1, "mxfp8": 2, "mxfp4": 3, "nvfp4": 4}[args.epilogue]
     if not args.grid:
         res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph, epi)
         for r in res:

@@ -100,69 +100,116 @@ def sample_rows(rows: int, n: int, seed: int = 0) -> np.ndarray:
 
 
 MX_REL = 1e-5
-_E4M3 = None
+_TABLES = {}
 
 
 def e4m3_table() -> np.ndarray:
     """Value of every E4M3 code (the oracle's decoder)."""
-    global _E4M3
-    if _E4M3 is None:
-        _E4M3 = np.array([oracle.e4m3_value(c) for c in range(256)])
-    return _E4M3
+    if "e4m3" not in _TABLES:
+        _TABLES["e4m3"] = np.array([oracle.e4m3_value(c) for c in range(256)])
+    return _TABLES["e4m3"]
 
 
-def compare_mx(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.ndarray, bias: float,
-               eps: float, dtype: str, rows_idx: np.ndarray | None = None) -> dict:
-    """Compare GPU MXFP8 rows (uint8 codes [rows, hidden], uint8 scales
-    [rows, hidden / 32]) with the oracle; raises AssertionError on a
-    violation.  Returns counts of exact and band-decided results."""
+def e2m1_table() -> np.ndarray:
+    if "e2m1" not in _TABLES:
+        _TABLES["e2m1"] = np.array([oracle.e2m1_value(c) for c in range(16)])
+    return _TABLES["e2m1"]
+
+
+# fmt -> (elements per block, bits per code, NaN scale code)
+QFMT = {"mxfp8": (32, 8, 0xFF), "mxfp4": (32, 4, 0xFF), "nvfp4": (16, 4, 0x7F)}
+
+
+def _oracle_q(x, w, bias, eps, dtype, fmt, gscale, rel=0.0):
+    if fmt == "mxfp8":
+        return oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype, rel=rel)
+    return oracle.rmsnorm_fp4(x, w, bias, eps, dtype, fmt, global_scale=gscale, rel=rel)
+
+
+def _decode(codes, fmt, hidden):
+    """Element values of stored codes [rows, hidden * bits / 8] -> [rows, hidden]."""
+    if QFMT[fmt][1] == 8:
+        return e4m3_table()[codes]
+    un = np.empty((codes.shape[0], hidden), dtype=np.uint8)
+    un[:, 0::2] = codes & 0xF
+    un[:, 1::2] = codes >> 4
+    return e2m1_table()[un]
+
+
+def _scale_values(scales, fmt, gscale):
+    if fmt == "nvfp4":
+        return e4m3_table()[scales] * gscale
+    return np.exp2(scales.astype(np.float64) - 127.0)
+
+
+def _half_step(t, fmt):
+    """Half the spacing of the element grid at magnitude t (scaled units)."""
+    if QFMT[fmt][1] == 8:
+        return np.where(t >= 2.0 ** -6,
+                        np.exp2(np.floor(np.log2(np.maximum(t, 2.0 ** -6))) - 4), 2.0 ** -10)
+    return np.where(t < 2, 0.25, np.where(t < 4, 0.5, 1.0))
+
+
+def compare_quant(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.ndarray,
+                  bias: float, eps: float, dtype: str, fmt: str = "mxfp8", gscale: float = 1.0,
+                  rows_idx: np.ndarray | None = None) -> dict:
+    """Compare GPU block-scaled rows (codes as stored, scales [rows, hidden /
+    block]) with the oracle; raises AssertionError on a violation."""
     if rows_idx is not None:
         x, codes, scales = x[rows_idx], codes[rows_idx], scales[rows_idx]
     if x.shape[0] == 0:
         return {"rows": 0}
+    block, bits, nan_code = QFMT[fmt]
     rows, hidden = x.shape
-    nb = hidden // 32
-    c0, s0 = oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype)
-    clo, slo = oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype, rel=-MX_REL)
-    chi, shi = oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype, rel=MX_REL)
+    nb = hidden // block
+    c0, s0 = _oracle_q(x, w, bias, eps, dtype, fmt, gscale)
+    clo, slo = _oracle_q(x, w, bias, eps, dtype, fmt, gscale, rel=-MX_REL)
+    chi, shi = _oracle_q(x, w, bias, eps, dtype, fmt, gscale, rel=MX_REL)
     band = (slo != shi) | (slo != s0) | (shi != s0)
     ok_s = (scales == s0) | (band & ((scales == slo) | (scales == shi)))
     if not ok_s.all():
         i, b = np.argwhere(~ok_s)[0]
-        raise AssertionError(f"scale mismatch row {i} block {b}: gpu {scales[i, b]} oracle "
-                             f"{s0[i, b]} (band {slo[i, b]}..{shi[i, b]})")
-    tab = e4m3_table()
-    g = tab[codes].reshape(rows, nb, 32)
-    lo = tab[clo].reshape(rows, nb, 32)
-    hi = tab[chi].reshape(rows, nb, 32)
-    ref = tab[c0].reshape(rows, nb, 32)
-    special = s0 == 0xFF                       # NaN / Inf in the block: the scale says it all
-    same = (scales == s0) & ~band & ~special   # the scale is the oracle's, not in the band
+        raise AssertionError(f"{fmt} scale mismatch row {i} block {b}: gpu {scales[i, b]} "
+                             f"oracle {s0[i, b]} (band {slo[i, b]}..{shi[i, b]})")
+    g = _decode(codes, fmt, hidden).reshape(rows, nb, block)
+    lo = _decode(clo, fmt, hidden).reshape(rows, nb, block)
+    hi = _decode(chi, fmt, hidden).reshape(rows, nb, block)
+    ref = _decode(c0, fmt, hidden).reshape(rows, nb, block)
+    special = s0 == nan_code                   # a NaN in the block: the scale says it all
+    same = (scales == s0) & ~band & ~special
     lo_v, hi_v = np.minimum(lo, hi), np.maximum(lo, hi)
     inside = (g >= lo_v) & (g <= hi_v)
     bad = same[:, :, None] & ~inside
     if bad.any():
         i, b, j = np.argwhere(bad)[0]
-        raise AssertionError(f"code mismatch row {i} col {b * 32 + j}: gpu {g[i, b, j]!r} "
-                             f"oracle {ref[i, b, j]!r} (band {lo[i, b, j]!r}..{hi[i, b, j]!r})")
-    # Blocks whose scale sits in the band: every element within the MX
-    # error bound of the binary64 result at the GPU's scale.
+        raise AssertionError(f"{fmt} code mismatch row {i} col {b * block + j}: gpu "
+                             f"{g[i, b, j]!r} oracle {ref[i, b, j]!r} "
+                             f"(band {lo[i, b, j]!r}..{hi[i, b, j]!r})")
+    # Blocks whose scale sits in the band: every element within the error
+    # bound of the element grid at the GPU's scale.
     amb = band & ~special
     if amb.any():
-        y = oracle.rmsnorm_bias_f64(x, w, bias, eps, dtype).reshape(rows, nb, 32)
-        X = np.exp2(scales.astype(np.float64) - 127.0)[:, :, None]
-        t = np.abs(y) / X
-        step = np.where(t >= 2.0 ** -6, np.exp2(np.floor(np.log2(np.maximum(t, 2.0 ** -6))) - 3),
-                        2.0 ** -9)
+        y = oracle.rmsnorm_bias_f64(x, w, bias, eps, dtype).reshape(rows, nb, block)
+        X = _scale_values(scales, fmt, gscale)[:, :, None]
+        with np.errstate(divide="ignore", invalid="ignore"):
+            t = np.where(X > 0, np.abs(y) / X, 0.0)
         err = np.abs(g * X - y)
-        sat = t >= 448
-        tol = (step / 2 * (1 + MX_REL) + MX_REL * t) * X
-        good = np.where(sat, np.abs(g) == 448, err <= tol)
+        maxmag = 448.0 if bits == 8 else 6.0
+        sat = t >= maxmag
+        tol = (_half_step(t, fmt) * (1 + MX_REL) + MX_REL * t) * X
+        good = np.where(X == 0, g == 0, np.where(sat, np.abs(g) == maxmag, err <= tol))
         badb = amb[:, :, None] & ~good
         if badb.any():
             i, b, j = np.argwhere(badb)[0]
-            raise AssertionError(f"band-scale block row {i} block {b} elem {j}: gpu "
-                                 f"{g[i, b, j]!r} * 2^{int(scales[i, b]) - 127} vs {y[i, b, j]!r}")
+            raise AssertionError(f"{fmt} band-scale block row {i} block {b} elem {j}: gpu "
+                                 f"{g[i, b, j]!r} x {X[i, b, 0]!r} vs {y[i, b, j]!r}")
+    same_e = np.repeat(same, block, axis=1)
     return {"rows": rows, "blocks": rows * nb, "band_blocks": int(band.sum()),
-            "exact_codes": float((codes == c0)[np.repeat(same, 32, axis=1)].mean())
-            if same.any() else 1.0}
+            "exact_codes": float((g.reshape(rows, hidden) == ref.reshape(rows, hidden))[same_e]
+                                 .mean()) if same.any() else 1.0}
+
+
+def compare_mx(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.ndarray, bias: float,
+               eps: float, dtype: str, rows_idx: np.ndarray | None = None) -> dict:
+    """compare_quant for MXFP8."""
+    return compare_quant(codes, scales, x, w, bias, eps, dtype, "mxfp8", 1.0, rows_idx)

@@ -348,11 +348,13 @@ def test_epilogue_kernel_sets():
         assert {key(k) for k in bias} == {key(k) for k in plain
                                           if k["variant"] not in (rn.VARIANT_STAGED,
                                                                   rn.VARIANT_CLUSTER)}
-        # MXFP8: the register and looped bodies except the 4-lane group
-        assert {key(k) for k in mx} == {key(k) for k in plain
-                                        if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
-                                                            rn.VARIANT_CTA_PER_ROW)
-                                        and k["tpr"] != 4}
+        # block-scaled outputs: the register and looped bodies except the 4-lane group
+        want = {key(k) for k in plain if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
+                                                          rn.VARIANT_CTA_PER_ROW)
+                and k["tpr"] != 4}
+        assert {key(k) for k in mx} == want
+        for epi in (rn.EPI_MXFP4, rn.EPI_NVFP4):
+            assert {key(k) for k in ks if k["dtype"] == dt and k["epilogue"] == epi} == want
 
 
 @pytest.mark.parametrize("epi", [rn.EPI_BIAS, rn.EPI_MXFP8])
@@ -474,3 +476,27 @@ def test_cluster_split_chosen_for_long_decode_rows():
                               (1, 65536, rn.EPI_BIAS), (1, 65536, rn.EPI_MXFP8)):
         rc, p = plan_epi(rows, hidden, rn.BF16, epi)
         assert rc == rn.OK and p.variant != rn.VARIANT_CLUSTER, (rows, hidden, epi)
+
+
+
+def test_fp4_argument_rules():
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_MXFP4)[0] == rn.OK
+    assert plan_epi(64, 4080, rn.BF16, rn.EPI_MXFP4)[0] == rn.ERR_INVALID_ARG
+    assert plan_epi(64, 4080, rn.BF16, rn.EPI_NVFP4)[0] == rn.OK        # 255 blocks of 16
+    assert plan_epi(64, 4088, rn.BF16, rn.EPI_NVFP4)[0] == rn.ERR_INVALID_ARG
+    assert plan_epi(64, 4096, rn.BF16, rn.EPI_NVFP4, x=A + 2)[0] == rn.ERR_MISALIGNED
+    assert plan_epi(64, 4096, rn.BF16, 5)[0] == rn.ERR_INVALID_ARG
+    for epi in (rn.EPI_MXFP4, rn.EPI_NVFP4):   # the block-scaled shapes of MXFP8
+        rc, p = plan_epi(16384, 4096, rn.BF16, epi)
+        rc8, p8 = plan_epi(16384, 4096, rn.BF16, rn.EPI_MXFP8)
+        d, d8 = p.as_dict(), p8.as_dict()
+        d.pop("kernel_index"), d8.pop("kernel_index")
+        assert rc == rn.OK and d == d8
+    lib = rn._load()
+    # codes are hidden / 2 bytes a row: scales right after the codes do not overlap
+    assert lib.rmsnorm_fwd_mxfp4(A, 3 * A, 5 * A, 5 * A + 4 * 2048, 4, 4096, 0.0, 1e-6, rn.BF16,
+                                 None) in (rn.ERR_NOT_INITIALIZED, rn.ERR_CUDA)  # past the checks
+    assert lib.rmsnorm_fwd_mxfp4(A, 3 * A, 5 * A, 5 * A + 4 * 2048 - 1, 4, 4096, 0.0, 1e-6,
+                                 rn.BF16, None) == rn.ERR_ALIASING
+    assert lib.rmsnorm_fwd_nvfp4(A, 3 * A, 5 * A, 7 * A, 4, 4096, 0.0, 0.0, 1e-6, rn.BF16,
+                                 None) == rn.ERR_INVALID_ARG

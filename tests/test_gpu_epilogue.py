@@ -1,7 +1,8 @@
 """GPU parity of the epilogues against the fp64 oracle: the weight offset
 (w + WEIGHT_BIAS of "CuTeDSL at Perplexity", section "QK Norm") and the
-fused MXFP8 output (same page, section "Blackwell support"; the OCP MX v1.0
-definition).
+fused block-scaled outputs MXFP8, MXFP4 (the OCP MX v1.0 definitions) and
+NVFP4 (NVIDIA's description) named in the same page's section "Blackwell
+support".
 
 * every workload shape (full compare where the oracle is quick, sampled rows
   at the 65536-row shapes), in the selector's automatic plan;
@@ -17,7 +18,7 @@ import pytest
 import rmsnorm_fwd_gb300 as rn
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, compare_mx, from_device, sample_rows, to_device
+from _parity import compare, compare_mx, compare_quant, from_device, sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -212,3 +213,96 @@ def test_mx_argument_errors():
     assert lib.rmsnorm_fwd_mxfp8(xd.data_ptr(), wd.data_ptr(), q.data_ptr(), s.data_ptr(), 0,
                                  4096, 0.0, 1e-6, rn.BF16, None) == rn.OK
     torch.cuda.synchronize()
+
+
+
+# ------------------------------------------------------------------ MXFP4 / NVFP4
+
+FP4 = [("mxfp4", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.0021)]
+
+
+def run_q(x_np, w_np, bias, eps, dtype, fmt, g, variant=rn.VARIANT_AUTO):
+    x = to_device(x_np, dtype)
+    w = to_device(w_np, dtype)
+    q, s = rn.rms_norm_quant(x, w, eps, fmt, weight_bias=bias, global_scale=g, variant=variant)
+    torch.cuda.synchronize()
+    return q.cpu().numpy(), s.cpu().numpy()
+
+
+@pytest.mark.parametrize("fmt,g", FP4)
+@pytest.mark.parametrize("name", SMALL)
+def test_fp4_workloads(name, fmt, g):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    q, s = run_q(x, w, 0.0, wl.eps, wl.dtype, fmt, g)
+    r = compare_quant(q, s, x, w, 0.0, wl.eps, wl.dtype, fmt, g)
+    assert r["rows"] == wl.rows and r["exact_codes"] > 0.999
+
+
+@pytest.mark.parametrize("fmt,g", FP4[:2])
+@pytest.mark.parametrize("name", WIDE)
+def test_fp4_wide_workloads_sampled(name, fmt, g):
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    idx = sample_rows(wl.rows, 32, seed=wl.key)
+    q, s = run_q(x, w, 0.5, wl.eps, wl.dtype, fmt, g)
+    compare_quant(q, s, x, w, 0.5, wl.eps, wl.dtype, fmt, g, rows_idx=idx)
+
+
+@pytest.mark.parametrize("fmt,g", FP4)
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows,hidden", SHAPES + [(77, 48), (9, 16), (300, 2064)])
+def test_fp4_shape_classes(dtype, rows, hidden, fmt, g):
+    if dtype == "f32" and hidden > 65536:
+        hidden //= 2
+    if fmt == "mxfp4" and hidden % 32:
+        return
+    x, w = inputs.random_case(rows, hidden, dtype, seed=rows + 3 * hidden)
+    idx = sample_rows(rows, 64, seed=hidden) if rows * hidden > (1 << 22) else None
+    q, s = run_q(x, w, 1.0, 1e-6, dtype, fmt, g)
+    compare_quant(q, s, x, w, 1.0, 1e-6, dtype, fmt, g, rows_idx=idx)
+
+
+@pytest.mark.parametrize("fmt,g", FP4)
+def test_fp4_special_blocks(fmt, g):
+    rows, hidden = 10, 512
+    for dtype in ("bf16", "f16", "f32"):
+        z = np.random.default_rng(5).standard_normal((rows, hidden)).astype(np.float32)
+        z[0] = 0.0
+        z[1, 5] = np.nan
+        z[2, 300] = np.inf
+        z[3, :32] = 0.0
+        z[4] *= 1e-15 if dtype == "f32" else 1e-3
+        z[5] *= 1e15 if dtype == "f32" else (1e4 if dtype == "f16" else 3e4)
+        z[6, ::2] = 0.0
+        z[6, 1] = 1e4 if dtype != "f16" else 6e4
+        x = inputs.to_storage(z, dtype)
+        _, w = inputs.random_case(1, hidden, dtype, seed=7)
+        for eps in (1e-6, 0.0):
+            q, s = run_q(x, w, 0.0, eps, dtype, fmt, g)
+            compare_quant(q, s, x, w, 0.0, eps, dtype, fmt, g)
+            nan_code = 0x7F if fmt == "nvfp4" else 0xFF
+            assert (s[1] == nan_code).all()
+            if eps > 0:
+                assert (s[0] == 0).all() and not (q[0] & 0x77).any()
+
+
+def test_fp4_argument_errors():
+    lib = rn._load()
+    x, w = inputs.random_case(8, 4096, "bf16", seed=13)
+    xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
+    q = torch.empty(8, 2048, dtype=torch.uint8, device="cuda")
+    s = torch.empty(8, 256, dtype=torch.uint8, device="cuda")
+    P = (xd.data_ptr(), wd.data_ptr(), q.data_ptr(), s.data_ptr())
+    assert lib.rmsnorm_fwd_mxfp4(*P, 8, 4080, 0.0, 1e-6, rn.BF16, None) == rn.ERR_INVALID_ARG
+    assert lib.rmsnorm_fwd_nvfp4(*P, 8, 4088, 1.0, 0.0, 1e-6, rn.BF16, None) == \
+        rn.ERR_INVALID_ARG
+    for gbad in (0.0, -1.0, float("inf"), float("nan")):
+        assert lib.rmsnorm_fwd_nvfp4(*P, 8, 4096, gbad, 0.0, 1e-6, rn.BF16, None) == \
+            rn.ERR_INVALID_ARG
+    assert lib.rmsnorm_fwd_nvfp4(xd.data_ptr(), wd.data_ptr(), q.data_ptr(), q.data_ptr() + 64,
+                                 8, 4096, 1.0, 0.0, 1e-6, rn.BF16, None) == rn.ERR_ALIASING
+    assert lib.rmsnorm_fwd_mxfp4(*P, 8, 4096, 0.0, 1e-6, rn.BF16, None) == rn.OK
+    assert lib.rmsnorm_fwd_nvfp4(*P, 8, 4096, 1.0, 0.0, 1e-6, rn.BF16, None) == rn.OK
+    torch.cuda.synchronize()
+    compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.0, 1e-6, "bf16", "nvfp4", 1.0)

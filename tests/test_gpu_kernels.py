@@ -1,5 +1,5 @@
 """Every compiled kernel instantiation, launched with explicit plans through
-rmsnorm_fwd_ex (plain) or rmsnorm_fwd_epilogue_ex (weight bias, MXFP8),
+rmsnorm_fwd_ex (plain) or rmsnorm_fwd_epilogue_ex (weight bias, MXFP8, MXFP4, NVFP4),
 against the fp64 oracle: full and partly filled rows, one row per block and
 grid-stride (fewer blocks than rows), odd row counts."""
 import numpy as np
@@ -8,7 +8,7 @@ import pytest
 import rmsnorm_fwd_gb300 as rn
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, compare_mx, from_device, to_device
+from _parity import compare, compare_quant, from_device, to_device
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -37,13 +37,14 @@ def plans_for(k, rows, sms, optin):
     """(hidden, plan dict) cases exercising kernel k.  MXFP8 kernels get
     row lengths of whole 32-element blocks."""
     cases = _plans_for(k, rows, sms, optin)
-    if k["epilogue"] != rn.EPI_MXFP8:
+    if k["epilogue"] not in rn.QUANT_FORMATS:
         return cases
+    block = rn.QUANT_FORMATS[k["epilogue"]][0]
     out = []
     for hidden, pd in cases:
-        h = hidden // 32 * 32
+        h = hidden // block * block
         if h == 0:
-            h = 32
+            h = block
         if pd["vecs_per_thread"] and h // (k["vec_bytes"] // ES[k["dtype"]]) > \
                 pd["threads_per_row"] * pd["vecs_per_thread"]:
             continue
@@ -150,13 +151,16 @@ def test_kernel_instantiation(index):
         x_np, w_np = inputs.random_case(rows, hidden, dt, seed=index)
         x = to_device(x_np, dt)
         w = to_device(w_np, dt)
-        if epi == rn.EPI_MXFP8:
-            q = torch.full((rows, hidden), 0xAA, dtype=torch.uint8, device="cuda")
-            sc = torch.full((rows, hidden // 32), 0xAA, dtype=torch.uint8, device="cuda")
-            rn.rms_norm_mxfp8(x, w, 1e-6, weight_bias=0.625, out=q, scales=sc,
-                              plan=rn.Plan(**pd))
+        if epi in rn.QUANT_FORMATS:
+            block, bits = rn.QUANT_FORMATS[epi]
+            fmt = rn.EPI_NAMES[epi]
+            q = torch.full((rows, hidden * bits // 8), 0xAA, dtype=torch.uint8, device="cuda")
+            sc = torch.full((rows, hidden // block), 0xAA, dtype=torch.uint8, device="cuda")
+            rn.rms_norm_quant(x, w, 1e-6, fmt, weight_bias=0.625, global_scale=0.01, out=q,
+                              scales=sc, plan=rn.Plan(**pd))
             torch.cuda.synchronize()
-            compare_mx(q.cpu().numpy(), sc.cpu().numpy(), x_np, w_np, 0.625, 1e-6, dt)
+            compare_quant(q.cpu().numpy(), sc.cpu().numpy(), x_np, w_np, 0.625, 1e-6, dt, fmt,
+                          0.01)
             continue
         y = torch.full_like(x, 3.0)
         if epi == rn.EPI_BIAS:

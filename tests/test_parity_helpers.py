@@ -6,7 +6,7 @@ import pytest
 import oracle
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, compare_mx
+from _parity import compare, compare_mx, compare_quant
 
 
 def test_compare_accepts_oracle_and_rejects_one_ulp_plus():
@@ -59,3 +59,28 @@ def test_compare_mx_band_scale_block():
     assert shi[0, 0] == s[0, 0] + 1
     assert compare_mx(c, s, x, w, 0.0, 0.0, "f32")["band_blocks"] == 1
     compare_mx(chi, shi, x, w, 0.0, 0.0, "f32")
+
+
+@pytest.mark.parametrize("fmt,g", [("mxfp4", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.004)])
+def test_compare_quant_fp4_accepts_band_and_rejects_planted(fmt, g):
+    x, w = inputs.random_case(48, 256, "bf16", seed=3)
+    c, s = oracle.rmsnorm_fp4(x, w, 0.5, 1e-6, "bf16", fmt, global_scale=g)
+    assert compare_quant(c, s, x, w, 0.5, 1e-6, "bf16", fmt, g)["exact_codes"] == 1.0
+    c3, s3 = oracle.rmsnorm_fp4(x, w, 0.5, 1e-6, "bf16", fmt, global_scale=g, rel=3e-6)
+    compare_quant(c3, s3, x, w, 0.5, 1e-6, "bf16", fmt, g)
+    c2 = c.copy()
+    nz = np.argwhere((c2 & 0x7) > 1)[0]      # a code with room to move down one step
+    c2[tuple(nz)] -= 1
+    with pytest.raises(AssertionError):
+        compare_quant(c2, s, x, w, 0.5, 1e-6, "bf16", fmt, g)
+    c2 = c.copy()
+    c2[0, 0] ^= 0x88                          # both signs of the first byte flipped
+    if (c[0, 0] & 0x77) != 0:
+        with pytest.raises(AssertionError):
+            compare_quant(c2, s, x, w, 0.5, 1e-6, "bf16", fmt, g)
+    s2 = s.copy()
+    s2[5, 2] += 1
+    with pytest.raises(AssertionError):
+        compare_quant(c, s2, x, w, 0.5, 1e-6, "bf16", fmt, g)
+    with pytest.raises(AssertionError):     # the nibble order swapped
+        compare_quant(((c & 0xF) << 4) | (c >> 4), s, x, w, 0.5, 1e-6, "bf16", fmt, g)
