@@ -435,6 +435,16 @@ __device__ inline float max_nan(float a, float m)
     return r;
 }
 
+// 1 / a by the hardware reciprocal (within one unit in the last place;
+// subnormal inputs kept).  The NVFP4 scale and element decisions it feeds
+// are checked against the exact quotients with a 1e-5 relative band.
+__device__ inline float rcp_approx(float a)
+{
+    float r;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+
 // One vector of a block-scaled epilogue (QFmt above).
 //
 // v = (x * r) * (w + bias) in fp32, two elements per packed instruction.
@@ -445,7 +455,8 @@ __device__ inline float max_nan(float a, float m)
 // = e - 127 - kEmax, clamped at -127: E8M0 code max(e - kEmax, 0), or 0xFF
 // when e = 255 (Inf / NaN); scaling by 2^(127 - code) is exact.  NVFP4: the
 // scale code is E4M3(max * (1 / (6 g))) and the values are multiplied by
-// 1 / (value(code) * g) (by 0 when the scale is 0).  The conversions round
+// 1 / (value(code) * g) (by 0 when the scale is 0), both reciprocals from
+// rcp.approx.  The conversions round
 // each scaled value to the element format.
 //
 // Every lane of the warp must call this (the shuffles span the full warp);
@@ -477,9 +488,9 @@ __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, fl
     uint32_t code;
     float mul;
     if constexpr (Q == kQNvfp4) {
-        code = e4m3_code(m * __frcp_rn(6.f * g));
+        code = e4m3_code(m * rcp_approx(6.f * g));
         const float d = e4m3_value(code);
-        mul = d == 0.f ? 0.f : __frcp_rn(d * g);
+        mul = d == 0.f ? 0.f : rcp_approx(d * g);
     } else {
         constexpr uint32_t EM = QFmt<Q>::kEmax;
         const uint32_t e = __float_as_uint(m) >> 23;

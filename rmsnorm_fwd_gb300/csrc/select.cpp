@@ -549,17 +549,30 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         if (plan_looped(s, RMSNORM_VARIANT_PERSISTENT, false, out) == RMSNORM_OK)
             return RMSNORM_OK;
     }
-    // Prefill with the MXFP8 output: its body issues about half again as many
-    // instructions per element as the plain one and is issue-bound at two
-    // vectors per thread, so it takes four (the per-row work spread over
-    // twice the elements): 2-16 KiB rows on blocks of nvec / 4 threads, 16-32
-    // KiB rows on 32-byte vectors with a persistent grid of 4 blocks per SM
-    // (the fastest plans of a sweep on GB300).
+    // Prefill with a block-scaled output (MXFP8 / MXFP4 / NVFP4): its body
+    // issues about half again as many instructions per element as the plain
+    // one, so it takes more elements per thread and, with 32-byte vectors,
+    // persistent grids (the fastest plans of sweeps on GB300 over 2-32 KiB
+    // bf16 rows for the three formats):
+    //   1-2 KiB rows: a warp per row, 4 vectors per lane, 16 blocks per SM;
+    //   2-16 KiB rows: 32-byte vectors, 2 per thread up to 8 KiB rows and 4
+    //     beyond, 16 blocks per SM while they fit (16-byte vectors, 4 per
+    //     thread, one block per row when unaligned for 32);
+    //   16-32 KiB rows: 32-byte vectors, 4 per thread, 4 blocks per SM.
     const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
-    if (blockq && s.a32 && nvec > 64 && nvec <= 128 &&
-        plan_cta_exact(s, 32, 1, 1024, 1, 1, 0, tpr_for(nvec / 2, 1), int64_t(s.sm_count) * 16,
-                       RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
-        return RMSNORM_OK; // 1-2 KiB rows: one 32-byte vector per thread, 16 blocks per SM
+    if (blockq && nvec > 64 && nvec <= 128 &&
+        plan_warp_exact(s, 32, 4, 0, int64_t(s.sm_count) * 16, out) == RMSNORM_OK)
+        return RMSNORM_OK;
+    if (blockq && s.a32 && nvec > 128 && nvec <= 1024) {
+        const int64_t n32 = nvec / 2;
+        const int nv = n32 <= 256 ? 2 : 4;
+        const int tpr = tpr_for(n32, nv);
+        const int64_t cap = int64_t(s.sm_count) * std::min(16, 2048 / tpr);
+        if (plan_cta_exact(s, 32, nv, nv == 2 ? 1024 : 512, 0, 1, 0, tpr, cap,
+                           cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW,
+                           out) == RMSNORM_OK)
+            return RMSNORM_OK;
+    }
     if (blockq && nvec > 128 && nvec <= 1024 &&
         plan_cta_exact(s, 16, 4, 256, 6, 1, 0, tpr_for(nvec, 4), INT_MAX,
                        RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)

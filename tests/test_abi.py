@@ -374,11 +374,14 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                 rc0, p0 = plan_epi(rows, hidden, dt, rn.EPI_PLAIN)
                 nvec = hidden * (4 if dt == rn.F32 else 2) // 16
                 if epi == rn.EPI_MXFP8 and rows > SMS and 64 < nvec <= 2048:
-                    # MXFP8 prefill rows of 1-32 KiB: its own shapes (four
-                    # vectors per thread; one 32-byte vector for 1-2 KiB rows)
-                    nv = 1 if nvec <= 128 else 4
-                    assert p.vecs_per_thread == nv and \
-                        p.threads_per_row * nv * p.vec_bytes >= nvec * 16, \
+                    # block-scaled prefill rows of 1-32 KiB: their own shapes
+                    # (a warp x 4 for 1-2 KiB rows, then 32-byte vectors, 2 or
+                    # 4 per thread)
+                    if nvec <= 128:
+                        assert p.variant == rn.VARIANT_WARP_PER_ROW and p.vecs_per_thread == 4
+                    else:
+                        assert p.vec_bytes == 32 and p.vecs_per_thread in (2, 4)
+                    assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
                 if p0.variant not in (rn.VARIANT_STAGED, rn.VARIANT_CLUSTER):
