@@ -554,14 +554,15 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // one, so it takes more elements per thread and, with 32-byte vectors,
     // persistent grids (the fastest plans of sweeps on GB300 over 2-32 KiB
     // bf16 rows for the three formats):
-    //   1-2 KiB rows: a warp per row, 4 vectors per lane, 16 blocks per SM;
+    //   1-2 KiB rows: a warp per row, 4 vectors per lane (register-capped
+    //     for 8 blocks of 256 threads per SM), 16 blocks per SM;
     //   2-16 KiB rows: 32-byte vectors, 2 per thread up to 8 KiB rows and 4
     //     beyond, 16 blocks per SM while they fit (16-byte vectors, 4 per
     //     thread, one block per row when unaligned for 32);
     //   16-32 KiB rows: 32-byte vectors, 4 per thread, 4 blocks per SM.
     const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
     if (blockq && nvec > 64 && nvec <= 128 &&
-        plan_warp_exact(s, 32, 4, 0, int64_t(s.sm_count) * 16, out) == RMSNORM_OK)
+        plan_warp_exact(s, 32, 4, 8, int64_t(s.sm_count) * 16, out) == RMSNORM_OK)
         return RMSNORM_OK;
     if (blockq && s.a32 && nvec > 128 && nvec <= 1024) {
         const int64_t n32 = nvec / 2;
