@@ -15,7 +15,9 @@
  *   y[i, j] = round( (x[i, j] * r_i) * w[j] ),   r_i = rsqrt( sum_j x[i, j]^2 / hidden + eps )
  *
  * computed in fp32 on the device and rounded to the element type with
- * round-to-nearest-even.
+ * round-to-nearest-even.  Variants of the output (the "epilogues": a weight
+ * offset, MXFP8 / MXFP4 / NVFP4 block-scaled codes) and the per-head QK norm
+ * are declared further down, each with its own definition.
  *
  * Memory layout.  x and y are row-major [rows, hidden], contiguous (row
  * stride = hidden elements); weight is [hidden].  x, weight and y share one

@@ -111,7 +111,7 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
                                         smem_bytes=staged_smem(rb, st), kernel_index=k["index"]))
         elif v == rn.VARIANT_CLUSTER:
             vb = k["vec_bytes"]
-            if hidden * es % vb or rows > 4 * sms:
+            if hidden * es % vb or (rows > 4 * sms and hidden * es < 16384):
                 continue
             nvec = hidden * es // vb
             for C in (2, 4, 8):
