@@ -23,8 +23,10 @@
  * stride = hidden elements); weight is [hidden].  x, weight and y share one
  * element type.  All three are DEVICE pointers owned by the caller; the
  * library never frees or retains them.  The only memory the library itself
- * allocates is a 4-byte device status word per device (rmsnorm_create) and
- * its host-side context.
+ * allocates is a 4-byte device status word per device (rmsnorm_create), its
+ * host-side context, and, for calls that take the grid variant, a per-call
+ * scratch area from the device's stream-ordered memory pool, freed in
+ * stream order.
  *
  * Aliasing.  y == x (exactly in place) is allowed.  Any other overlap between
  * y and x, or between y and weight, is rejected with RMSNORM_ERR_ALIASING.
@@ -105,7 +107,15 @@ typedef enum {
     /* Decode shapes with long rows: each row split over a thread-block
      * cluster of 2, 4 or 8 blocks (on as many SMs); the blocks' partial sums
      * meet through distributed shared memory.  Plain output only. */
-    RMSNORM_VARIANT_CLUSTER = 6
+    RMSNORM_VARIANT_CLUSTER = 6,
+    /* Decode shapes with rows longer than a cluster holds: every row spread
+     * over all SMs (a cooperative launch of 2 blocks per SM), one grid
+     * barrier through global memory between the sums and the scaling
+     * (bounded wait; a wait that runs out records RMSNORM_ERR_DEVICE_TIMEOUT).
+     * Per call it takes rows * grid * 4 + 16 bytes of scratch from the
+     * device's stream-ordered memory pool (cudaMallocAsync / cudaFreeAsync
+     * on `stream`).  Plain output only; at most 64 rows. */
+    RMSNORM_VARIANT_GRID = 7
 } rmsnorm_variant_t;
 
 /* A launch plan: what the selector chose.  Filled by rmsnorm_plan. */
@@ -397,6 +407,14 @@ int rmsnorm_get_pdl(void);
  * without touching y.  No fault, trap or hang is involved. */
 int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int64_t rows,
                                 int64_t hidden, int dtype, uint64_t limit_ns, void *stream);
+
+/* Failure-detection test hook for the grid variant: the grid-barrier
+ * arrival of block 0 is withheld, so every block's bounded wait runs out
+ * after `limit_ns`; the kernel records RMSNORM_ERR_DEVICE_TIMEOUT, leaves y
+ * untouched and clears its barrier counters.  rows in 1..64.  No fault,
+ * trap or hang is involved. */
+int rmsnorm_test_grid_timeout(const void *x, const void *weight, void *y, int64_t rows,
+                              int64_t hidden, int dtype, uint64_t limit_ns, void *stream);
 
 /* rmsnorm_fwd for callers that cannot allocate device memory.
  *

@@ -43,8 +43,9 @@ VARIANT_STAGED = 3
 VARIANT_PERSISTENT = 4
 VARIANT_GENERIC = 5
 VARIANT_CLUSTER = 6
+VARIANT_GRID = 7
 VARIANT_NAMES = {0: "auto", 1: "warp_per_row", 2: "cta_per_row", 3: "staged", 4: "persistent",
-                 5: "generic", 6: "cluster"}
+                 5: "generic", 6: "cluster", 7: "grid"}
 
 # epilogues (rmsnorm_epilogue_t)
 EPI_PLAIN, EPI_BIAS, EPI_MXFP8, EPI_MXFP4, EPI_NVFP4 = 0, 1, 2, 3, 4
@@ -144,6 +145,7 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_set_pdl": ([i32], i32),
             "rmsnorm_get_pdl": ([], i32),
             "rmsnorm_test_staged_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
+            "rmsnorm_test_grid_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
             "rmsnorm_fwd_staged_noalloc": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
             "rmsnorm_status_string": ([i32], ctypes.c_char_p),
             "rmsnorm_version": ([], i32),
@@ -367,6 +369,12 @@ def rmsnorm_test_staged_timeout(x: int, weight: int, y: int, rows: int, hidden: 
                                 limit_ns: int, stream: int | None) -> None:
     _check(_load().rmsnorm_test_staged_timeout(x, weight, y, rows, hidden, dtype, limit_ns,
                                                stream or None), "rmsnorm_test_staged_timeout")
+
+
+def rmsnorm_test_grid_timeout(x: int, weight: int, y: int, rows: int, hidden: int, dtype: int,
+                              limit_ns: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_test_grid_timeout(x, weight, y, rows, hidden, dtype, limit_ns,
+                                             stream or None), "rmsnorm_test_grid_timeout")
 
 
 def rmsnorm_fwd_staged_noalloc(x: int, weight: int, y: int, rows: int, hidden: int, eps: float,

@@ -20,6 +20,7 @@ OUT = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT, "librmsnorm.so")
 
 SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu", "cluster.cu",
+           "gridrow.cu",
            "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu",
            "rowreg_epi_f32.cu", "rowreg_epi_bf16.cu", "rowreg_epi_f16.cu",
            "rowreg_fp4_f32.cu", "rowreg_fp4_bf16.cu", "rowreg_fp4_f16.cu"]

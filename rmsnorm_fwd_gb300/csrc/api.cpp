@@ -25,7 +25,8 @@ const KernelDesc *kernel_table(int *n)
             rowreg_kernels_f32,     rowreg_kernels_bf16,     rowreg_kernels_f16,
             staged_kernels,         generic_kernels,         rowreg_epi_kernels_f32,
             rowreg_epi_kernels_bf16, rowreg_epi_kernels_f16, cluster_kernels,
-            rowreg_fp4_kernels_f32, rowreg_fp4_kernels_bf16, rowreg_fp4_kernels_f16};
+            rowreg_fp4_kernels_f32, rowreg_fp4_kernels_bf16, rowreg_fp4_kernels_f16,
+            grid_kernels};
         for (auto part : parts) {
             int m = 0;
             const KernelDesc *t = part(&m);
@@ -258,8 +259,24 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
                      static_cast<long long>(rows), static_cast<long long>(hidden), dtype, epi,
                      p.variant, p.vec_bytes, p.threads_per_row, p.vecs_per_thread,
                      p.block_threads, p.grid, p.stages, p.smem_bytes, p.kernel_index);
-    if (d.launch(p, a) != cudaSuccess)
+    if (d.variant == RMSNORM_VARIANT_GRID) {
+        // Per-call scratch from the stream-ordered pool: counters (zeroed)
+        // and rows * grid partial sums; freed in stream order after the
+        // kernel, so concurrent calls on other streams never share it.
+        const size_t bytes = static_cast<size_t>(kGridCounterBytes) +
+                             static_cast<size_t>(rows) * static_cast<size_t>(p.grid) * sizeof(float);
+        void *scratch = nullptr;
+        if (cudaMallocAsync(&scratch, bytes, a.stream) != cudaSuccess)
+            return RMSNORM_ERR_CUDA;
+        a.scratch = scratch;
+        const bool ok = cudaMemsetAsync(scratch, 0, kGridCounterBytes, a.stream) == cudaSuccess &&
+                        d.launch(p, a) == cudaSuccess;
+        const bool freed = cudaFreeAsync(scratch, a.stream) == cudaSuccess;
+        if (!ok || !freed)
+            return RMSNORM_ERR_CUDA;
+    } else if (d.launch(p, a) != cudaSuccess) {
         return RMSNORM_ERR_CUDA;
+    }
     t_last_variant = p.variant;
     if (plan && plan->variant == RMSNORM_VARIANT_AUTO)
         *plan = p;
@@ -813,6 +830,15 @@ int rmsnorm_test_staged_timeout(const void *x, const void *weight, void *y, int6
     if (rows <= 0 || limit_ns == 0)
         return RMSNORM_ERR_INVALID_ARG;
     return launch(x, weight, y, rows, hidden, 0.f, dtype, stream, RMSNORM_VARIANT_STAGED, nullptr,
+                  kFlagWithholdCopies, limit_ns);
+}
+
+int rmsnorm_test_grid_timeout(const void *x, const void *weight, void *y, int64_t rows,
+                              int64_t hidden, int dtype, uint64_t limit_ns, void *stream)
+{
+    if (rows <= 0 || limit_ns == 0)
+        return RMSNORM_ERR_INVALID_ARG;
+    return launch(x, weight, y, rows, hidden, 0.f, dtype, stream, RMSNORM_VARIANT_GRID, nullptr,
                   kFlagWithholdCopies, limit_ns);
 }
 

@@ -1,0 +1,243 @@
+// gridrow.cu -- a few very long rows spread over every SM, with one grid
+// barrier between the sum of squares and the scaling.
+//
+// "CuTeDSL at Perplexity", section "Grid synchronization": to spread work
+// over as many blocks as possible, all participating blocks synchronise
+// through global memory; that is only safe when every block is resident at
+// once (no more blocks than the SMs hold), which a cooperative launch
+// enforces, and the barrier costs about as much as splitting the work into
+// two launches.  Here it serves decode rows longer than a thread-block
+// cluster holds in registers (above 512 KiB).
+//
+// Block b of G takes the same range of 16-byte vectors [b*S, min((b+1)*S,
+// nvec)), S = ceil(nvec / G), of every row.
+//   Phase 1: the block's sum of squares of its range of each row, written to
+//            partial[row * G + b].
+//   Barrier: one thread per block adds one to an arrival counter (release)
+//            and waits, bounded by %globaltimer, until all G have arrived
+//            (acquire).  A wait that runs out records RMSNORM_ERR_DEVICE_TIMEOUT
+//            in the status word and its block skips phase 2 (y is left as it
+//            was); it never hangs.
+//   Phase 2: every block sums the G partials of a row in the same order, so
+//            every block forms the bit-identical row factor, re-reads its
+//            range of x (an L2 hit: phase 1 just read it) and writes y.
+//   Exit:    each block adds one to a departure counter; the last block to
+//            leave sets both counters back to zero for the next call.
+#include "internal.h"
+#include "device_common.cuh"
+
+namespace rmsnorm {
+namespace {
+
+__device__ inline uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ inline uint32_t ld_acquire(const uint32_t *p)
+{
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ inline uint32_t add_release(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.release.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ inline uint32_t add_acq_rel(uint32_t *p, uint32_t v)
+{
+    uint32_t old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "l"(p), "r"(v)
+                 : "memory");
+    return old;
+}
+
+__device__ inline float ld_l2(const float *p)
+{
+    float v;
+    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    return v;
+}
+
+template <int VB>
+__device__ inline void vzero(Vec<VB> &v)
+{
+#pragma unroll
+    for (int k = 0; k < Vec<VB>::kWords; ++k)
+        v.w[k] = 0u;
+}
+
+// Block-wide sum (every thread gets it); `part` holds one float per warp.
+__device__ inline float block_sum(float s, float *part)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    s = group_allreduce<32>(s);
+    if (lane == 0)
+        part[warp] = s;
+    __syncthreads();
+    float tot = lane < nwarps ? part[lane] : 0.f;
+    tot = group_allreduce<32>(tot);
+    __syncthreads(); // part is reused by the next call
+    return tot;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(512, 2)
+grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+                 int32_t hidden, float eps, float *partial, uint32_t *counters, int *status,
+                 uint64_t limit_ns, uint32_t flags)
+{
+    using E = Elem<DT>;
+    constexpr int VB = 16;
+    constexpr int VPE = VB / E::kSize;
+    constexpr int U = 4;
+    __shared__ float part[32];
+    __shared__ int passed;
+
+    const int G = gridDim.x;
+    const int b = blockIdx.x;
+    const int t = threadIdx.x;
+    const int tpr = blockDim.x;
+    const int nvec = hidden / VPE;
+    const int S = (nvec + G - 1) / G;
+    const int v0 = min(nvec, b * S);
+    const int v1 = min(nvec, v0 + S);
+    const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
+    const float n = static_cast<float>(hidden);
+
+    // ---- phase 1: partial sums of squares
+    for (int64_t row = 0; row < rows; ++row) {
+        const char *xr = static_cast<const char *>(x) + row * row_bytes;
+        float s = 0.f;
+        for (int v = v0 + t; v < v1; v += U * tpr) {
+            Vec<VB> xv[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int vv = v + u * tpr;
+                if (vv < v1)
+                    ld_stream<1>(xv[u], xr + static_cast<int64_t>(vv) * VB);
+                else
+                    vzero(xv[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                s = sumsq<DT, VB>(xv[u], s);
+        }
+        s = block_sum(s, part);
+        if (t == 0)
+            partial[row * G + b] = s;
+    }
+
+    // ---- grid barrier (counters[0]: arrivals, counters[1]: departures)
+    __syncthreads();
+    if (t == 0) {
+        // kFlagWithholdCopies (failure-detection test only): block 0 does not
+        // arrive, so every wait runs out.
+        if (!((flags & kFlagWithholdCopies) && b == 0))
+            add_release(&counters[0], 1u); // orders this block's partials before it
+        int ok = 1;
+        if (ld_acquire(&counters[0]) < static_cast<uint32_t>(G)) {
+            const uint64_t t0 = globaltimer_ns();
+            while (ld_acquire(&counters[0]) < static_cast<uint32_t>(G)) {
+                if (globaltimer_ns() - t0 > limit_ns) {
+                    ok = 0;
+                    atomicCAS(status, 0, static_cast<int>(RMSNORM_ERR_DEVICE_TIMEOUT));
+                    break;
+                }
+            }
+        }
+        passed = ok;
+    }
+    __syncthreads();
+
+    // ---- phase 2: the row factor from all partials, then scale and store
+    if (passed) {
+        for (int64_t row = 0; row < rows; ++row) {
+            float a = 0.f;
+            for (int i = t; i < G; i += tpr) // the same order in every block
+                a += ld_l2(partial + row * G + i);
+            const float r = row_factor(block_sum(a, part), n, eps);
+            const char *xr = static_cast<const char *>(x) + row * row_bytes;
+            char *yr = static_cast<char *>(y) + row * row_bytes;
+            const char *wb = static_cast<const char *>(w);
+            for (int v = v0 + t; v < v1; v += U * tpr) {
+                Vec<VB> xv[U], wv[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int vv = v + u * tpr;
+                    if (vv < v1) {
+                        ld_stream<0>(xv[u], xr + static_cast<int64_t>(vv) * VB);
+                        ld_weight(wv[u], wb + static_cast<int64_t>(vv) * VB);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int vv = v + u * tpr;
+                    if (vv < v1) {
+                        Vec<VB> o;
+                        scale<DT, VB>(o, xv[u], wv[u], r);
+                        st_stream<1>(yr + static_cast<int64_t>(vv) * VB, o);
+                    }
+                }
+            }
+        }
+    }
+
+    // ---- departure: the last block out clears the counters (every block
+    // has passed or given up on the barrier and read its partials by now)
+    __syncthreads();
+    if (t == 0 && add_acq_rel(&counters[1], 1u) == static_cast<uint32_t>(G) - 1u) {
+        counters[0] = 0u;
+        counters[1] = 0u;
+    }
+}
+
+template <int DT>
+cudaError_t launch_grid(const rmsnorm_plan_t &p, const LaunchArgs &a)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.block_threads));
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = a.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative; // every block resident at once, or no launch
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // scratch: two counters (zeroed by the caller), then rows * G partials
+    uint32_t *counters = static_cast<uint32_t *>(a.scratch);
+    float *partial = reinterpret_cast<float *>(static_cast<char *>(a.scratch) + kGridCounterBytes);
+    const cudaError_t err =
+        cudaLaunchKernelEx(&cfg, grid_rows_kernel<DT>, a.x, a.w, a.y, a.rows, a.hidden, a.eps,
+                           partial, counters, a.status, a.wait_limit_ns, a.flags);
+    return err != cudaSuccess ? err : cudaGetLastError();
+}
+
+#define GRID_ENTRY(DT)                                                                         \
+    KernelDesc{RMSNORM_VARIANT_GRID, DT, 16, 0, 0, 512, 2, 1, &launch_grid<DT>,               \
+               reinterpret_cast<const void *>(&grid_rows_kernel<DT>)}
+
+const KernelDesc kTable[] = {GRID_ENTRY(RMSNORM_F32), GRID_ENTRY(RMSNORM_BF16),
+                             GRID_ENTRY(RMSNORM_F16)};
+
+} // namespace
+
+const KernelDesc *grid_kernels(int *n)
+{
+    *n = static_cast<int>(sizeof(kTable) / sizeof(kTable[0]));
+    return kTable;
+}
+
+} // namespace rmsnorm

@@ -32,6 +32,7 @@ struct LaunchArgs {
     float bias = -0.0f;     // weight offset (BIAS / MXFP8 epilogues); -0 adds nothing
     void *scales = nullptr; // block-scaled epilogues: the scales; y holds the codes
     float gscale = 1.0f;    // NVFP4: the per-tensor scale
+    void *scratch = nullptr; // grid variant: counters + partial sums (stream-ordered, per call)
 };
 
 #if defined(__CUDACC__)
@@ -91,6 +92,13 @@ const KernelDesc *rowreg_fp4_kernels_bf16(int *n);
 const KernelDesc *rowreg_fp4_kernels_f16(int *n);
 const KernelDesc *staged_kernels(int *n);
 const KernelDesc *cluster_kernels(int *n);
+const KernelDesc *grid_kernels(int *n);
+
+// Grid variant scratch: two 32-bit counters padded to 16 bytes, then
+// rows * grid floats.
+constexpr int64_t kGridCounterBytes = 16;
+constexpr int kGridBlocksPerSm = 2;  // 512-thread blocks, <= 64 registers
+constexpr int64_t kGridMaxRows = 64; // bounds the scratch: rows * grid floats
 const KernelDesc *generic_kernels(int *n);
 
 const KernelDesc *kernel_table(int *n);

@@ -429,6 +429,31 @@ int plan_cluster_exact(const Shape &s, int C, int vb, rmsnorm_plan_t *p)
     return RMSNORM_ERR_VARIANT;
 }
 
+// ---- grid: rows spread over every SM with one grid barrier (a cooperative
+// launch of kGridBlocksPerSm 512-thread blocks per SM); <= kGridMaxRows rows.
+int plan_grid(const Shape &s, rmsnorm_plan_t *p)
+{
+    clear(p);
+    if (s.epi != RMSNORM_EPI_PLAIN || s.rows > kGridMaxRows)
+        return RMSNORM_ERR_VARIANT;
+    if (!s.a16)
+        return RMSNORM_ERR_MISALIGNED;
+    const int idx = find_rowreg(RMSNORM_VARIANT_GRID, s.dtype, 16, 0, 0, 512, kGridBlocksPerSm, 1,
+                                s.epi);
+    if (idx < 0)
+        return RMSNORM_ERR_VARIANT;
+    p->variant = RMSNORM_VARIANT_GRID;
+    p->vec_bytes = 16;
+    p->block_threads = 512;
+    p->grid = s.sm_count * kGridBlocksPerSm;
+    p->threads_per_row = p->block_threads * p->grid;
+    p->vecs_per_thread = 0;
+    p->rows_per_block = static_cast<int>(s.rows); // every block works on every row
+    p->stages = 0;
+    p->kernel_index = idx;
+    return RMSNORM_OK;
+}
+
 // Forced cluster: the smallest cluster whose slices are <= 8 KiB (at most 8
 // blocks), 16-byte vectors.
 int plan_cluster(const Shape &s, rmsnorm_plan_t *p)
@@ -497,6 +522,8 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         return plan_staged_auto(s, out);
     case RMSNORM_VARIANT_CLUSTER:
         return plan_cluster(s, out);
+    case RMSNORM_VARIANT_GRID:
+        return plan_grid(s, out);
     case RMSNORM_VARIANT_GENERIC:
         if (s.epi >= RMSNORM_EPI_MXFP8) { // no scalar body for the block-scaled outputs
             clear(out);
@@ -534,6 +561,10 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
             if (s.rows * C <= s.sm_count &&
                 ((s.a32 && plan_cluster_exact(s, C, 32, out) == RMSNORM_OK) ||
                  plan_cluster_exact(s, C, 16, out) == RMSNORM_OK))
+                return RMSNORM_OK;
+            // Rows longer than a cluster holds in registers: spread over
+            // every SM with one grid barrier.
+            if (s.row_bytes > 512 * 1024 && plan_grid(s, out) == RMSNORM_OK)
                 return RMSNORM_OK;
         }
         // Decode: a whole warp per row up to 1 KiB rows (idle lanes cost less
@@ -669,6 +700,12 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
         break;
     }
     case RMSNORM_VARIANT_GENERIC:
+        break;
+    case RMSNORM_VARIANT_GRID:
+        // every block resident at once: at most the blocks the SMs hold
+        if (p.grid > sm_count * kGridBlocksPerSm || p.block_threads > d.block ||
+            rows > kGridMaxRows || p.rows_per_block != rows)
+            return RMSNORM_ERR_VARIANT;
         break;
     case RMSNORM_VARIANT_CLUSTER: {
         const int C = p.stages;

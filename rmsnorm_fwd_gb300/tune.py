@@ -122,6 +122,14 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
                 out.append(dict(variant=v, vec_bytes=vb, threads_per_row=tpr * C,
                                 vecs_per_thread=k["nv"], block_threads=tpr, rows_per_block=1,
                                 stages=C, grid=rows * C, smem_bytes=0, kernel_index=k["index"]))
+        elif v == rn.VARIANT_GRID:
+            if hidden * es % 16 or rows > 64:
+                continue
+            for g in (sms, 2 * sms):
+                for b in (256, 512):
+                    out.append(dict(variant=v, vec_bytes=16, threads_per_row=b * g,
+                                    vecs_per_thread=0, block_threads=b, rows_per_block=rows,
+                                    stages=0, grid=g, smem_bytes=0, kernel_index=k["index"]))
         elif v == rn.VARIANT_GENERIC:
             for b in (256, 512, 1024):
                 out.append(dict(variant=v, vec_bytes=0, threads_per_row=b, vecs_per_thread=0,
@@ -301,7 +309,7 @@ def plan_label(p: dict, kinfo: dict) -> str:
     """Short text for a plan: variant, vector bytes, threads/row, vectors/thread,
     block, grid, stages, register floor, cache policy."""
     v = {1: "warp", 2: "block", 3: "staged", 4: "persistent", 5: "generic",
-         6: "cluster"}[p["variant"]]
+         6: "cluster", 7: "grid"}[p["variant"]]
     k = kinfo[p["kernel_index"]]
     nv = p["vecs_per_thread"] if p["variant"] != 3 else 0
     extra = f" W{p['threads_per_row'] // 32}" if p["variant"] == 3 else f" {nv}v"

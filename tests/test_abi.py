@@ -343,11 +343,12 @@ def test_epilogue_kernel_sets():
         mx = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_MXFP8]
         key = lambda k: (k["variant"], k["vec_bytes"], k["tpr"], k["nv"], k["block"],
                          k["min_blocks"], k["cache_policy"])
-        # every register / looped / generic body has a bias twin; the staged and
-        # cluster ones have none
+        # every register / looped / generic body has a bias twin; the staged,
+        # cluster and grid ones have none
         assert {key(k) for k in bias} == {key(k) for k in plain
                                           if k["variant"] not in (rn.VARIANT_STAGED,
-                                                                  rn.VARIANT_CLUSTER)}
+                                                                  rn.VARIANT_CLUSTER,
+                                                                  rn.VARIANT_GRID)}
         # block-scaled outputs: the register and looped bodies except the 4-lane group
         want = {key(k) for k in plain if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
                                                           rn.VARIANT_CTA_PER_ROW)
@@ -503,3 +504,23 @@ def test_fp4_argument_rules():
                                  rn.BF16, None) == rn.ERR_ALIASING
     assert lib.rmsnorm_fwd_nvfp4(A, 3 * A, 5 * A, 7 * A, 4, 4096, 0.0, 0.0, 1e-6, rn.BF16,
                                  None) == rn.ERR_INVALID_ARG
+
+
+
+def test_grid_plans():
+    # rows too long for a cluster: the grid variant, 2 blocks of 512 threads per SM
+    for rows, hidden, dt in ((1, 1 << 20, rn.BF16), (8, 300000, rn.F32), (64, 262152, rn.BF16)):
+        rc, p = plan(rows, hidden, dt)
+        assert rc == rn.OK and p.variant == rn.VARIANT_GRID, (rows, hidden, p.as_dict())
+        assert p.grid == 2 * SMS and p.block_threads == 512 and p.rows_per_block == rows
+        assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, rows, hidden, dt, SMS,
+                                        OPTIN) == rn.OK
+        bad = rn.Plan(**p.as_dict())
+        bad.grid = 2 * SMS + 1          # more blocks than the SMs hold at once
+        assert rn.rmsnorm_validate_plan(bad, A, 3 * A, 5 * A, rows, hidden, dt, SMS,
+                                        OPTIN) == rn.ERR_VARIANT
+    # rows a cluster holds, more rows than 64, or an epilogue: not the grid variant
+    assert plan(1, 1 << 18, rn.BF16)[1].variant == rn.VARIANT_CLUSTER
+    assert plan(65, 1 << 20, rn.BF16, rn.VARIANT_GRID)[0] == rn.ERR_VARIANT
+    assert plan_epi(1, 1 << 20, rn.BF16, rn.EPI_BIAS, rn.VARIANT_GRID)[0] == rn.ERR_VARIANT
+    assert plan(1, 1 << 20, rn.BF16, rn.VARIANT_GRID, xoff=2)[0] == rn.ERR_MISALIGNED

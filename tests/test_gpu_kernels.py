@@ -118,6 +118,16 @@ def _plans_for(k, rows, sms, optin):
                                                  vecs_per_thread=k["nv"], block_threads=tpr,
                                                  rows_per_block=1, stages=C, grid=rows * C,
                                                  smem_bytes=0, kernel_index=k["index"])))
+    elif v == rn.VARIANT_GRID:
+        vpe = 16 // es
+        for grid in (sms, 2 * sms, 7):
+            for block in (64, 512):
+                for nvec in (1, grid - 1, grid * 4 + 3, 40000):
+                    out.append((nvec * vpe, dict(variant=v, vec_bytes=16,
+                                                 threads_per_row=block * grid,
+                                                 vecs_per_thread=0, block_threads=block,
+                                                 rows_per_block=rows, stages=0, grid=grid,
+                                                 smem_bytes=0, kernel_index=k["index"])))
     elif v == rn.VARIANT_GENERIC:
         for hidden in (1, 33, 1000, 4097):
             for block in (32, 256):

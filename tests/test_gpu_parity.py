@@ -72,7 +72,7 @@ def test_wide_workload_sampled(name):
 
 @pytest.mark.parametrize("variant", [rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
                                      rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT,
-                                     rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER])
+                                     rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER, rn.VARIANT_GRID])
 def test_headline_shape_every_variant(variant):
     wl = inputs.WORKLOADS["prefill_bf16_16384x4096"]
     x, w = inputs.make_inputs(wl)
@@ -91,7 +91,8 @@ HIDDEN = [1, 2, 3, 7, 8, 9, 31, 33, 127, 128, 129, 1000, 1023, 1024, 1025, 2880,
           7168, 8191, 16384, 32768]
 ROWS = [0, 1, 2, 31, 160, 161]
 VARIANTS = [rn.VARIANT_AUTO, rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW,
-            rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT, rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER]
+            rn.VARIANT_STAGED, rn.VARIANT_PERSISTENT, rn.VARIANT_GENERIC, rn.VARIANT_CLUSTER,
+            rn.VARIANT_GRID]
 
 
 def accepts(rows, hidden, dtype, variant):
@@ -240,3 +241,25 @@ def test_long_decode_rows(dtype, rows, hidden):
     if hidden * es >= 65536 and hidden * es % 16 == 0:
         assert rn.rmsnorm_last_variant() == rn.VARIANT_CLUSTER
     compare(y, x, w, 1e-6, dtype)
+
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+@pytest.mark.parametrize("rows,hidden", [(1, 1 << 20), (4, 300000), (2, 262152), (64, 140000),
+                                         (1, 2 * 1024 * 1024 + 8)])
+def test_huge_decode_rows_grid(dtype, rows, hidden):
+    """Decode rows longer than a cluster holds (above 512 KiB): the automatic
+    plan spreads them over every SM with one grid barrier."""
+    if dtype == "f32" and hidden > (1 << 20):
+        hidden //= 2
+    x, w = inputs.random_case(rows, hidden, dtype, seed=hidden % 1000 + rows)
+    y = run(x, w, 1e-6, dtype)
+    es = 4 if dtype == "f32" else 2
+    if hidden * es > 512 * 1024 and hidden * es % 16 == 0:
+        assert rn.rmsnorm_last_variant() == rn.VARIANT_GRID
+    compare(y, x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 8, seed=rows))
+    # in place
+    xd = to_device(x, dtype)
+    rn.rms_norm(xd, to_device(w, dtype), 1e-6, out=xd, variant=rn.VARIANT_GRID)
+    torch.cuda.synchronize()
+    compare(from_device(xd, dtype), x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 8, seed=rows))

@@ -1,8 +1,8 @@
-"""Failure detection on the GPU without a fault: the staged kernel's bounded
-waits.  The test withholds the row copies (a flag nothing sets), so every
-consumer wait runs out after a short limit; the kernel must record
-RMSNORM_ERR_DEVICE_TIMEOUT in the status word, leave y untouched, and leave
-the context usable."""
+"""Failure detection on the GPU without a fault: the bounded waits of the
+staged kernel (the row copies withheld, a flag nothing sets) and of the
+grid variant's barrier (one block's arrival withheld).  Every wait runs out
+after a short limit; the kernel must record RMSNORM_ERR_DEVICE_TIMEOUT in
+the status word, leave y untouched, and leave the context usable."""
 import numpy as np
 import pytest
 
@@ -53,3 +53,25 @@ def test_wait_limit_setting_round_trips():
     rn.rmsnorm_set_wait_limit_ns(0)  # back to the default
     assert rn.rmsnorm_get_device_status() == rn.OK
     compare(from_device(out, wl.dtype), x_np, w_np, wl.eps, wl.dtype)
+
+
+def test_grid_barrier_timeout_is_reported_and_context_survives():
+    dtype, rows, hidden = "bf16", 3, 1 << 19   # 1 MiB rows: the grid variant's shapes
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=10)
+    x = to_device(x_np, dtype)
+    w = to_device(w_np, dtype)
+    y = torch.full_like(x, 5.0)
+    assert rn.rmsnorm_get_device_status() == rn.OK
+    rn.rmsnorm_test_grid_timeout(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden,
+                                 rn.BF16, 20_000_000, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rn.rmsnorm_get_device_status() == rn.ERR_DEVICE_TIMEOUT
+    assert rn.rmsnorm_get_device_status() == rn.OK
+    assert (y == 5.0).all()
+    # the context still works, on the same kernel, twice in a row (the
+    # barrier counters start from zero again)
+    for _ in range(2):
+        out = rn.rms_norm(x, w, 1e-6, variant=rn.VARIANT_GRID)
+        torch.cuda.synchronize()
+        compare(from_device(out, dtype), x_np, w_np, 1e-6, dtype)
+    assert rn.rmsnorm_get_device_status() == rn.OK
