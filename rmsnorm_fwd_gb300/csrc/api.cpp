@@ -260,8 +260,8 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
                      p.variant, p.vec_bytes, p.threads_per_row, p.vecs_per_thread,
                      p.block_threads, p.grid, p.stages, p.smem_bytes, p.kernel_index);
     if (d.variant == RMSNORM_VARIANT_GRID) {
-        // Per-call scratch from the stream-ordered pool: counters (zeroed)
-        // and rows * grid partial sums; freed in stream order after the
+        // Per-call scratch from the stream-ordered pool: counters and rows *
+        // grid partial sums, zeroed; freed in stream order after the
         // kernel, so concurrent calls on other streams never share it.
         const size_t bytes = static_cast<size_t>(kGridCounterBytes) +
                              static_cast<size_t>(rows) * static_cast<size_t>(p.grid) * sizeof(float);
@@ -269,7 +269,7 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
         if (cudaMallocAsync(&scratch, bytes, a.stream) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
         a.scratch = scratch;
-        const bool ok = cudaMemsetAsync(scratch, 0, kGridCounterBytes, a.stream) == cudaSuccess &&
+        const bool ok = cudaMemsetAsync(scratch, 0, bytes, a.stream) == cudaSuccess &&
                         d.launch(p, a) == cudaSuccess;
         const bool freed = cudaFreeAsync(scratch, a.stream) == cudaSuccess;
         if (!ok || !freed)

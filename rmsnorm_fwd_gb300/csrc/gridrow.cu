@@ -9,10 +9,11 @@
 // two launches.  Here it serves decode rows longer than a thread-block
 // cluster holds in registers (above 512 KiB).
 //
-// Block b of G takes the same range of 16-byte vectors [b*S, min((b+1)*S,
-// nvec)), S = ceil(nvec / G), of every row.
-//   Phase 1: the block's sum of squares of its range of each row, written to
-//            partial[row * G + b].
+// The rows' 16-byte vectors, taken one row after the other, are cut into G
+// equal ranges, one per block (a block may cover a part of one row or parts
+// of a few).
+//   Phase 1: the block's sum of squares of its part of each row it touches,
+//            written to partial[row * G + b] (the rest of partial is zero).
 //   Barrier: one thread per block adds one to an arrival counter (release)
 //            and waits, bounded by %globaltimer, until all G have arrived
 //            (acquire).  A wait that runs out records RMSNORM_ERR_DEVICE_TIMEOUT
@@ -109,15 +110,23 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     const int b = blockIdx.x;
     const int t = threadIdx.x;
     const int tpr = blockDim.x;
-    const int nvec = hidden / VPE;
-    const int S = (nvec + G - 1) / G;
-    const int v0 = min(nvec, b * S);
-    const int v1 = min(nvec, v0 + S);
+    const int64_t nvec = hidden / VPE;
+    // Block b owns the range [f0, f1) of the rows' vectors taken one row
+    // after the other (an equal share of all of them, so a few rows each of
+    // some blocks or a part of one row each).
+    const int64_t total = rows * nvec;
+    const int64_t share = (total + G - 1) / G;
+    const int64_t f0 = min(total, b * share);
+    const int64_t f1 = min(total, f0 + share);
+    const int64_t row_lo = f0 / nvec;
+    const int64_t row_hi = f1 > f0 ? (f1 - 1) / nvec : row_lo - 1; // last row touched
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
     const float n = static_cast<float>(hidden);
 
-    // ---- phase 1: partial sums of squares
-    for (int64_t row = 0; row < rows; ++row) {
+    // ---- phase 1: this block's partial sum of squares of every row it touches
+    for (int64_t row = row_lo; row <= row_hi; ++row) {
+        const int v0 = static_cast<int>(max(f0, row * nvec) - row * nvec);
+        const int v1 = static_cast<int>(min(f1, (row + 1) * nvec) - row * nvec);
         const char *xr = static_cast<const char *>(x) + row * row_bytes;
         float s = 0.f;
         for (int v = v0 + t; v < v1; v += U * tpr) {
@@ -136,7 +145,7 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
         }
         s = block_sum(s, part);
         if (t == 0)
-            partial[row * G + b] = s;
+            partial[row * G + b] = s; // (row, block) pairs never touched stay 0
     }
 
     // ---- grid barrier (counters[0]: arrivals, counters[1]: departures)
@@ -161,16 +170,19 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     }
     __syncthreads();
 
-    // ---- phase 2: the row factor from all partials, then scale and store
+    // ---- phase 2: each touched row's factor from all G partials, then scale
+    // and store this block's part of it
     if (passed) {
-        for (int64_t row = 0; row < rows; ++row) {
+        const char *wb = static_cast<const char *>(w);
+        for (int64_t row = row_lo; row <= row_hi; ++row) {
             float a = 0.f;
             for (int i = t; i < G; i += tpr) // the same order in every block
                 a += ld_l2(partial + row * G + i);
             const float r = row_factor(block_sum(a, part), n, eps);
+            const int v0 = static_cast<int>(max(f0, row * nvec) - row * nvec);
+            const int v1 = static_cast<int>(min(f1, (row + 1) * nvec) - row * nvec);
             const char *xr = static_cast<const char *>(x) + row * row_bytes;
             char *yr = static_cast<char *>(y) + row * row_bytes;
-            const char *wb = static_cast<const char *>(w);
             for (int v = v0 + t; v < v1; v += U * tpr) {
                 Vec<VB> xv[U], wv[U];
 #pragma unroll
@@ -216,7 +228,7 @@ cudaError_t launch_grid(const rmsnorm_plan_t &p, const LaunchArgs &a)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // scratch: two counters (zeroed by the caller), then rows * G partials
+    // scratch (zeroed by the caller): two counters, then rows * G partials
     uint32_t *counters = static_cast<uint32_t *>(a.scratch);
     float *partial = reinterpret_cast<float *>(static_cast<char *>(a.scratch) + kGridCounterBytes);
     const cudaError_t err =
