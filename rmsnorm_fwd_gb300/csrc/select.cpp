@@ -396,8 +396,10 @@ int plan_staged_wide(const Shape &s, rmsnorm_plan_t *p)
 
 // ---- cluster: a row over C blocks of one cluster (decode, long rows).
 // Slice S = ceil(nvec / C) vectors per block; the fewest vectors per thread
-// that keep the block at <= 512 threads (<= 1024 with 4 per thread).
-int plan_cluster_exact(const Shape &s, int C, int vb, rmsnorm_plan_t *p)
+// (at least `min_thread_bytes` per thread) that keep the block at <= 512
+// threads (<= 1024 with 4 per thread).
+int plan_cluster_exact(const Shape &s, int C, int vb, rmsnorm_plan_t *p,
+                       int min_thread_bytes = 0)
 {
     clear(p);
     if (s.epi != RMSNORM_EPI_PLAIN)
@@ -410,7 +412,7 @@ int plan_cluster_exact(const Shape &s, int C, int vb, rmsnorm_plan_t *p)
     const int64_t S = (nvec + C - 1) / C;
     for (int nv : {1, 2, 4}) {
         const int tpr = tpr_for(S, nv);
-        if (tpr > (nv == 4 ? 1024 : 512))
+        if (tpr > (nv == 4 ? 1024 : 512) || nv * vb < min_thread_bytes)
             continue;
         const int idx = find_rowreg(RMSNORM_VARIANT_CLUSTER, s.dtype, vb, 0, nv, 1024, 0, 1, s.epi);
         if (idx < 0)
@@ -548,23 +550,32 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     }
     const int64_t nvec = s.row_bytes / 16;
     if (s.rows <= s.sm_count) {
-        // Decode rows longer than 32 KiB (up to 8 of them; any number from 48
-        // KiB): one row over a cluster of blocks, as large a cluster (<= 8) as
-        // keeps every block on its own SM (measured on GB300: 1 x 64 Ki bf16
-        // 6.1 -> 2.6 us, 8 x 64 Ki 9.1 -> 3.3 us, 8 x 24 Ki 2.9 -> 2.4 us,
-        // 32 x 32 Ki 4.0 -> 3.6 us; 32 KiB rows and shorter gain nothing).
-        if (s.epi == RMSNORM_EPI_PLAIN && s.row_bytes > 32 * 1024 &&
-            (s.rows <= 8 || s.row_bytes >= 48 * 1024)) {
-            int C = 8;
-            while (C > 2 && s.rows * C > s.sm_count)
-                C /= 2;
-            if (s.rows * C <= s.sm_count &&
-                ((s.a32 && plan_cluster_exact(s, C, 32, out) == RMSNORM_OK) ||
-                 plan_cluster_exact(s, C, 16, out) == RMSNORM_OK))
+        // Long decode rows over thread-block clusters or the whole GPU
+        // (fitted to sweeps of rows 1..152 x rows of 32 KiB..2 MiB on GB300;
+        // e.g. 1 x 64 Ki bf16 6.1 -> 2.6 us, 8 x 64 Ki 9.1 -> 3.3 us, 77 x
+        // 64 Ki 10.7 -> 7.5 us, 1 x 1 Mi 117 -> 12.6 us):
+        //  * rows above 32 KiB (up to 8 rows below 48 KiB): one wave of
+        //    clusters, as large (<= 8) as keeps every block on its own SM --
+        //    at least 4 blocks, or 2 for rows of 64 KiB and more;
+        //  * 128..256 KiB rows, up to 80 of them: clusters of 8 over several
+        //    waves, 64 bytes per thread;
+        //  * longer rows, up to 64 of them: every SM on every row, one grid
+        //    barrier.
+        // Other long-row decode shapes keep the block-per-row bodies below.
+        if (s.epi == RMSNORM_EPI_PLAIN && s.row_bytes > 32 * 1024) {
+            if (s.rows <= 8 || s.row_bytes >= 48 * 1024) {
+                int C = 8;
+                while (C > 2 && s.rows * C > s.sm_count)
+                    C /= 2;
+                if (s.rows * C <= s.sm_count && (C >= 4 || s.row_bytes >= 64 * 1024) &&
+                    ((s.a32 && plan_cluster_exact(s, C, 32, out) == RMSNORM_OK) ||
+                     plan_cluster_exact(s, C, 16, out) == RMSNORM_OK))
+                    return RMSNORM_OK;
+            }
+            if (s.rows <= 80 && s.row_bytes >= 128 * 1024 && s.row_bytes <= 256 * 1024 &&
+                plan_cluster_exact(s, 8, 16, out, 64) == RMSNORM_OK)
                 return RMSNORM_OK;
-            // Rows longer than a cluster holds in registers: spread over
-            // every SM with one grid barrier.
-            if (s.row_bytes > 512 * 1024 && plan_grid(s, out) == RMSNORM_OK)
+            if (s.row_bytes > 256 * 1024 && plan_grid(s, out) == RMSNORM_OK)
                 return RMSNORM_OK;
         }
         // Decode: a whole warp per row up to 1 KiB rows (idle lanes cost less
