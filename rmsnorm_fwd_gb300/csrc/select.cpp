@@ -446,8 +446,10 @@ int plan_grid(const Shape &s, rmsnorm_plan_t *p)
         return RMSNORM_ERR_VARIANT;
     p->variant = RMSNORM_VARIANT_GRID;
     p->vec_bytes = 16;
-    p->block_threads = 512;
-    p->grid = s.sm_count * kGridBlocksPerSm;
+    // one row: one 256-thread block per SM (less barrier traffic; measured
+    // 12.0 -> 10.4 us on a 2 MiB row); more rows: two 512-thread blocks
+    p->block_threads = s.rows == 1 ? 256 : 512;
+    p->grid = s.sm_count * (s.rows == 1 ? 1 : kGridBlocksPerSm);
     p->threads_per_row = p->block_threads * p->grid;
     p->vecs_per_thread = 0;
     p->rows_per_block = static_cast<int>(s.rows); // every block works on every row

@@ -518,7 +518,8 @@ def test_grid_plans():
     for rows, hidden, dt in ((1, 1 << 20, rn.BF16), (8, 300000, rn.F32), (64, 262152, rn.BF16)):
         rc, p = plan(rows, hidden, dt)
         assert rc == rn.OK and p.variant == rn.VARIANT_GRID, (rows, hidden, p.as_dict())
-        assert p.grid == 2 * SMS and p.block_threads == 512 and p.rows_per_block == rows
+        assert p.grid == (SMS if rows == 1 else 2 * SMS) and p.rows_per_block == rows
+        assert p.block_threads == (256 if rows == 1 else 512)
         assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, rows, hidden, dt, SMS,
                                         OPTIN) == rn.OK
         bad = rn.Plan(**p.as_dict())
