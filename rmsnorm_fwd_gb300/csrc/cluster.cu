@@ -125,8 +125,10 @@ cluster_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
     float tot = static_cast<uint32_t>(lane) < C ? ld_peer(cta_smem_addr(&block_total), lane) : 0.f;
     tot = group_allreduce<32>(tot);
     // No block leaves (or lets its shared memory go) before every peer has
-    // read its total: arrive now, wait at the end.
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+    // read its total: arrive now, wait at the end.  Relaxed: the peer reads
+    // above have completed (their values are used), and nothing written
+    // here needs to be seen through this barrier.
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     const float r = row_factor(tot, static_cast<float>(hidden), eps);
 #pragma unroll
     for (int k = 0; k < NV; ++k)

@@ -600,24 +600,27 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // bf16 rows for the three formats):
     //   1-2 KiB rows: a warp per row, 4 vectors per lane (register-capped
     //     for 8 blocks of 256 threads per SM), 16 blocks per SM;
-    //   2-16 KiB rows: 32-byte vectors, 2 per thread up to 8 KiB rows and 4
-    //     beyond, 16 blocks per SM while they fit (16-byte vectors, 4 per
-    //     thread, one block per row when unaligned for 32);
+    //   2-4 KiB rows: 32-byte vectors, 2 per thread, 16 blocks per SM;
+    //   4-16 KiB rows: 32-byte vectors, 2 per thread, register-capped for 6
+    //     blocks of 256 threads per SM, one block per row (16-byte vectors,
+    //     4 per thread, when unaligned for 32);
     //   16-32 KiB rows: 32-byte vectors, 4 per thread, 4 blocks per SM.
     const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
     if (blockq && nvec > 64 && nvec <= 128 &&
         plan_warp_exact(s, 32, 4, 8, int64_t(s.sm_count) * 16, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    if (blockq && s.a32 && nvec > 128 && nvec <= 1024) {
-        const int64_t n32 = nvec / 2;
-        const int nv = n32 <= 256 ? 2 : 4;
-        const int tpr = tpr_for(n32, nv);
+    if (blockq && s.a32 && nvec > 128 && nvec <= 256) {
+        const int tpr = tpr_for(nvec / 2, 2);
         const int64_t cap = int64_t(s.sm_count) * std::min(16, 2048 / tpr);
-        if (plan_cta_exact(s, 32, nv, nv == 2 ? 1024 : 512, 0, 1, 0, tpr, cap,
+        if (plan_cta_exact(s, 32, 2, 1024, 0, 1, 0, tpr, cap,
                            cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW,
                            out) == RMSNORM_OK)
             return RMSNORM_OK;
     }
+    if (blockq && s.a32 && nvec > 256 && nvec <= 1024 &&
+        plan_cta_exact(s, 32, 2, 256, 6, 1, 0, tpr_for(nvec / 2, 2), INT_MAX,
+                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+        return RMSNORM_OK;
     if (blockq && nvec > 128 && nvec <= 1024 &&
         plan_cta_exact(s, 16, 4, 256, 6, 1, 0, tpr_for(nvec, 4), INT_MAX,
                        RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)

@@ -382,6 +382,8 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                         assert p.variant == rn.VARIANT_WARP_PER_ROW and p.vecs_per_thread == 4
                     else:
                         assert p.vec_bytes == 32 and p.vecs_per_thread in (2, 4)
+                        if 256 < nvec <= 1024:   # the register-capped 2-vector body
+                            assert ks[p.kernel_index]["min_blocks"] == 6
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
