@@ -164,13 +164,22 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
 // per call; each block zeroes its own word when it starts, and a group whose
 // wait ran out writes its remaining rows of y as NaN so the failure is
 // visible in the output.
-template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false>
+//
+// EPI: the output (rmsnorm_epilogue_t).  BIAS adds `bias` to the weight;
+// the block-scaled outputs (never with TMA_STORE: their codes are smaller
+// than the slot) write codes and scales with q_store, in a warp-uniform loop
+// so every lane of a warp takes part in each scale block's shuffles.
+template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false, int EPI = RMSNORM_EPI_PLAIN>
 __global__ void __launch_bounds__(32 * 17)
 staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                    int32_t hidden, float eps, int32_t stages, int32_t wpr, int *status,
-                   uint64_t limit_ns, uint32_t flags)
+                   uint64_t limit_ns, uint32_t flags, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
+    constexpr int Q = MX ? EPI - RMSNORM_EPI_MXFP8 : 0;
+    static_assert(!(MX && TMA_STORE), "block-scaled outputs are stored from registers");
+    static_assert(!(BLOCK_STATUS && EPI != RMSNORM_EPI_PLAIN), "status-per-block: plain only");
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int32_t row_bytes = hidden * E::kSize;
@@ -316,7 +325,10 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                 const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
                 Vec<16> o;
-                scale<DT, 16>(o, xv, wv, r);
+                if constexpr (EPI == RMSNORM_EPI_BIAS)
+                    scale_bias<DT, 16>(o, xv, wv, r, bias);
+                else
+                    scale<DT, 16>(o, xv, wv, r);
                 *reinterpret_cast<Vec<16> *>(dst + v * 16) = o;
             }
             // The slot's new contents must be visible to the bulk copy (async proxy).
@@ -333,13 +345,41 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                     mbar_arrive(smem_u32(&bars[stages + prev_slot]));
             }
             prev_slot = s;
+        } else if constexpr (MX) {
+            using G = QGeo<DT, 16, Q>;
+            char *qr = yb + row * (static_cast<int64_t>(hidden) * QFmt<Q>::kBits / 8);
+            uint8_t *sr = scales + row * (hidden / QFmt<Q>::kBlock);
+            // lane l of the warp starting at vector vb takes vector vb + l:
+            // the same vectors as gl, gl + gsize, ...
+            for (int vb = wi * 32; vb < nvec; vb += gsize) {
+                const int v = vb + lane;
+                const bool live = v < nvec;
+                Vec<16> xv, wv;
+                if (live) {
+                    xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                    wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        xv.w[k] = wv.w[k] = 0u;
+                }
+                q_store<DT, 16, Q>(xv, wv, r, bias, gscale, live, lane % G::kLanes == 0,
+                                   qr + static_cast<int64_t>(v) * G::kCodeBytes,
+                                   sr + v / G::kLanes);
+            }
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_u32(&bars[stages + s]));
         } else {
 #pragma unroll 4
             for (int v = gl; v < nvec; v += gsize) {
                 const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
                 Vec<16> o;
-                scale<DT, 16>(o, xv, wv, r);
+                if constexpr (EPI == RMSNORM_EPI_BIAS)
+                    scale_bias<DT, 16>(o, xv, wv, r, bias);
+                else
+                    scale<DT, 16>(o, xv, wv, r);
                 st_stream<1>(yr + static_cast<int64_t>(v) * 16, o);
             }
             __syncwarp();
@@ -367,21 +407,30 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
     }
 }
 
-template <int DT, bool TS>
+template <int DT, bool TS, int EPI>
 cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(staged_rows_kernel<DT, TS>, p.grid, p.block_threads, p.smem_bytes, a,
-                         a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32,
-                         a.status, a.wait_limit_ns, a.flags);
+    return launch_kernel(staged_rows_kernel<DT, TS, false, EPI>, p.grid, p.block_threads,
+                         p.smem_bytes, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages,
+                         p.threads_per_row / 32, a.status, a.wait_limit_ns, a.flags, a.bias,
+                         static_cast<uint8_t *>(a.scales), a.gscale);
 }
 
-#define STAGED_ENTRY(DT, TS)                                                                   \
-    KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, 0, TS ? 3 : 0, &launch_staged<DT, TS>, \
-               reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS>)}
+#define STAGED_ENTRY(DT, TS, EPI)                                                              \
+    KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, 0, TS ? 3 : 0,                       \
+               &launch_staged<DT, TS, EPI>,                                                    \
+               reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS, false, EPI>), EPI}
 
-const KernelDesc kTable[] = {STAGED_ENTRY(RMSNORM_F32, false), STAGED_ENTRY(RMSNORM_BF16, false),
-                             STAGED_ENTRY(RMSNORM_F16, false), STAGED_ENTRY(RMSNORM_F32, true),
-                             STAGED_ENTRY(RMSNORM_BF16, true), STAGED_ENTRY(RMSNORM_F16, true)};
+// Plain and weight-bias outputs with both write-back modes; the block-scaled
+// outputs with register stores only.
+#define STAGED_SET(DT)                                                                         \
+    STAGED_ENTRY(DT, false, RMSNORM_EPI_PLAIN), STAGED_ENTRY(DT, true, RMSNORM_EPI_PLAIN),     \
+        STAGED_ENTRY(DT, false, RMSNORM_EPI_BIAS), STAGED_ENTRY(DT, true, RMSNORM_EPI_BIAS),   \
+        STAGED_ENTRY(DT, false, RMSNORM_EPI_MXFP8), STAGED_ENTRY(DT, false, RMSNORM_EPI_MXFP4), \
+        STAGED_ENTRY(DT, false, RMSNORM_EPI_NVFP4)
+
+const KernelDesc kTable[] = {STAGED_SET(RMSNORM_F32), STAGED_SET(RMSNORM_BF16),
+                             STAGED_SET(RMSNORM_F16)};
 
 // ---------------------------------------------------------------- no allocation
 
@@ -407,7 +456,7 @@ cudaError_t launch_staged_noalloc(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
     staged_rows_kernel<DT, false, true><<<p.grid, p.block_threads, p.smem_bytes, a.stream>>>(
         a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32, a.status,
-        a.wait_limit_ns, a.flags);
+        a.wait_limit_ns, a.flags, -0.0f, nullptr, 1.0f);
     return cudaGetLastError();
 }
 

@@ -343,16 +343,17 @@ def test_epilogue_kernel_sets():
         mx = [k for k in ks if k["dtype"] == dt and k["epilogue"] == rn.EPI_MXFP8]
         key = lambda k: (k["variant"], k["vec_bytes"], k["tpr"], k["nv"], k["block"],
                          k["min_blocks"], k["cache_policy"])
-        # every register / looped / generic body has a bias twin; the staged,
+        # every register / looped / staged / generic body has a bias twin; the
         # cluster and grid ones have none
         assert {key(k) for k in bias} == {key(k) for k in plain
-                                          if k["variant"] not in (rn.VARIANT_STAGED,
-                                                                  rn.VARIANT_CLUSTER,
+                                          if k["variant"] not in (rn.VARIANT_CLUSTER,
                                                                   rn.VARIANT_GRID)}
-        # block-scaled outputs: the register and looped bodies except the 4-lane group
-        want = {key(k) for k in plain if k["variant"] in (rn.VARIANT_WARP_PER_ROW,
-                                                          rn.VARIANT_CTA_PER_ROW)
-                and k["tpr"] != 4}
+        # block-scaled outputs: the register and looped bodies except the 4-lane
+        # group, and the staged ring with register stores
+        want = {key(k) for k in plain if (k["variant"] in (rn.VARIANT_WARP_PER_ROW,
+                                                           rn.VARIANT_CTA_PER_ROW)
+                                          and k["tpr"] != 4)
+                or (k["variant"] == rn.VARIANT_STAGED and k["cache_policy"] != 3)}
         assert {key(k) for k in mx} == want
         for epi in (rn.EPI_MXFP4, rn.EPI_NVFP4):
             assert {key(k) for k in ks if k["dtype"] == dt and k["epilogue"] == epi} == want
@@ -361,9 +362,9 @@ def test_epilogue_kernel_sets():
 @pytest.mark.parametrize("epi", [rn.EPI_BIAS, rn.EPI_MXFP8])
 def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
     """The epilogues take the same body as the plain output wherever that is
-    not the staged ring or the cluster split (MXFP8: nor the 1-32 KiB prefill
-    rows, where it takes its own shapes), and a kernel of their own
-    epilogue."""
+    not the cluster split or the grid variant (block-scaled outputs: nor the
+    1-32 KiB prefill rows, where they take their own shapes), and a kernel of
+    their own epilogue."""
     ks = rn.kernels()
     for rows in (1, 8, 100, 152, 4096, 65536):
         for hidden in (128, 512, 1024, 2048, 4096, 8192, 16384, 20480, 36864, 65536, 131072):
@@ -371,7 +372,6 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                 rc, p = plan_epi(rows, hidden, dt, epi)
                 assert rc == rn.OK, (rows, hidden, dt, rc)
                 assert ks[p.kernel_index]["epilogue"] == epi
-                assert p.variant != rn.VARIANT_STAGED
                 rc0, p0 = plan_epi(rows, hidden, dt, rn.EPI_PLAIN)
                 nvec = hidden * (4 if dt == rn.F32 else 2) // 16
                 if epi == rn.EPI_MXFP8 and rows > SMS and 64 < nvec <= 2048:
@@ -387,7 +387,7 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
-                if p0.variant not in (rn.VARIANT_STAGED, rn.VARIANT_CLUSTER):
+                if p0.variant not in (rn.VARIANT_CLUSTER, rn.VARIANT_GRID):
                     k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
                     strip = lambda k: {a: b for a, b in k.items() if a not in ("index", "epilogue")}
                     assert strip(k) == strip(k0)
@@ -406,8 +406,11 @@ def test_epilogue_argument_rules():
     rc, p = plan_epi(64, 4097, rn.BF16, rn.EPI_BIAS)
     assert rc == rn.OK and p.variant == rn.VARIANT_GENERIC
     assert rn.kernels()[p.kernel_index]["epilogue"] == rn.EPI_BIAS
-    # forced variants the epilogues do not have
-    assert plan_epi(64, 4096, rn.BF16, rn.EPI_BIAS, rn.VARIANT_STAGED)[0] == rn.ERR_VARIANT
+    # forced variants: the staged ring takes every output, the scalar body
+    # no block-scaled one
+    for epi in (rn.EPI_BIAS, rn.EPI_MXFP8, rn.EPI_NVFP4):
+        rc, p = plan_epi(64, 4096, rn.BF16, epi, rn.VARIANT_STAGED)
+        assert rc == rn.OK and rn.kernels()[p.kernel_index]["epilogue"] == epi
     assert plan_epi(64, 4096, rn.BF16, rn.EPI_MXFP8, rn.VARIANT_GENERIC)[0] == rn.ERR_VARIANT
     assert plan_epi(64, 4096, rn.BF16, 7)[0] == rn.ERR_INVALID_ARG
     # a plan naming another epilogue's kernel is refused

@@ -129,7 +129,7 @@ def test_bias_every_forced_variant():
     x, w = inputs.random_case(300, 4096, "bf16", seed=9)
     xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
     for v in (rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT,
-              rn.VARIANT_GENERIC):
+              rn.VARIANT_GENERIC, rn.VARIANT_STAGED):
         try:
             y = rn.rms_norm_bias(xd, wd, 2.0, 1e-6, variant=v)
         except rn.RmsnormError as e:
@@ -137,9 +137,10 @@ def test_bias_every_forced_variant():
             continue
         torch.cuda.synchronize()
         compare(from_device(y, "bf16"), x, w, 1e-6, "bf16", bias=2.0)
-    with pytest.raises(rn.RmsnormError) as e:
-        rn.rms_norm_bias(xd, wd, 2.0, 1e-6, variant=rn.VARIANT_STAGED)
-    assert e.value.status == rn.ERR_VARIANT
+    for v in (rn.VARIANT_CLUSTER, rn.VARIANT_GRID):   # plain output only
+        with pytest.raises(rn.RmsnormError) as e:
+            rn.rms_norm_bias(xd, wd, 2.0, 1e-6, variant=v)
+        assert e.value.status == rn.ERR_VARIANT
 
 
 def test_mx_special_blocks():
@@ -174,7 +175,8 @@ def test_mx_every_forced_variant_and_guard_bytes():
     x, w = inputs.random_case(rows, hidden, "bf16", seed=12)
     xd, wd = to_device(x, "bf16"), to_device(w, "bf16")
     pad = 4096
-    for v in (rn.VARIANT_AUTO, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT):
+    for v in (rn.VARIANT_AUTO, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT,
+              rn.VARIANT_STAGED):
         qb = torch.full((rows * hidden + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
         sb = torch.full((rows * hidden // 32 + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
         q = qb[pad:pad + rows * hidden].view(rows, hidden)
@@ -184,7 +186,7 @@ def test_mx_every_forced_variant_and_guard_bytes():
         for b in (qb, sb):
             assert (b[:pad] == 0x5A).all() and (b[-pad:] == 0x5A).all()
         compare_mx(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.0, 1e-6, "bf16")
-    for v, st in ((rn.VARIANT_STAGED, rn.ERR_VARIANT), (rn.VARIANT_GENERIC, rn.ERR_VARIANT)):
+    for v, st in ((rn.VARIANT_CLUSTER, rn.ERR_VARIANT), (rn.VARIANT_GENERIC, rn.ERR_VARIANT)):
         with pytest.raises(rn.RmsnormError) as e:
             rn.rms_norm_mxfp8(xd, wd, 1e-6, variant=v)
         assert e.value.status == st
@@ -306,3 +308,29 @@ def test_fp4_argument_errors():
     assert lib.rmsnorm_fwd_nvfp4(*P, 8, 4096, 1.0, 0.0, 1e-6, rn.BF16, None) == rn.OK
     torch.cuda.synchronize()
     compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.0, 1e-6, "bf16", "nvfp4", 1.0)
+
+
+
+@pytest.mark.parametrize("epi", ["bias", "mxfp8", "mxfp4", "nvfp4"])
+@pytest.mark.parametrize("rows,hidden,dtype", [(2048, 20480, "bf16"), (1024, 32768, "f16"),
+                                               (600, 9000, "f32"), (160, 36864, "bf16")])
+def test_epilogues_on_the_staged_ring(epi, rows, hidden, dtype):
+    """32-72 KiB rows: the epilogues run on the shared-memory ring."""
+    x, w = inputs.random_case(rows, hidden, dtype, seed=hidden + 7)
+    idx = sample_rows(rows, 48, seed=rows)
+    xd, wd = to_device(x, dtype), to_device(w, dtype)
+    if epi == "bias":
+        y = rn.rms_norm_bias(xd, wd, 0.5, 1e-6)
+        torch.cuda.synchronize()
+        if hidden * (4 if dtype == "f32" else 2) > 32768:
+            assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
+        compare(from_device(y, dtype), x, w, 1e-6, dtype, rows_idx=idx, bias=0.5)
+        return
+    if hidden % 32:
+        return
+    q, s = rn.rms_norm_quant(xd, wd, 1e-6, epi, weight_bias=0.5, global_scale=0.004)
+    torch.cuda.synchronize()
+    if hidden * (4 if dtype == "f32" else 2) > 32768:
+        assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
+    compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.5, 1e-6, dtype, epi, 0.004,
+                  rows_idx=idx)

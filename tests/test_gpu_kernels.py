@@ -45,6 +45,10 @@ def plans_for(k, rows, sms, optin):
         h = hidden // block * block
         if h == 0:
             h = block
+        if pd["variant"] == rn.VARIANT_STAGED:   # the ring's layout follows the row length
+            pd = dict(pd, smem_bytes=layout_bytes(h * ES[k["dtype"]], pd["stages"]))
+            if pd["smem_bytes"] > optin:
+                continue
         if pd["vecs_per_thread"] and h // (k["vec_bytes"] // ES[k["dtype"]]) > \
                 pd["threads_per_row"] * pd["vecs_per_thread"]:
             continue
