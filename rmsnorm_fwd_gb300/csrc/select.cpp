@@ -648,8 +648,10 @@ wide:
     // 16..32 KiB rows: the register bodies on a persistent grid.
     if (nvec <= 2048 && plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    // 32..72 KiB rows: the shared-memory ring.
-    if (nvec <= 4608 && plan_staged_wide(s, out) == RMSNORM_OK)
+    // 32..72 KiB rows: the shared-memory ring (plain and weight-bias outputs;
+    // the block-scaled ones starve its 8-16 consumer warps of issue slots --
+    // 2.8-3.0 TB/s against 4.3-4.9 on the looped body below -- and stay there).
+    if (nvec <= 4608 && s.epi <= RMSNORM_EPI_BIAS && plan_staged_wide(s, out) == RMSNORM_OK)
         return RMSNORM_OK;
     // Longer rows: the looped body, one block per row.
     if (plan_cta_exact(s, 16, 0, 512, 2, 1, 0, nvec <= 5120 ? 256 : 512, INT_MAX,

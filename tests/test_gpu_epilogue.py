@@ -315,7 +315,8 @@ def test_fp4_argument_errors():
 @pytest.mark.parametrize("rows,hidden,dtype", [(2048, 20480, "bf16"), (1024, 32768, "f16"),
                                                (600, 9000, "f32"), (160, 36864, "bf16")])
 def test_epilogues_on_the_staged_ring(epi, rows, hidden, dtype):
-    """32-72 KiB rows: the epilogues run on the shared-memory ring."""
+    """32-72 KiB rows: the weight-bias output runs on the shared-memory ring;
+    the block-scaled outputs on the looped body, and on the ring when forced."""
     x, w = inputs.random_case(rows, hidden, dtype, seed=hidden + 7)
     idx = sample_rows(rows, 48, seed=rows)
     xd, wd = to_device(x, dtype), to_device(w, dtype)
@@ -328,9 +329,10 @@ def test_epilogues_on_the_staged_ring(epi, rows, hidden, dtype):
         return
     if hidden % 32:
         return
-    q, s = rn.rms_norm_quant(xd, wd, 1e-6, epi, weight_bias=0.5, global_scale=0.004)
-    torch.cuda.synchronize()
-    if hidden * (4 if dtype == "f32" else 2) > 32768:
-        assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
-    compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.5, 1e-6, dtype, epi, 0.004,
-                  rows_idx=idx)
+    # the automatic plan (the looped body) and the ring, forced
+    for v in (rn.VARIANT_AUTO, rn.VARIANT_STAGED):
+        q, s = rn.rms_norm_quant(xd, wd, 1e-6, epi, weight_bias=0.5, global_scale=0.004,
+                                 variant=v)
+        torch.cuda.synchronize()
+        compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, 0.5, 1e-6, dtype, epi, 0.004,
+                      rows_idx=idx)
