@@ -29,7 +29,7 @@ struct LaunchArgs {
     uint32_t flags;         // kFlagWithholdCopies: failure-detection test only
     cudaStream_t stream;
     bool pdl = false;       // launch with a programmatic dependency on the stream's last kernel
-    float bias = -0.0f;     // weight offset (BIAS / MXFP8 epilogues); -0 adds nothing
+    float bias = -0.0f;     // weight offset (every epilogue but PLAIN); -0 adds nothing
     void *scales = nullptr; // block-scaled epilogues: the scales; y holds the codes
     float gscale = 1.0f;    // NVFP4: the per-tensor scale
     void *scratch = nullptr; // grid variant: counters + partial sums (stream-ordered, per call)

@@ -23,6 +23,12 @@
 // least MINB resident blocks per SM (a register cap) and, with more than one
 // vector per thread, loads the weight after the reduction instead of holding
 // it in registers across rows.
+//
+// EPI selects what the kernels write (rmsnorm_epilogue_t): the plain output,
+// the weight plus a bias, or a block-scaled output (MXFP8 / MXFP4 / NVFP4
+// codes and scales, q_store in device_common.cuh).  Only the plain
+// instantiations feed the plain entry points; the others are separate
+// template instances with their own table entries.
 #pragma once
 
 #include "internal.h"
@@ -420,8 +426,8 @@ constexpr int kWarpBlock = 256;
 // MINB caps registers so at least MINB blocks of MAXT threads fit on an SM
 // (65536 registers): MAXT x MINB = 2048 -> 32 registers per thread.  The
 // selector (select.cpp) names these entries by their parameters.  The
-// 4-lane warp body is left out of the MXFP8 set (a 32-element f32 block
-// spans 8 lanes).
+// 4-lane warp body is left out of the block-scaled sets (a 32-element f32
+// block spans 8 lanes).
 #define ROWREG_SET_WIDE(DT, EPI)                                                               \
     WARP_ENTRY(DT, 16, 8, 1, 0, 0, EPI), WARP_ENTRY(DT, 16, 8, 2, 0, 0, EPI),                  \
         WARP_ENTRY(DT, 16, 16, 1, 0, 0, EPI), WARP_ENTRY(DT, 16, 16, 2, 0, 0, EPI),            \
@@ -434,7 +440,7 @@ constexpr int kWarpBlock = 256;
         CTA_ENTRY(DT, 32, 4, 512, 0, 1, EPI), CTA_ENTRY(DT, 16, 2, 256, 8, 1, EPI),            \
         CTA_ENTRY(DT, 16, 3, 512, 3, 1, EPI), CTA_ENTRY(DT, 16, 4, 256, 6, 1, EPI),            \
         CTA_ENTRY(DT, 16, 4, 512, 2, 1, EPI), CTA_ENTRY(DT, 16, 8, 512, 0, 1, EPI),            \
-        CTAF_ENTRY(DT, 16, 512, 1, 0, 0, EPI), LOOP_ENTRY(DT, 16, 512, 2, 1, EPI),         \
+        CTAF_ENTRY(DT, 16, 512, 1, 0, 0, EPI), LOOP_ENTRY(DT, 16, 512, 2, 1, EPI),             \
         CTA_ENTRY(DT, 32, 2, 256, 6, 1, EPI)
 
 #define ROWREG_SET(DT, EPI) WARP_ENTRY(DT, 16, 4, 1, 0, 0, EPI), ROWREG_SET_WIDE(DT, EPI)

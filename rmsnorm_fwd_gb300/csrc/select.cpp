@@ -9,10 +9,14 @@
 // specialization": pick the per-thread vector first (16 bytes: 8 x bf16/f16,
 // 4 x f32; 32 bytes on Blackwell), derive how many threads a row needs, and
 // size the grid against the SM count: when there are fewer rows than SMs
-// (decode) give every row its own block on its own SM; when there are many
+// (decode) give every row its own block on its own SM -- or, for rows too
+// long for one SM, several SMs through a thread-block cluster or a grid
+// barrier (same page, section "Grid synchronization"); when there are many
 // (prefill) use enough warps per SM to keep HBM busy.  The SM count is read
 // from the device at context creation, not compiled in (same page, section
-// "Blackwell support").
+// "Blackwell support").  The epilogue (rmsnorm_epilogue_t) narrows the
+// choice to the bodies compiled for it and, for the block-scaled outputs,
+// has launch shapes of its own.
 #include <algorithm>
 #include <climits>
 #include <cstdint>
