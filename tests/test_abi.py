@@ -539,3 +539,10 @@ def test_grid_plans():
     assert plan(65, 1 << 20, rn.BF16, rn.VARIANT_GRID)[0] == rn.ERR_VARIANT
     assert plan_epi(1, 1 << 20, rn.BF16, rn.EPI_BIAS, rn.VARIANT_GRID)[0] == rn.ERR_VARIANT
     assert plan(1, 1 << 20, rn.BF16, rn.VARIANT_GRID, xoff=2)[0] == rn.ERR_MISALIGNED
+
+
+
+def test_maximum_row_length_rule():
+    assert plan(1, 1 << 26, rn.BF16)[0] == rn.OK
+    assert plan(1, (1 << 26) + 8, rn.BF16)[0] == rn.ERR_INVALID_ARG
+    assert plan(1, 1 << 26, rn.BF16)[1].variant == rn.VARIANT_GRID

@@ -264,3 +264,18 @@ def test_huge_decode_rows_grid(dtype, rows, hidden):
     rn.rms_norm(xd, to_device(w, dtype), 1e-6, out=xd, variant=rn.VARIANT_GRID)
     torch.cuda.synchronize()
     compare(from_device(xd, dtype), x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 8, seed=rows))
+
+
+
+def test_maximum_row_length():
+    """The longest row the library takes (2^26 elements, a 128 MiB bf16 row):
+    the grid variant, and the scalar body forced; one element more is refused."""
+    hidden = 1 << 26
+    x, w = inputs.random_case(1, hidden, "bf16", seed=26)
+    for v in (rn.VARIANT_AUTO, rn.VARIANT_GENERIC):
+        y = run(x, w, 1e-6, "bf16", variant=v)
+        compare(y, x, w, 1e-6, "bf16")
+    sms, optin = rn.rmsnorm_device_limits()
+    base = 1 << 30
+    rc, _ = rn.rmsnorm_plan_status(base, 3 * base, 5 * base, 1, hidden + 8, rn.BF16, sms, optin)
+    assert rc == rn.ERR_INVALID_ARG
