@@ -345,8 +345,8 @@ __device__ inline void st_codes(void *p, const uint32_t (&w)[(NB + 3) / 4])
 }
 
 // Two fp32 lanes in one 64-bit register for the sm_100-family packed
-// arithmetic (add / mul / fma .rn.f32x2: one instruction for two IEEE
-// operations, each rounded exactly as its scalar form).
+// arithmetic (add / mul .rn.f32x2: one instruction for two IEEE operations,
+// each rounded exactly as its scalar form).
 __device__ inline uint64_t f2(float a, float b)
 {
     uint64_t r;
@@ -367,12 +367,6 @@ __device__ inline uint64_t mul2(uint64_t a, uint64_t b)
 {
     uint64_t r;
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-    return r;
-}
-__device__ inline uint64_t fma2(uint64_t a, uint64_t b, uint64_t c)
-{
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
     return r;
 }
 
