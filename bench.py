@@ -2,7 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
-                    [--op rmsnorm|qk_norm|bias|mxfp8|mxfp4|nvfp4]
+                    [--op rmsnorm|qk_norm|bias|mxfp8|mxfp4|nvfp4|latency]
 
 A step is one RMSNorm forward over one batch: the headline workload is the
 prefill-shaped batch, 16384 rows x 4096 hidden, bf16 in/out, fp32
@@ -640,6 +640,98 @@ def run_epi(args, world, rank, local):
     return 0
 
 
+def run_latency(args, world, rank, local):
+    """--op latency: per-call time of the automatic plan on one workload --
+    back-to-back launches (one event pair over K), the same K launches
+    replayed from a CUDA graph, and cold calls (L2 flushed by writing a
+    buffer of twice its size before each, one event pair around each call;
+    median) -- with the GB/s each implies."""
+    import torch
+
+    import rmsnorm_fwd_gb300 as rn
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = inputs.WORKLOADS[args.workload]
+    x_np, w_np = inputs.make_inputs(wl, seed=rank)
+    x = to_torch(x_np, wl.dtype, torch).to(device)
+    w = to_torch(w_np, wl.dtype, torch).to(device)
+    y = torch.empty_like(x)
+    rn.ensure_context(local)
+    stream = torch.cuda.current_stream(device)
+    sptr = stream.cuda_stream
+    dt = rn.DTYPE_CODES[wl.dtype]
+    plan = rn.Plan()
+    rn.rmsnorm_fwd_ex(x.data_ptr(), w.data_ptr(), y.data_ptr(), wl.rows, wl.hidden, wl.eps, dt,
+                      sptr, rn.VARIANT_AUTO, plan)
+    fwd = rn._load().rmsnorm_fwd_ex
+    pref = rn.ctypes.byref(plan)
+    args_ = (x.data_ptr(), w.data_ptr(), y.data_ptr(), wl.rows, wl.hidden, wl.eps, dt)
+
+    def call(s):
+        rc = fwd(*args_, s, 0, pref)
+        if rc != rn.OK:
+            raise rn.RmsnormError(rc, "rmsnorm_fwd_ex")
+
+    K = args.steps
+    for _ in range(max(3, args.warmup)):
+        call(sptr)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        call(sptr)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    warm_us = e0.elapsed_time(e1) / K * 1e3
+
+    cs = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=cs):
+        for _ in range(K):
+            call(cs.cuda_stream)
+    g.replay()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    graph_us = e0.elapsed_time(e1) / K * 1e3
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
+    cold = []
+    for i in range(min(K, 200)):
+        flush.fill_(float(i))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        call(sptr)
+        b.record(stream)
+        b.synchronize()
+        cold.append(a.elapsed_time(b) * 1e3)
+    cold_us = statistics.median(cold)
+    nbytes = wl.bytes_per_call
+
+    def gbs(us):
+        return round(nbytes / (us * 1e-6) / 1e9, 2)
+
+    line = {
+        "metric": "RMSNorm per-call time (us) and GB/s", "value": round(graph_us, 3),
+        "unit": "us per call (graph-replayed)", "n_gpus": world, "steps": K,
+        "warmup": max(3, args.warmup), "higher_is_better": False, "data": "synthetic",
+        "dtype": "f32", "config": {"workload": wl.name, "rows": wl.rows, "hidden": wl.hidden,
+                                   "io_dtype": wl.dtype,
+                                   "variant": rn.VARIANT_NAMES[plan.variant],
+                                   "plan": plan.as_dict()},
+        "back_to_back_us": round(warm_us, 3), "back_to_back_GBps": gbs(warm_us),
+        "graph_us": round(graph_us, 3), "graph_GBps": gbs(graph_us),
+        "cold_median_us": round(cold_us, 3), "cold_GBps": gbs(cold_us),
+        "cold_basis": "L2 flushed (2 x L2 written) before each call; one event pair per call",
+        "gpu_launches": K, "device_status": rn.rmsnorm_get_device_status(),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -650,8 +742,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-budget-s", type=float, default=60.0)
-    ap.add_argument("--op", choices=["rmsnorm", "qk_norm", "bias", "mxfp8", "mxfp4", "nvfp4"],
-                    default="rmsnorm")
+    ap.add_argument("--op", choices=["rmsnorm", "qk_norm", "bias", "mxfp8", "mxfp4", "nvfp4",
+                                     "latency"], default="rmsnorm")
     ap.add_argument("--qk-workload", default="qk_bf16_16384tok_32q8k_128",
                     choices=sorted(inputs.QK_WORKLOADS))
     args = ap.parse_args(argv)
@@ -660,6 +752,8 @@ def main(argv=None):
         return run_qk(args, world, rank, local)
     if args.op in ("bias", "mxfp8", "mxfp4", "nvfp4"):
         return run_epi(args, world, rank, local)
+    if args.op == "latency":
+        return run_latency(args, world, rank, local)
     if args.impl == "reference":
         return run_reference(args, world, rank)
     return run_ours(args, world, rank, local)
