@@ -334,28 +334,28 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                                      yr + static_cast<int64_t>(v) * OB, sr + v / LPB);
                 }
             }
-            continue;
-        }
-        for (int v0 = t; v0 < nvec; v0 += U * tpr) {
-            Vec<VB> xv[U], wv[U];
+        } else {
+            for (int v0 = t; v0 < nvec; v0 += U * tpr) {
+                Vec<VB> xv[U], wv[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * tpr;
-                if (v < nvec) {
-                    ld_stream<0>(xv[u], xr + static_cast<int64_t>(v) * VB);
-                    ld_weight(wv[u], wb + static_cast<int64_t>(v) * VB);
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + u * tpr;
+                    if (v < nvec) {
+                        ld_stream<0>(xv[u], xr + static_cast<int64_t>(v) * VB);
+                        ld_weight(wv[u], wb + static_cast<int64_t>(v) * VB);
+                    }
                 }
-            }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int v = v0 + u * tpr;
-                if (v < nvec) {
-                    Vec<VB> o;
-                    if constexpr (EPI == RMSNORM_EPI_BIAS)
-                        scale_bias<DT, VB>(o, xv[u], wv[u], r, bias);
-                    else
-                        scale<DT, VB>(o, xv[u], wv[u], r);
-                    st_stream<CP>(yr + static_cast<int64_t>(v) * VB, o);
+                for (int u = 0; u < U; ++u) {
+                    const int v = v0 + u * tpr;
+                    if (v < nvec) {
+                        Vec<VB> o;
+                        if constexpr (EPI == RMSNORM_EPI_BIAS)
+                            scale_bias<DT, VB>(o, xv[u], wv[u], r, bias);
+                        else
+                            scale<DT, VB>(o, xv[u], wv[u], r);
+                        st_stream<CP>(yr + static_cast<int64_t>(v) * VB, o);
+                    }
                 }
             }
         }
