@@ -16,17 +16,24 @@
 namespace rmsnorm {
 namespace {
 
+// out = (x * r) * (w + bias), two elements per packed fp32x2 instruction
+// (each result rounded as its scalar form), rounded to the element type.
 template <int DT>
-__device__ inline void scale_bias(Vec<16> &out, const Vec<16> &xv, const Vec<16> &wv, float r,
-                                  float bias)
+__device__ inline void scale_bias2(Vec<16> &out, const Vec<16> &xv, const Vec<16> &wv, float r,
+                                   float bias)
 {
+    const uint64_t r2 = f2(r, r), b2 = f2(bias, bias);
+    float f[8];
 #pragma unroll
-    for (int k = 0; k < Vec<16>::kWords; ++k) {
-        float xa, xb = 0.f, wa, wb = 0.f;
-        Elem<DT>::widen(xv.w[k], xa, xb);
-        Elem<DT>::widen(wv.w[k], wa, wb);
-        out.w[k] = Elem<DT>::narrow((xa * r) * (wa + bias), (xb * r) * (wb + bias));
+    for (int p = 0; p < 8 / Elem<DT>::kSize; ++p) {
+        const uint64_t v = mul2(mul2(widen_pair<DT, 16>(xv, p), r2),
+                                add2(widen_pair<DT, 16>(wv, p), b2));
+        f2split(v, f[2 * p], f[2 * p + 1]);
     }
+#pragma unroll
+    for (int k = 0; k < Vec<16>::kWords; ++k)
+        out.w[k] = Elem<DT>::kPerWord == 2 ? Elem<DT>::narrow(f[2 * k], f[2 * k + 1])
+                                           : Elem<DT>::narrow(f[k], 0.f);
 }
 
 __device__ inline void vzero16(Vec<16> &v)
@@ -103,7 +110,7 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < NV; ++j)
-                s = sumsq<DT, 16>(xv[r][j], s);
+                s = sumsq_mixed<DT, 16>(xv[r][j], s);
             s = group_allreduce<TPR>(s);
             const float rf = row_factor(s, n, eps);
 #pragma unroll
@@ -113,7 +120,7 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
             for (int j = 0; j < NV; ++j) {
                 if (active[r] && t + j * TPR < nvec) {
                     Vec<16> o;
-                    scale_bias<DT>(o, xv[r][j], wv[r][j], rf, bias);
+                    scale_bias2<DT>(o, xv[r][j], wv[r][j], rf, bias);
                     st_stream<0>(ht[r] + j * TPR * 16, o);
                 }
             }
