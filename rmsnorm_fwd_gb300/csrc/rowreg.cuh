@@ -203,7 +203,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
         float s = 0.f;
 #pragma unroll
         for (int k = 0; k < NV; ++k)
-            s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
+            s = sumsq_mixed<DT, VB>(xv[k], s);
         s = group_allreduce<32>(s);
         if (TPRC != 32) {
             if (lane == 0)
@@ -241,7 +241,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
                     scale_bias<DT, VB>(o, xv[k], wk, r, bias);
                 else
-                    scale<DT, VB>(o, xv[k], wk, r);
+                    scale_packed<DT, VB>(o, xv[k], wk, r);
                 st_stream<CP>(yr + k * stride, o);
             }
         }
