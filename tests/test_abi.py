@@ -546,3 +546,22 @@ def test_maximum_row_length_rule():
     assert plan(1, 1 << 26, rn.BF16)[0] == rn.OK
     assert plan(1, (1 << 26) + 8, rn.BF16)[0] == rn.ERR_INVALID_ARG
     assert plan(1, 1 << 26, rn.BF16)[1].variant == rn.VARIANT_GRID
+
+
+@pytest.mark.parametrize("epi", ["plain", "bias", "mxfp8", "mxfp4", "nvfp4"])
+def test_tuning_candidates_are_valid_plans(epi):
+    """The plans the tuning sweep would time are well formed: the library's own
+    plan check (host only) takes them, or refuses them only because the shape
+    does not fit the body (the sweep skips those), for decode, mid, wide and
+    very long rows."""
+    from rmsnorm_fwd_gb300 import tune
+    code = {"plain": 0, "bias": 1, "mxfp8": 2, "mxfp4": 3, "nvfp4": 4}[epi]
+    n = 0
+    for rows, hidden in ((1, 4096), (32, 65536), (8192, 1024), (16384, 4096), (4096, 24576),
+                         (64, 262144), (1, 1 << 20)):
+        for p in tune.candidates(rows, hidden, "bf16", SMS, OPTIN, code):
+            rc = rn.rmsnorm_validate_plan_epilogue(rn.Plan(**p), A, 3 * A, 5 * A, rows, hidden,
+                                                   rn.BF16, code, SMS, OPTIN)
+            assert rc in (rn.OK, rn.ERR_VARIANT), (rows, hidden, p, rc)
+            n += rc == rn.OK
+    assert n > 50
