@@ -387,8 +387,10 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
-                if epi == rn.EPI_MXFP8 and p0.variant == rn.VARIANT_STAGED:
-                    assert p.variant != rn.VARIANT_STAGED   # the looped body instead
+                if epi == rn.EPI_MXFP8 and rows > SMS and nvec > 2048:
+                    # rows above 32 KiB: the looped body (not the ring, not the
+                    # plain output's 32-byte blocks)
+                    assert p.variant != rn.VARIANT_STAGED and p.vecs_per_thread == 0
                     continue
                 if p0.variant not in (rn.VARIANT_CLUSTER, rn.VARIANT_GRID):
                     k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
@@ -565,3 +567,13 @@ def test_tuning_candidates_are_valid_plans(epi):
             assert rc in (rn.OK, rn.ERR_VARIANT), (rows, hidden, p, rc)
             n += rc == rn.OK
     assert n > 50
+
+
+
+def test_prefill_rows_of_16_to_24_and_32_to_40_kib_take_32_byte_blocks():
+    for hidden in (10240, 12288, 18432, 20480):
+        rc, p = plan(16384, hidden, rn.BF16)
+        assert rc == rn.OK and p.variant == rn.VARIANT_CTA_PER_ROW and p.vec_bytes == 32
+        assert p.vecs_per_thread == 4 and p.grid == 16384, (hidden, p.as_dict())
+    assert plan(16384, 16384, rn.BF16)[1].variant == rn.VARIANT_PERSISTENT   # 32 KiB rows
+    assert plan(16384, 24576, rn.BF16)[1].variant == rn.VARIANT_STAGED       # 48 KiB rows

@@ -279,3 +279,15 @@ def test_maximum_row_length():
     base = 1 << 30
     rc, _ = rn.rmsnorm_plan_status(base, 3 * base, 5 * base, 1, hidden + 8, rn.BF16, sms, optin)
     assert rc == rn.ERR_INVALID_ARG
+
+
+
+@pytest.mark.parametrize("hidden,dtype", [(10240, "bf16"), (12288, "f16"), (20480, "bf16"),
+                                          (5120, "f32"), (10000, "bf16")])
+def test_prefill_20_to_40_kib_rows(hidden, dtype):
+    """Prefill rows of 20-40 KiB (32-byte vectors, one block per row), in the
+    automatic plan, sampled rows against the oracle."""
+    rows = 3000
+    x, w = inputs.random_case(rows, hidden, dtype, seed=hidden)
+    y = run(x, w, 1e-6, dtype)
+    compare(y, x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 64, seed=hidden))
