@@ -652,7 +652,10 @@ wide:
     // 16-24 KiB and 32-40 KiB rows: 32-byte vectors, 4 per thread, one block
     // per row (on the final sweep 2.6-6.8 % faster there than the persistent
     // and staged bodies below; at 32 KiB the persistent one stays ahead).
-    if (s.epi <= RMSNORM_EPI_BIAS && s.a32 &&
+    // Plain output only: the weight-offset build of this body needs 107
+    // registers, which leaves one 320-thread block per SM instead of two
+    // (4.5 against 6.5 TB/s on 40 KiB rows).
+    if (s.epi == RMSNORM_EPI_PLAIN && s.a32 &&
         ((s.row_bytes > 16384 && s.row_bytes <= 24576) ||
          (s.row_bytes > 32768 && s.row_bytes <= 40960)) &&
         plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), INT_MAX,

@@ -392,6 +392,14 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                     # plain output's 32-byte blocks)
                     assert p.variant != rn.VARIANT_STAGED and p.vecs_per_thread == 0
                     continue
+                row_bytes = nvec * 16
+                if epi == rn.EPI_BIAS and rows > SMS and \
+                        (16384 < row_bytes <= 24576 or 32768 < row_bytes <= 40960):
+                    # the plain output's 32-byte four-vector blocks are not
+                    # taken with the weight offset (one block per SM there)
+                    assert p0.vec_bytes == 32 and p0.vecs_per_thread == 4
+                    assert not (p.vec_bytes == 32 and p.vecs_per_thread == 4)
+                    continue
                 if p0.variant not in (rn.VARIANT_CLUSTER, rn.VARIANT_GRID):
                     k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
                     strip = lambda k: {a: b for a, b in k.items() if a not in ("index", "epilogue")}
@@ -577,3 +585,8 @@ def test_prefill_rows_of_16_to_24_and_32_to_40_kib_take_32_byte_blocks():
         assert p.vecs_per_thread == 4 and p.grid == 16384, (hidden, p.as_dict())
     assert plan(16384, 16384, rn.BF16)[1].variant == rn.VARIANT_PERSISTENT   # 32 KiB rows
     assert plan(16384, 24576, rn.BF16)[1].variant == rn.VARIANT_STAGED       # 48 KiB rows
+    # the weight-offset output keeps the other bodies (its build of this one
+    # holds one block per SM, not two)
+    rc, p = rn.rmsnorm_plan_epilogue_status(A, 3 * A, 5 * A, 16384, 20480, rn.BF16,
+                                            rn.EPI_BIAS, SMS, OPTIN)
+    assert rc == rn.OK and p.variant == rn.VARIANT_STAGED
