@@ -3,6 +3,7 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME] [--e2e-steps E] [--cpu-seconds S]
                     [--op rmsnorm|qk_norm|bias|mxfp8|mxfp4|nvfp4|latency]
+                    [--weight-bias B]
 
 A step is one RMSNorm forward over one batch: the headline workload is the
 prefill-shaped batch, 16384 rows x 4096 hidden, bf16 in/out, fp32
@@ -531,10 +532,11 @@ def run_qk(args, world, rank, local):
 
 
 def run_epi(args, world, rank, local):
-    """--op bias | mxfp8: the row norm with the weight offset, or with the
-    fused MXFP8 output (E4M3 codes + one E8M0 scale per 32 elements), on the
-    chosen workload; the plain kernel on the same inputs is timed beside it
-    for context."""
+    """--op bias | mxfp8 | mxfp4 | nvfp4: the row norm with the weight offset
+    (1.0 unless --weight-bias), or with a fused block-scaled output (codes and
+    one scale per 32 or 16 elements; no weight offset unless --weight-bias),
+    on the chosen workload; the plain kernel on the same inputs is timed
+    beside it for context."""
     import torch
 
     import rmsnorm_fwd_gb300 as rn
@@ -564,7 +566,10 @@ def run_epi(args, world, rank, local):
     stream = torch.cuda.current_stream(device)
     sptr = stream.cuda_stream
     dt = rn.DTYPE_CODES[wl.dtype]
-    bias = 1.0
+    # the weight offset: 1.0 for --op bias; none (-0.0, the identity) for the
+    # block-scaled outputs unless --weight-bias says otherwise
+    bias = args.weight_bias if args.weight_bias is not None else \
+        (1.0 if epi == rn.EPI_BIAS else -0.0)
     gscale = 1.0 / (448 * 6) * 4.0  # a per-tensor NVFP4 scale for values of magnitude ~4
     plan = rn.Plan()
     rn.rmsnorm_fwd_epilogue_ex(xs[0].data_ptr(), w.data_ptr(), ys[0].data_ptr(),
@@ -746,6 +751,9 @@ def main(argv=None):
                                      "latency"], default="rmsnorm")
     ap.add_argument("--qk-workload", default="qk_bf16_16384tok_32q8k_128",
                     choices=sorted(inputs.QK_WORKLOADS))
+    ap.add_argument("--weight-bias", type=float, default=None,
+                    help="weight offset for --op bias|mxfp8|mxfp4|nvfp4 (default 1.0 for bias, "
+                         "-0.0 = no offset for the block-scaled outputs)")
     args = ap.parse_args(argv)
     world, rank, local = dist_env()
     if args.op == "qk_norm":

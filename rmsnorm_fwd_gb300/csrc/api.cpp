@@ -252,6 +252,7 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     a.bias = bias;
     a.scales = scales;
     a.gscale = gscale;
+    a.xw = quant_exact_products(dtype, epi, bias, gscale);
     if (log_enabled())
         std::fprintf(stderr,
                      "rmsnorm: rows=%lld hidden=%lld dtype=%d epi=%d -> variant=%d vec=%d tpr=%d "
@@ -330,9 +331,13 @@ int rmsnorm_create(void)
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
     for (int i = 0; i < n; ++i) {
-        if (t[i].variant == RMSNORM_VARIANT_STAGED &&
-            cudaFuncSetAttribute(t[i].func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
-                cudaSuccess) {
+        if (t[i].variant != RMSNORM_VARIANT_STAGED)
+            continue;
+        if (cudaFuncSetAttribute(t[i].func, cudaFuncAttributeMaxDynamicSharedMemorySize, optin) !=
+                cudaSuccess ||
+            (t[i].func_xw != nullptr &&
+             cudaFuncSetAttribute(t[i].func_xw, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  optin) != cudaSuccess)) {
             cudaFree(status);
             return RMSNORM_ERR_CUDA;
         }

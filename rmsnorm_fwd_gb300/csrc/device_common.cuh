@@ -458,59 +458,173 @@ __device__ inline float rcp_approx(float a)
     return r;
 }
 
-// One vector of a block-scaled epilogue (QFmt above).
-//
-// v = (x * r) * (w + bias) in fp32, two elements per packed instruction.
-// The block maximum of |v| is a NaN-propagating max (a NaN or an Inf in the
-// block must reach the scale; fmaxf would drop a NaN), reduced over the
-// block's kLanes lanes with butterfly shuffles.  MX formats: the biased
-// exponent e of the maximum gives the shared exponent floor(log2 max) - kEmax
-// = e - 127 - kEmax, clamped at -127: E8M0 code max(e - kEmax, 0), or 0xFF
-// when e = 255 (Inf / NaN); scaling by 2^(127 - code) is exact.  NVFP4: the
-// scale code is E4M3(max * (1 / (6 g))) and the values are multiplied by
-// 1 / (value(code) * g) (by 0 when the scale is 0), both reciprocals from
-// rcp.approx.  The conversions round
-// each scaled value to the element format.
-//
-// Every lane of the warp must call this (the shuffles span the full warp);
-// `live` says whether this lane's vector is part of the row.  The lane
-// holding the first vector of a block (`leader`) stores the scale byte.
-template <int DT, int VB, int Q>
-__device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, float r, float bias,
-                               float g, bool live, bool leader, void *q, uint8_t *scale)
+// 1 / a by the hardware reciprocal with subnormal inputs and results
+// flushed to zero: for an `a` and a 1 / a that are both normal floats.
+__device__ inline float rcp_approx_ftz(float a)
 {
-    using G = QGeo<DT, VB, Q>;
-    constexpr int NE = G::kElems;
-    constexpr int LPB = G::kLanes;
-    constexpr int P = NE / 2;
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+
+// The exact products x * w of element pair p of two 16-bit vectors, in fp32:
+// the mixed-precision fma with a -0 addend (the product of two bf16 or two
+// f16 values has at most 16 or 22 significant bits, so it is exact in fp32
+// unless it leaves fp32's normal range, and x * w + (-0) is x * w with its
+// sign, zeros included).
+template <int DT>
+__device__ inline void exact_products(uint32_t xw, uint32_t ww, float &a, float &b)
+{
+    static_assert(DT != RMSNORM_F32, "16-bit elements only");
+    if constexpr (DT == RMSNORM_BF16)
+        asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.bf16 %0, xl, wl, 0f80000000;\n\tfma.rn.f32.bf16 %1, xh, wh, 0f80000000;\n\t}"
+            : "=f"(a), "=f"(b)
+            : "r"(xw), "r"(ww));
+    else
+        asm("{\n\t.reg .b16 xl, xh, wl, wh;\n\tmov.b32 {xl, xh}, %2;\n\tmov.b32 {wl, wh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, xl, wl, 0f80000000;\n\tfma.rn.f32.f16 %1, xh, wh, 0f80000000;\n\t}"
+            : "=f"(a), "=f"(b)
+            : "r"(xw), "r"(ww));
+}
+
+// Per-launch constants of a block-scaled epilogue.
+struct QParams {
+    float bias; // weight offset
+    float g;    // NVFP4 per-tensor scale
+};
+__device__ inline QParams q_params(float bias, float g)
+{
+    QParams p;
+    p.bias = bias;
+    p.g = g;
+    return p;
+}
+
+// v = (x * r) * (w + bias) of one vector, two elements per packed
+// instruction, and max |v| of this lane (NaN-propagating).
+template <int DT, int VB>
+__device__ inline float q_values(const Vec<VB> &xv, const Vec<VB> &wv, float r, float bias,
+                                 uint64_t (&v)[VB / Elem<DT>::kSize / 2])
+{
+    constexpr int P = VB / Elem<DT>::kSize / 2;
     const uint64_t r2 = f2(r, r), b2 = f2(bias, bias);
-    uint64_t v[P];
     float m = 0.f;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-        const uint64_t x = widen_pair<DT, VB>(xv, p);
-        const uint64_t w = widen_pair<DT, VB>(wv, p);
-        v[p] = mul2(mul2(x, r2), add2(w, b2));
+        v[p] = mul2(mul2(widen_pair<DT, VB>(xv, p), r2), add2(widen_pair<DT, VB>(wv, p), b2));
         float a, b;
         f2split(v[p], a, b);
         m = absmax3_nan(a, b, m);
     }
+    return m;
+}
+
+// NaN-propagating maximum over the kLanes lanes of a scale block.
+template <int LPB>
+__device__ inline float block_max(float m)
+{
 #pragma unroll
     for (int off = 1; off < LPB; off <<= 1)
         m = max_nan(__shfl_xor_sync(0xFFFFFFFFu, m, off, 32), m);
+    return m;
+}
+
+// One vector of a block-scaled epilogue (QFmt above).
+//
+// The values are v = (x * r) * (w + bias) in fp32.  The block maximum of |v|
+// is a NaN-propagating max (a NaN or an Inf in the block must reach the
+// scale; fmaxf would drop a NaN), reduced over the block's kLanes lanes with
+// butterfly shuffles.  MX formats: the biased exponent e of the maximum gives
+// the shared exponent floor(log2 max) - kEmax = e - 127 - kEmax, clamped at
+// -127: E8M0 code max(e - kEmax, 0), or 0xFF when e = 255 (Inf / NaN);
+// scaling by 2^(127 - code) is exact.  NVFP4: the scale code is
+// E4M3(max * (1 / (6 g))) and the values are multiplied by
+// 1 / (value(code) * g) (by 0 when the scale is 0), both reciprocals from
+// rcp.approx.  The conversions round each scaled value to the element format.
+//
+// With XW (16-bit elements, weight offset -0 and, for NVFP4, a per-tensor
+// scale g in [2^-117, 2^100], so that every value(code) * g and its
+// reciprocal are normal floats and the flush-to-zero reciprocal serves; the
+// launch picks this instantiation) the values are formed the other way round, as the exact
+// products u = x * w (one mixed-precision fma per element, no widening),
+// the block maximum as max |u| * r and the scaled values as u * (r * mul):
+// the same quantities up to one or two fp32 roundings (the decisions they
+// feed are checked against the exact values with a 1e-5 relative band).
+// That holds while the products and the block maximum are normal fp32
+// numbers well away from overflow, so a block whose max |u| or max |u| * r
+// falls outside [2^-100, 2^100) (zero blocks, NaN, Inf, extreme ranges) is
+// redone in the order above, from x and w read again at xp and wp (a rare,
+// warp-uniform branch: the registers holding x and w are not kept for it;
+// neither the codes nor the scales may overlap x or w).
+// An element below 2^-119 of its block's maximum is below half the smallest
+// nonzero code of every format, so at 2^-100 nothing that can reach a code
+// is subnormal.
+//
+// Every lane of the warp must call this (the shuffles span the full warp);
+// `live` says whether this lane's vector is part of the row.  The lane
+// holding the first vector of a block (`leader`) stores the scale byte.
+template <int DT, int VB, int Q, bool XW>
+__device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void *xp,
+                               const void *wp, float r, const QParams &qp, bool live, bool leader,
+                               void *q, uint8_t *scale)
+{
+    static_assert(!XW || DT != RMSNORM_F32, "exact products: 16-bit elements only");
+    using G = QGeo<DT, VB, Q>;
+    constexpr int NE = G::kElems;
+    constexpr int LPB = G::kLanes;
+    constexpr int P = NE / 2;
+    uint64_t v[P];
+    float m, fac;
+    if constexpr (XW) {
+        m = 0.f;
+#pragma unroll
+        for (int p = 0; p < P; ++p) {
+            float a, b;
+            exact_products<DT>(xv.w[p], wv.w[p], a, b);
+            v[p] = f2(a, b);
+            m = absmax3_nan(a, b, m);
+        }
+        m = block_max<LPB>(m);
+        const float mr = m * r;
+        const bool redo = !(m >= 0x1p-100f && m < 0x1p100f && mr >= 0x1p-100f && mr < 0x1p100f);
+        m = mr;
+        fac = r;
+        if (__any_sync(0xFFFFFFFFu, redo)) {
+            if (redo) {
+                Vec<VB> xa, wa;
+                if (live) {
+                    xa = *static_cast<const Vec<VB> *>(xp);
+                    wa = *static_cast<const Vec<VB> *>(wp);
+                } else {
+#pragma unroll
+                    for (int k = 0; k < Vec<VB>::kWords; ++k)
+                        xa.w[k] = wa.w[k] = 0u;
+                }
+                m = q_values<DT, VB>(xa, wa, r, qp.bias, v);
+                fac = 1.f;
+            }
+            m = block_max<LPB>(m); // a block's lanes all redo or all keep theirs
+        }
+    } else {
+        m = block_max<LPB>(q_values<DT, VB>(xv, wv, r, qp.bias, v));
+        fac = 1.f;
+    }
     uint32_t code;
     float mul;
     if constexpr (Q == kQNvfp4) {
-        code = e4m3_code(m * rcp_approx(6.f * g));
+        code = e4m3_code(m * rcp_approx(6.f * qp.g));
         const float d = e4m3_value(code);
-        mul = d == 0.f ? 0.f : rcp_approx(d * g);
+        const float dg = d * qp.g;
+        mul = d == 0.f ? 0.f : (XW ? rcp_approx_ftz(dg) : rcp_approx(dg));
     } else {
         constexpr uint32_t EM = QFmt<Q>::kEmax;
         const uint32_t e = __float_as_uint(m) >> 23;
         code = e == 255u ? 255u : (e > EM ? e - EM : 0u);
         mul = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
     }
-    const uint64_t mul2v = f2(mul, mul);
+    const float f = mul * fac;
+    const uint64_t mul2v = f2(f, f);
     float sv[NE];
 #pragma unroll
     for (int p = 0; p < P; ++p)

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cstring>
 
 #include <cuda_runtime.h>
 
@@ -33,7 +34,29 @@ struct LaunchArgs {
     void *scales = nullptr; // block-scaled epilogues: the scales; y holds the codes
     float gscale = 1.0f;    // NVFP4: the per-tensor scale
     void *scratch = nullptr; // grid variant: counters + partial sums (stream-ordered, per call)
+    bool xw = false;        // block-scaled output formed from exact x * w products (q_store)
 };
+
+// Whether a block-scaled output of 16-bit elements may form its values from
+// the exact products x * w (q_store's second instantiation): the weight
+// offset is -0 (adds nothing, zeros' signs included) and, for NVFP4, every
+// scale value times the per-tensor scale g and its reciprocal are normal
+// floats (g in [2^-117, 2^100]).
+inline bool quant_exact_products(int dtype, int epi, float bias, float gscale)
+{
+    if (dtype == RMSNORM_F32 || epi < RMSNORM_EPI_MXFP8)
+        return false;
+    uint32_t bits;
+    std::memcpy(&bits, &bias, sizeof bits);
+    if (bits != 0x80000000u)
+        return false;
+    return epi != RMSNORM_EPI_NVFP4 || (gscale >= 0x1p-117f && gscale <= 0x1p100f);
+}
+
+// Instantiations with the exact-product form exist for 16-bit elements'
+// block-scaled outputs only.
+template <int DT, int EPI>
+constexpr bool kHasExactProducts = DT != RMSNORM_F32 && EPI >= RMSNORM_EPI_MXFP8;
 
 #if defined(__CUDACC__)
 // Launches `kernel` on a.stream, with the programmatic-stream-serialization
@@ -78,6 +101,8 @@ struct KernelDesc {
     LaunchFn launch;
     const void *func;    // the __global__ function (attributes)
     int32_t epi = RMSNORM_EPI_PLAIN; // what it writes (rmsnorm_epilogue_t)
+    const void *func_xw = nullptr; // its exact-product instantiation where the launcher has one
+                                   // and it needs attributes set (staged: dynamic shared memory)
 };
 
 // Per translation unit tables, concatenated by kernel_table().

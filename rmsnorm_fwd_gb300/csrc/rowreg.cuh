@@ -50,7 +50,7 @@ __device__ inline void vzero(Vec<VB> &v)
 // TPR lanes (4..32, power of two) per row, BLOCK/TPR rows per block per
 // iteration, grid-stride over rows.  The loop bound is block-uniform so every
 // lane takes part in every shuffle.
-template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI>
+template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI, bool XW = false>
 __global__ void __launch_bounds__(BLOCK, MINB > 0 ? MINB : 1)
 warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                  int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
@@ -69,6 +69,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0);
 
     pdl_begin();
+    const QParams qp = q_params(bias, gscale);
     const int nvec = hidden / VPE;
     const int t = threadIdx.x % TPR;
     const int g = threadIdx.x / TPR;
@@ -124,8 +125,8 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                     ld_weight(wk, wt + k * TPR * VB);
                 else
                     vzero(wk);
-                q_store<DT, VB, Q>(xv[k], wk, r, bias, gscale, live, t % LPB == 0,
-                                   yr + k * TPR * OB,
+                q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * TPR * VB, wt + k * TPR * VB, r, qp, live,
+                                   t % LPB == 0, yr + k * TPR * OB,
                                    scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
             } else if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
@@ -150,7 +151,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 // rows.  Warp totals go through a double-buffered shared array so one
 // __syncthreads per row suffices.  TPRC > 0 fixes blockDim.x = TPRC at
 // compile time (vector offsets become immediates).
-template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
+template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI, bool XW = false>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                 int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
@@ -165,6 +166,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     __shared__ float part[2][32];
 
     pdl_begin();
+    const QParams qp = q_params(bias, gscale);
     const int nvec = hidden / VPE;
     const int t = threadIdx.x;
     const int tpr = TPRC > 0 ? TPRC : blockDim.x;
@@ -228,8 +230,8 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                     ld_weight(wk, wt + k * stride);
                 else
                     vzero(wk);
-                q_store<DT, VB, Q>(xv[k], wk, r, bias, gscale, live, t % LPB == 0,
-                                   yr + k * tpr * OB,
+                q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * stride, wt + k * stride, r, qp, live,
+                                   t % LPB == 0, yr + k * tpr * OB,
                                    scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
             } else if (t + k * tpr < nvec) {
                 Vec<VB> o;
@@ -255,7 +257,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 // the squares, the second re-reads the row (an L2 hit: the resident blocks'
 // rows are a few tens of MB against a 129 MB L2), scales and stores.  DRAM
 // sees x once and y once.  For rows longer than the register bodies hold.
-template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
+template <int DT, int VB, int MAXT, int MINB, int CP, int EPI, bool XW = false>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
 cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                 int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
@@ -270,6 +272,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     __shared__ float part[2][32];
 
     pdl_begin();
+    const QParams qp = q_params(bias, gscale);
     const int nvec = hidden / VPE;
     const int t = threadIdx.x;
     const int tpr = blockDim.x;
@@ -330,8 +333,10 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + lane + u * tpr;
-                    q_store<DT, VB, Q>(xv[u], wv[u], r, bias, gscale, v < nvec, lane % LPB == 0,
-                                     yr + static_cast<int64_t>(v) * OB, sr + v / LPB);
+                    q_store<DT, VB, Q, XW>(xv[u], wv[u], xr + static_cast<int64_t>(v) * VB,
+                                       wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
+                                       lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
+                                       sr + v / LPB);
                 }
             }
         } else {
@@ -364,28 +369,45 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 
 // ---------------------------------------------------------------- launchers
 
+// Each launcher takes the exact-product instantiation of a block-scaled
+// body when the call allows it (LaunchArgs::xw), else the general one.
 template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI>
 cudaError_t launch_warp(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP, EPI>, p.grid, BLOCK,
-                         0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales), a.gscale);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, p.grid, BLOCK, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps,
+                             a.bias, static_cast<uint8_t *>(a.scales), a.gscale);
+    };
+    if constexpr (kHasExactProducts<DT, EPI>)
+        if (a.xw)
+            return go(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP, EPI, true>);
+    return go(warp_rows_kernel<DT, VB, TPR, NV, BLOCK, MINB, CP, EPI>);
 }
 
 template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI>
 cudaError_t launch_cta(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC, EPI>, p.grid,
-                         p.block_threads, 0, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales), a.gscale);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, p.grid, p.block_threads, 0, a, a.x, a.w, a.y, a.rows,
+                             a.hidden, a.eps, a.bias, static_cast<uint8_t *>(a.scales), a.gscale);
+    };
+    if constexpr (kHasExactProducts<DT, EPI>)
+        if (a.xw)
+            return go(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC, EPI, true>);
+    return go(cta_rows_kernel<DT, VB, NV, MAXT, MINB, CP, TPRC, EPI>);
 }
 
 template <int DT, int VB, int MAXT, int MINB, int CP, int EPI>
 cudaError_t launch_loop(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI>, p.grid, p.block_threads, 0,
-                         a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, a.bias,
-                         static_cast<uint8_t *>(a.scales), a.gscale);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, p.grid, p.block_threads, 0, a, a.x, a.w, a.y, a.rows,
+                             a.hidden, a.eps, a.bias, static_cast<uint8_t *>(a.scales), a.gscale);
+    };
+    if constexpr (kHasExactProducts<DT, EPI>)
+        if (a.xw)
+            return go(cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI, true>);
+    return go(cta_loop_kernel<DT, VB, MAXT, MINB, CP, EPI>);
 }
 
 constexpr int kWarpBlock = 256;

@@ -169,7 +169,8 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
 // the block-scaled outputs (never with TMA_STORE: their codes are smaller
 // than the slot) write codes and scales with q_store, in a warp-uniform loop
 // so every lane of a warp takes part in each scale block's shuffles.
-template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false, int EPI = RMSNORM_EPI_PLAIN>
+template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false, int EPI = RMSNORM_EPI_PLAIN,
+          bool XW = false>
 __global__ void __launch_bounds__(32 * 17)
 staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
                    int32_t hidden, float eps, int32_t stages, int32_t wpr, int *status,
@@ -200,6 +201,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
         rows > blockIdx.x ? (rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
     pdl_begin();
+    const QParams qp = q_params(bias, gscale);
     if (BLOCK_STATUS) {
         status += blockIdx.x;
         if (threadIdx.x == 0)
@@ -363,7 +365,8 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                     for (int k = 0; k < 4; ++k)
                         xv.w[k] = wv.w[k] = 0u;
                 }
-                q_store<DT, 16, Q>(xv, wv, r, bias, gscale, live, lane % G::kLanes == 0,
+                q_store<DT, 16, Q, XW>(xv, wv, src + v * 16, wsm + v * 16, r, qp, live,
+                                   lane % G::kLanes == 0,
                                    qr + static_cast<int64_t>(v) * G::kCodeBytes,
                                    sr + v / G::kLanes);
             }
@@ -410,16 +413,34 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
 template <int DT, bool TS, int EPI>
 cudaError_t launch_staged(const rmsnorm_plan_t &p, const LaunchArgs &a)
 {
-    return launch_kernel(staged_rows_kernel<DT, TS, false, EPI>, p.grid, p.block_threads,
-                         p.smem_bytes, a, a.x, a.w, a.y, a.rows, a.hidden, a.eps, p.stages,
-                         p.threads_per_row / 32, a.status, a.wait_limit_ns, a.flags, a.bias,
-                         static_cast<uint8_t *>(a.scales), a.gscale);
+    auto go = [&](auto kernel) {
+        return launch_kernel(kernel, p.grid, p.block_threads, p.smem_bytes, a, a.x, a.w, a.y,
+                             a.rows, a.hidden, a.eps, p.stages, p.threads_per_row / 32, a.status,
+                             a.wait_limit_ns, a.flags, a.bias, static_cast<uint8_t *>(a.scales),
+                             a.gscale);
+    };
+    // the exact-product instantiation of a block-scaled output when the call allows it
+    if constexpr (kHasExactProducts<DT, EPI>)
+        if (a.xw)
+            return go(staged_rows_kernel<DT, TS, false, EPI, true>);
+    return go(staged_rows_kernel<DT, TS, false, EPI>);
+}
+
+// The exact-product instantiation launch_staged may pick (null where there is none).
+template <int DT, bool TS, int EPI>
+const void *staged_xw_func()
+{
+    if constexpr (kHasExactProducts<DT, EPI>)
+        return reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS, false, EPI, true>);
+    else
+        return nullptr;
 }
 
 #define STAGED_ENTRY(DT, TS, EPI)                                                              \
     KernelDesc{RMSNORM_VARIANT_STAGED, DT, 16, 32, 0, 0, 0, TS ? 3 : 0,                       \
                &launch_staged<DT, TS, EPI>,                                                    \
-               reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS, false, EPI>), EPI}
+               reinterpret_cast<const void *>(&staged_rows_kernel<DT, TS, false, EPI>), EPI,    \
+               staged_xw_func<DT, TS, EPI>()}
 
 // Plain and weight-bias outputs with both write-back modes; the block-scaled
 // outputs with register stores only.

@@ -185,6 +185,13 @@ def compare_quant(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.nd
         raise AssertionError(f"{fmt} code mismatch row {i} col {b * block + j}: gpu "
                              f"{g[i, b, j]!r} oracle {ref[i, b, j]!r} "
                              f"(band {lo[i, b, j]!r}..{hi[i, b, j]!r})")
+    # A zero code carries the sign of the value it stands for (IEEE signs of
+    # zero products included), which the comparison of values above ignores.
+    zsign = same[:, :, None] & (ref == 0) & (np.signbit(g) != np.signbit(ref))
+    if zsign.any():
+        i, b, j = np.argwhere(zsign)[0]
+        raise AssertionError(f"{fmt} zero-code sign mismatch row {i} col {b * block + j}: gpu "
+                             f"{g[i, b, j]!r} oracle {ref[i, b, j]!r}")
     # Blocks whose scale sits in the band: every element within the error
     # bound of the element grid at the GPU's scale.
     amb = band & ~special
@@ -198,6 +205,7 @@ def compare_quant(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.nd
         sat = t >= maxmag
         tol = (_half_step(t, fmt) * (1 + MX_REL) + MX_REL * t) * X
         good = np.where(X == 0, g == 0, np.where(sat, np.abs(g) == maxmag, err <= tol))
+        good &= (g != 0) | np.isnan(y) | (np.signbit(g) == np.signbit(y))
         badb = amb[:, :, None] & ~good
         if badb.any():
             i, b, j = np.argwhere(badb)[0]

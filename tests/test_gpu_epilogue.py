@@ -289,6 +289,96 @@ def test_fp4_special_blocks(fmt, g):
                 assert (s[0] == 0).all() and not (q[0] & 0x77).any()
 
 
+QFMTS = [("mxfp8", 1.0), ("mxfp4", 1.0), ("nvfp4", 1.0), ("nvfp4", 0.0021)]
+
+
+@pytest.mark.parametrize("fmt,g", QFMTS)
+@pytest.mark.parametrize("name", SMALL)
+def test_quant_workloads_without_offset(name, fmt, g):
+    """Weight offset -0 (no offset, the binding's default): 16-bit inputs take
+    the exact-product path (x * w by the mixed-precision fma, then r)."""
+    wl = inputs.WORKLOADS[name]
+    x, w = inputs.make_inputs(wl)
+    q, s = run_q(x, w, -0.0, wl.eps, wl.dtype, fmt, g)
+    r = compare_quant(q, s, x, w, -0.0, wl.eps, wl.dtype, fmt, g)
+    assert r["rows"] == wl.rows and r["exact_codes"] > 0.999
+
+
+@pytest.mark.parametrize("fmt,g", QFMTS + [("nvfp4", 1e-37), ("nvfp4", 1e31)])
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_quant_exact_products_special_and_extreme_blocks(dtype, fmt, g):
+    """Blocks the exact-product path hands back to the (x * r) * w order --
+    zero, NaN and Inf blocks, products below 2^-100 or above 2^100 -- next to
+    blocks it keeps, in the same warps; zero weights of both signs (zero
+    codes keep the IEEE sign of x * w); NVFP4 global scales outside the
+    flush-to-zero range (1e-37, 1e31) take the order above throughout."""
+    rows, hidden = 12, 1024
+    rng = np.random.default_rng(11)
+    z = rng.standard_normal((rows, hidden)).astype(np.float32)
+    z[0] = 0.0
+    z[1, 5] = np.nan
+    z[2, 700] = np.inf
+    z[3, :32] = 0.0
+    z[3, 64:96] = 0.0
+    wz = np.abs(np.random.default_rng(12).normal(1.0, 0.1, hidden)).astype(np.float32)
+    if dtype == "f16":                           # f16 products never leave fp32's range
+        z[4, 32:64] *= 1e-3
+        z[5] *= 1e-2
+        z[6, 96:128] *= 300.0
+        wz[96:128] *= 100.0
+    else:
+        # one block of products below 2^-100 beside normal blocks; a row of
+        # tiny x whose sum of squares stays a normal fp32 number, meeting
+        # tiny weights in one block; products above 2^100 from large weights
+        z[4, 32:64] *= 1e-32
+        z[5] *= 1e-18 if dtype == "bf16" else 1e-15
+        wz[232:264] *= 1e-14
+        z[6, 96:128] *= 1e9
+        wz[96:128] *= 1e25
+    z[7, ::2] = 0.0
+    z[7, 1] = 1e4 if dtype != "f16" else 6e4
+    z[8] = -np.abs(z[8])
+    x = inputs.to_storage(z, dtype)
+    wz[200:216] = -0.0
+    wz[216:232] = 0.0
+    w = inputs.to_storage(wz[None, :], dtype)[0]
+    if dtype == "f32":
+        assert w[200] == 0 and np.signbit(w[200])
+    else:
+        assert int(w[200]) == 0x8000 and int(w[216]) == 0
+    for eps in (1e-6, 0.0):
+        for bias in (-0.0, 0.0):
+            q, s = run_q(x, w, bias, eps, dtype, fmt, g)
+            compare_quant(q, s, x, w, bias, eps, dtype, fmt, g)
+
+
+@pytest.mark.parametrize("fmt,g", QFMTS)
+def test_quant_without_offset_every_forced_variant(fmt, g):
+    """The exact-product path in every body that writes block-scaled rows:
+    warp-per-row (short rows), block-per-row, persistent, looped (long rows)
+    and the shared-memory ring (x read back from its slot on a fallback)."""
+    cases = [(700, 1024, (rn.VARIANT_AUTO, rn.VARIANT_WARP_PER_ROW, rn.VARIANT_CTA_PER_ROW)),
+             (161, 4096, (rn.VARIANT_AUTO, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT,
+                          rn.VARIANT_STAGED)),
+             (40, 36864, (rn.VARIANT_AUTO, rn.VARIANT_CTA_PER_ROW, rn.VARIANT_STAGED))]
+    for rows, hidden, variants in cases:
+        for dtype in ("bf16", "f16"):
+            x, w = inputs.random_case(rows, hidden, dtype, seed=rows + hidden)
+            x = x.copy()
+            x[1, 32:96] = 0                      # fallback blocks inside a live row
+            x[2, :] = 0                          # and a zero row
+            xd, wd = to_device(x, dtype), to_device(w, dtype)
+            idx = sample_rows(rows, 48, seed=hidden) if rows * hidden > (1 << 22) else None
+            if idx is not None:
+                idx = np.union1d(idx, [1, 2])
+            for v in variants:
+                q, s = rn.rms_norm_quant(xd, wd, 1e-6, fmt, weight_bias=-0.0, global_scale=g,
+                                         variant=v)
+                torch.cuda.synchronize()
+                compare_quant(q.cpu().numpy(), s.cpu().numpy(), x, w, -0.0, 1e-6, dtype, fmt,
+                              g, rows_idx=idx)
+
+
 def test_fp4_argument_errors():
     lib = rn._load()
     x, w = inputs.random_case(8, 4096, "bf16", seed=13)
@@ -315,20 +405,16 @@ def test_fp4_argument_errors():
 @pytest.mark.parametrize("rows,hidden,dtype", [(2048, 20480, "bf16"), (1024, 32768, "f16"),
                                                (600, 9000, "f32"), (160, 36864, "bf16")])
 def test_epilogues_on_the_staged_ring(epi, rows, hidden, dtype):
-    """32-72 KiB rows: the weight-bias output runs on the shared-memory ring
-    above 40 KiB (one 32-byte-vector block per row from 32 to 40 KiB); the
-    block-scaled outputs on the looped body, and on the ring when forced."""
+    """32-72 KiB rows: the weight-bias output runs on the shared-memory ring;
+    the block-scaled outputs on the looped body, and on the ring when forced."""
     x, w = inputs.random_case(rows, hidden, dtype, seed=hidden + 7)
     idx = sample_rows(rows, 48, seed=rows)
     xd, wd = to_device(x, dtype), to_device(w, dtype)
     if epi == "bias":
         y = rn.rms_norm_bias(xd, wd, 0.5, 1e-6)
         torch.cuda.synchronize()
-        row_bytes = hidden * (4 if dtype == "f32" else 2)
-        if row_bytes > 40960:
+        if hidden * (4 if dtype == "f32" else 2) > 32768:
             assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
-        elif row_bytes > 32768:
-            assert rn.rmsnorm_last_variant() == rn.VARIANT_CTA_PER_ROW
         compare(from_device(y, dtype), x, w, 1e-6, dtype, rows_idx=idx, bias=0.5)
         return
     if hidden % 32:

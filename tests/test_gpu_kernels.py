@@ -168,13 +168,17 @@ def test_kernel_instantiation(index):
         if epi in rn.QUANT_FORMATS:
             block, bits = rn.QUANT_FORMATS[epi]
             fmt = rn.EPI_NAMES[epi]
-            q = torch.full((rows, hidden * bits // 8), 0xAA, dtype=torch.uint8, device="cuda")
-            sc = torch.full((rows, hidden // block), 0xAA, dtype=torch.uint8, device="cuda")
-            rn.rms_norm_quant(x, w, 1e-6, fmt, weight_bias=0.625, global_scale=0.01, out=q,
-                              scales=sc, plan=rn.Plan(**pd))
-            torch.cuda.synchronize()
-            compare_quant(q.cpu().numpy(), sc.cpu().numpy(), x_np, w_np, 0.625, 1e-6, dt, fmt,
-                          0.01)
+            # both instantiations of a 16-bit body: weight offset 0.625, and
+            # -0 (no offset: the exact-product form)
+            for bias in (0.625, -0.0):
+                q = torch.full((rows, hidden * bits // 8), 0xAA, dtype=torch.uint8,
+                               device="cuda")
+                sc = torch.full((rows, hidden // block), 0xAA, dtype=torch.uint8, device="cuda")
+                rn.rms_norm_quant(x, w, 1e-6, fmt, weight_bias=bias, global_scale=0.01, out=q,
+                                  scales=sc, plan=rn.Plan(**pd))
+                torch.cuda.synchronize()
+                compare_quant(q.cpu().numpy(), sc.cpu().numpy(), x_np, w_np, bias, 1e-6, dt, fmt,
+                              0.01)
             continue
         y = torch.full_like(x, 3.0)
         if epi == rn.EPI_BIAS:

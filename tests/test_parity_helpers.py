@@ -84,3 +84,32 @@ def test_compare_quant_fp4_accepts_band_and_rejects_planted(fmt, g):
         compare_quant(c, s2, x, w, 0.5, 1e-6, "bf16", fmt, g)
     with pytest.raises(AssertionError):     # the nibble order swapped
         compare_quant(((c & 0xF) << 4) | (c >> 4), s, x, w, 0.5, 1e-6, "bf16", fmt, g)
+
+
+@pytest.mark.parametrize("fmt,g", [("mxfp8", 1.0), ("mxfp4", 1.0), ("nvfp4", 0.004)])
+def test_compare_quant_checks_the_sign_of_zero_codes(fmt, g):
+    """A zero weight with a -0 or +0 offset: the zero codes' signs follow the
+    IEEE signs of (x * r) * (w + offset); a flipped zero sign is rejected."""
+    x, w = inputs.random_case(8, 256, "bf16", seed=4)
+    w = w.copy()
+    w[:64] = 0x8000                             # -0.0 weights (bf16 bits)
+    w[64:96] = 0x0000                           # +0.0 weights
+    for bias in (-0.0, 0.0):
+        if fmt == "mxfp8":
+            c, s = oracle.rmsnorm_mxfp8(x, w, bias, 1e-6, "bf16")
+        else:
+            c, s = oracle.rmsnorm_fp4(x, w, bias, 1e-6, "bf16", fmt, global_scale=g)
+        compare_quant(c, s, x, w, bias, 1e-6, "bf16", fmt, g)
+        c2 = c.copy()
+        if fmt == "mxfp8":
+            c2[0, 0] ^= 0x80                    # column 0: a zero code, its sign flipped
+        else:
+            c2[0, 0] ^= 0x08
+        with pytest.raises(AssertionError):
+            compare_quant(c2, s, x, w, bias, 1e-6, "bf16", fmt, g)
+    # the two offsets give different signs where x > 0 and w = -0
+    c_m, _ = (oracle.rmsnorm_mxfp8(x, w, -0.0, 1e-6, "bf16") if fmt == "mxfp8" else
+              oracle.rmsnorm_fp4(x, w, -0.0, 1e-6, "bf16", fmt, global_scale=g))
+    c_p, _ = (oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "bf16") if fmt == "mxfp8" else
+              oracle.rmsnorm_fp4(x, w, 0.0, 1e-6, "bf16", fmt, global_scale=g))
+    assert (c_m != c_p).any()
