@@ -200,7 +200,15 @@ int rmsnorm_fwd_bias(const void *x, const void *weight, void *y, int64_t rows, i
  * hidden must be a multiple of 32 (RMSNORM_ERR_INVALID_ARG otherwise);
  * misaligned x / weight / q give RMSNORM_ERR_MISALIGNED (there is no scalar
  * MX body).  q and scales may not overlap each other, x or weight
- * (RMSNORM_ERR_ALIASING).  Otherwise as rmsnorm_fwd. */
+ * (RMSNORM_ERR_ALIASING).  Otherwise as rmsnorm_fwd.
+ *
+ * weight_bias = -0.0f means no offset (w exactly; +0.0f turns a -0 weight
+ * into +0, which shows in the sign of that element's zero code).  With
+ * -0.0f and bf16 / f16 elements the device forms the same values as
+ * (x * w) * r, x * w exact (a faster path; the results agree with the
+ * definition above within the 1e-5 relative band the decisions are checked
+ * with); a block whose products leave [2^-100, 2^100) is formed in the
+ * order above.  This holds for all three block-scaled formats. */
 int rmsnorm_fwd_mxfp8(const void *x, const void *weight, void *q, void *scales, int64_t rows,
                       int64_t hidden, float weight_bias, float eps, int dtype, void *stream);
 
