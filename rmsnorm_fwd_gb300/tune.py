@@ -140,9 +140,14 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
 
 
 def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
-               epi: int = 0) -> list[dict]:
+               epi: int = 0, bias: float | None = None) -> list[dict]:
     """Time the automatic plan and every candidate; sorted fastest first.
-    epi: the epilogue (0 plain, 1 weight bias, 2 MXFP8 output)."""
+    epi: the epilogue (0 plain, 1 weight bias, 2-4 MXFP8 / MXFP4 / NVFP4
+    output); bias: its weight offset (default 1.0 for the weight-bias output,
+    -0.0 -- no offset, the exact-product form of 16-bit inputs -- for the
+    block-scaled ones)."""
+    if bias is None:
+        bias = 1.0 if epi == 1 else -0.0
     import torch
 
     import rmsnorm_fwd_gb300 as rn
@@ -177,7 +182,7 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
     def fwd(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref, j=0):
         if epi == 0:
             return lib.rmsnorm_fwd_ex(x, wp, y, rows_, hidden_, eps, dt_, stream, variant, ref)
-        return lib.rmsnorm_fwd_epilogue_ex(x, wp, y, sp[j], rows_, hidden_, epi, 1.0, 0.01, eps,
+        return lib.rmsnorm_fwd_epilogue_ex(x, wp, y, sp[j], rows_, hidden_, epi, bias, 0.01, eps,
                                            dt_, stream, variant, ref)
 
     auto = rn.Plan()
@@ -353,6 +358,9 @@ def main(argv=None) -> int:
     ap.add_argument("--qk-workload", default="", help="sweep the QK-norm launch shapes instead")
     ap.add_argument("--epilogue", default="plain",
                     choices=["plain", "bias", "mxfp8", "mxfp4", "nvfp4"])
+    ap.add_argument("--weight-bias", type=float, default=None,
+                    help="weight offset of the epilogue (default 1.0 for bias, -0.0 = none for "
+                         "the block-scaled outputs)")
     args = ap.parse_args(argv)
     if args.qk_workload:
         if args.pdl is not None:
@@ -371,7 +379,8 @@ def main(argv=None) -> int:
     _AUTO_ONLY = args.auto_only
     epi = {"plain": 0, "bias": 1, "mxfp8": 2, "mxfp4": 3, "nvfp4": 4}[args.epilogue]
     if not args.grid:
-        res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph, epi)
+        res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph, epi,
+                         args.weight_bias)
         for r in res:
             print(json.dumps(r), flush=True)
         return 0
@@ -386,7 +395,7 @@ def main(argv=None) -> int:
         if "decode" in classes:
             points += [(f"decode{r}", r, 200, True) for r in (1, 8, 32, 128)]
         for cls, rows, iters, graph in points:
-            res = time_plans(rows, h, "bf16", iters, graph, epi)
+            res = time_plans(rows, h, "bf16", iters, graph, epi, args.weight_bias)
             auto = next((r for r in res if r["auto"]), None)
             print(json.dumps({"hidden_bf16": h, "row_bytes": 2 * h, "rows": rows, "class": cls,
                               "top": res[:args.keep], "auto": auto}), flush=True)
