@@ -119,6 +119,7 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_fwd": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
             "rmsnorm_fwd_ex": ([vp, vp, vp, i64, i64, f32, i32, vp, i32, pp], i32),
             "rmsnorm_plan": ([vp, vp, vp, i64, i64, i32, i32, i32, i32, pp], i32),
+            "rmsnorm_plan_host_mapped": ([vp, vp, vp, i64, i64, i32, i32, i32, pp], i32),
             "rmsnorm_fwd_host": ([vp, vp, vp, i64, i64, f32, i32, vp, ctypes.c_size_t, i64, vp],
                                  i32),
             "rmsnorm_qk_norm": ([vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, f32, f32, i32, vp],
@@ -310,6 +311,15 @@ def rmsnorm_plan_status(x: int, weight: int, y: int, rows: int, hidden: int, dty
     p = Plan()
     rc = _load().rmsnorm_plan(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant,
                               ctypes.byref(p))
+    return rc, p
+
+
+def rmsnorm_plan_host_mapped_status(x_host: int, weight: int, y_host: int, rows: int,
+                                    hidden: int, dtype: int, sm_count: int, smem_optin: int):
+    """(status, plan) of rmsnorm_fwd_host's page-locked path, without raising."""
+    p = Plan()
+    rc = _load().rmsnorm_plan_host_mapped(x_host, weight, y_host, rows, hidden, dtype, sm_count,
+                                          smem_optin, ctypes.byref(p))
     return rc, p
 
 

@@ -24,7 +24,7 @@ SOURCES = ["api.cpp", "select.cpp", "generic.cu", "staged.cu", "qknorm.cu", "clu
            "rowreg_f32.cu", "rowreg_bf16.cu", "rowreg_f16.cu",
            "rowreg_epi_f32.cu", "rowreg_epi_bf16.cu", "rowreg_epi_f16.cu",
            "rowreg_fp4_f32.cu", "rowreg_fp4_bf16.cu", "rowreg_fp4_f16.cu"]
-HEADERS = ["internal.h", "device_common.cuh", "rowreg.cuh"]
+HEADERS = ["internal.h", "host_link.h", "device_common.cuh", "rowreg.cuh"]
 GENCODE = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-Xcompiler", "-fPIC"]
 CUDA_FLAGS = ["-lineinfo"]

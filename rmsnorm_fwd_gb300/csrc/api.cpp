@@ -11,6 +11,7 @@
 
 #include <cuda_runtime.h>
 
+#include "host_link.h"
 #include "internal.h"
 
 namespace rmsnorm {
@@ -511,9 +512,15 @@ int rmsnorm_fwd_host(const void *x_host, const void *weight, void *y_host, int64
 
     // Page-locked, device-mapped host buffers: the kernel reads x and writes
     // y in host memory directly (over the CPU-GPU link), no staging.
-    if (host_mapped(x_host, rows * row_bytes) && host_mapped(y_host, rows * row_bytes))
+    if (host_mapped(x_host, rows * row_bytes) && host_mapped(y_host, rows * row_bytes)) {
+        rmsnorm_plan_t p;
+        rc = plan_host_link(x_host, weight, y_host, rows, hidden, dtype, ctx.sm_count,
+                            ctx.smem_optin, &p);
+        if (rc != RMSNORM_OK)
+            return rc;
         return launch(x_host, weight, y_host, rows, hidden, eps, dtype, stream,
-                      RMSNORM_VARIANT_AUTO, nullptr, 0u, g_wait_limit.load());
+                      RMSNORM_VARIANT_AUTO, &p, 0u, g_wait_limit.load());
+    }
 
     std::lock_guard<std::mutex> plk(g_pipe_mu[dev]);
     HostPipe *hp = nullptr;
@@ -715,6 +722,15 @@ int rmsnorm_plan(const void *x, const void *weight, const void *y, int64_t rows,
                  int dtype, int sm_count, int smem_optin, int variant, rmsnorm_plan_t *out)
 {
     return plan_launch(x, weight, y, rows, hidden, dtype, sm_count, smem_optin, variant, out);
+}
+
+int rmsnorm_plan_host_mapped(const void *x_host, const void *weight, const void *y_host,
+                             int64_t rows, int64_t hidden, int dtype, int sm_count,
+                             int smem_optin, rmsnorm_plan_t *out)
+{
+    if (!out)
+        return RMSNORM_ERR_INVALID_ARG;
+    return plan_host_link(x_host, weight, y_host, rows, hidden, dtype, sm_count, smem_optin, out);
 }
 
 int rmsnorm_validate_plan(const rmsnorm_plan_t *plan, const void *x, const void *weight,

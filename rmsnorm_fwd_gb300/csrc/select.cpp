@@ -21,6 +21,7 @@
 #include <climits>
 #include <cstdint>
 
+#include "host_link.h"
 #include "internal.h"
 
 namespace rmsnorm {
@@ -758,6 +759,30 @@ int validate_plan(const rmsnorm_plan_t &p, const void *x, const void *w, const v
         return RMSNORM_ERR_INVALID_ARG;
     if (dv != RMSNORM_VARIANT_STAGED && p.smem_bytes != 0)
         return RMSNORM_ERR_INVALID_ARG;
+    return RMSNORM_OK;
+}
+
+// Over the CPU-GPU link the link, not the SMs, sets the pace: on GB300 every
+// plan with enough rows in flight moves 16384 x 4096 bf16 host rows at about
+// 337 GB/s (the copy engines with both directions busy reach 336), except
+// the one-block-per-row grid of 16384 blocks, at 322 GB/s.  A persistent grid
+// of two blocks per SM is at the plateau (337-338 GB/s), so block-per-row and
+// wider persistent grids of the register bodies (which loop over rows at any
+// grid size) are cut to it; other plans are kept.
+int plan_host_link(const void *x, const void *w, const void *y, int64_t rows, int64_t hidden,
+                   int dtype, int sm_count, int smem_optin, rmsnorm_plan_t *out)
+{
+    const int rc = plan_launch(x, w, y, rows, hidden, dtype, sm_count, smem_optin,
+                               RMSNORM_VARIANT_AUTO, out);
+    if (rc != RMSNORM_OK)
+        return rc;
+    const int cap = kHostLinkBlocksPerSm * sm_count;
+    if ((out->variant == RMSNORM_VARIANT_CTA_PER_ROW ||
+         out->variant == RMSNORM_VARIANT_PERSISTENT) &&
+        out->grid > cap) {
+        out->variant = RMSNORM_VARIANT_PERSISTENT;
+        out->grid = cap;
+    }
     return RMSNORM_OK;
 }
 

@@ -590,3 +590,30 @@ def test_prefill_rows_of_16_to_24_and_32_to_40_kib_take_32_byte_blocks():
     rc, p = rn.rmsnorm_plan_epilogue_status(A, 3 * A, 5 * A, 16384, 20480, rn.BF16,
                                             rn.EPI_BIAS, SMS, OPTIN)
     assert rc == rn.OK and p.variant == rn.VARIANT_STAGED
+
+
+def test_host_mapped_plan_caps_wide_row_grids_at_two_blocks_per_sm():
+    """rmsnorm_fwd_host's page-locked path: block-per-row and wide persistent
+    grids of the register bodies become two persistent blocks per SM; short
+    batches, warp-per-row, staged and looped plans are rmsnorm_plan's."""
+    def both(rows, hidden, dt=rn.BF16):
+        rc, p = rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, rows, hidden, dt, SMS, OPTIN)
+        rc0, p0 = plan(rows, hidden, dt)
+        assert rc == rc0 == rn.OK
+        return p, p0
+    p, p0 = both(16384, 4096)
+    assert p0.variant == rn.VARIANT_CTA_PER_ROW and p0.grid == 16384
+    assert p.variant == rn.VARIANT_PERSISTENT and p.grid == 2 * SMS
+    d, d0 = p.as_dict(), p0.as_dict()
+    for k in ("variant", "grid"):
+        d.pop(k), d0.pop(k)
+    assert d == d0                                   # the same body and block
+    assert rn.rmsnorm_validate_plan(p, A, 3 * A, 5 * A, 16384, 4096, rn.BF16, SMS, OPTIN) == rn.OK
+    for rows, hidden in ((100, 4096), (2 * SMS, 4096), (16384, 512), (16384, 24576), (4, 131072)):
+        p, p0 = both(rows, hidden)
+        if p0.variant in (rn.VARIANT_CTA_PER_ROW, rn.VARIANT_PERSISTENT) and p0.grid > 2 * SMS:
+            assert p.variant == rn.VARIANT_PERSISTENT and p.grid == 2 * SMS
+        else:
+            assert p.as_dict() == p0.as_dict(), (rows, hidden)
+    assert rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, 8, 4096, 7, SMS, OPTIN)[0] == \
+        rn.ERR_UNSUPPORTED_DTYPE

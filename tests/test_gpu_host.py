@@ -104,3 +104,24 @@ def test_host_pipeline_rejects_small_workspace_and_handles_zero_rows():
     assert e.value.status == rn.ERR_INVALID_ARG
     rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), xh.data_ptr(), 0, 4096, 1e-6, rn.BF16,
                         ws.data_ptr(), 1024, 0, torch.cuda.current_stream().cuda_stream)
+
+
+def test_host_mapped_path_launches_the_host_link_plan():
+    """Page-locked buffers: the kernel runs the plan rmsnorm_plan_host_mapped
+    gives (a persistent grid of two blocks per SM for many rows)."""
+    dtype, rows, hidden = "bf16", 4096, 4096
+    x_np, w_np = inputs.random_case(rows, hidden, dtype, seed=21)
+    xh = host_tensor(x_np, dtype, True)
+    yh = host_tensor(np.zeros_like(x_np), dtype, True)
+    w = to_device(w_np, dtype)
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    sms, optin = rn.rmsnorm_device_limits()
+    rc, p = rn.rmsnorm_plan_host_mapped_status(xh.data_ptr(), w.data_ptr(), yh.data_ptr(), rows,
+                                               hidden, rn.BF16, sms, optin)
+    assert rc == rn.OK and p.variant == rn.VARIANT_PERSISTENT and p.grid == 2 * sms
+    rn.rmsnorm_fwd_host(xh.data_ptr(), w.data_ptr(), yh.data_ptr(), rows, hidden, 1e-6, rn.BF16,
+                        ws.data_ptr(), 1 << 20, 0, s.cuda_stream)
+    s.synchronize()
+    assert rn.rmsnorm_last_variant() == rn.VARIANT_PERSISTENT
+    compare(to_numpy(yh, dtype), x_np, w_np, 1e-6, dtype)
