@@ -140,14 +140,18 @@ def candidates(rows: int, hidden: int, dtype: str, sms: int, optin: int,
 
 
 def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
-               epi: int = 0, bias: float | None = None) -> list[dict]:
+               epi: int = 0, bias: float | None = None, host: bool = False) -> list[dict]:
     """Time the automatic plan and every candidate; sorted fastest first.
     epi: the epilogue (0 plain, 1 weight bias, 2-4 MXFP8 / MXFP4 / NVFP4
     output); bias: its weight offset (default 1.0 for the weight-bias output,
     -0.0 -- no offset, the exact-product form of 16-bit inputs -- for the
-    block-scaled ones)."""
+    block-scaled ones).  host: x and y in page-locked host memory (the
+    kernel reads and writes it over the CPU-GPU link; plain output), the
+    automatic plan being rmsnorm_fwd_host's (rmsnorm_plan_host_mapped)."""
     if bias is None:
         bias = 1.0 if epi == 1 else -0.0
+    if host and epi != 0:
+        raise ValueError("host buffers: the plain output only")
     import torch
 
     import rmsnorm_fwd_gb300 as rn
@@ -157,10 +161,14 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[dtype]
     es = ES[dtype]
     set_bytes = 2 * rows * hidden * es
-    nsets = min(64, max(2, -(-3 * L2 // set_bytes)))
-    base = [torch.randn(rows, hidden, device=dev).to(tdt) for _ in range(min(nsets, 4))]
-    xs = [base[i % len(base)] if i < len(base) else base[i % len(base)].clone()
-          for i in range(nsets)]
+    nsets = 2 if host else min(64, max(2, -(-3 * L2 // set_bytes)))
+    if host:
+        base = [torch.randn(rows, hidden).to(tdt).pin_memory() for _ in range(nsets)]
+        xs = base
+    else:
+        base = [torch.randn(rows, hidden, device=dev).to(tdt) for _ in range(min(nsets, 4))]
+        xs = [base[i % len(base)] if i < len(base) else base[i % len(base)].clone()
+              for i in range(nsets)]
     mx = epi in rn.QUANT_FORMATS
     block, bits = rn.QUANT_FORMATS.get(epi, (1, 8 * es))
     if mx:
@@ -170,7 +178,8 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
               for _ in range(nsets)]
         sp = [t.data_ptr() for t in ss]
     else:
-        ys = [torch.empty_like(xs[0]) for _ in range(nsets)]
+        ys = [torch.empty_like(xs[0]).pin_memory() if host else torch.empty_like(xs[0])
+              for _ in range(nsets)]
         sp = [None] * nsets
     w = (1 + 0.1 * torch.randn(hidden, device=dev)).to(tdt)
     lib = rn._load()
@@ -186,7 +195,13 @@ def time_plans(rows: int, hidden: int, dtype: str, iters: int, graph: bool,
                                            dt_, stream, variant, ref)
 
     auto = rn.Plan()
-    fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, rn.ctypes.byref(auto))
+    if host:
+        rc, auto = rn.rmsnorm_plan_host_mapped_status(xp[0], w.data_ptr(), yp[0], rows, hidden,
+                                                      dt, sms, optin)
+        if rc != rn.OK:
+            raise rn.RmsnormError(rc, "rmsnorm_plan_host_mapped")
+    else:
+        fwd(xp[0], w.data_ptr(), yp[0], rows, hidden, 1e-6, dt, s, 0, rn.ctypes.byref(auto))
     cands = [auto.as_dict()] + ([] if _AUTO_ONLY else candidates(rows, hidden, dtype, sms, optin,
                                                                   epi))
     out_bytes = rows * hidden * bits // 8 + rows * hidden // block if mx else rows * hidden * es
@@ -358,6 +373,8 @@ def main(argv=None) -> int:
     ap.add_argument("--qk-workload", default="", help="sweep the QK-norm launch shapes instead")
     ap.add_argument("--epilogue", default="plain",
                     choices=["plain", "bias", "mxfp8", "mxfp4", "nvfp4"])
+    ap.add_argument("--host-buffers", action="store_true",
+                    help="x and y in page-locked host memory (plain output)")
     ap.add_argument("--weight-bias", type=float, default=None,
                     help="weight offset of the epilogue (default 1.0 for bias, -0.0 = none for "
                          "the block-scaled outputs)")
@@ -380,7 +397,7 @@ def main(argv=None) -> int:
     epi = {"plain": 0, "bias": 1, "mxfp8": 2, "mxfp4": 3, "nvfp4": 4}[args.epilogue]
     if not args.grid:
         res = time_plans(args.rows, args.hidden, args.dtype, args.iters, args.graph, epi,
-                         args.weight_bias)
+                         args.weight_bias, args.host_buffers)
         for r in res:
             print(json.dumps(r), flush=True)
         return 0
