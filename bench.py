@@ -23,7 +23,8 @@ value = algorithmic bytes (read x + read weight + write y) of every step of
 every rank / the slowest rank's time, in GB/s.  e2e = the same metric through
 the public API with the step's input copied host->device from pinned memory
 and the result copied back, every step.  cpu_baseline = the fp64 CPU oracle
-timed on this host on a bounded sample of the same workload.
+timed on this host on a bounded sample of the same workload (one thread; its
+row_parallel entry: the same oracle on every host core).
 
 --impl reference times the oracle itself (there is no other implementation
 of this path to compare with): rank 0 only, each step a bounded sample of the
@@ -243,6 +244,39 @@ def oracle_sample(wl, seconds: float, max_rows: int | None = None):
     return bytes_done / el / 1e9, done / el, done, el
 
 
+def oracle_sample_parallel(wl, seconds: float, threads: int):
+    """The same oracle run row-parallel: `threads` host threads each
+    normalise their own block of the workload's leading rows (the C call
+    releases the interpreter lock) until `seconds` have passed.  Returns
+    (GB/s, rows/s, rows done, seconds)."""
+    import threading as th
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+    block = max(1, min(wl.rows, 64))
+    x, w = inputs.make_inputs(wl.with_shape(block))
+    oracle.rmsnorm(x[:1], w, wl.eps, wl.dtype)
+    stop = th.Event()
+
+    def worker(_):
+        done = 0
+        while not stop.is_set():
+            oracle.rmsnorm(x, w, wl.eps, wl.dtype)
+            done += block
+        return done
+
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        futs = [ex.submit(worker, i) for i in range(threads)]
+        time.sleep(seconds)
+        stop.set()
+        done = sum(f.result() for f in futs)
+    el = time.perf_counter() - t0
+    es = inputs.ITEMSIZE[wl.dtype]
+    bytes_done = 2 * done * wl.hidden * es + wl.hidden * es
+    return bytes_done / el / 1e9, done / el, done, el
+
+
 def run_reference(args, world, rank):
     """--impl reference: the oracle timed on the host cores (rank 0 only)."""
     if rank != 0:
@@ -440,6 +474,13 @@ def run_ours(args, world, rank, local):
             "sample": (f"first {min(wl.rows, 256)} rows of the same seeded workload, repeated: "
                        f"{rows_done} rows x {wl.hidden} in {el:.1f} s, one thread"),
             "rows_per_s": round(rps, 2)}
+        ncores = os.cpu_count() or 1
+        pg, prps, pdone, pel = oracle_sample_parallel(wl, min(args.cpu_seconds, 5.0), ncores)
+        line["cpu_baseline"]["row_parallel"] = {
+            "value": round(pg, 5), "unit": UNIT, "cores": ncores,
+            "sample": (f"the same oracle on {ncores} host threads, each repeating the first "
+                       f"{min(wl.rows, 64)} rows: {pdone} rows x {wl.hidden} in {pel:.1f} s"),
+            "rows_per_s": round(prps, 2)}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
