@@ -564,8 +564,10 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         //  * rows above 32 KiB (up to 8 rows below 48 KiB): one wave of
         //    clusters, as large (<= 8) as keeps every block on its own SM --
         //    at least 4 blocks, or 2 for rows of 64 KiB and more;
-        //  * 128..256 KiB rows, up to 80 of them: clusters of 8 over several
-        //    waves, 64 bytes per thread;
+        //  * 64..256 KiB rows, up to 128 of them (more than one wave holds):
+        //    clusters over several waves, 64 bytes per thread, of 4 blocks
+        //    below 128 KiB and 8 from there (96 and 128 rows of 80, 128 and
+        //    256 KiB: 6-34 % faster than the looped body);
         //  * longer rows, up to 64 of them: every SM on every row, one grid
         //    barrier.
         // Other long-row decode shapes keep the block-per-row bodies below.
@@ -579,8 +581,9 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
                      plan_cluster_exact(s, C, 16, out) == RMSNORM_OK))
                     return RMSNORM_OK;
             }
-            if (s.rows <= 80 && s.row_bytes >= 128 * 1024 && s.row_bytes <= 256 * 1024 &&
-                plan_cluster_exact(s, 8, 16, out, 64) == RMSNORM_OK)
+            if (s.rows <= 128 && s.row_bytes > 64 * 1024 && s.row_bytes <= 256 * 1024 &&
+                plan_cluster_exact(s, s.row_bytes >= 128 * 1024 ? 8 : 4, 16, out, 64) ==
+                    RMSNORM_OK)
                 return RMSNORM_OK;
             if (s.row_bytes > 256 * 1024 && plan_grid(s, out) == RMSNORM_OK)
                 return RMSNORM_OK;

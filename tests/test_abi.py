@@ -488,19 +488,23 @@ def test_cluster_split_chosen_for_long_decode_rows():
             (rows, hidden, p.as_dict())
         assert p.vec_bytes == 32 and p.block_threads <= 512
         assert ks[p.kernel_index]["variant"] == rn.VARIANT_CLUSTER
-    # 128-256 KiB rows, up to 80 of them: clusters of 8 over several waves
-    for rows, hidden in ((77, 65536), (48, 131072), (80, 65536)):
+    # 64-256 KiB rows, up to 128 of them, more than one wave holds: clusters
+    # over several waves (4 blocks below 128 KiB rows, 8 from there)
+    for rows, hidden, C in ((77, 65536, 8), (48, 131072, 8), (80, 65536, 8), (96, 65536, 8),
+                            (128, 65536, 8), (128, 131072, 8), (77, 40960, 4), (96, 40960, 4),
+                            (128, 40960, 4), (128, 36864, 4)):
         rc, p = plan(rows, hidden, rn.BF16)
-        assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == 8
-        assert p.grid == rows * 8 > SMS and p.vecs_per_thread * p.vec_bytes >= 64
+        assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == C, \
+            (rows, hidden, p.as_dict())
+        assert p.grid == rows * C > SMS and p.vecs_per_thread * p.vec_bytes >= 64
     # 512 KiB rows: 16-byte vectors, four per thread, 1024 threads per block
     rc, p = plan(1, 131072, rn.F32)
     assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == 8
     assert p.vec_bytes == 16 and p.vecs_per_thread == 4 and p.block_threads == 1024
     # shorter rows, more rows than fit one block per SM, or an epilogue: no cluster
     for rows, hidden, epi in ((1, 16384, 0), (32, 16384, 0), (77, 32768, 0), (153, 65536, 0),
-                              (9, 20480, 0), (32, 20480, 0), (48, 24576, 0), (81, 65536, 0),
-                              (128, 131072, 0),
+                              (9, 20480, 0), (32, 20480, 0), (48, 24576, 0), (129, 65536, 0),
+                              (128, 32768, 0), (152, 131072, 0), (129, 40960, 0),
                               (1, 65536, rn.EPI_BIAS), (1, 65536, rn.EPI_MXFP8)):
         rc, p = plan_epi(rows, hidden, rn.BF16, epi)
         assert rc == rn.OK and p.variant != rn.VARIANT_CLUSTER, (rows, hidden, epi)

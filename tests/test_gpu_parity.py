@@ -232,14 +232,16 @@ def test_plan_written_back_and_replayed():
 @pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
 @pytest.mark.parametrize("rows,hidden", [(1, 65536), (8, 65536), (1, 131072), (20, 32768),
                                          (32, 32768), (76, 32768), (3, 40000), (77, 65536),
-                                         (48, 131072), (24, 24576)])
+                                         (48, 131072), (24, 24576), (96, 40960), (128, 65536),
+                                         (128, 131072)])
 def test_long_decode_rows(dtype, rows, hidden):
     """Decode rows of 64 KiB and more: the automatic plan splits each row over
-    a thread-block cluster (f32 rows twice as long in bytes)."""
+    a thread-block cluster, in one wave or, for up to 128 rows of 64-256 KiB,
+    several (f32 rows twice as long in bytes)."""
     x, w = inputs.random_case(rows, hidden, dtype, seed=hidden + rows)
     y = run(x, w, 1e-6, dtype)
     es = 4 if dtype == "f32" else 2
-    if hidden * es >= 65536 and hidden * es <= 256 * 1024 and rows <= 77:
+    if hidden * es >= 65536 and hidden * es <= 256 * 1024 and rows <= 128:
         assert rn.rmsnorm_last_variant() == rn.VARIANT_CLUSTER
     compare(y, x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 16, seed=rows))
 
