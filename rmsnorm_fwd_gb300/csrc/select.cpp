@@ -673,10 +673,16 @@ wide:
     // 2.8-3.0 TB/s against 4.3-4.9 on the looped body below -- and stay there).
     if (nvec <= 4608 && s.epi <= RMSNORM_EPI_BIAS && plan_staged_wide(s, out) == RMSNORM_OK)
         return RMSNORM_OK;
-    // Longer rows: the looped body, one block per row.
-    if (plan_cta_exact(s, 16, 0, 512, 2, 1, 0, nvec <= 5120 ? 256 : 512, INT_MAX,
-                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
-        return RMSNORM_OK;
+    // Longer rows: the looped body, one block per row -- 512 threads, or 256
+    // for rows up to 80 KiB in batches of more than two rows per SM (with
+    // fewer rows per SM, 256 x 80 KiB rows, the wider block is 17 % faster).
+    {
+        const bool narrow =
+            nvec <= 5120 && (s.epi >= RMSNORM_EPI_MXFP8 || s.rows > 2 * int64_t(s.sm_count));
+        if (plan_cta_exact(s, 16, 0, 512, 2, 1, 0, narrow ? 256 : 512, INT_MAX,
+                           RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+            return RMSNORM_OK;
+    }
     return plan_generic(s, out);
 }
 

@@ -621,3 +621,17 @@ def test_host_mapped_plan_caps_wide_row_grids_at_two_blocks_per_sm():
             assert p.as_dict() == p0.as_dict(), (rows, hidden)
     assert rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, 8, 4096, 7, SMS, OPTIN)[0] == \
         rn.ERR_UNSUPPORTED_DTYPE
+
+
+def test_looped_body_block_size_for_72_to_80_kib_rows():
+    """Rows beyond the staged ring up to 80 KiB: 256-thread looped blocks in
+    batches of more than two rows per SM, 512 threads below that."""
+    for rows, threads in ((2 * SMS + 1, 256), (512, 256), (2 * SMS, 512), (256, 512),
+                          (SMS + 1, 512)):
+        rc, p = plan(rows, 40960, rn.BF16)
+        assert rc == rn.OK and p.vecs_per_thread == 0 and p.block_threads == threads, \
+            (rows, p.as_dict())
+    rc, p = plan(256, 65536, rn.BF16)                # longer rows: 512 threads always
+    assert rc == rn.OK and p.vecs_per_thread == 0 and p.block_threads == 512
+    rc, p = plan_epi(256, 40960, rn.BF16, rn.EPI_MXFP8)   # block-scaled: unchanged
+    assert rc == rn.OK and p.vecs_per_thread == 0 and p.block_threads == 256
