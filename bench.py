@@ -315,6 +315,14 @@ def run_reference(args, world, rank):
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+    if args.cpu_seconds > 0:   # context: the same oracle on every host core
+        ncores = os.cpu_count() or 1
+        pg, prps, pdone, pel = oracle_sample_parallel(wl, min(args.cpu_seconds, 5.0), ncores)
+        line["cpu_baseline"]["row_parallel"] = {
+            "value": round(pg, 5), "unit": UNIT, "cores": ncores,
+            "sample": (f"the same oracle on {ncores} host threads, each repeating the first "
+                       f"{min(wl.rows, 64)} rows: {pdone} rows x {wl.hidden} in {pel:.1f} s"),
+            "rows_per_s": round(prps, 2)}
     print(json.dumps(line), flush=True)
     return 0
 
