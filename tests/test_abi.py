@@ -621,6 +621,14 @@ def test_host_mapped_plan_caps_wide_row_grids_at_two_blocks_per_sm():
             assert p.as_dict() == p0.as_dict(), (rows, hidden)
     assert rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, 8, 4096, 7, SMS, OPTIN)[0] == \
         rn.ERR_UNSUPPORTED_DTYPE
+    # the same argument rules as rmsnorm_plan: zero rows plan nothing, a null
+    # plan pointer or no SMs are refused
+    assert rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, 0, 4096, rn.BF16, SMS,
+                                              OPTIN)[0] == rn.OK
+    assert rn._load().rmsnorm_plan_host_mapped(A, 3 * A, 5 * A, 8, 4096, rn.BF16, SMS, OPTIN,
+                                               None) == rn.ERR_INVALID_ARG
+    assert rn.rmsnorm_plan_host_mapped_status(A, 3 * A, 5 * A, 8, 4096, rn.BF16, 0,
+                                              OPTIN)[0] == rn.ERR_INVALID_ARG
 
 
 def test_looped_body_block_size_for_72_to_80_kib_rows():
