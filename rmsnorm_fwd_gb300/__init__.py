@@ -14,7 +14,6 @@ tensors, reads their data pointers and the current stream, and calls
 from __future__ import annotations
 
 import ctypes
-import os
 import threading
 
 # element types (rmsnorm_dtype_t)

@@ -5,7 +5,6 @@ collective; this is the only cross-rank step."""
 import os
 import socket
 
-import pytest
 import torch.multiprocessing as mp
 
 

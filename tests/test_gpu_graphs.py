@@ -4,7 +4,6 @@ every body, including the cluster split and the grid barrier variant with
 its per-call stream-ordered scratch, against the oracle."""
 import threading
 
-import numpy as np
 import pytest
 
 import rmsnorm_fwd_gb300 as rn

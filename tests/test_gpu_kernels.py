@@ -2,7 +2,6 @@
 rmsnorm_fwd_ex (plain) or rmsnorm_fwd_epilogue_ex (weight bias, MXFP8, MXFP4, NVFP4),
 against the fp64 oracle: full and partly filled rows, one row per block and
 grid-stride (fewer blocks than rows), odd row counts."""
-import numpy as np
 import pytest
 
 import rmsnorm_fwd_gb300 as rn

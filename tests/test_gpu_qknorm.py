@@ -10,7 +10,7 @@ import oracle
 import rmsnorm_fwd_gb300 as rn
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, from_device, to_device
+from _parity import from_device, to_device
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")

@@ -3,7 +3,6 @@ staged kernel (the row copies withheld, a flag nothing sets) and of the
 grid variant's barrier (one block's arrival withheld).  Every wait runs out
 after a short limit; the kernel must record RMSNORM_ERR_DEVICE_TIMEOUT in
 the status word, leave y untouched, and leave the context usable."""
-import numpy as np
 import pytest
 
 import rmsnorm_fwd_gb300 as rn
