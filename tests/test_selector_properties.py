@@ -74,3 +74,72 @@ def test_host_mapped_plans_validate(seed):
             continue
         check_plan(p, dt, rows, hidden, rn.EPI_PLAIN, x, y)
         assert p.grid <= max(p0.grid, 2 * SMS)
+
+
+FIELDS = ("variant", "grid", "block_threads", "stages", "smem_bytes", "kernel_index",
+          "threads_per_row", "rows_per_block")
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_validator_accepts_no_plan_that_breaks_its_body(seed):
+    """Mutate one or two fields of the selector's plans at random: whatever
+    rmsnorm_validate_plan_epilogue still accepts launches a body that covers
+    the row with the block size its kernel allows (the checks a launch
+    relies on to stay inside its buffers and its resources)."""
+    rng = np.random.default_rng(1000 + seed)
+    ks = rn.kernels()
+    accepted = 0
+    for dt, rows, hidden, epi, xoff, yoff in random_cases(300, 200 + seed):
+        x, y = A + xoff, 5 * A + yoff
+        rc, p0 = rn.rmsnorm_plan_epilogue_status(x, 3 * A, y, rows, hidden, dt, epi, SMS, OPTIN)
+        if rc != rn.OK:
+            continue
+        for _ in range(12):
+            d = p0.as_dict()
+            for f in rng.choice(FIELDS, size=int(rng.integers(1, 3)), replace=False):
+                if f == "kernel_index":
+                    d[f] = int(rng.integers(-2, len(ks) + 2))
+                elif f == "variant":
+                    d[f] = int(rng.integers(-1, 9))
+                elif f == "block_threads":
+                    d[f] = int(rng.choice([0, 16, 32, 48, 64, 96, 128, 256, 288, 512, 640,
+                                           1024, 1056, 2048]))
+                elif f == "stages":
+                    d[f] = int(rng.integers(-1, 10))
+                else:
+                    d[f] = int(rng.choice([-1, 0, 1, 2, 8, SMS, 2 * SMS, rows, rows * 4,
+                                           rows + 1, 1 << 20]))
+            p = rn.Plan(**d)
+            if rn.rmsnorm_validate_plan_epilogue(p, x, 3 * A, y, rows, hidden, dt, epi, SMS,
+                                                 OPTIN) != rn.OK:
+                continue
+            accepted += 1
+            k = ks[p.kernel_index]
+            assert k["dtype"] == dt and k["epilogue"] == epi
+            assert p.grid >= 1 and 32 <= p.block_threads <= 1024 and p.block_threads % 32 == 0
+            row_bytes = hidden * ES[dt]
+            v = k["variant"]
+            assert p.variant == v or (v == rn.VARIANT_CTA_PER_ROW and
+                                      p.variant == rn.VARIANT_PERSISTENT)
+            if v == rn.VARIANT_WARP_PER_ROW:
+                assert p.block_threads == k["block"]
+                assert k["tpr"] * k["nv"] * k["vec_bytes"] >= row_bytes
+            elif v == rn.VARIANT_CTA_PER_ROW:
+                assert p.block_threads <= k["block"]
+                if k["nv"] > 0:
+                    assert p.block_threads * k["nv"] * k["vec_bytes"] >= row_bytes
+                if k["tpr"] > 0:
+                    assert p.block_threads == k["tpr"]
+            elif v == rn.VARIANT_CLUSTER:
+                assert p.stages in (2, 4, 8) and p.grid == rows * p.stages
+                assert p.block_threads <= k["block"]
+                assert p.block_threads * k["nv"] * k["vec_bytes"] * p.stages >= row_bytes
+            elif v == rn.VARIANT_GRID:
+                assert rows <= 64 and p.grid <= 2 * SMS and p.rows_per_block == rows
+            elif v == rn.VARIANT_STAGED:
+                assert 1 <= p.grid <= rows and p.smem_bytes <= OPTIN and p.stages >= 1
+            if v not in (rn.VARIANT_STAGED, rn.VARIANT_CLUSTER):
+                assert p.stages == 0
+            if v != rn.VARIANT_STAGED:
+                assert p.smem_bytes == 0
+    assert accepted > 100
