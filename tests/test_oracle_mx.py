@@ -344,3 +344,35 @@ def test_nvfp4_scale_and_error_bound():
         oracle.nvfp4_quantize(np.zeros((1, 24)), 1.0)
     with pytest.raises(ValueError):
         oracle.nvfp4_quantize(np.zeros((1, 16)), 0.0)
+
+
+def test_nvfp4_extreme_global_scales_saturate_or_vanish():
+    """Closed forms at the per-tensor scales the GPU tests use outside the
+    flush-to-zero range: with g = 1e-37 every nonzero block's max / (6 g) is
+    far above 448, so the scale saturates to 448 (code 0x7E) and each element
+    becomes E2M1(v / (448 g)): +-6 for |v / (448 g)| >= 5, the rest follow the
+    E2M1 grid; with g = 1e31 max / (6 g) is far below E4M3's smallest
+    subnormal half-step (2^-10), so the scale is 0 and every code is a zero of
+    the element's sign."""
+    rng = np.random.default_rng(21)
+    v = rng.standard_normal((8, 64))
+    v[3, 16:32] = 0.0
+    codes, scales = oracle.nvfp4_quantize(v, 1e-37)
+    q = _e2m1(_unpack(codes, 64)).reshape(8, 64)
+    for r in range(8):
+        for b in range(4):
+            blk = v[r, 16 * b:16 * (b + 1)]
+            if not blk.any():
+                assert scales[r, b] == 0 and not q[r, 16 * b:16 * (b + 1)].any()
+                continue
+            assert scales[r, b] == 0x7E                     # 448
+            t = np.abs(blk) / (448 * 1e-37)
+            assert (np.abs(q[r, 16 * b:16 * (b + 1)])[t >= 5] == 6).all()
+            assert np.array_equal(np.sign(q[r, 16 * b:16 * (b + 1)])[t >= 5],
+                                  np.sign(blk)[t >= 5])
+    codes, scales = oracle.nvfp4_quantize(v, 1e31)
+    assert not scales.any()
+    q = _e2m1(_unpack(codes, 64)).reshape(8, 64)
+    assert not q.any()
+    nz = v != 0
+    assert np.array_equal(np.signbit(q)[nz], np.signbit(v)[nz])
