@@ -376,3 +376,21 @@ def test_nvfp4_extreme_global_scales_saturate_or_vanish():
     assert not q.any()
     nz = v != 0
     assert np.array_equal(np.signbit(q)[nz], np.signbit(v)[nz])
+
+
+def test_zero_weight_codes_carry_the_ieee_sign_of_the_product():
+    """(x * r) * (w + offset) with w = -0: offset -0 keeps w = -0, so the
+    zero code's sign is the opposite of x's; offset +0 makes w + 0 = +0, so
+    it is x's own sign (MXFP8 bytes 0x80 / 0x00, E2M1 nibbles 0x8 / 0x0)."""
+    x, w = inputs.random_case(4, 64, "bf16", seed=8)
+    w = w.copy()
+    w[:32] = 0x8000                                     # bf16 -0.0
+    xs = np.signbit(oracle.widen(x, "bf16"))[:, :32]
+    for bias, flip in ((-0.0, True), (0.0, False)):
+        c8, _ = oracle.rmsnorm_mxfp8(x, w, bias, 1e-6, "bf16")
+        assert np.array_equal(c8[:, :32] == 0x80, xs != flip)
+        assert np.isin(c8[:, :32], (0x00, 0x80)).all()
+        c4, _ = oracle.rmsnorm_fp4(x, w, bias, 1e-6, "bf16", "nvfp4", global_scale=0.01)
+        nib = _unpack(c4, 64)[:, :32]
+        assert np.isin(nib, (0x0, 0x8)).all()
+        assert np.array_equal(nib == 0x8, xs != flip)
