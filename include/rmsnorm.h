@@ -23,10 +23,10 @@
  * stride = hidden elements); weight is [hidden].  x, weight and y share one
  * element type.  All three are DEVICE pointers owned by the caller; the
  * library never frees or retains them.  The only memory the library itself
- * allocates is a 4-byte device status word per device (rmsnorm_create), its
- * host-side context, and, for calls that take the grid variant, a per-call
- * scratch area from the device's stream-ordered memory pool, freed in
- * stream order.
+ * allocates is its per-device context, at rmsnorm_create: a 4-byte device
+ * status word, the grid variant's fixed scratch (status word + fixed
+ * scratch, allocated at create) and host-side state.  No call after
+ * rmsnorm_create allocates device memory.
  *
  * Aliasing.  y == x (exactly in place) is allowed.  Any other overlap between
  * y and x, or between y and weight, is rejected with RMSNORM_ERR_ALIASING.
@@ -70,7 +70,7 @@ typedef enum {
     RMSNORM_ERR_CUDA = 5,               /* a CUDA runtime call or a launch failed */
     RMSNORM_ERR_DEVICE_TIMEOUT = 6,     /* a kernel's bounded wait ran out (device status word) */
     RMSNORM_ERR_MISALIGNED = 7,         /* a forced vector variant got pointers it cannot load */
-    RMSNORM_ERR_UNSUPPORTED_DEVICE = 8, /* current device is not compute capability 10.x */
+    RMSNORM_ERR_UNSUPPORTED_DEVICE = 8, /* current device is not compute capability 10.3 */
     RMSNORM_ERR_VARIANT = 9,            /* forced variant cannot take this shape */
     RMSNORM_ERR_TOO_LARGE = 10          /* beyond the static scratch of rmsnorm_fwd_staged_noalloc */
 } rmsnorm_status_t;
@@ -112,9 +112,13 @@ typedef enum {
      * over all SMs (a cooperative launch of 2 blocks per SM), one grid
      * barrier through global memory between the sums and the scaling
      * (bounded wait; a wait that runs out records RMSNORM_ERR_DEVICE_TIMEOUT).
-     * Per call it takes rows * grid * 4 + 16 bytes of scratch from the
-     * device's stream-ordered memory pool (cudaMallocAsync / cudaFreeAsync
-     * on `stream`).  Plain output only; at most 64 rows. */
+     * Its counters and partial sums live in the context's fixed scratch,
+     * shared by every grid-variant call on the device: each such call makes
+     * its stream wait for the previous one (an event the context records
+     * after each), so calls on different streams take turns.  Calls captured
+     * into a CUDA graph are ordered by the graph alone: a replay must not
+     * overlap another grid-variant call.  Plain output only; at most 64
+     * rows. */
     RMSNORM_VARIANT_GRID = 7
 } rmsnorm_variant_t;
 
@@ -135,13 +139,18 @@ typedef struct {
 
 /* Create (or add a reference to) the context of the CURRENT CUDA device:
  * queries SM count, shared memory limits and compute capability (must be
- * 10.x; the kernels are built for sm_103a), allocates the device status word.
+ * 10.3; the kernels are built for sm_103a), and allocates everything the
+ * library will ever hold on the device: the device status word and the grid
+ * variant's fixed scratch (16 + 64 rows * 2 blocks per SM * SMs * 8 bytes,
+ * about 156 KB on a 152-SM GB300), both zeroed.  It waits for those zeroing
+ * copies (the legacy default stream), so call it outside any stream capture.
  * Idempotent and reference counted.  Returns RMSNORM_OK,
  * RMSNORM_ERR_UNSUPPORTED_DEVICE or RMSNORM_ERR_CUDA. */
 int rmsnorm_create(void);
 
 /* Drop one reference to the current device's context; at zero the status
- * word is freed.  Returns RMSNORM_ERR_NOT_INITIALIZED if there is none. */
+ * word and the scratch are freed.  Returns RMSNORM_ERR_NOT_INITIALIZED if
+ * there is none. */
 int rmsnorm_destroy(void);
 
 /* y = RMSNorm(x) * weight, per row (see the top of this file).

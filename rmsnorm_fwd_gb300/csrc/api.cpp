@@ -62,10 +62,24 @@ struct DeviceCtx {
     int smem_optin = 0;
     int *status = nullptr; // device word
     HostPipe *pipe = nullptr;
+    // Grid variant: its counters and partial sums, allocated once (the
+    // counters are left at zero by every launch), and the event its last
+    // launch recorded, which the next one's stream waits on.
+    void *grid_scratch = nullptr;
+    cudaEvent_t grid_done = nullptr;
 };
 
 std::mutex g_mu;
 DeviceCtx g_ctx[kMaxDevices];
+std::mutex g_grid_mu[kMaxDevices]; // one grid-variant launch enqueues at a time per device
+
+// Bytes of the grid variant's scratch on a device with `sms` SMs.
+size_t grid_scratch_bytes(int sms)
+{
+    return static_cast<size_t>(kGridCounterBytes) +
+           static_cast<size_t>(kGridMaxRows) * static_cast<size_t>(sms) *
+               static_cast<size_t>(kGridBlocksPerSm) * sizeof(double);
+}
 std::mutex g_pipe_mu[kMaxDevices]; // one host-buffer call enqueues at a time per device
 
 void destroy_pipe(HostPipe *hp)
@@ -215,7 +229,8 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
     if (rc != RMSNORM_OK)
         return rc;
     DeviceCtx ctx;
-    rc = current_ctx(&ctx, nullptr);
+    int dev = 0;
+    rc = current_ctx(&ctx, &dev);
     if (rc != RMSNORM_OK)
         return rc;
     if (rows == 0) {
@@ -262,19 +277,25 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
                      p.variant, p.vec_bytes, p.threads_per_row, p.vecs_per_thread,
                      p.block_threads, p.grid, p.stages, p.smem_bytes, p.kernel_index);
     if (d.variant == RMSNORM_VARIANT_GRID) {
-        // Per-call scratch from the stream-ordered pool: counters and rows *
-        // grid partial sums, zeroed; freed in stream order after the
-        // kernel, so concurrent calls on other streams never share it.
-        const size_t bytes = static_cast<size_t>(kGridCounterBytes) +
-                             static_cast<size_t>(rows) * static_cast<size_t>(p.grid) * sizeof(float);
-        void *scratch = nullptr;
-        if (cudaMallocAsync(&scratch, bytes, a.stream) != cudaSuccess)
+        // The context's scratch, shared by every grid-variant call on the
+        // device: each launch waits for the previous one (its event) and
+        // records its own, so calls on different streams take turns.  A
+        // launch being captured into a CUDA graph is ordered by the graph's
+        // own dependencies instead (an event recorded outside a capture
+        // cannot be waited on inside it).
+        if (static_cast<size_t>(kGridCounterBytes) +
+                static_cast<size_t>(rows) * static_cast<size_t>(p.grid) * sizeof(double) >
+            grid_scratch_bytes(ctx.sm_count))
+            return RMSNORM_ERR_INVALID_ARG; // validate_plan bounds rows and grid: unreachable
+        std::lock_guard<std::mutex> lk(g_grid_mu[dev]);
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(a.stream, &cs) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
-        a.scratch = scratch;
-        const bool ok = cudaMemsetAsync(scratch, 0, bytes, a.stream) == cudaSuccess &&
-                        d.launch(p, a) == cudaSuccess;
-        const bool freed = cudaFreeAsync(scratch, a.stream) == cudaSuccess;
-        if (!ok || !freed)
+        const bool capturing = cs != cudaStreamCaptureStatusNone;
+        a.scratch = ctx.grid_scratch;
+        if ((!capturing && cudaStreamWaitEvent(a.stream, ctx.grid_done, 0) != cudaSuccess) ||
+            d.launch(p, a) != cudaSuccess ||
+            (!capturing && cudaEventRecord(ctx.grid_done, a.stream) != cudaSuccess))
             return RMSNORM_ERR_CUDA;
     } else if (d.launch(p, a) != cudaSuccess) {
         return RMSNORM_ERR_CUDA;
@@ -322,13 +343,26 @@ int rmsnorm_create(void)
     // The kernels are compiled for sm_103a only.
     if (major != 10 || minor != 3)
         return RMSNORM_ERR_UNSUPPORTED_DEVICE;
+    // Everything the context owns on the device, allocated here and only
+    // here: the status word and the grid variant's scratch (zeroed: its
+    // counters start at zero).
     int *status = nullptr;
-    if (cudaMalloc(&status, sizeof(int)) != cudaSuccess)
-        return RMSNORM_ERR_CUDA;
-    if (cudaMemset(status, 0, sizeof(int)) != cudaSuccess) {
+    void *scratch = nullptr;
+    cudaEvent_t grid_done = nullptr;
+    auto fail = [&] {
         cudaFree(status);
+        cudaFree(scratch);
+        if (grid_done)
+            cudaEventDestroy(grid_done);
         return RMSNORM_ERR_CUDA;
-    }
+    };
+    const size_t sbytes = grid_scratch_bytes(sms);
+    if (cudaMalloc(&status, sizeof(int)) != cudaSuccess ||
+        cudaMemset(status, 0, sizeof(int)) != cudaSuccess ||
+        cudaMalloc(&scratch, sbytes) != cudaSuccess ||
+        cudaMemset(scratch, 0, sbytes) != cudaSuccess ||
+        cudaEventCreateWithFlags(&grid_done, cudaEventDisableTiming) != cudaSuccess)
+        return fail();
     int n = 0;
     const KernelDesc *t = kernel_table(&n);
     for (int i = 0; i < n; ++i) {
@@ -338,14 +372,18 @@ int rmsnorm_create(void)
                 cudaSuccess ||
             (t[i].func_xw != nullptr &&
              cudaFuncSetAttribute(t[i].func_xw, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  optin) != cudaSuccess)) {
-            cudaFree(status);
-            return RMSNORM_ERR_CUDA;
-        }
+                                  optin) != cudaSuccess))
+            return fail();
     }
+    // The zeroed words are in place before any launch reads them (the
+    // memsets run on the legacy stream; launches may use non-blocking ones).
+    if (cudaStreamSynchronize(cudaStreamLegacy) != cudaSuccess)
+        return fail();
     c.sm_count = sms;
     c.smem_optin = optin;
     c.status = status;
+    c.grid_scratch = scratch;
+    c.grid_done = grid_done;
     c.refs = 1;
     return RMSNORM_OK;
 }
@@ -363,7 +401,10 @@ int rmsnorm_destroy(void)
         return RMSNORM_ERR_NOT_INITIALIZED;
     if (--c.refs == 0) {
         std::lock_guard<std::mutex> plk(g_pipe_mu[dev]);
+        std::lock_guard<std::mutex> glk(g_grid_mu[dev]);
         cudaFree(c.status);
+        cudaFree(c.grid_scratch);
+        cudaEventDestroy(c.grid_done);
         destroy_pipe(c.pipe);
         c = DeviceCtx{};
     }

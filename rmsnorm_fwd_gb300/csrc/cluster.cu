@@ -47,14 +47,27 @@ __device__ inline uint32_t cluster_size()
     return n;
 }
 
-// The float at shared address `local` in block `rank` of this cluster.
-__device__ inline float ld_peer(uint32_t local, uint32_t rank)
+// The two floats at shared address `local` in block `rank` of this cluster.
+__device__ inline float2 ld_peer2(uint32_t local, uint32_t rank)
 {
     uint32_t remote;
-    float v;
+    float2 v;
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];"
+                 : "=f"(v.x), "=f"(v.y)
+                 : "r"(remote)
+                 : "memory");
     return v;
+}
+
+// Butterfly sum of a double over the 32 lanes (every lane gets the total,
+// formed in the same order in every block).
+__device__ inline double warp_sum_f64(double d)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, off, 32);
+    return d;
 }
 
 template <int VB>
@@ -70,13 +83,13 @@ __device__ inline void vzero(Vec<VB> &v)
 // vectors c * S + t + k * blockDim.x, k < NV.  blockDim.x * NV >= S.
 template <int DT, int VB, int NV>
 __global__ void __launch_bounds__(1024)
-cluster_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+cluster_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                     int32_t hidden, float eps)
 {
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
     __shared__ float part[32];
-    __shared__ float block_total;
+    __shared__ __align__(8) float2 block_total; // (sum of (k x)^2 over the slice, k)
 
     pdl_begin();
     const uint32_t C = cluster_size();
@@ -114,22 +127,69 @@ cluster_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
     if (lane == 0)
         part[warp] = s;
     __syncthreads();
-    if (warp == 0) {
-        float b = lane < nwarps ? part[lane] : 0.f;
-        b = group_allreduce<32>(b);
-        if (lane == 0)
-            block_total = b;
+    float bt = group_allreduce<32>(lane < nwarps ? part[lane] : 0.f); // block-uniform
+    float bk = 1.f;
+    if constexpr (kRangeGuard<DT>) {
+        // Range guard (device_common.cuh) on this block's slice: its sum
+        // formed again from k x when the plain one left fp32's trusted range.
+        if (sum_needs_rescale(bt, eps)) {
+            bk = rescale_k(bt);
+            float sk = 0.f;
+#pragma unroll
+            for (int k = 0; k < NV; ++k)
+                sk = sumsq_k<DT, VB>(xv[k], bk, sk);
+            sk = group_allreduce<32>(sk);
+            __syncthreads(); // every warp has read part[] above
+            if (lane == 0)
+                part[warp] = sk;
+            __syncthreads();
+            bt = group_allreduce<32>(lane < nwarps ? part[lane] : 0.f);
+        }
     }
+    if (t == 0)
+        block_total = make_float2(bt, bk);
     // Every block's total is visible to the whole cluster past this barrier.
     cluster_sync_all();
-    float tot = static_cast<uint32_t>(lane) < C ? ld_peer(cta_smem_addr(&block_total), lane) : 0.f;
-    tot = group_allreduce<32>(tot);
+    const float2 pk = static_cast<uint32_t>(lane) < C ? ld_peer2(cta_smem_addr(&block_total), lane)
+                                                      : make_float2(0.f, 1.f);
+    const float tot = group_allreduce<32>(pk.x);
     // No block leaves (or lets its shared memory go) before every peer has
     // read its total: arrive now, wait at the end.  Relaxed: the peer reads
     // above have completed (their values are used), and nothing written
     // here needs to be seen through this barrier.
     asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
-    const float r = row_factor(tot, static_cast<float>(hidden), eps);
+    const float nf = static_cast<float>(hidden);
+    const float r = row_factor(tot, nf, eps);
+    if constexpr (kRangeGuard<DT>) {
+        // A block rescaled its slice, or the fp32 total left the trusted
+        // range: the total again in binary64 from (Sk / k^2) of every block,
+        // in the same order in every block (exact scalings by powers of two).
+        if (__any_sync(0xFFFFFFFFu, pk.y != 1.f) || sum_needs_rescale(tot, eps)) {
+            const double kd = pk.y;
+            const double D = warp_sum_f64(static_cast<double>(pk.x) / (kd * kd));
+            float Sk, kk;
+            wide_total(D, eps, Sk, kk);
+            const Factor f = rescaled_factor(Sk, kk, nf, eps);
+            // The slice again from memory (nothing of it is written yet),
+            // one vector at a time, so the registers above are not kept
+            // alive for this rare path.
+#pragma unroll 1
+            for (int k = 0; k < NV; ++k) {
+                const int v = v0 + t + k * tpr;
+                if (live_row && v < v1) {
+                    Vec<VB> xk, wk, o;
+                    ld_stream<0>(xk, xr + static_cast<int64_t>(v) * VB);
+                    ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                    if (f.up)
+                        scale_up<DT, VB>(xk);
+                    scale<DT, VB>(o, xk, wk, f.r);
+                    st_stream<1>(yr + static_cast<int64_t>(v) * VB, o);
+                }
+            }
+            asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+            return;
+        }
+    }
 #pragma unroll
     for (int k = 0; k < NV; ++k)
         reuse_barrier(xv[k]);

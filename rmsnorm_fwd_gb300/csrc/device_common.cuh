@@ -211,6 +211,116 @@ __device__ inline void scale(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB> &wv,
     }
 }
 
+// ---------------------------------------------------------------- range guard
+//
+// The squares are summed in fp32 ("CuTeDSL at Perplexity", section "QK
+// Norm"), but bf16 and f32 elements span fp32's whole exponent range: the sum
+// S overflows to +inf once |x| reaches about 2^64, and squares below 2^-126
+// lose bits (below 2^-150 all of them).  Either way the plain factor is
+// wrong where the definition (mean of the squares, plus eps, reciprocal
+// square root, in exact arithmetic) is not.  f16 elements cannot get there
+// (their squares lie in [2^-48, 2^32]), so only bf16 and f32 bodies carry
+// the guard.
+//
+// The guard is one compare per row.  S is trusted when it is finite and
+// either at least 2^-100 (the squares lost to underflow are then at most
+// hidden * 2^-150 <= 2^-124, below one part in 2^24 of S for rows up to 2^26
+// elements) or eps >= 2^-120 (eps then outweighs what underflow lost by 2^29
+// or more).  Otherwise the row's sum is formed again from k * x, a power of
+// two: k = 2^-80 after an overflow (the rescaled squares stay below 2^96 and
+// their sum below 2^122; squares that now underflow are below 2^10 against
+// S >= 2^128), k = 2^100 after an underflow (every nonzero square of a bf16 or f32
+// value becomes at least 2^-98, and a sum below 2^-100 becomes one below
+// 2^100).  k * x is exact for every element that can matter.  A row holding
+// an Inf or a NaN keeps its +inf or NaN sum: the plain factor is then what
+// IEEE arithmetic gives (0 for +inf), as in the definition.
+template <int DT>
+constexpr bool kRangeGuard = DT != RMSNORM_F16;
+
+__device__ inline bool sum_needs_rescale(float S, float eps)
+{
+    return S > 0x1.fffffep127f || (S < 0x1p-100f && eps < 0x1p-120f);
+}
+
+// The power of two the redo scales x by.
+__device__ inline float rescale_k(float S)
+{
+    return S > 0x1.fffffep127f ? 0x1p-80f : 0x1p100f;
+}
+
+// Sum of the squares of k * x over one vector, accumulated into s.
+template <int DT, int VB>
+__device__ inline float sumsq_k(const Vec<VB> &v, float k, float s)
+{
+#pragma unroll
+    for (int i = 0; i < Vec<VB>::kWords; ++i) {
+        float a, b = 0.f;
+        Elem<DT>::widen(v.w[i], a, b);
+        a *= k;
+        s = fmaf(a, a, s);
+        if (Elem<DT>::kPerWord == 2) {
+            b *= k;
+            s = fmaf(b, b, s);
+        }
+    }
+    return s;
+}
+
+// x <- 2^100 * x for one vector, exact (used only on rows whose elements
+// are all below 2^-100 in magnitude, so nothing overflows).
+template <int DT, int VB>
+__device__ inline void scale_up(Vec<VB> &v)
+{
+#pragma unroll
+    for (int i = 0; i < Vec<VB>::kWords; ++i) {
+        float a, b = 0.f;
+        Elem<DT>::widen(v.w[i], a, b);
+        v.w[i] = Elem<DT>::narrow(a * 0x1p100f, b * 0x1p100f);
+    }
+}
+
+// The factor from the rescaled sum Sk = sum (k x)^2:
+//   r = 1 / sqrt(Sk / (k^2 n) + eps) = k * rsqrt(Sk / n + (eps * k) * k),
+// with (eps * k) * k exact where it matters (on the 2^100 side eps < 2^-120,
+// so it stays below 2^80; on the 2^-80 side it is exact unless it falls
+// below 2^-126, where it is negligible against Sk / n >= 2^-58).
+// k * rho is exact while it is a normal float.  It would overflow only on the
+// 2^100 side with rho >= 2^27, i.e. a row whose RMS with eps is below 2^-127
+// (eps = 0 and every element tiny); then `up` is set, r = rho, and the caller
+// multiplies x by 2^100 before scaling (scale_up; exact there), so that
+// (x * 2^100) * rho = x * r without leaving the float range.  An all-zero
+// row with eps = 0 gives rho = inf, up, and 0 * inf = NaN, as the definition.
+struct Factor {
+    float r;
+    bool up;
+};
+__device__ inline Factor rescaled_factor(float Sk, float k, float n, float eps)
+{
+    const float rho = rsqrtf(Sk / n + (eps * k) * k);
+    Factor f;
+    f.up = k > 1.f && !(rho < 0x1p27f);
+    f.r = f.up ? rho : k * rho;
+    return f;
+}
+
+// For bodies whose row total is combined from several partial sums held in
+// binary64 (thread-block clusters, the grid variant): the total's (Sk, k)
+// form for rescaled_factor -- k = 1 when it fits fp32's trusted range, else
+// the power of two sum_needs_rescale would have chosen.  D * k^2 is exact.
+__device__ inline void wide_total(double D, float eps, float &Sk, float &k)
+{
+    if (D > 0x1.fffffep127) {
+        k = 0x1p-80f;
+        Sk = static_cast<float>(D * 0x1p-160);
+    } else if (D < 0x1p-100 && eps < 0x1p-120f) {
+        k = 0x1p100f;
+        Sk = static_cast<float>(D * 0x1p200);
+    } else {
+        k = 1.f;
+        Sk = static_cast<float>(D);
+    }
+}
+
 // ---------------------------------------------------------------- epilogues
 
 // out = (x * r) * (w + bias) per element -- the weight offset WEIGHT_BIAS of
@@ -564,10 +674,12 @@ __device__ inline float block_max(float m)
 // Every lane of the warp must call this (the shuffles span the full warp);
 // `live` says whether this lane's vector is part of the row.  The lane
 // holding the first vector of a block (`leader`) stores the scale byte.
+// `up`: the caller has multiplied the registers xv by 2^100 (range guard,
+// rescaled_factor); the redo applies the same factor to x read again.
 template <int DT, int VB, int Q, bool XW>
 __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void *xp,
                                const void *wp, float r, const QParams &qp, bool live, bool leader,
-                               void *q, uint8_t *scale)
+                               void *q, uint8_t *scale, bool up = false)
 {
     static_assert(!XW || DT != RMSNORM_F32, "exact products: 16-bit elements only");
     using G = QGeo<DT, VB, Q>;
@@ -596,6 +708,8 @@ __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void 
                 if (live) {
                     xa = *static_cast<const Vec<VB> *>(xp);
                     wa = *static_cast<const Vec<VB> *>(wp);
+                    if (up)
+                        scale_up<DT, VB>(xa);
                 } else {
 #pragma unroll
                     for (int k = 0; k < Vec<VB>::kWords; ++k)

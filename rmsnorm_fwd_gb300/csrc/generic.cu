@@ -18,11 +18,12 @@ namespace {
 // EPI: RMSNORM_EPI_PLAIN, or RMSNORM_EPI_BIAS (the weight plus `bias`).
 template <int DT, int EPI>
 __global__ void __launch_bounds__(1024)
-generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+generic_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                     int32_t hidden, float eps, float bias)
 {
     using E = Elem<DT>;
     __shared__ float part[2][32];
+    __shared__ float rare[32]; // the range guard's own reduction
     pdl_begin();
     const int t = threadIdx.x;
     const int lane = t & 31;
@@ -46,9 +47,29 @@ generic_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void
         __syncthreads();
         float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
         tot = group_allreduce<32>(tot);
-        const float r = row_factor(tot, n, eps);
+        float r = row_factor(tot, n, eps);
+        float pre = 1.f; // 2^100 when the range guard scales x up (exact)
+        if constexpr (kRangeGuard<DT>) {
+            if (sum_needs_rescale(tot, eps)) { // block-uniform; a third pass over the row
+                const float kk = rescale_k(tot);
+                float sk = 0.f;
+                for (int j = t; j < hidden; j += blockDim.x) {
+                    const float v = E::widen1(x, base + j) * kk;
+                    sk = fmaf(v, v, sk);
+                }
+                sk = group_allreduce<32>(sk);
+                if (lane == 0)
+                    rare[warp] = sk;
+                __syncthreads();
+                sk = group_allreduce<32>(lane < nwarps ? rare[lane] : 0.f);
+                __syncthreads();
+                const Factor f = rescaled_factor(sk, kk, n, eps);
+                r = f.r;
+                pre = f.up ? 0x1p100f : 1.f;
+            }
+        }
         for (int j = t; j < hidden; j += blockDim.x) {
-            const float v = E::widen1(x, base + j);
+            const float v = E::widen1(x, base + j) * pre;
             if constexpr (EPI == RMSNORM_EPI_BIAS)
                 E::store1(y, base + j, (v * r) * (E::widen1(w, j) + bias));
             else

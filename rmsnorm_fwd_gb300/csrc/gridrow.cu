@@ -19,9 +19,11 @@
 //            (acquire).  A wait that runs out records RMSNORM_ERR_DEVICE_TIMEOUT
 //            in the status word and its block skips phase 2 (y is left as it
 //            was); it never hangs.
-//   Phase 2: every block sums the G partials of a row in the same order, so
-//            every block forms the bit-identical row factor, re-reads its
-//            range of x (an L2 hit: phase 1 just read it) and writes y.
+//   Phase 2: every block sums the partials of a row -- those of the blocks
+//            whose ranges meet it, all written in phase 1 of this call -- in
+//            the same order, so every block forms the bit-identical row
+//            factor, re-reads its range of x (an L2 hit: phase 1 just read
+//            it) and writes y.
 //   Exit:    each block adds one to a departure counter; the last block to
 //            leave sets both counters back to zero for the next call.
 #include "internal.h"
@@ -64,10 +66,10 @@ __device__ inline uint32_t add_acq_rel(uint32_t *p, uint32_t v)
     return old;
 }
 
-__device__ inline float ld_l2(const float *p)
+__device__ inline double ld_l2(const double *p)
 {
-    float v;
-    asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+    double v;
+    asm volatile("ld.global.cg.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
     return v;
 }
 
@@ -93,10 +95,29 @@ __device__ inline float block_sum(float s, float *part)
     return tot;
 }
 
+// Block-wide sum of doubles (every thread gets it, formed in the same order
+// in every block); `part` holds one double per warp.
+__device__ inline double block_sum_f64(double d, double *part)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        d += __shfl_xor_sync(0xFFFFFFFFu, d, off, 32);
+    if (lane == 0)
+        part[warp] = d;
+    __syncthreads();
+    double tot = lane < nwarps ? part[lane] : 0.0;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1)
+        tot += __shfl_xor_sync(0xFFFFFFFFu, tot, off, 32);
+    __syncthreads();
+    return tot;
+}
+
 template <int DT>
 __global__ void __launch_bounds__(512, 2)
-grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
-                 int32_t hidden, float eps, float *partial, uint32_t *counters, int *status,
+grid_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
+                 int32_t hidden, float eps, double *partial, uint32_t *counters, int *status,
                  uint64_t limit_ns, uint32_t flags)
 {
     using E = Elem<DT>;
@@ -104,6 +125,7 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     constexpr int VPE = VB / E::kSize;
     constexpr int U = 4;
     __shared__ float part[32];
+    __shared__ double part64[32];
     __shared__ int passed;
 
     const int G = gridDim.x;
@@ -144,8 +166,34 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                 s = sumsq<DT, VB>(xv[u], s);
         }
         s = block_sum(s, part);
+        double sd = s;
+        if constexpr (kRangeGuard<DT>) {
+            // Range guard (device_common.cuh) on this block's part of the
+            // row: formed again from k x, read again (an L2 hit), and kept
+            // exactly as Sk / k^2 in binary64.
+            if (sum_needs_rescale(s, eps)) {
+                const float kk = rescale_k(s);
+                float sk = 0.f;
+                for (int v = v0 + t; v < v1; v += U * tpr) {
+                    Vec<VB> xv[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int vv = v + u * tpr;
+                        if (vv < v1)
+                            ld_stream<0>(xv[u], xr + static_cast<int64_t>(vv) * VB);
+                        else
+                            vzero(xv[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        sk = sumsq_k<DT, VB>(xv[u], kk, sk);
+                }
+                const double kd = kk;
+                sd = static_cast<double>(block_sum(sk, part)) / (kd * kd);
+            }
+        }
         if (t == 0)
-            partial[row * G + b] = s; // (row, block) pairs never touched stay 0
+            partial[row * G + b] = sd;
     }
 
     // ---- grid barrier (counters[0]: arrivals, counters[1]: departures)
@@ -175,10 +223,29 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
     if (passed) {
         const char *wb = static_cast<const char *>(w);
         for (int64_t row = row_lo; row <= row_hi; ++row) {
-            float a = 0.f;
-            for (int i = t; i < G; i += tpr) // the same order in every block
-                a += ld_l2(partial + row * G + i);
-            const float r = row_factor(block_sum(a, part), n, eps);
+            // The partials in the same order in every block: in fp32 (each is
+            // an fp32 sum unless the range guard rescaled it), and again in
+            // binary64 when a partial or the fp32 total is out of fp32's
+            // trusted range (block-uniform).
+            const int b_lo = static_cast<int>(row * nvec / share);
+            const int b_hi = static_cast<int>(min(static_cast<int64_t>(G - 1), ((row + 1) * nvec - 1) / share));
+            double ad = 0.0;
+            for (int i = b_lo + t; i <= b_hi; i += tpr)
+                ad += ld_l2(partial + row * G + i);
+            const float tot = block_sum(static_cast<float>(ad), part);
+            float r = row_factor(tot, n, eps);
+            bool up = false;
+            if constexpr (kRangeGuard<DT>) {
+                const float af = static_cast<float>(ad);
+                const bool wide = static_cast<double>(af) != ad || sum_needs_rescale(tot, eps);
+                if (__syncthreads_or(wide)) {
+                    float Sk, kk;
+                    wide_total(block_sum_f64(ad, part64), eps, Sk, kk);
+                    const Factor f = rescaled_factor(Sk, kk, n, eps);
+                    r = f.r;
+                    up = f.up;
+                }
+            }
             const int v0 = static_cast<int>(max(f0, row * nvec) - row * nvec);
             const int v1 = static_cast<int>(min(f1, (row + 1) * nvec) - row * nvec);
             const char *xr = static_cast<const char *>(x) + row * row_bytes;
@@ -197,6 +264,8 @@ grid_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                 for (int u = 0; u < U; ++u) {
                     const int vv = v + u * tpr;
                     if (vv < v1) {
+                        if (up)
+                            scale_up<DT, VB>(xv[u]);
                         Vec<VB> o;
                         scale<DT, VB>(o, xv[u], wv[u], r);
                         st_stream<1>(yr + static_cast<int64_t>(vv) * VB, o);
@@ -228,9 +297,9 @@ cudaError_t launch_grid(const rmsnorm_plan_t &p, const LaunchArgs &a)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // scratch (zeroed by the caller): two counters, then rows * G partials
+    // scratch: two counters (zero between calls), then rows * G partials
     uint32_t *counters = static_cast<uint32_t *>(a.scratch);
-    float *partial = reinterpret_cast<float *>(static_cast<char *>(a.scratch) + kGridCounterBytes);
+    double *partial = reinterpret_cast<double *>(static_cast<char *>(a.scratch) + kGridCounterBytes);
     const cudaError_t err =
         cudaLaunchKernelEx(&cfg, grid_rows_kernel<DT>, a.x, a.w, a.y, a.rows, a.hidden, a.eps,
                            partial, counters, a.status, a.wait_limit_ns, a.flags);

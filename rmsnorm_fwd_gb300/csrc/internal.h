@@ -120,10 +120,10 @@ const KernelDesc *cluster_kernels(int *n);
 const KernelDesc *grid_kernels(int *n);
 
 // Grid variant scratch: two 32-bit counters padded to 16 bytes, then
-// rows * grid floats.
+// rows * grid partial sums in binary64.
 constexpr int64_t kGridCounterBytes = 16;
 constexpr int kGridBlocksPerSm = 2;  // 512-thread blocks, <= 64 registers
-constexpr int64_t kGridMaxRows = 64; // bounds the scratch: rows * grid floats
+constexpr int64_t kGridMaxRows = 64; // bounds the scratch: rows * grid doubles
 const KernelDesc *generic_kernels(int *n);
 
 const KernelDesc *kernel_table(int *n);

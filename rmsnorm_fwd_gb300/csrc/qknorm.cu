@@ -113,6 +113,45 @@ qk_norm_kernel(void *q, void *k, const void *__restrict__ qw, const void *__rest
                 s = sumsq_mixed<DT, 16>(xv[r][j], s);
             s = group_allreduce<TPR>(s);
             const float rf = row_factor(s, n, eps);
+            if constexpr (kRangeGuard<DT>) {
+                // Range guard (device_common.cuh), warp-uniform: the groups
+                // of a warp reduce with whole-warp shuffles.  The heads are
+                // done again from memory (none of them is written yet), one
+                // vector at a time, so the registers above are not kept
+                // alive for this rare path.
+                const bool redo = sum_needs_rescale(s, eps);
+                if (__any_sync(0xFFFFFFFFu, redo)) {
+                    const int64_t hrow = base + g + r * GROUPS;
+                    const bool hq = active[r] && static_cast<int>(hrow % heads) < q_heads;
+                    const char *wt = static_cast<const char *>(hq ? qw : kw) + t * 16;
+                    const float kk = rescale_k(s);
+                    float sk = 0.f;
+#pragma unroll 1
+                    for (int j = 0; j < NV; ++j) {
+                        if (active[r] && t + j * TPR < nvec) {
+                            Vec<16> xk;
+                            ld_stream<0>(xk, ht[r] + j * TPR * 16);
+                            sk = sumsq_k<DT, 16>(xk, kk, sk);
+                        }
+                    }
+                    const Factor f = rescaled_factor(group_allreduce<TPR>(sk), kk, n, eps);
+                    const float rr = redo ? f.r : rf;
+                    const bool up = redo && f.up;
+#pragma unroll 1
+                    for (int j = 0; j < NV; ++j) {
+                        if (active[r] && t + j * TPR < nvec) {
+                            Vec<16> xk, wk, o;
+                            ld_stream<0>(xk, ht[r] + j * TPR * 16);
+                            ld_weight(wk, wt + j * TPR * 16);
+                            if (up)
+                                scale_up<DT, 16>(xk);
+                            scale_bias2<DT>(o, xk, wk, rr, bias);
+                            st_stream<0>(ht[r] + j * TPR * 16, o);
+                        }
+                    }
+                    continue;
+                }
+            }
 #pragma unroll
             for (int j = 0; j < NV; ++j)
                 reuse_barrier(xv[r][j]);
@@ -158,9 +197,23 @@ qk_norm_scalar_kernel(void *q, void *k, const void *__restrict__ qw, const void 
             s = fmaf(v, v, s);
         }
         s = group_allreduce<32>(s);
-        const float r = row_factor(s, n, eps);
+        float r = row_factor(s, n, eps);
+        float pre = 1.f; // 2^100 when the range guard scales x up (exact)
+        if constexpr (kRangeGuard<DT>) {
+            if (sum_needs_rescale(s, eps)) { // warp-uniform; a third pass over the head
+                const float kk = rescale_k(s);
+                float sk = 0.f;
+                for (int d = lane; d < head_dim; d += 32) {
+                    const float v = E::widen1(base, off + d) * kk;
+                    sk = fmaf(v, v, sk);
+                }
+                const Factor f = rescaled_factor(group_allreduce<32>(sk), kk, n, eps);
+                r = f.r;
+                pre = f.up ? 0x1p100f : 1.f;
+            }
+        }
         for (int d = lane; d < head_dim; d += 32) {
-            const float v = E::widen1(base, off + d);
+            const float v = E::widen1(base, off + d) * pre;
             E::store1(base, off + d, (v * r) * (E::widen1(w, d) + bias));
         }
     }

@@ -45,6 +45,50 @@ __device__ inline void vzero(Vec<VB> &v)
         v.w[k] = 0u;
 }
 
+// ---------------------------------------------------------------- range guard
+
+// v, hidden from the compiler's value numbering: the range guard's redo
+// recomputes its row pointers from it instead of keeping the main path's
+// alive across the reduction (they are dead there on the main path).
+__device__ inline int64_t opaque(int64_t v)
+{
+    asm volatile("mov.b64 %0, %0;" : "+l"(v));
+    return v;
+}
+
+// Block-wide total of the warp totals `s` for the range guard's redo: one
+// float per warp through its own shared array, with a barrier on each side
+// of the read so it never meets the main reduction's double buffer.
+__device__ inline float block_total_rare(float s, float *sh, int lane, int warp, int nwarps)
+{
+    if (lane == 0)
+        sh[warp] = s;
+    __syncthreads();
+    const float tot = group_allreduce<32>(lane < nwarps ? sh[lane] : 0.f);
+    __syncthreads();
+    return tot;
+}
+
+// The range guard's redo of a row's statistic (device_common.cuh): the sum
+// of the squares of k x, read again from memory one vector at a time (rolled,
+// so the registers holding the row are free meanwhile; nothing of the row is
+// written yet), over the vectors t + j * tpr, j < NV, of this thread.
+template <int DT, int VB, int NV>
+__device__ inline float redo_sumsq(const char *xr, int t, int tpr, int nvec, bool active,
+                                   float k)
+{
+    float sk = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < NV; ++j) {
+        if (active && t + j * tpr < nvec) {
+            Vec<VB> xk;
+            ld_stream<0>(xk, xr + j * tpr * VB);
+            sk = sumsq_k<DT, VB>(xk, k, sk);
+        }
+    }
+    return sk;
+}
+
 // ---------------------------------------------------------------- warp-per-row
 
 // TPR lanes (4..32, power of two) per row, BLOCK/TPR rows per block per
@@ -52,7 +96,7 @@ __device__ inline void vzero(Vec<VB> &v)
 // lane takes part in every shuffle.
 template <int DT, int VB, int TPR, int NV, int BLOCK, int MINB, int CP, int EPI, bool XW = false>
 __global__ void __launch_bounds__(BLOCK, MINB > 0 ? MINB : 1)
-warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                  int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
@@ -109,7 +153,38 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
         for (int k = 0; k < NV; ++k)
             s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<TPR>(s);
-        const float r = row_factor(s, n, eps);
+        const float r0 = row_factor(s, n, eps);
+        float r = r0;
+        bool up = false;
+        if constexpr (kRangeGuard<DT>) {
+            // Range guard, warp-uniform (the groups of a warp reduce with
+            // whole-warp shuffles).  The statistic is formed again from
+            // memory and the row registers are loaded again (scaled up where
+            // the factor needs it), so their old contents are dead here.
+            const bool redo = sum_needs_rescale(s, eps);
+            if (__any_sync(0xFFFFFFFFu, redo)) {
+                const int64_t row2 = opaque(row);
+                const char *xr2 = static_cast<const char *>(x) + row2 * row_bytes + t * VB;
+                const float kk = rescale_k(s);
+                const Factor f = rescaled_factor(
+                    group_allreduce<TPR>(redo_sumsq<DT, VB, NV>(xr2, t, TPR, nvec, active, kk)),
+                    kk, n, eps);
+                if (redo) {
+                    r = f.r;
+                    up = f.up;
+                }
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    if (active && t + k * TPR < nvec) {
+                        ld_stream<0>(xv[k], xr2 + k * TPR * VB);
+                        if (up)
+                            scale_up<DT, VB>(xv[k]);
+                    } else {
+                        vzero(xv[k]);
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int k = 0; k < NV; ++k)
             reuse_barrier(xv[k]);
@@ -127,7 +202,8 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
                     vzero(wk);
                 q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * TPR * VB, wt + k * TPR * VB, r, qp, live,
                                    t % LPB == 0, yr + k * TPR * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB,
+                                   up);
             } else if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -153,7 +229,7 @@ warp_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y
 // compile time (vector offsets become immediates).
 template <int DT, int VB, int NV, int MAXT, int MINB, int CP, int TPRC, int EPI, bool XW = false>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
-cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                 int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
@@ -164,6 +240,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     constexpr int OB = MX ? QGeo<DT, VB, Q>::kCodeBytes : VB;
     constexpr bool W_HELD = NV * VB <= 64 && (NV == 1 || MINB == 0); // as above
     __shared__ float part[2][32];
+    __shared__ float rare[32]; // the range guard's own reduction
 
     pdl_begin();
     const QParams qp = q_params(bias, gscale);
@@ -214,7 +291,36 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
             const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
             s = group_allreduce<32>(tot);
         }
-        const float r = row_factor(s, n, eps);
+        const float r0 = row_factor(s, n, eps);
+        float r = r0;
+        bool up = false;
+        if constexpr (kRangeGuard<DT>) {
+            // Range guard, block-uniform (every warp holds the same s).  The
+            // statistic is formed again from memory and the row registers
+            // are loaded again (scaled up where the factor needs it), so
+            // their old contents are dead here.
+            if (sum_needs_rescale(s, eps)) {
+                const int64_t row2 = opaque(row);
+                const char *xr2 = static_cast<const char *>(x) + row2 * row_bytes + t * VB;
+                const float kk = rescale_k(s);
+                float sk = group_allreduce<32>(redo_sumsq<DT, VB, NV>(xr2, t, tpr, nvec, true, kk));
+                if (TPRC != 32)
+                    sk = block_total_rare(sk, rare, lane, warp, nwarps);
+                const Factor f = rescaled_factor(sk, kk, n, eps);
+                r = f.r;
+                up = f.up;
+#pragma unroll
+                for (int k = 0; k < NV; ++k) {
+                    if (t + k * tpr < nvec) {
+                        ld_stream<0>(xv[k], xr2 + k * stride);
+                        if (up)
+                            scale_up<DT, VB>(xv[k]);
+                    } else {
+                        vzero(xv[k]);
+                    }
+                }
+            }
+        }
 #pragma unroll
         for (int k = 0; k < NV; ++k)
             reuse_barrier(xv[k]);
@@ -232,7 +338,8 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                     vzero(wk);
                 q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * stride, wt + k * stride, r, qp, live,
                                    t % LPB == 0, yr + k * tpr * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB,
+                                   up);
             } else if (t + k * tpr < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -259,7 +366,7 @@ cta_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
 // sees x once and y once.  For rows longer than the register bodies hold.
 template <int DT, int VB, int MAXT, int MINB, int CP, int EPI, bool XW = false>
 __global__ void __launch_bounds__(MAXT, MINB > 0 ? MINB : 1)
-cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                 int32_t hidden, float eps, float bias, uint8_t *scales, float gscale)
 {
     using E = Elem<DT>;
@@ -270,6 +377,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
     constexpr int LPB = QGeo<DT, VB, Q>::kLanes;
     constexpr int OB = QGeo<DT, VB, Q>::kCodeBytes;
     __shared__ float part[2][32];
+    __shared__ float rare[32]; // the range guard's own reduction
 
     pdl_begin();
     const QParams qp = q_params(bias, gscale);
@@ -309,8 +417,34 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
         // Also orders every first-pass read of this row before any write of
         // it (in-place calls).
         __syncthreads();
-        const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
-        const float r = row_factor(group_allreduce<32>(tot), n, eps);
+        const float tot = group_allreduce<32>(lane < nwarps ? part[it & 1][lane] : 0.f);
+        float r = row_factor(tot, n, eps);
+        bool up = false;
+        if constexpr (kRangeGuard<DT>) {
+            if (sum_needs_rescale(tot, eps)) { // block-uniform; a third pass over the row
+                const float kk = rescale_k(tot);
+                float sk = 0.f;
+                for (int v0 = t; v0 < nvec; v0 += U * tpr) {
+                    Vec<VB> xv[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int v = v0 + u * tpr;
+                        if (v < nvec)
+                            ld_stream<0>(xv[u], xr + static_cast<int64_t>(v) * VB);
+                        else
+                            vzero(xv[u]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        sk = sumsq_k<DT, VB>(xv[u], kk, sk);
+                }
+                const Factor f = rescaled_factor(
+                    block_total_rare(group_allreduce<32>(sk), rare, lane, warp, nwarps), kk, n,
+                    eps);
+                r = f.r;
+                up = f.up;
+            }
+        }
 
         if constexpr (MX) {
             // Warp-uniform trip count (the block maximum is a shuffle over
@@ -329,6 +463,8 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                         vzero(xv[u]);
                         vzero(wv[u]);
                     }
+                    if (up)
+                        scale_up<DT, VB>(xv[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -336,7 +472,7 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                     q_store<DT, VB, Q, XW>(xv[u], wv[u], xr + static_cast<int64_t>(v) * VB,
                                        wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
                                        lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
-                                       sr + v / LPB);
+                                       sr + v / LPB, up);
                 }
             }
         } else {
@@ -354,6 +490,8 @@ cta_loop_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y,
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + u * tpr;
                     if (v < nvec) {
+                        if (up)
+                            scale_up<DT, VB>(xv[u]);
                         Vec<VB> o;
                         if constexpr (EPI == RMSNORM_EPI_BIAS)
                             scale_bias<DT, VB>(o, xv[u], wv[u], r, bias);

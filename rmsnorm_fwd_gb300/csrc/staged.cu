@@ -172,7 +172,7 @@ __device__ inline bool wait_warp(uint32_t bar, uint32_t parity, uint64_t limit_n
 template <int DT, bool TMA_STORE, bool BLOCK_STATUS = false, int EPI = RMSNORM_EPI_PLAIN,
           bool XW = false>
 __global__ void __launch_bounds__(32 * 17)
-staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void *y, int64_t rows,
+staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows,
                    int32_t hidden, float eps, int32_t stages, int32_t wpr, int *status,
                    uint64_t limit_ns, uint32_t flags, float bias, uint8_t *scales, float gscale)
 {
@@ -316,7 +316,32 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
             failed_at = k;
             break;
         }
-        const float r = row_factor(acc, n, eps);
+        float r = row_factor(acc, n, eps);
+        bool up = false;
+        if constexpr (kRangeGuard<DT>) {
+            if (sum_needs_rescale(acc, eps)) { // group-uniform: the range guard's redo
+                const float kk = rescale_k(acc);
+                float sk = 0.f;
+                for (int v = gl; v < nvec; v += gsize)
+                    sk = sumsq_k<DT, 16>(*reinterpret_cast<const Vec<16> *>(src + v * 16), kk, sk);
+                sk = group_allreduce<32>(sk);
+                if (wpr > 1) {
+                    // The other half of the double buffer: its last readers
+                    // (the previous row) are past this row's barrier; the
+                    // second barrier keeps the next row's writes after these
+                    // reads.
+                    if (lane == 0)
+                        red[((it + 1) & 1) * 16 + c] = sk;
+                    group_sync(1 + g, gsize);
+                    const int base = ((it + 1) & 1) * 16 + g * wpr;
+                    sk = group_allreduce<32>(lane < wpr ? red[base + lane] : 0.f);
+                    group_sync(1 + g, gsize);
+                }
+                const Factor f = rescaled_factor(sk, kk, n, eps);
+                r = f.r;
+                up = f.up;
+            }
+        }
 
         const int64_t row = blockIdx.x + k * static_cast<int64_t>(gridDim.x);
         char *yr = yb + row * row_bytes;
@@ -324,8 +349,10 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
             unsigned char *dst = slots + static_cast<int64_t>(s) * L.slot_stride;
 #pragma unroll 4
             for (int v = gl; v < nvec; v += gsize) {
-                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
+                Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                if (up)
+                    scale_up<DT, 16>(xv);
                 Vec<16> o;
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
                     scale_bias<DT, 16>(o, xv, wv, r, bias);
@@ -360,6 +387,8 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                 if (live) {
                     xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                     wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                    if (up)
+                        scale_up<DT, 16>(xv);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -368,7 +397,7 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
                 q_store<DT, 16, Q, XW>(xv, wv, src + v * 16, wsm + v * 16, r, qp, live,
                                    lane % G::kLanes == 0,
                                    qr + static_cast<int64_t>(v) * G::kCodeBytes,
-                                   sr + v / G::kLanes);
+                                   sr + v / G::kLanes, up);
             }
             __syncwarp();
             if (lane == 0)
@@ -376,8 +405,10 @@ staged_rows_kernel(const void *__restrict__ x, const void *__restrict__ w, void 
         } else {
 #pragma unroll 4
             for (int v = gl; v < nvec; v += gsize) {
-                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                if (up)
+                    scale_up<DT, 16>(xv);
                 Vec<16> o;
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
                     scale_bias<DT, 16>(o, xv, wv, r, bias);
