@@ -467,9 +467,12 @@ int rmsnorm_test_grid_timeout(const void *x, const void *weight, void *y, int64_
  * set-up with that device current (it looks up the static array's device
  * address and the device's limits); make that first call before any stream
  * capture.  Returns RMSNORM_OK, an argument error as rmsnorm_fwd does,
- * RMSNORM_ERR_UNSUPPORTED_DEVICE, RMSNORM_ERR_CUDA, or RMSNORM_ERR_TOO_LARGE
- * when the row does not fit the staged kernel's shared memory or the launch
- * would need more than 1024 blocks.
+ * RMSNORM_ERR_UNSUPPORTED_DEVICE, RMSNORM_ERR_CUDA, RMSNORM_ERR_MISALIGNED
+ * when x, weight or y is not 16-byte aligned or a row's byte length is not a
+ * multiple of 16 (the staged kernel copies whole rows with bulk copies;
+ * rmsnorm_fwd takes such shapes through its scalar body, this entry point
+ * does not), or RMSNORM_ERR_TOO_LARGE when the row does not fit the staged
+ * kernel's shared memory or the launch would need more than 1024 blocks.
  *
  * Every call shares the static array and it keeps the last call's contents;
  * each block clears its own word when it starts.  Calls that overlap on the
@@ -479,6 +482,23 @@ int rmsnorm_test_grid_timeout(const void *x, const void *weight, void *y, int64_
  * block could not compute are written as NaN. */
 int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, void *y, int64_t rows,
                                int64_t hidden, float eps, int dtype, void *stream);
+
+/* Failure-detection test hook for rmsnorm_fwd_staged_noalloc (eps 1e-6):
+ * the row copies are withheld, so every bounded wait runs out after
+ * `limit_ns`; each block records RMSNORM_ERR_DEVICE_TIMEOUT in its word of
+ * the static array and writes its rows as NaN.  No fault, trap or hang is
+ * involved.  Allocates nothing. */
+int rmsnorm_test_staged_noalloc_timeout(const void *x, const void *weight, void *y, int64_t rows,
+                                        int64_t hidden, int dtype, uint64_t limit_ns,
+                                        void *stream);
+
+/* Copies the first n (<= 1024) words of rmsnorm_fwd_staged_noalloc's static
+ * status array (one per block of the last launch: 0, or
+ * RMSNORM_ERR_DEVICE_TIMEOUT) to host memory, after waiting for the device
+ * (a blocking copy).  The same one-time set-up as that entry point; allocates
+ * nothing.  Returns RMSNORM_OK, RMSNORM_ERR_INVALID_ARG, RMSNORM_ERR_CUDA or
+ * RMSNORM_ERR_UNSUPPORTED_DEVICE. */
+int rmsnorm_noalloc_block_status(int *host_out, int n);
 
 /* Static text for a status code. */
 const char *rmsnorm_status_string(int status);

@@ -147,6 +147,8 @@ def _load() -> ctypes.CDLL:
             "rmsnorm_test_staged_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
             "rmsnorm_test_grid_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
             "rmsnorm_fwd_staged_noalloc": ([vp, vp, vp, i64, i64, f32, i32, vp], i32),
+            "rmsnorm_test_staged_noalloc_timeout": ([vp, vp, vp, i64, i64, i32, u64, vp], i32),
+            "rmsnorm_noalloc_block_status": ([ctypes.POINTER(ctypes.c_int), i32], i32),
             "rmsnorm_status_string": ([i32], ctypes.c_char_p),
             "rmsnorm_version": ([], i32),
         }
@@ -392,6 +394,21 @@ def rmsnorm_fwd_staged_noalloc(x: int, weight: int, y: int, rows: int, hidden: i
     device pointers as integers, stream as a cudaStream_t integer."""
     _check(_load().rmsnorm_fwd_staged_noalloc(x, weight, y, rows, hidden, eps, dtype,
                                               stream or None), "rmsnorm_fwd_staged_noalloc")
+
+
+def rmsnorm_test_staged_noalloc_timeout(x: int, weight: int, y: int, rows: int, hidden: int,
+                                        dtype: int, limit_ns: int, stream: int | None) -> None:
+    _check(_load().rmsnorm_test_staged_noalloc_timeout(x, weight, y, rows, hidden, dtype,
+                                                       limit_ns, stream or None),
+           "rmsnorm_test_staged_noalloc_timeout")
+
+
+def rmsnorm_noalloc_block_status(n: int) -> list[int]:
+    """The first n words of the allocation-free entry point's static status
+    array (one per block of its last launch)."""
+    buf = (ctypes.c_int * max(n, 1))()
+    _check(_load().rmsnorm_noalloc_block_status(buf, n), "rmsnorm_noalloc_block_status")
+    return list(buf[:n])
 
 
 def rmsnorm_status_string(status: int) -> str:

@@ -576,11 +576,15 @@ const KernelDesc *staged_kernels(int *n)
 
 } // namespace rmsnorm
 
-extern "C" int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, void *y,
-                                          int64_t rows, int64_t hidden, float eps, int dtype,
-                                          void *stream)
+namespace rmsnorm {
+namespace {
+
+// The allocation-free launch.  flags / limit_ns: the bounded waits'
+// settings (kFlagWithholdCopies and a short limit only from the
+// failure-detection test hook).
+int noalloc_call(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
+                 float eps, int dtype, void *stream, uint32_t flags, uint64_t limit_ns)
 {
-    using namespace rmsnorm;
     int rc = check_call_args(x, weight, y, rows, hidden, eps, dtype);
     if (rc != RMSNORM_OK)
         return rc;
@@ -605,8 +609,8 @@ extern "C" int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, voi
     a.hidden = static_cast<int32_t>(hidden);
     a.eps = eps;
     a.status = d.status;
-    a.wait_limit_ns = 1000000000ull;
-    a.flags = 0u;
+    a.wait_limit_ns = limit_ns;
+    a.flags = flags;
     a.stream = static_cast<cudaStream_t>(stream);
     cudaError_t err;
     switch (dtype) {
@@ -621,4 +625,40 @@ extern "C" int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, voi
         break;
     }
     return err == cudaSuccess ? RMSNORM_OK : RMSNORM_ERR_CUDA;
+}
+
+} // namespace
+} // namespace rmsnorm
+
+extern "C" int rmsnorm_fwd_staged_noalloc(const void *x, const void *weight, void *y,
+                                          int64_t rows, int64_t hidden, float eps, int dtype,
+                                          void *stream)
+{
+    return rmsnorm::noalloc_call(x, weight, y, rows, hidden, eps, dtype, stream, 0u,
+                                 1000000000ull);
+}
+
+extern "C" int rmsnorm_test_staged_noalloc_timeout(const void *x, const void *weight, void *y,
+                                                   int64_t rows, int64_t hidden, int dtype,
+                                                   uint64_t limit_ns, void *stream)
+{
+    return rmsnorm::noalloc_call(x, weight, y, rows, hidden, 1e-6f, dtype, stream,
+                                 rmsnorm::kFlagWithholdCopies, limit_ns);
+}
+
+extern "C" int rmsnorm_noalloc_block_status(int *host_out, int n)
+{
+    using namespace rmsnorm;
+    if (!host_out || n < 0 || n > kNoAllocMaxBlocks)
+        return RMSNORM_ERR_INVALID_ARG;
+    NoAllocDevice d;
+    const int rc = noalloc_setup(&d);
+    if (rc != RMSNORM_OK)
+        return rc;
+    if (n == 0)
+        return RMSNORM_OK;
+    return cudaMemcpy(host_out, d.status, static_cast<size_t>(n) * sizeof(int),
+                      cudaMemcpyDeviceToHost) == cudaSuccess
+               ? RMSNORM_OK
+               : RMSNORM_ERR_CUDA;
 }
