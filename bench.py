@@ -12,12 +12,14 @@ resident in HBM before the timed region; consecutive steps rotate over
 several input/output sets whose total is larger than the 129 MB L2, so every
 step reads x from HBM.
 
-Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
-and torch.cuda.synchronize() on both sides; one pair of CUDA events on the
-launching stream around the region (which holds only the kernel's K
-back-to-back launches, so region time / K is the kernel's average launch
-duration, launch gaps included); max over ranks.  SM clocks
-and throttle reasons are sampled with nvidia-smi during the timed region.
+Timing: W untimed warm-up steps, then R timed regions (--regions, default 5)
+of exactly K steps each, every region bracketed by a barrier and
+torch.cuda.synchronize() on both sides, with one pair of CUDA events on the
+launching stream around it (it holds only the kernel's K back-to-back
+launches, so region time / K is the kernel's average launch duration, launch
+gaps included); max over ranks per region; the median region is reported,
+the others beside it.  SM clocks and throttle reasons are sampled with
+nvidia-smi over all the regions.
 
 value = algorithmic bytes (read x + read weight + write y) of every step of
 every rank / the slowest rank's time, in GB/s.  e2e = the same metric through
@@ -53,6 +55,7 @@ from rmsnorm_fwd_gb300 import inputs  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0
 METRIC = "RMSNorm achieved HBM GB/s (% of GB300 peak) and rows/s at 16384x4096 bf16"
 UNIT = "GB/s"
 
@@ -219,6 +222,16 @@ def ncu_traffic(workload: str, variant: str):
     return None
 
 
+def workload(args):
+    """The named workload, or its inputs at another shape (--shape ROWSxHIDDEN:
+    same element type, eps and distributions; for profiling other bodies)."""
+    wl = inputs.WORKLOADS[args.workload]
+    if args.shape:
+        rows, hidden = (int(v) for v in args.shape.lower().split("x"))
+        wl = wl.with_shape(rows, hidden)
+    return wl
+
+
 # ----------------------------------------------------------------- CPU oracle
 
 def oracle_sample(wl, seconds: float, max_rows: int | None = None):
@@ -282,7 +295,7 @@ def run_reference(args, world, rank):
     if rank != 0:
         return 0
     import oracle
-    wl = inputs.WORKLOADS[args.workload]
+    wl = workload(args)
     es = inputs.ITEMSIZE[wl.dtype]
     x, w = inputs.make_inputs(wl.with_shape(min(wl.rows, 64)))
     oracle.rmsnorm(x[:1], w, wl.eps, wl.dtype)
@@ -348,7 +361,7 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     dist = init_dist(world, "nccl")
-    wl = inputs.WORKLOADS[args.workload]
+    wl = workload(args)
     es = inputs.ITEMSIZE[wl.dtype]
     step_bytes = wl.bytes_per_call
 
@@ -384,27 +397,48 @@ def run_ours(args, world, rank, local):
         step(i)
     torch.cuda.synchronize()
 
+    if args.profile_range > 0:
+        # For a profiler's range replay (ncu --replay-mode range
+        # --profile-from-start off): exactly N back-to-back launches of the
+        # plan between cudaProfilerStart and cudaProfilerStop, nothing else.
+        torch.cuda.profiler.start()
+        for i in range(args.profile_range):
+            step(i)
+        torch.cuda.synchronize()
+        torch.cuda.profiler.stop()
+        if rank == 0:
+            print(json.dumps({"profile_range": {
+                "launches": args.profile_range, "workload": wl.name, "variant": variant,
+                "plan": plan.as_dict(), "sets": nsets,
+                "algorithmic_bytes_per_launch": step_bytes}}), flush=True)
+        return 0
+
     K = args.steps
+    R = max(1, args.regions)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     sampler = ClockSampler(local)
     sampler.start()
-    barrier(dist, device)
-    torch.cuda.synchronize()
     t_wall0 = time.time()
-    start.record(stream)
-    for i in range(K):
-        step(i)
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(dist, device)
+    region_ms = []
+    for reg in range(R):
+        barrier(dist, device)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(K):
+            step(reg * K + i)
+        end.record(stream)
+        torch.cuda.synchronize()
+        barrier(dist, device)
+        region_ms.append(reduce_max(start.elapsed_time(end), dist, device))
     t_wall1 = time.time()
     sampler.stop()
-    total_ms = start.elapsed_time(end)
-    max_ms = reduce_max(total_ms, dist, device)
-    # The timed region holds nothing but this kernel's K back-to-back launches
-    # on one stream, so its average launch duration (launch gaps included) is
-    # the region's time / K.
+    # Each timed region holds nothing but this kernel's K back-to-back
+    # launches on one stream, so its average launch duration (launch gaps
+    # included) is the region's time / K.  Reported: the median region (the
+    # regions are short, so one alone carries the run-to-run noise of a
+    # sub-millisecond event pair), with the others beside it.
+    max_ms = statistics.median(region_ms)
     max_kernel_ms = max_ms / K
     clocks = sampler.summary(t_wall0, t_wall1)
     status = rn.rmsnorm_get_device_status()
@@ -458,15 +492,24 @@ def run_ours(args, world, rank, local):
         },
         "rows_per_s": round(world * K * wl.rows / (max_ms / 1e3), 1),
         "pct_of_peak": round(100 * value / peak, 2),
+        "pct_of_nominal_hbm": round(100 * value / NOMINAL_HBM_GBS, 2),
         "gpu_launches": K,
+        "timing": {"regions": R, "launches_per_region": K, "statistic": "median region",
+                   "region_ms": [round(t, 6) for t in region_ms],
+                   "per_launch_ms_min": round(min(region_ms) / K, 6),
+                   "per_launch_ms_max": round(max(region_ms) / K, 6),
+                   "spread_pct": round(100 * (max(region_ms) - min(region_ms)) / max_ms, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_source": "GB300 HBM3e nominal bandwidth, 7.9 TB/s",
                      "traffic": ncu_traffic(wl.name, variant),
                      "algorithmic_bytes_per_launch": step_bytes,
                      "kernel_ms_avg": round(max_kernel_ms, 6),
-                     "kernel_ms_basis": "timed region / launches (gaps included)"},
+                     "kernel_ms_basis": "median timed region / launches (gaps included)"},
         "e2e": {"value": round(e2e_gbs, 2) if e2e_gbs is not None else None, "unit": UNIT,
                 "steps": E, "api": "rmsnorm_fwd_host: pinned host x/y read and written by the "
                 "kernel over NVLink-C2C; weight resident on the device",
@@ -591,7 +634,7 @@ def run_epi(args, world, rank, local):
     import rmsnorm_fwd_gb300 as rn
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    wl = inputs.WORKLOADS[args.workload]
+    wl = workload(args)
     es = inputs.ITEMSIZE[wl.dtype]
     x_np, w_np = inputs.make_inputs(wl, seed=rank)
     x_host = to_torch(x_np, wl.dtype, torch)
@@ -705,7 +748,7 @@ def run_latency(args, world, rank, local):
     import rmsnorm_fwd_gb300 as rn
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    wl = inputs.WORKLOADS[args.workload]
+    wl = workload(args)
     x_np, w_np = inputs.make_inputs(wl, seed=rank)
     x = to_torch(x_np, wl.dtype, torch).to(device)
     w = to_torch(w_np, wl.dtype, torch).to(device)
@@ -739,17 +782,30 @@ def run_latency(args, world, rank, local):
     warm_us = e0.elapsed_time(e1) / K * 1e3
 
     cs = torch.cuda.Stream(device)
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g, stream=cs):
-        for _ in range(K):
-            call(cs.cuda_stream)
-    g.replay()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    g.replay()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    graph_us = e0.elapsed_time(e1) / K * 1e3
+
+    def graph_time(fn):
+        """Per-call us of K calls of fn(stream) captured in a CUDA graph, replayed."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cs):
+            for _ in range(K):
+                fn(cs.cuda_stream)
+        g.replay()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / K * 1e3
+
+    graph_us = graph_time(call)
+    # The same calls without programmatic dependent launch, and the floor: a
+    # kernel that does nothing but write one float, replayed the same way.
+    pdl_was = rn.rmsnorm_get_pdl()
+    rn.rmsnorm_set_pdl(False)
+    graph_nopdl_us = graph_time(call)
+    rn.rmsnorm_set_pdl(pdl_was)
+    one = torch.zeros(1, dtype=torch.float32, device=device)
+    floor_us = graph_time(lambda _s: one.fill_(1.0))
 
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=device)
     cold = []
@@ -777,6 +833,9 @@ def run_latency(args, world, rank, local):
                                    "plan": plan.as_dict()},
         "back_to_back_us": round(warm_us, 3), "back_to_back_GBps": gbs(warm_us),
         "graph_us": round(graph_us, 3), "graph_GBps": gbs(graph_us),
+        "graph_us_without_pdl": round(graph_nopdl_us, 3),
+        "graph_floor_us": round(floor_us, 3),
+        "graph_floor_basis": "a one-element fill kernel, K launches replayed from a graph",
         "cold_median_us": round(cold_us, 3), "cold_GBps": gbs(cold_us),
         "cold_basis": "L2 flushed (2 x L2 written) before each call; one event pair per call",
         "gpu_launches": K, "device_status": rn.rmsnorm_get_device_status(),
@@ -791,6 +850,13 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--shape", default=None,
+                    help="ROWSxHIDDEN: the workload's inputs at another shape (profiling)")
+    ap.add_argument("--profile-range", type=int, default=0,
+                    help="N > 0: only N launches between cudaProfilerStart/Stop (for ncu's "
+                         "range replay), then exit")
+    ap.add_argument("--regions", type=int, default=5,
+                    help="timed regions of K launches each; the median region is reported")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=inputs.HEADLINE, choices=sorted(inputs.WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=50)
