@@ -183,20 +183,32 @@ def mxfp8_quantize(v: np.ndarray) -> tuple:
     return codes, scales
 
 
+def _decision_values(y: np.ndarray, rel: float, absolute: float) -> np.ndarray:
+    """The row results in binary32, the precision a kernel holding fp32 values
+    takes its decisions in (nearest-even from the binary64 results); with
+    ``rel`` != 0 their magnitudes moved by |y| * rel and by ``absolute`` in
+    the same direction (away from zero for rel > 0, towards it, never across
+    it, for rel < 0), which brackets the codes any binary32 result within that
+    distance may take."""
+    y32 = round_to(y, "f32").astype(np.float64)
+    if not rel:
+        return y32
+    with np.errstate(invalid="ignore"):
+        mag = np.abs(y32) * (1.0 + rel) + np.copysign(absolute, rel)
+        return np.copysign(np.maximum(mag, 0.0), y32)
+
+
 def rmsnorm_mxfp8(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float, dtype,
-                  rel: float = 0.0) -> tuple:
-    """The normalised rows quantised to MXFP8.
+                  rel: float = 0.0, absolute: float = 0.0) -> tuple:
+    """The normalised rows quantised to MXFP8 (OCP MX v1.0).
 
     The value that decides each code is the row result in binary32 (the
     binary64 result rounded nearest-even to binary32), as a kernel holding
-    fp32 values decides it; ``rel`` scales those values by (1 + rel) first,
-    which brackets the codes any result within that relative distance may
-    take."""
+    fp32 values decides it; ``rel`` and ``absolute`` move those values first
+    (_decision_values), which brackets the codes any result within that
+    distance may take."""
     y = rmsnorm_bias_f64(x, w, weight_bias, eps, dtype)
-    y32 = round_to(y, "f32").astype(np.float64)
-    if rel:
-        y32 = y32 * (1.0 + rel)
-    return mxfp8_quantize(y32)
+    return mxfp8_quantize(_decision_values(y, rel, absolute))
 
 
 def mxfp4_quantize(v: np.ndarray) -> tuple:
@@ -227,18 +239,15 @@ def nvfp4_quantize(v: np.ndarray, global_scale: float) -> tuple:
 
 
 def rmsnorm_fp4(x: np.ndarray, w: np.ndarray, weight_bias: float, eps: float, dtype, fmt: str,
-                global_scale: float = 1.0, rel: float = 0.0) -> tuple:
+                global_scale: float = 1.0, rel: float = 0.0, absolute: float = 0.0) -> tuple:
     """The normalised rows quantised to "mxfp4" or "nvfp4"; the deciding
-    values are the binary32 row results, scaled by (1 + rel), as for
-    rmsnorm_mxfp8."""
-    y = rmsnorm_bias_f64(x, w, weight_bias, eps, dtype)
-    y32 = round_to(y, "f32").astype(np.float64)
-    if rel:
-        y32 = y32 * (1.0 + rel)
+    values are the binary32 row results, moved by ``rel`` and ``absolute``,
+    as for rmsnorm_mxfp8."""
+    y = _decision_values(rmsnorm_bias_f64(x, w, weight_bias, eps, dtype), rel, absolute)
     if fmt == "mxfp4":
-        return mxfp4_quantize(y32)
+        return mxfp4_quantize(y)
     if fmt == "nvfp4":
-        return nvfp4_quantize(y32, global_scale)
+        return nvfp4_quantize(y, global_scale)
     raise ValueError(fmt)
 
 

@@ -7,12 +7,15 @@ Tolerance (stated for the method's outputs):
   the oracle's binary64 result rounded to the format with nearest-even
   (distance measured on the monotone integer line of the bit patterns, so it
   is exact across binades and signs); NaN must meet NaN.
-* MXFP8 codes: the scale and every code the oracle gives for the row result
-  in binary32, unless a relative change of at most MX_REL (the f32 bar) in
-  that result moves the decision -- then the GPU's choice must lie within the
-  codes the oracle gives at both ends of that band (a code is an integer that
-  floating point decides; the band is where fp32 rounding order may decide
-  it either way).
+* Block-scaled codes (MXFP8, MXFP4, NVFP4): the scale and every code the
+  oracle gives for the row result in binary32 (a code is an integer that
+  floating point decides, so both sides decide on values of the kernel's
+  precision), unless moving that result by MX_REL relative (the f32 bar)
+  plus MX_ABS absolute changes the decision -- then the GPU's choice must
+  lie within the codes the oracle gives at both ends of that band (the band
+  is where the device's rounding order may decide it either way; MX_ABS,
+  four units of binary32's smallest subnormal, covers results in binary32's
+  subnormal range, which carry fewer than 24 bits).
 """
 from __future__ import annotations
 
@@ -100,6 +103,7 @@ def sample_rows(rows: int, n: int, seed: int = 0) -> np.ndarray:
 
 
 MX_REL = 1e-5
+MX_ABS = 2.0 ** -147
 _TABLES = {}
 
 
@@ -121,9 +125,11 @@ QFMT = {"mxfp8": (32, 8, 0xFF), "mxfp4": (32, 4, 0xFF), "nvfp4": (16, 4, 0x7F)}
 
 
 def _oracle_q(x, w, bias, eps, dtype, fmt, gscale, rel=0.0):
+    a = MX_ABS if rel else 0.0
     if fmt == "mxfp8":
-        return oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype, rel=rel)
-    return oracle.rmsnorm_fp4(x, w, bias, eps, dtype, fmt, global_scale=gscale, rel=rel)
+        return oracle.rmsnorm_mxfp8(x, w, bias, eps, dtype, rel=rel, absolute=a)
+    return oracle.rmsnorm_fp4(x, w, bias, eps, dtype, fmt, global_scale=gscale, rel=rel,
+                              absolute=a)
 
 
 def _decode(codes, fmt, hidden):
@@ -203,7 +209,7 @@ def compare_quant(codes: np.ndarray, scales: np.ndarray, x: np.ndarray, w: np.nd
         err = np.abs(g * X - y)
         maxmag = 448.0 if bits == 8 else 6.0
         sat = t >= maxmag
-        tol = (_half_step(t, fmt) * (1 + MX_REL) + MX_REL * t) * X
+        tol = (_half_step(t, fmt) * (1 + MX_REL) + MX_REL * t) * X + MX_ABS
         good = np.where(X == 0, g == 0, np.where(sat, np.abs(g) == maxmag, err <= tol))
         good &= (g != 0) | np.isnan(y) | (np.signbit(g) == np.signbit(y))
         badb = amb[:, :, None] & ~good

@@ -113,3 +113,35 @@ def test_compare_quant_checks_the_sign_of_zero_codes(fmt, g):
     c_p, _ = (oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "bf16") if fmt == "mxfp8" else
               oracle.rmsnorm_fp4(x, w, 0.0, 1e-6, "bf16", fmt, global_scale=g))
     assert (c_m != c_p).any()
+
+
+def test_compare_quant_subnormal_results_band():
+    """Row results in binary32's subnormal range (f32 rows of subnormal
+    numbers, eps 1e-6: y about 2^-133) carry fewer than 24 bits, so a kernel
+    that rounds twice can land a unit of 2^-149 away from the oracle's single
+    rounding; the bar's absolute term (four such units) accepts that and
+    still rejects a code one step off."""
+    rng = np.random.default_rng(4)
+    f = (rng.standard_normal((4, 64)) * 2.0 ** -143).astype(np.float32)
+    x, w = f, np.ones(64, np.float32) * np.float32(1.5)
+    for fmt, g in (("mxfp8", 1.0), ("nvfp4", 1.0)):
+        c, s = (oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "f32") if fmt == "mxfp8"
+                else oracle.rmsnorm_fp4(x, w, 0.0, 1e-6, "f32", fmt, global_scale=g))
+        compare_quant(c, s, x, w, 0.0, 1e-6, "f32", fmt, g)
+        # every result one unit of 2^-149 further from zero, and nearer to it
+        for sgn in (1.0, -1.0):
+            y = oracle.rmsnorm_bias_f64(x, w, 0.0, 1e-6, "f32")
+            y32 = oracle.round_to(y, "f32").astype(np.float64)
+            moved = np.copysign(np.maximum(np.abs(y32) + sgn * 2.0 ** -149, 0.0), y32)
+            cm, sm = (oracle.mxfp8_quantize(moved) if fmt == "mxfp8"
+                      else oracle.nvfp4_quantize(moved, g))
+            compare_quant(cm, sm, x, w, 0.0, 1e-6, "f32", fmt, g)
+    # a code one step off in a block the band leaves alone
+    c, s = oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "f32")
+    lo, _ = oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "f32", rel=-1e-5, absolute=2.0 ** -147)
+    hi, _ = oracle.rmsnorm_mxfp8(x, w, 0.0, 1e-6, "f32", rel=1e-5, absolute=2.0 ** -147)
+    i, j = np.argwhere((lo == c) & (hi == c) & (c != 0))[0]
+    bad = c.copy()
+    bad[i, j] ^= 1
+    with pytest.raises(AssertionError):
+        compare_quant(bad, s, x, w, 0.0, 1e-6, "f32", "mxfp8", 1.0)
