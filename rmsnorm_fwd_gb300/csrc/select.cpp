@@ -564,7 +564,8 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
         //  * rows above 32 KiB (up to 8 rows below 48 KiB): one wave of
         //    clusters, as large (<= 8) as keeps every block on its own SM --
         //    at least 4 blocks, or 2 for rows of 64 KiB and more;
-        //  * 64..256 KiB rows, up to 128 of them (more than one wave holds):
+        //  * rows above 64 KiB, up to 256 KiB, and up to 128 of them (more
+        //    than one wave holds; exactly 64 KiB rows stay with the rule above):
         //    clusters over several waves, 64 bytes per thread, of 4 blocks
         //    below 128 KiB and 8 from there (96 and 128 rows of 80, 128 and
         //    256 KiB: 6-34 % faster than the looped body);

@@ -497,6 +497,14 @@ def test_cluster_split_chosen_for_long_decode_rows():
         assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == C, \
             (rows, hidden, p.as_dict())
         assert p.grid == rows * C > SMS and p.vecs_per_thread * p.vec_bytes >= 64
+    # exactly 64 KiB rows: one wave of clusters while rows * 2 <= SMs; beyond
+    # that the several-waves rule (rows above 64 KiB only) does not apply and
+    # the block-per-row body keeps them
+    for rows in (77, 96, 128):
+        rc, p = plan(rows, 32768, rn.BF16)
+        assert rc == rn.OK and p.variant == rn.VARIANT_PERSISTENT, (rows, p.as_dict())
+    rc, p = plan(76, 32768, rn.BF16)
+    assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == 2
     # 512 KiB rows: 16-byte vectors, four per thread, 1024 threads per block
     rc, p = plan(1, 131072, rn.F32)
     assert rc == rn.OK and p.variant == rn.VARIANT_CLUSTER and p.stages == 8
