@@ -206,15 +206,16 @@ def kernel_source_hash(dtype: str = "bf16") -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str, variant: str):
+def ncu_traffic(wl, variant: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
+    on the current kernel sources for this workload; else None."""
+    workload = wl.name
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     try:
         text = open(path).read()
     except OSError:
         return None
-    src = kernel_source_hash(inputs.WORKLOADS[workload].dtype)
+    src = kernel_source_hash(wl.dtype)
     for m in re.finditer(r"^workload=(\S+) variant=(\S+) src=(\S+) dram_bytes_per_launch=(\d+)",
                          text, flags=re.M):
         if m.group(1) == workload and m.group(2) == variant and m.group(3) == src:
@@ -506,7 +507,7 @@ def run_ours(args, world, rank, local):
                      "nominal_peak": NOMINAL_HBM_GBS,
                      "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "nominal_source": "GB300 HBM3e nominal bandwidth, 7.9 TB/s",
-                     "traffic": ncu_traffic(wl.name, variant),
+                     "traffic": ncu_traffic(wl, variant),
                      "algorithmic_bytes_per_launch": step_bytes,
                      "kernel_ms_avg": round(max_kernel_ms, 6),
                      "kernel_ms_basis": "median timed region / launches (gaps included)"},

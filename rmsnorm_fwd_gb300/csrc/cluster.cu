@@ -15,7 +15,9 @@
 // factor -- then scales and stores its slice.  A second cluster barrier
 // keeps each block's shared memory alive until every peer has read it.
 // No multicast, no spin-waits: the only waits are the hardware cluster
-// barriers, which every thread of every block reaches exactly twice.
+// barriers, which every thread of every block reaches exactly twice (four
+// times on the range guard's path, which every block of the cluster takes
+// or skips together).
 #include "internal.h"
 #include "device_common.cuh"
 
@@ -45,6 +47,16 @@ __device__ inline uint32_t cluster_size()
     uint32_t n;
     asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
     return n;
+}
+
+// The float at shared address `local` in block `rank` of this cluster.
+__device__ inline float ld_peer(uint32_t local, uint32_t rank)
+{
+    uint32_t remote;
+    float v;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
 }
 
 // The two floats at shared address `local` in block `rank` of this cluster.
@@ -89,7 +101,8 @@ cluster_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t 
     using E = Elem<DT>;
     constexpr int VPE = VB / E::kSize;
     __shared__ float part[32];
-    __shared__ __align__(8) float2 block_total; // (sum of (k x)^2 over the slice, k)
+    __shared__ float block_total;
+    __shared__ __align__(8) float2 block_pair; // range guard: (sum of (k x)^2 over the slice, k)
 
     pdl_begin();
     const uint32_t C = cluster_size();
@@ -127,32 +140,16 @@ cluster_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t 
     if (lane == 0)
         part[warp] = s;
     __syncthreads();
-    float bt = group_allreduce<32>(lane < nwarps ? part[lane] : 0.f); // block-uniform
-    float bk = 1.f;
-    if constexpr (kRangeGuard<DT>) {
-        // Range guard (device_common.cuh) on this block's slice: its sum
-        // formed again from k x when the plain one left fp32's trusted range.
-        if (sum_needs_rescale(bt, eps)) {
-            bk = rescale_k(bt);
-            float sk = 0.f;
-#pragma unroll
-            for (int k = 0; k < NV; ++k)
-                sk = sumsq_k<DT, VB>(xv[k], bk, sk);
-            sk = group_allreduce<32>(sk);
-            __syncthreads(); // every warp has read part[] above
-            if (lane == 0)
-                part[warp] = sk;
-            __syncthreads();
-            bt = group_allreduce<32>(lane < nwarps ? part[lane] : 0.f);
-        }
+    if (warp == 0) {
+        float b = lane < nwarps ? part[lane] : 0.f;
+        b = group_allreduce<32>(b);
+        if (lane == 0)
+            block_total = b;
     }
-    if (t == 0)
-        block_total = make_float2(bt, bk);
     // Every block's total is visible to the whole cluster past this barrier.
     cluster_sync_all();
-    const float2 pk = static_cast<uint32_t>(lane) < C ? ld_peer2(cta_smem_addr(&block_total), lane)
-                                                      : make_float2(0.f, 1.f);
-    const float tot = group_allreduce<32>(pk.x);
+    float tot = static_cast<uint32_t>(lane) < C ? ld_peer(cta_smem_addr(&block_total), lane) : 0.f;
+    tot = group_allreduce<32>(tot);
     // No block leaves (or lets its shared memory go) before every peer has
     // read its total: arrive now, wait at the end.  Relaxed: the peer reads
     // above have completed (their values are used), and nothing written
@@ -161,18 +158,50 @@ cluster_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t 
     const float nf = static_cast<float>(hidden);
     const float r = row_factor(tot, nf, eps);
     if constexpr (kRangeGuard<DT>) {
-        // A block rescaled its slice, or the fp32 total left the trusted
-        // range: the total again in binary64 from (Sk / k^2) of every block,
-        // in the same order in every block (exact scalings by powers of two).
-        if (__any_sync(0xFFFFFFFFu, pk.y != 1.f) || sum_needs_rescale(tot, eps)) {
+        // Range guard (device_common.cuh), taken by every block of the
+        // cluster together (they all hold the same total).  Each block forms
+        // its slice's sum again from k x where its own plain sum left fp32's
+        // trusted range, the blocks exchange (Sk, k) in a second round, and
+        // every block adds Sk / k^2 in binary64 in rank order (exact
+        // scalings by powers of two; the same value in every block).  The
+        // slice is then read again from memory (nothing of it is written
+        // yet), one vector at a time, so the registers above are not kept
+        // alive for this rare path.
+        if (sum_needs_rescale(tot, eps)) {
+            const float bt = block_total; // this block's own plain sum
+            float bk = 1.f, bs = bt;
+            if (sum_needs_rescale(bt, eps)) { // block-uniform
+                bk = rescale_k(bt);
+                float sk = 0.f;
+#pragma unroll 1
+                for (int k = 0; k < NV; ++k) {
+                    const int v = v0 + t + k * tpr;
+                    if (live_row && v < v1) {
+                        Vec<VB> xk;
+                        ld_stream<0>(xk, xr + static_cast<int64_t>(v) * VB);
+                        sk = sumsq_k<DT, VB>(xk, bk, sk);
+                    }
+                }
+                sk = group_allreduce<32>(sk);
+                if (lane == 0)
+                    part[warp] = sk; // part's last readers passed the cluster barrier
+                __syncthreads();
+                bs = group_allreduce<32>(lane < nwarps ? part[lane] : 0.f);
+            }
+            if (t == 0)
+                block_pair = make_float2(bs, bk);
+            // Close the first round (every peer has read block_total), then
+            // one full cluster barrier makes every block's pair visible.
+            asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+            cluster_sync_all();
+            const float2 pk = static_cast<uint32_t>(lane) < C
+                                  ? ld_peer2(cta_smem_addr(&block_pair), lane)
+                                  : make_float2(0.f, 1.f);
+            asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
             const double kd = pk.y;
-            const double D = warp_sum_f64(static_cast<double>(pk.x) / (kd * kd));
             float Sk, kk;
-            wide_total(D, eps, Sk, kk);
+            wide_total(warp_sum_f64(static_cast<double>(pk.x) / (kd * kd)), eps, Sk, kk);
             const Factor f = rescaled_factor(Sk, kk, nf, eps);
-            // The slice again from memory (nothing of it is written yet),
-            // one vector at a time, so the registers above are not kept
-            // alive for this rare path.
 #pragma unroll 1
             for (int k = 0; k < NV; ++k) {
                 const int v = v0 + t + k * tpr;

@@ -250,6 +250,21 @@ grid_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
             const int v1 = static_cast<int>(min(f1, (row + 1) * nvec) - row * nvec);
             const char *xr = static_cast<const char *>(x) + row * row_bytes;
             char *yr = static_cast<char *>(y) + row * row_bytes;
+            if (kRangeGuard<DT> && up) {
+                // The range guard's rows of subnormals (x scaled up by 2^100
+                // before the scaling): one vector at a time, so the loop below
+                // carries no test for them.
+#pragma unroll 1
+                for (int v = v0 + t; v < v1; v += tpr) {
+                    Vec<VB> xk, wk, o;
+                    ld_stream<0>(xk, xr + static_cast<int64_t>(v) * VB);
+                    ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                    scale_up<DT, VB>(xk);
+                    scale<DT, VB>(o, xk, wk, r);
+                    st_stream<1>(yr + static_cast<int64_t>(v) * VB, o);
+                }
+                continue;
+            }
             for (int v = v0 + t; v < v1; v += U * tpr) {
                 Vec<VB> xv[U], wv[U];
 #pragma unroll
@@ -264,8 +279,6 @@ grid_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
                 for (int u = 0; u < U; ++u) {
                     const int vv = v + u * tpr;
                     if (vv < v1) {
-                        if (up)
-                            scale_up<DT, VB>(xv[u]);
                         Vec<VB> o;
                         scale<DT, VB>(o, xv[u], wv[u], r);
                         st_stream<1>(yr + static_cast<int64_t>(vv) * VB, o);

@@ -69,24 +69,84 @@ __device__ inline float block_total_rare(float s, float *sh, int lane, int warp,
     return tot;
 }
 
-// The range guard's redo of a row's statistic (device_common.cuh): the sum
-// of the squares of k x, read again from memory one vector at a time (rolled,
-// so the registers holding the row are free meanwhile; nothing of the row is
-// written yet), over the vectors t + j * tpr, j < NV, of this thread.
-template <int DT, int VB, int NV>
-__device__ inline float redo_sumsq(const char *xr, int t, int tpr, int nvec, bool active,
-                                   float k)
+// One vector of a row, scaled by rr and written: the plain, weight-bias or
+// block-scaled output (every lane of the warp calls it for the block-scaled
+// ones; `live`: the vector is part of the row).
+template <int DT, int VB, int CP, int EPI, bool XW, bool PACKED>
+__device__ inline void emit_vec(const Vec<VB> &xk, const Vec<VB> &wk, const char *xp,
+                                const char *wp, float rr, float bias, const QParams &qp,
+                                bool live, bool leader, char *yp, uint8_t *sp, bool up)
 {
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
+    if constexpr (MX) {
+        q_store<DT, VB, EPI - RMSNORM_EPI_MXFP8, XW>(xk, wk, xp, wp, rr, qp, live, leader, yp, sp,
+                                                      up);
+    } else if (live) {
+        Vec<VB> o;
+        if constexpr (EPI == RMSNORM_EPI_BIAS)
+            scale_bias<DT, VB>(o, xk, wk, rr, bias);
+        else if constexpr (PACKED)
+            scale_packed<DT, VB>(o, xk, wk, rr);
+        else
+            scale<DT, VB>(o, xk, wk, rr);
+        st_stream<CP>(yp, o);
+    }
+}
+
+// The range guard's redo of one row (device_common.cuh): the row is read
+// again from memory (nothing of it is written yet), its sum formed from k x,
+// and the whole row scaled and written, one vector at a time (rolled loops,
+// the weight read again), so that the register bodies' allocation is not
+// raised for it.  Lane t of a group of `tpr` lanes (a warp
+// group, WARP, or the whole block) owns vectors t + j * tpr, j < NV.
+// `redo`: this group's row needs it (WARP: the other groups of the warp come
+// along for the shuffles and write their rows with the plain factor `r`).
+template <int DT, int VB, int NV, int TPR, int CP, int EPI, bool XW, bool PACKED>
+__device__ __forceinline__ void redo_row(const char *xr, const char *wt, char *yr, uint8_t *sr,
+                                      int t, int tpr, int nvec, bool active, bool redo, float s,
+                                      float r, float n, float eps, float bias, QParams qp,
+                                      float *sh)
+{
+    constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
+    constexpr int Q = MX ? EPI - RMSNORM_EPI_MXFP8 : 0;
+    constexpr int LPB = QGeo<DT, VB, Q>::kLanes;
+    constexpr int OB = MX ? QGeo<DT, VB, Q>::kCodeBytes : VB;
+    const float kk = rescale_k(s);
     float sk = 0.f;
 #pragma unroll 1
     for (int j = 0; j < NV; ++j) {
         if (active && t + j * tpr < nvec) {
             Vec<VB> xk;
             ld_stream<0>(xk, xr + j * tpr * VB);
-            sk = sumsq_k<DT, VB>(xk, k, sk);
+            sk = sumsq_k<DT, VB>(xk, kk, sk);
         }
     }
-    return sk;
+    if constexpr (TPR > 0) {
+        sk = group_allreduce<TPR>(sk);
+    } else {
+        const int lane = t & 31;
+        sk = block_total_rare(group_allreduce<32>(sk), sh, lane, t >> 5, tpr >> 5);
+    }
+    const Factor f = rescaled_factor(sk, kk, n, eps);
+    const float rr = redo ? f.r : r;
+    const bool up = redo && f.up;
+#pragma unroll 1
+    for (int j = 0; j < NV; ++j) {
+        const bool live = active && t + j * tpr < nvec;
+        Vec<VB> xk, wk;
+        if (live) {
+            ld_stream<0>(xk, xr + j * tpr * VB);
+            ld_weight(wk, wt + j * tpr * VB);
+            if (up)
+                scale_up<DT, VB>(xk);
+        } else {
+            vzero(xk);
+            vzero(wk);
+        }
+        emit_vec<DT, VB, CP, EPI, false, PACKED>(xk, wk, xr + j * tpr * VB, wt + j * tpr * VB, rr,
+                                              bias, qp, live, t % LPB == 0, yr + j * tpr * OB,
+                                              sr + (t + j * tpr) / LPB, up);
+    }
 }
 
 // ---------------------------------------------------------------- warp-per-row
@@ -153,36 +213,18 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
         for (int k = 0; k < NV; ++k)
             s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<TPR>(s);
-        const float r0 = row_factor(s, n, eps);
-        float r = r0;
-        bool up = false;
+        const float r = row_factor(s, n, eps);
         if constexpr (kRangeGuard<DT>) {
             // Range guard, warp-uniform (the groups of a warp reduce with
-            // whole-warp shuffles).  The statistic is formed again from
-            // memory and the row registers are loaded again (scaled up where
-            // the factor needs it), so their old contents are dead here.
+            // whole-warp shuffles): rare rows are redone from memory.
             const bool redo = sum_needs_rescale(s, eps);
             if (__any_sync(0xFFFFFFFFu, redo)) {
                 const int64_t row2 = opaque(row);
-                const char *xr2 = static_cast<const char *>(x) + row2 * row_bytes + t * VB;
-                const float kk = rescale_k(s);
-                const Factor f = rescaled_factor(
-                    group_allreduce<TPR>(redo_sumsq<DT, VB, NV>(xr2, t, TPR, nvec, active, kk)),
-                    kk, n, eps);
-                if (redo) {
-                    r = f.r;
-                    up = f.up;
-                }
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    if (active && t + k * TPR < nvec) {
-                        ld_stream<0>(xv[k], xr2 + k * TPR * VB);
-                        if (up)
-                            scale_up<DT, VB>(xv[k]);
-                    } else {
-                        vzero(xv[k]);
-                    }
-                }
+                redo_row<DT, VB, NV, TPR, CP, EPI, XW, false>(
+                    static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt, yr,
+                    MX ? scales + row2 * (hidden / QFmt<Q>::kBlock) : nullptr, t, TPR, nvec,
+                    active, redo, s, r, n, eps, bias, qp, nullptr);
+                continue;
             }
         }
 #pragma unroll
@@ -202,8 +244,7 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
                     vzero(wk);
                 q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * TPR * VB, wt + k * TPR * VB, r, qp, live,
                                    t % LPB == 0, yr + k * TPR * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB,
-                                   up);
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
             } else if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -291,34 +332,17 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
             const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
             s = group_allreduce<32>(tot);
         }
-        const float r0 = row_factor(s, n, eps);
-        float r = r0;
-        bool up = false;
+        const float r = row_factor(s, n, eps);
         if constexpr (kRangeGuard<DT>) {
-            // Range guard, block-uniform (every warp holds the same s).  The
-            // statistic is formed again from memory and the row registers
-            // are loaded again (scaled up where the factor needs it), so
-            // their old contents are dead here.
+            // Range guard, block-uniform (every warp holds the same s): a
+            // rare row is redone from memory.
             if (sum_needs_rescale(s, eps)) {
                 const int64_t row2 = opaque(row);
-                const char *xr2 = static_cast<const char *>(x) + row2 * row_bytes + t * VB;
-                const float kk = rescale_k(s);
-                float sk = group_allreduce<32>(redo_sumsq<DT, VB, NV>(xr2, t, tpr, nvec, true, kk));
-                if (TPRC != 32)
-                    sk = block_total_rare(sk, rare, lane, warp, nwarps);
-                const Factor f = rescaled_factor(sk, kk, n, eps);
-                r = f.r;
-                up = f.up;
-#pragma unroll
-                for (int k = 0; k < NV; ++k) {
-                    if (t + k * tpr < nvec) {
-                        ld_stream<0>(xv[k], xr2 + k * stride);
-                        if (up)
-                            scale_up<DT, VB>(xv[k]);
-                    } else {
-                        vzero(xv[k]);
-                    }
-                }
+                redo_row<DT, VB, NV, TPRC == 32 ? 32 : 0, CP, EPI, XW, true>(
+                    static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt, yr,
+                    MX ? scales + row2 * (hidden / QFmt<Q>::kBlock) : nullptr, t, tpr, nvec, true,
+                    true, s, r, n, eps, bias, qp, rare);
+                continue;
             }
         }
 #pragma unroll
@@ -338,8 +362,7 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                     vzero(wk);
                 q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * stride, wt + k * stride, r, qp, live,
                                    t % LPB == 0, yr + k * tpr * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB,
-                                   up);
+                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
             } else if (t + k * tpr < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -446,6 +469,46 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
             }
         }
 
+        if (kRangeGuard<DT> && up) {
+            // The range guard's rows of subnormals (x scaled up by 2^100 before
+            // the scaling): a second pass of its own, one vector at a time, so
+            // the loops below carry no test for them.
+            if constexpr (MX) {
+                uint8_t *sr = scales + row * (hidden / QFmt<Q>::kBlock);
+#pragma unroll 1
+                for (int v0 = t & ~31; v0 < nvec; v0 += tpr) {
+                    const int v = v0 + lane;
+                    Vec<VB> xk, wk;
+                    if (v < nvec) {
+                        ld_stream<0>(xk, xr + static_cast<int64_t>(v) * VB);
+                        ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                        scale_up<DT, VB>(xk);
+                    } else {
+                        vzero(xk);
+                        vzero(wk);
+                    }
+                    q_store<DT, VB, Q, XW>(xk, wk, xr + static_cast<int64_t>(v) * VB,
+                                       wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
+                                       lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
+                                       sr + v / LPB, true);
+                }
+            } else {
+#pragma unroll 1
+                for (int v = t; v < nvec; v += tpr) {
+                    Vec<VB> xk, wk, o;
+                    ld_stream<0>(xk, xr + static_cast<int64_t>(v) * VB);
+                    ld_weight(wk, wb + static_cast<int64_t>(v) * VB);
+                    scale_up<DT, VB>(xk);
+                    if constexpr (EPI == RMSNORM_EPI_BIAS)
+                        scale_bias<DT, VB>(o, xk, wk, r, bias);
+                    else
+                        scale<DT, VB>(o, xk, wk, r);
+                    st_stream<CP>(yr + static_cast<int64_t>(v) * VB, o);
+                }
+            }
+            continue;
+        }
+
         if constexpr (MX) {
             // Warp-uniform trip count (the block maximum is a shuffle over
             // the whole warp): lane l of the warp starting at vector v0
@@ -463,8 +526,6 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                         vzero(xv[u]);
                         vzero(wv[u]);
                     }
-                    if (up)
-                        scale_up<DT, VB>(xv[u]);
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
@@ -472,7 +533,7 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                     q_store<DT, VB, Q, XW>(xv[u], wv[u], xr + static_cast<int64_t>(v) * VB,
                                        wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
                                        lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
-                                       sr + v / LPB, up);
+                                       sr + v / LPB);
                 }
             }
         } else {
@@ -490,8 +551,6 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + u * tpr;
                     if (v < nvec) {
-                        if (up)
-                            scale_up<DT, VB>(xv[u]);
                         Vec<VB> o;
                         if constexpr (EPI == RMSNORM_EPI_BIAS)
                             scale_bias<DT, VB>(o, xv[u], wv[u], r, bias);

@@ -317,7 +317,6 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
             break;
         }
         float r = row_factor(acc, n, eps);
-        bool up = false;
         if constexpr (kRangeGuard<DT>) {
             if (sum_needs_rescale(acc, eps)) { // group-uniform: the range guard's redo
                 const float kk = rescale_k(acc);
@@ -339,7 +338,18 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
                 }
                 const Factor f = rescaled_factor(sk, kk, n, eps);
                 r = f.r;
-                up = f.up;
+                if (f.up) {
+                    // x scaled up by 2^100 in place in the slot: each thread
+                    // scales the vectors it alone reads back below (the same
+                    // vectors in every write-back mode).
+                    unsigned char *slot = slots + static_cast<int64_t>(s) * L.slot_stride;
+                    for (int v = gl; v < nvec; v += gsize) {
+                        Vec<16> *p = reinterpret_cast<Vec<16> *>(slot + v * 16);
+                        Vec<16> xv = *p;
+                        scale_up<DT, 16>(xv);
+                        *p = xv;
+                    }
+                }
             }
         }
 
@@ -349,10 +359,8 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
             unsigned char *dst = slots + static_cast<int64_t>(s) * L.slot_stride;
 #pragma unroll 4
             for (int v = gl; v < nvec; v += gsize) {
-                Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
+                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(dst + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
-                if (up)
-                    scale_up<DT, 16>(xv);
                 Vec<16> o;
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
                     scale_bias<DT, 16>(o, xv, wv, r, bias);
@@ -387,8 +395,6 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
                 if (live) {
                     xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                     wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
-                    if (up)
-                        scale_up<DT, 16>(xv);
                 } else {
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
@@ -397,7 +403,7 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
                 q_store<DT, 16, Q, XW>(xv, wv, src + v * 16, wsm + v * 16, r, qp, live,
                                    lane % G::kLanes == 0,
                                    qr + static_cast<int64_t>(v) * G::kCodeBytes,
-                                   sr + v / G::kLanes, up);
+                                   sr + v / G::kLanes);
             }
             __syncwarp();
             if (lane == 0)
@@ -405,10 +411,8 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
         } else {
 #pragma unroll 4
             for (int v = gl; v < nvec; v += gsize) {
-                Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                const Vec<16> xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
                 const Vec<16> wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
-                if (up)
-                    scale_up<DT, 16>(xv);
                 Vec<16> o;
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
                     scale_bias<DT, 16>(o, xv, wv, r, bias);
