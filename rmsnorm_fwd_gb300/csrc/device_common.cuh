@@ -656,30 +656,29 @@ __device__ inline float block_max(float m)
 // With XW (16-bit elements, weight offset -0 and, for NVFP4, a per-tensor
 // scale g in [2^-117, 2^100], so that every value(code) * g and its
 // reciprocal are normal floats and the flush-to-zero reciprocal serves; the
-// launch picks this instantiation) the values are formed the other way round, as the exact
-// products u = x * w (one mixed-precision fma per element, no widening),
-// the block maximum as max |u| * r and the scaled values as u * (r * mul):
-// the same quantities up to one or two fp32 roundings (the decisions they
-// feed are checked against the exact values with a 1e-5 relative band).
-// That holds while the products and the block maximum are normal fp32
-// numbers well away from overflow, so a block whose max |u| or max |u| * r
-// falls outside [2^-100, 2^100) (zero blocks, NaN, Inf, extreme ranges) is
-// redone in the order above, from x and w read again at xp and wp (a rare,
-// warp-uniform branch: the registers holding x and w are not kept for it;
-// neither the codes nor the scales may overlap x or w).
+// launch picks this instantiation) the values are formed the other way round,
+// as the exact products u = x * w (one mixed-precision fma per element, no
+// widening), the block maximum as max |u| * r and the scaled values as
+// u * (r * mul): the same quantities up to one or two fp32 roundings (the
+// decisions they feed are checked against the exact values with a 1e-5
+// relative band).  That holds while the products and the block maximum are
+// normal fp32 numbers well away from overflow.  The return value says that
+// this lane's block is outside that range -- max |u| or max |u| * r outside
+// [2^-100, 2^100): zero blocks, NaN, Inf, extreme ranges -- and that what it
+// stored there must be replaced: the caller then writes the vectors of the
+// whole warp again in the order above, from x and w read again (a rare,
+// warp-uniform branch after the warp's last vector, so the common path holds
+// no registers for it; neither the codes nor the scales may overlap x or w).
 // An element below 2^-119 of its block's maximum is below half the smallest
 // nonzero code of every format, so at 2^-100 nothing that can reach a code
-// is subnormal.
+// is subnormal.  Without XW the return value is false.
 //
 // Every lane of the warp must call this (the shuffles span the full warp);
 // `live` says whether this lane's vector is part of the row.  The lane
 // holding the first vector of a block (`leader`) stores the scale byte.
-// `up`: the caller has multiplied the registers xv by 2^100 (range guard,
-// rescaled_factor); the redo applies the same factor to x read again.
 template <int DT, int VB, int Q, bool XW>
-__device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void *xp,
-                               const void *wp, float r, const QParams &qp, bool live, bool leader,
-                               void *q, uint8_t *scale, bool up = false)
+__device__ inline bool q_emit(const Vec<VB> &xv, const Vec<VB> &wv, float r, const QParams &qp,
+                              bool live, bool leader, void *q, uint8_t *scale)
 {
     static_assert(!XW || DT != RMSNORM_F32, "exact products: 16-bit elements only");
     using G = QGeo<DT, VB, Q>;
@@ -688,6 +687,7 @@ __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void 
     constexpr int P = NE / 2;
     uint64_t v[P];
     float m, fac;
+    bool bad = false;
     if constexpr (XW) {
         m = 0.f;
 #pragma unroll
@@ -699,45 +699,36 @@ __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void 
         }
         m = block_max<LPB>(m);
         const float mr = m * r;
-        const bool redo = !(m >= 0x1p-100f && m < 0x1p100f && mr >= 0x1p-100f && mr < 0x1p100f);
+        bad = !(m >= 0x1p-100f && m < 0x1p100f && mr >= 0x1p-100f && mr < 0x1p100f);
         m = mr;
         fac = r;
-        if (__any_sync(0xFFFFFFFFu, redo)) {
-            if (redo) {
-                Vec<VB> xa, wa;
-                if (live) {
-                    xa = *static_cast<const Vec<VB> *>(xp);
-                    wa = *static_cast<const Vec<VB> *>(wp);
-                    if (up)
-                        scale_up<DT, VB>(xa);
-                } else {
-#pragma unroll
-                    for (int k = 0; k < Vec<VB>::kWords; ++k)
-                        xa.w[k] = wa.w[k] = 0u;
-                }
-                m = q_values<DT, VB>(xa, wa, r, qp.bias, v);
-                fac = 1.f;
-            }
-            m = block_max<LPB>(m); // a block's lanes all redo or all keep theirs
-        }
     } else {
         m = block_max<LPB>(q_values<DT, VB>(xv, wv, r, qp.bias, v));
         fac = 1.f;
     }
     uint32_t code;
-    float mul;
+    float f;
     if constexpr (Q == kQNvfp4) {
         code = e4m3_code(m * rcp_approx(6.f * qp.g));
         const float d = e4m3_value(code);
         const float dg = d * qp.g;
-        mul = d == 0.f ? 0.f : (XW ? rcp_approx_ftz(dg) : rcp_approx(dg));
+        f = (d == 0.f ? 0.f : (XW ? rcp_approx_ftz(dg) : rcp_approx(dg))) * fac;
+    } else if constexpr (XW) {
+        // A block in the trusted range has 2^-100 <= max |u| * r < 2^100, so
+        // its biased exponent e lies in [27, 227): the code is e - kEmax, and
+        // r * 2^(127 - code) -- a normal float, the scaled block maximum being
+        // in [2^kEmax, 2^(kEmax + 1)) -- is r with 127 - code added to its
+        // exponent field.  Blocks outside the range are written again (above).
+        constexpr uint32_t EM = QFmt<Q>::kEmax;
+        const uint32_t eb = __float_as_uint(m) & 0x7F800000u; // m >= 0 or NaN
+        code = (eb >> 23) - EM;
+        f = __uint_as_float(__float_as_uint(r) + ((127u + EM) << 23) - eb);
     } else {
         constexpr uint32_t EM = QFmt<Q>::kEmax;
         const uint32_t e = __float_as_uint(m) >> 23;
         code = e == 255u ? 255u : (e > EM ? e - EM : 0u);
-        mul = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23);
+        f = __uint_as_float(code == 255u ? 0x3F800000u : (254u - code) << 23) * fac;
     }
-    const float f = mul * fac;
     const uint64_t mul2v = f2(f, f);
     float sv[NE];
 #pragma unroll
@@ -765,6 +756,7 @@ __device__ inline void q_store(const Vec<VB> &xv, const Vec<VB> &wv, const void 
         if (leader)
             *scale = static_cast<uint8_t>(code);
     }
+    return bad;
 }
 
 // ---------------------------------------------------------------- launch order
@@ -800,6 +792,28 @@ __device__ inline float group_allreduce(float s)
 __device__ inline float row_factor(float S, float n, float eps)
 {
     return rsqrtf(S / n + eps);
+}
+
+// The count n of a row and what the division by it needs: when n is a power
+// of two, S / n is S * (1 / n) exactly (a product by a power of two rounds
+// as the quotient does, subnormal results included), which the block-scaled
+// bodies take instead of the division (the plain ones keep the division:
+// their register caps leave no room for the flag).
+struct RowCount {
+    float n, inv;
+    bool pow2;
+};
+__device__ inline RowCount row_count(int32_t hidden)
+{
+    RowCount c;
+    c.n = static_cast<float>(hidden);
+    c.pow2 = (hidden & (hidden - 1)) == 0;
+    c.inv = c.pow2 ? __uint_as_float(static_cast<uint32_t>(127 - __ffs(hidden) + 1) << 23) : 0.f;
+    return c;
+}
+__device__ inline float row_factor(float S, const RowCount &c, float eps)
+{
+    return rsqrtf((c.pow2 ? S * c.inv : S / c.n) + eps);
 }
 
 } // namespace rmsnorm

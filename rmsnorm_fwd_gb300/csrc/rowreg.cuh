@@ -26,7 +26,7 @@
 //
 // EPI selects what the kernels write (rmsnorm_epilogue_t): the plain output,
 // the weight plus a bias, or a block-scaled output (MXFP8 / MXFP4 / NVFP4
-// codes and scales, q_store in device_common.cuh).  Only the plain
+// codes and scales, q_emit in device_common.cuh).  Only the plain
 // instantiations feed the plain entry points; the others are separate
 // template instances with their own table entries.
 #pragma once
@@ -71,16 +71,14 @@ __device__ inline float block_total_rare(float s, float *sh, int lane, int warp,
 
 // One vector of a row, scaled by rr and written: the plain, weight-bias or
 // block-scaled output (every lane of the warp calls it for the block-scaled
-// ones; `live`: the vector is part of the row).
-template <int DT, int VB, int CP, int EPI, bool XW, bool PACKED>
-__device__ inline void emit_vec(const Vec<VB> &xk, const Vec<VB> &wk, const char *xp,
-                                const char *wp, float rr, float bias, const QParams &qp,
-                                bool live, bool leader, char *yp, uint8_t *sp, bool up)
+// ones, in the (x * r) * w order; `live`: the vector is part of the row).
+template <int DT, int VB, int CP, int EPI, bool PACKED>
+__device__ inline void emit_vec(const Vec<VB> &xk, const Vec<VB> &wk, float rr, float bias,
+                                const QParams &qp, bool live, bool leader, char *yp, uint8_t *sp)
 {
     constexpr bool MX = EPI >= RMSNORM_EPI_MXFP8;
     if constexpr (MX) {
-        q_store<DT, VB, EPI - RMSNORM_EPI_MXFP8, XW>(xk, wk, xp, wp, rr, qp, live, leader, yp, sp,
-                                                      up);
+        q_emit<DT, VB, EPI - RMSNORM_EPI_MXFP8, false>(xk, wk, rr, qp, live, leader, yp, sp);
     } else if (live) {
         Vec<VB> o;
         if constexpr (EPI == RMSNORM_EPI_BIAS)
@@ -93,6 +91,32 @@ __device__ inline void emit_vec(const Vec<VB> &xk, const Vec<VB> &wk, const char
     }
 }
 
+// The exact-product form's fallback (q_emit): the vectors t + j * tpr, j < NV,
+// of lane t of a group of tpr lanes written again in the (x * r) * w order,
+// from x and w read again (rolled, so that the common path's register
+// allocation is not raised for it).  Every lane of the warp calls it.
+template <int DT, int VB, int NV, int Q>
+__device__ __forceinline__ void q_redo(const char *xr, const char *wt, char *yr, uint8_t *sr, int t,
+                                    int tpr, int nvec, bool active, float r, const QParams &qp)
+{
+    constexpr int LPB = QGeo<DT, VB, Q>::kLanes;
+    constexpr int OB = QGeo<DT, VB, Q>::kCodeBytes;
+#pragma unroll 1
+    for (int j = 0; j < NV; ++j) {
+        const bool live = active && t + j * tpr < nvec;
+        Vec<VB> xk, wk;
+        if (live) {
+            ld_stream<0>(xk, xr + j * tpr * VB);
+            ld_weight(wk, wt + j * tpr * VB);
+        } else {
+            vzero(xk);
+            vzero(wk);
+        }
+        q_emit<DT, VB, Q, false>(xk, wk, r, qp, live, t % LPB == 0, yr + j * tpr * OB,
+                                 sr + (t + j * tpr) / LPB);
+    }
+}
+
 // The range guard's redo of one row (device_common.cuh): the row is read
 // again from memory (nothing of it is written yet), its sum formed from k x,
 // and the whole row scaled and written, one vector at a time (rolled loops,
@@ -101,7 +125,7 @@ __device__ inline void emit_vec(const Vec<VB> &xk, const Vec<VB> &wk, const char
 // group, WARP, or the whole block) owns vectors t + j * tpr, j < NV.
 // `redo`: this group's row needs it (WARP: the other groups of the warp come
 // along for the shuffles and write their rows with the plain factor `r`).
-template <int DT, int VB, int NV, int TPR, int CP, int EPI, bool XW, bool PACKED>
+template <int DT, int VB, int NV, int TPR, int CP, int EPI, bool PACKED>
 __device__ __forceinline__ void redo_row(const char *xr, const char *wt, char *yr, uint8_t *sr,
                                       int t, int tpr, int nvec, bool active, bool redo, float s,
                                       float r, float n, float eps, float bias, QParams qp,
@@ -143,9 +167,8 @@ __device__ __forceinline__ void redo_row(const char *xr, const char *wt, char *y
             vzero(xk);
             vzero(wk);
         }
-        emit_vec<DT, VB, CP, EPI, false, PACKED>(xk, wk, xr + j * tpr * VB, wt + j * tpr * VB, rr,
-                                              bias, qp, live, t % LPB == 0, yr + j * tpr * OB,
-                                              sr + (t + j * tpr) / LPB, up);
+        emit_vec<DT, VB, CP, EPI, PACKED>(xk, wk, rr, bias, qp, live, t % LPB == 0,
+                                          yr + j * tpr * OB, sr + (t + j * tpr) / LPB);
     }
 }
 
@@ -177,7 +200,8 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
     const int nvec = hidden / VPE;
     const int t = threadIdx.x % TPR;
     const int g = threadIdx.x / TPR;
-    const float n = static_cast<float>(hidden);
+    const RowCount rc = row_count(hidden);
+    const float n = rc.n;
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
     const int64_t out_row = MX ? int64_t(hidden) * QFmt<Q>::kBits / 8 : row_bytes; // per row
     const char *wt = static_cast<const char *>(w) + t * VB;
@@ -213,14 +237,14 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
         for (int k = 0; k < NV; ++k)
             s = MX ? sumsq_mixed<DT, VB>(xv[k], s) : sumsq<DT, VB>(xv[k], s);
         s = group_allreduce<TPR>(s);
-        const float r = row_factor(s, n, eps);
+        const float r = MX ? row_factor(s, rc, eps) : row_factor(s, n, eps);
         if constexpr (kRangeGuard<DT>) {
             // Range guard, warp-uniform (the groups of a warp reduce with
             // whole-warp shuffles): rare rows are redone from memory.
             const bool redo = sum_needs_rescale(s, eps);
             if (__any_sync(0xFFFFFFFFu, redo)) {
                 const int64_t row2 = opaque(row);
-                redo_row<DT, VB, NV, TPR, CP, EPI, XW, false>(
+                redo_row<DT, VB, NV, TPR, CP, EPI, false>(
                     static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt, yr,
                     MX ? scales + row2 * (hidden / QFmt<Q>::kBlock) : nullptr, t, TPR, nvec,
                     active, redo, s, r, n, eps, bias, qp, nullptr);
@@ -231,6 +255,7 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
         for (int k = 0; k < NV; ++k)
             reuse_barrier(xv[k]);
 
+        bool bad = false; // exact-product blocks to write again (q_emit)
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if constexpr (MX) {
@@ -242,9 +267,10 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
                     ld_weight(wk, wt + k * TPR * VB);
                 else
                     vzero(wk);
-                q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * TPR * VB, wt + k * TPR * VB, r, qp, live,
-                                   t % LPB == 0, yr + k * TPR * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
+                const bool b = q_emit<DT, VB, Q, XW>(
+                    xv[k], wk, r, qp, live, t % LPB == 0, yr + k * TPR * OB,
+                    scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * TPR) / LPB);
+                bad |= b && live;
             } else if (active && t + k * TPR < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -258,6 +284,13 @@ warp_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t row
                     scale<DT, VB>(o, xv[k], wk, r);
                 st_stream<CP>(yr + k * TPR * VB, o);
             }
+        }
+        if (XW && __any_sync(0xFFFFFFFFu, bad)) {
+            const int64_t row2 = opaque(row);
+            q_redo<DT, VB, NV, Q>(static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt,
+                                  static_cast<char *>(y) + row2 * out_row + t * OB,
+                                  scales + row2 * (hidden / QFmt<Q>::kBlock), t, TPR, nvec,
+                                  active, r, qp);
         }
     }
 }
@@ -292,7 +325,8 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
     const int warp = t >> 5;
     const int nwarps = tpr >> 5;
     const int stride = tpr * VB; // bytes between a thread's consecutive vectors
-    const float n = static_cast<float>(hidden);
+    const RowCount rc = row_count(hidden);
+    const float n = rc.n;
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
     const int64_t out_row = MX ? int64_t(hidden) * QFmt<Q>::kBits / 8 : row_bytes;
     const char *wt = static_cast<const char *>(w) + t * VB;
@@ -332,13 +366,13 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
             const float tot = lane < nwarps ? part[it & 1][lane] : 0.f;
             s = group_allreduce<32>(tot);
         }
-        const float r = row_factor(s, n, eps);
+        const float r = MX ? row_factor(s, rc, eps) : row_factor(s, n, eps);
         if constexpr (kRangeGuard<DT>) {
             // Range guard, block-uniform (every warp holds the same s): a
             // rare row is redone from memory.
             if (sum_needs_rescale(s, eps)) {
                 const int64_t row2 = opaque(row);
-                redo_row<DT, VB, NV, TPRC == 32 ? 32 : 0, CP, EPI, XW, true>(
+                redo_row<DT, VB, NV, TPRC == 32 ? 32 : 0, CP, EPI, true>(
                     static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt, yr,
                     MX ? scales + row2 * (hidden / QFmt<Q>::kBlock) : nullptr, t, tpr, nvec, true,
                     true, s, r, n, eps, bias, qp, rare);
@@ -349,6 +383,7 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
         for (int k = 0; k < NV; ++k)
             reuse_barrier(xv[k]);
 
+        bool bad = false; // exact-product blocks to write again (q_emit)
 #pragma unroll
         for (int k = 0; k < NV; ++k) {
             if constexpr (MX) {
@@ -360,9 +395,10 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                     ld_weight(wk, wt + k * stride);
                 else
                     vzero(wk);
-                q_store<DT, VB, Q, XW>(xv[k], wk, xr + k * stride, wt + k * stride, r, qp, live,
-                                   t % LPB == 0, yr + k * tpr * OB,
-                                   scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
+                const bool b = q_emit<DT, VB, Q, XW>(
+                    xv[k], wk, r, qp, live, t % LPB == 0, yr + k * tpr * OB,
+                    scales + row * (hidden / QFmt<Q>::kBlock) + (t + k * tpr) / LPB);
+                bad |= b && live;
             } else if (t + k * tpr < nvec) {
                 Vec<VB> o;
                 Vec<VB> wk;
@@ -376,6 +412,13 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                     scale_packed<DT, VB>(o, xv[k], wk, r);
                 st_stream<CP>(yr + k * stride, o);
             }
+        }
+        if (XW && __any_sync(0xFFFFFFFFu, bad)) {
+            const int64_t row2 = opaque(row);
+            q_redo<DT, VB, NV, Q>(static_cast<const char *>(x) + row2 * row_bytes + t * VB, wt,
+                                  static_cast<char *>(y) + row2 * out_row + t * OB,
+                                  scales + row2 * (hidden / QFmt<Q>::kBlock), t, tpr, nvec, true,
+                                  r, qp);
         }
     }
 }
@@ -410,7 +453,8 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
     const int lane = t & 31;
     const int warp = t >> 5;
     const int nwarps = tpr >> 5;
-    const float n = static_cast<float>(hidden);
+    const RowCount rc = row_count(hidden);
+    const float n = rc.n;
     const int64_t row_bytes = static_cast<int64_t>(hidden) * E::kSize;
     const char *wb = static_cast<const char *>(w);
 
@@ -441,7 +485,7 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
         // it (in-place calls).
         __syncthreads();
         const float tot = group_allreduce<32>(lane < nwarps ? part[it & 1][lane] : 0.f);
-        float r = row_factor(tot, n, eps);
+        float r = MX ? row_factor(tot, rc, eps) : row_factor(tot, n, eps);
         bool up = false;
         if constexpr (kRangeGuard<DT>) {
             if (sum_needs_rescale(tot, eps)) { // block-uniform; a third pass over the row
@@ -487,10 +531,8 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                         vzero(xk);
                         vzero(wk);
                     }
-                    q_store<DT, VB, Q, XW>(xk, wk, xr + static_cast<int64_t>(v) * VB,
-                                       wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
-                                       lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
-                                       sr + v / LPB, true);
+                    q_emit<DT, VB, Q, false>(xk, wk, r, qp, v < nvec, lane % LPB == 0,
+                                             yr + static_cast<int64_t>(v) * OB, sr + v / LPB);
                 }
             } else {
 #pragma unroll 1
@@ -527,13 +569,22 @@ cta_loop_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                         vzero(wv[u]);
                     }
                 }
+                bool bad = false; // exact-product blocks to write again (q_emit)
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int v = v0 + lane + u * tpr;
-                    q_store<DT, VB, Q, XW>(xv[u], wv[u], xr + static_cast<int64_t>(v) * VB,
-                                       wb + static_cast<int64_t>(v) * VB, r, qp, v < nvec,
-                                       lane % LPB == 0, yr + static_cast<int64_t>(v) * OB,
-                                       sr + v / LPB);
+                    const bool b = q_emit<DT, VB, Q, XW>(xv[u], wv[u], r, qp, v < nvec,
+                                                         lane % LPB == 0,
+                                                         yr + static_cast<int64_t>(v) * OB,
+                                                         sr + v / LPB);
+                    bad |= b && v < nvec;
+                }
+                if (XW && __any_sync(0xFFFFFFFFu, bad)) {
+                    // q_redo takes lane-based pointers (lane + j * tpr, j < U,
+                    // from v0) and the row's scale base
+                    const int64_t vl = v0 + lane;
+                    q_redo<DT, VB, U, Q>(xr + vl * VB, wb + vl * VB, yr + vl * OB,
+                                         sr + v0 / LPB, lane, tpr, nvec - v0, true, r, qp);
                 }
             }
         } else {
@@ -663,6 +714,14 @@ constexpr int kWarpBlock = 256;
         CTA_ENTRY(DT, 32, 2, 256, 6, 1, EPI)
 
 #define ROWREG_SET(DT, EPI) WARP_ENTRY(DT, 16, 4, 1, 0, 0, EPI), ROWREG_SET_WIDE(DT, EPI)
+
+// The block-scaled outputs add blocks of a compile-time size (64, 96 or 128
+// threads, vector offsets and warp count known to the compiler) with four
+// 32-byte vectors per thread, register-capped at 64 (16, 10 or 8 resident
+// blocks per SM): rows of up to 256, 384 or 512 such vectors.
+#define ROWREG_SET_Q(DT, EPI)                                                                  \
+    ROWREG_SET_WIDE(DT, EPI), CTAF_ENTRY(DT, 32, 64, 4, 16, 1, EPI),                           \
+        CTAF_ENTRY(DT, 32, 96, 4, 10, 1, EPI), CTAF_ENTRY(DT, 32, 128, 4, 8, 1, EPI)
 
 } // namespace rowreg
 } // namespace rmsnorm

@@ -7,7 +7,7 @@ namespace rmsnorm {
 namespace rowreg {
 namespace {
 const KernelDesc kTable[] = {ROWREG_SET(RMSNORM_BF16, RMSNORM_EPI_BIAS),
-                             ROWREG_SET_WIDE(RMSNORM_BF16, RMSNORM_EPI_MXFP8)};
+                             ROWREG_SET_Q(RMSNORM_BF16, RMSNORM_EPI_MXFP8)};
 } // namespace
 } // namespace rowreg
 

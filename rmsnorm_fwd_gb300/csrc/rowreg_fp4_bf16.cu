@@ -6,8 +6,8 @@
 namespace rmsnorm {
 namespace rowreg {
 namespace {
-const KernelDesc kTable[] = {ROWREG_SET_WIDE(RMSNORM_BF16, RMSNORM_EPI_MXFP4),
-                             ROWREG_SET_WIDE(RMSNORM_BF16, RMSNORM_EPI_NVFP4)};
+const KernelDesc kTable[] = {ROWREG_SET_Q(RMSNORM_BF16, RMSNORM_EPI_MXFP4),
+                             ROWREG_SET_Q(RMSNORM_BF16, RMSNORM_EPI_NVFP4)};
 } // namespace
 } // namespace rowreg
 

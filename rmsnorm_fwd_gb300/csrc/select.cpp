@@ -626,6 +626,17 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
                            out) == RMSNORM_OK)
             return RMSNORM_OK;
     }
+    if (blockq && s.a32 && nvec > 256 && nvec <= 1024) {
+        // Blocks of a compile-time size with 4 vectors per thread where the
+        // row fills at least three quarters of their lanes.
+        const int64_t n32 = nvec / 2;
+        const int tprc = n32 <= 256 ? 64 : (n32 <= 384 ? 96 : 128);
+        const int minb = tprc == 64 ? 16 : (tprc == 96 ? 10 : 8);
+        if (4 * n32 > 3 * 4 * int64_t(tprc) &&
+            plan_cta_exact(s, 32, 4, tprc, minb, 1, tprc, tprc, INT_MAX,
+                           RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+            return RMSNORM_OK;
+    }
     if (blockq && s.a32 && nvec > 256 && nvec <= 1024 &&
         plan_cta_exact(s, 32, 2, 256, 6, 1, 0, tpr_for(nvec / 2, 2), INT_MAX,
                        RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)

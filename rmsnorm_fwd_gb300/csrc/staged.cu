@@ -400,10 +400,20 @@ staged_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t r
                     for (int k = 0; k < 4; ++k)
                         xv.w[k] = wv.w[k] = 0u;
                 }
-                q_store<DT, 16, Q, XW>(xv, wv, src + v * 16, wsm + v * 16, r, qp, live,
-                                   lane % G::kLanes == 0,
-                                   qr + static_cast<int64_t>(v) * G::kCodeBytes,
-                                   sr + v / G::kLanes);
+                const bool b = q_emit<DT, 16, Q, XW>(xv, wv, r, qp, live, lane % G::kLanes == 0,
+                                                     qr + static_cast<int64_t>(v) * G::kCodeBytes,
+                                                     sr + v / G::kLanes);
+                if (XW && __any_sync(0xFFFFFFFFu, b && live)) {
+                    // exact-product blocks outside their range: this vector again in
+                    // the (x * r) * w order, from the slot
+                    if (live) {
+                        xv = *reinterpret_cast<const Vec<16> *>(src + v * 16);
+                        wv = *reinterpret_cast<const Vec<16> *>(wsm + v * 16);
+                    }
+                    q_emit<DT, 16, Q, false>(xv, wv, r, qp, live, lane % G::kLanes == 0,
+                                             qr + static_cast<int64_t>(v) * G::kCodeBytes,
+                                             sr + v / G::kLanes);
+                }
             }
             __syncwarp();
             if (lane == 0)

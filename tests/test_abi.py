@@ -349,11 +349,14 @@ def test_epilogue_kernel_sets():
                                           if k["variant"] not in (rn.VARIANT_CLUSTER,
                                                                   rn.VARIANT_GRID)}
         # block-scaled outputs: the register and looped bodies except the 4-lane
-        # group, and the staged ring with register stores
+        # group, the staged ring with register stores, and their own blocks of
+        # 64, 96 and 128 threads (compile-time size) with four 32-byte vectors
+        # per thread, register-capped at 64
         want = {key(k) for k in plain if (k["variant"] in (rn.VARIANT_WARP_PER_ROW,
                                                            rn.VARIANT_CTA_PER_ROW)
                                           and k["tpr"] != 4)
                 or (k["variant"] == rn.VARIANT_STAGED and k["cache_policy"] != 3)}
+        want |= {(rn.VARIANT_CTA_PER_ROW, 32, t, 4, t, 1024 // t, 1) for t in (64, 96, 128)}
         assert {key(k) for k in mx} == want
         for epi in (rn.EPI_MXFP4, rn.EPI_NVFP4):
             assert {key(k) for k in ks if k["dtype"] == dt and k["epilogue"] == epi} == want
@@ -382,8 +385,19 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                         assert p.variant == rn.VARIANT_WARP_PER_ROW and p.vecs_per_thread == 4
                     else:
                         assert p.vec_bytes == 32 and p.vecs_per_thread in (2, 4)
-                        if 256 < nvec <= 1024:   # the register-capped 2-vector body
-                            assert ks[p.kernel_index]["min_blocks"] == 6
+                        if 256 < nvec <= 1024:
+                            # a compile-time block of 64 / 96 / 128 threads x 4
+                            # vectors where the row fills >= 3/4 of its lanes,
+                            # else the register-capped 2-vector body
+                            n32 = nvec // 2
+                            tprc = 64 if n32 <= 256 else (96 if n32 <= 384 else 128)
+                            if 4 * n32 > 3 * 4 * tprc:
+                                k = ks[p.kernel_index]
+                                assert (k["tpr"], k["nv"], k["min_blocks"]) == \
+                                    (tprc, 4, 1024 // tprc), (rows, hidden, dt, k)
+                                assert p.block_threads == tprc
+                            else:
+                                assert ks[p.kernel_index]["min_blocks"] == 6
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
