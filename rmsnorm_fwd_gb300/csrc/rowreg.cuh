@@ -715,13 +715,16 @@ constexpr int kWarpBlock = 256;
 
 #define ROWREG_SET(DT, EPI) WARP_ENTRY(DT, 16, 4, 1, 0, 0, EPI), ROWREG_SET_WIDE(DT, EPI)
 
-// The block-scaled outputs add blocks of a compile-time size (64, 96 or 128
-// threads, vector offsets and warp count known to the compiler) with four
-// 32-byte vectors per thread, register-capped at 64 (16, 10 or 8 resident
-// blocks per SM): rows of up to 256, 384 or 512 such vectors.
+// The block-scaled outputs add blocks of a compile-time size (vector offsets
+// and warp count known to the compiler; a single warp reduces with shuffles
+// only) with four 32-byte vectors per thread: one warp (up to 128 registers,
+// for 16 resident blocks per SM), 64, 96 or 128 threads (register-capped at
+// 64: 16, 10 or 8 resident blocks): rows of up to 128, 256, 384 or 512 such
+// vectors.
 #define ROWREG_SET_Q(DT, EPI)                                                                  \
-    ROWREG_SET_WIDE(DT, EPI), CTAF_ENTRY(DT, 32, 64, 4, 16, 1, EPI),                           \
-        CTAF_ENTRY(DT, 32, 96, 4, 10, 1, EPI), CTAF_ENTRY(DT, 32, 128, 4, 8, 1, EPI)
+    ROWREG_SET_WIDE(DT, EPI), CTAF_ENTRY(DT, 32, 32, 4, 16, 1, EPI),                           \
+        CTAF_ENTRY(DT, 32, 64, 4, 16, 1, EPI), CTAF_ENTRY(DT, 32, 96, 4, 10, 1, EPI),          \
+        CTAF_ENTRY(DT, 32, 128, 4, 8, 1, EPI)
 
 } // namespace rowreg
 } // namespace rmsnorm

@@ -154,15 +154,15 @@ int blocks_per_sm(int tpr, int maxt, int minb)
 
 // ---- warp-per-row: a group of TPR lanes (<= 32) per row
 int plan_warp_exact(const Shape &s, int tpr, int nv, int minb, int64_t grid_cap,
-                    rmsnorm_plan_t *p)
+                    rmsnorm_plan_t *p, int vb = 16)
 {
     clear(p);
     const int idx =
-        find_rowreg(RMSNORM_VARIANT_WARP_PER_ROW, s.dtype, 16, tpr, nv, 256, minb, 0, s.epi);
+        find_rowreg(RMSNORM_VARIANT_WARP_PER_ROW, s.dtype, vb, tpr, nv, 256, minb, 0, s.epi);
     if (idx < 0)
         return RMSNORM_ERR_VARIANT;
     p->variant = RMSNORM_VARIANT_WARP_PER_ROW;
-    p->vec_bytes = 16;
+    p->vec_bytes = vb;
     p->threads_per_row = tpr;
     p->vecs_per_thread = nv;
     p->block_threads = 256;
@@ -607,17 +607,30 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     // one, so it takes more elements per thread and, with 32-byte vectors,
     // persistent grids (the fastest plans of sweeps on GB300 over 2-32 KiB
     // bf16 rows for the three formats):
-    //   1-2 KiB rows: a warp per row, 4 vectors per lane (register-capped
-    //     for 8 blocks of 256 threads per SM), 16 blocks per SM;
-    //   2-4 KiB rows: 32-byte vectors, 2 per thread, 16 blocks per SM;
-    //   4-16 KiB rows: 32-byte vectors, 2 per thread, register-capped for 6
-    //     blocks of 256 threads per SM, one block per row (16-byte vectors,
-    //     4 per thread, when unaligned for 32);
+    //   1-2 KiB rows: a warp per row, 2 32-byte vectors per lane, 4 blocks
+    //     of 256 threads per SM (16-byte vectors, 4 per lane, register-capped
+    //     for 8 blocks, when unaligned for 32);
+    //   2-3 KiB rows: one warp, a block of its own, 4 32-byte vectors per
+    //     lane, 16 blocks per SM; 3-4 KiB rows: 32-byte vectors, 2 per
+    //     thread, 16 blocks per SM;
+    //   4-16 KiB rows: blocks of 64, 96 or 128 threads (a compile-time size)
+    //     with 4 32-byte vectors per thread, one block per row (16-byte
+    //     vectors, 4 per thread, when unaligned for 32);
     //   16-32 KiB rows: 32-byte vectors, 4 per thread, 4 blocks per SM.
     const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
+    if (blockq && s.a32 && nvec > 64 && nvec <= 128 &&
+        plan_warp_exact(s, 32, 2, 0, int64_t(s.sm_count) * 4, out, 32) == RMSNORM_OK)
+        return RMSNORM_OK;
     if (blockq && nvec > 64 && nvec <= 128 &&
         plan_warp_exact(s, 32, 4, 8, int64_t(s.sm_count) * 16, out) == RMSNORM_OK)
         return RMSNORM_OK;
+    if (blockq && s.a32 && nvec > 128 && nvec <= 192) {
+        const int64_t cap = int64_t(s.sm_count) * 16;
+        if (plan_cta_exact(s, 32, 4, 32, 16, 1, 32, 32, cap,
+                           cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW,
+                           out) == RMSNORM_OK)
+            return RMSNORM_OK;
+    }
     if (blockq && s.a32 && nvec > 128 && nvec <= 256) {
         const int tpr = tpr_for(nvec / 2, 2);
         const int64_t cap = int64_t(s.sm_count) * std::min(16, 2048 / tpr);
@@ -627,13 +640,13 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
             return RMSNORM_OK;
     }
     if (blockq && s.a32 && nvec > 256 && nvec <= 1024) {
-        // Blocks of a compile-time size with 4 vectors per thread where the
-        // row fills at least three quarters of their lanes.
+        // Blocks of a compile-time size with 4 vectors per thread, the
+        // smallest that holds the row (faster than the 2-vector body sized to
+        // the row even where the row fills only 70 % of their lanes).
         const int64_t n32 = nvec / 2;
         const int tprc = n32 <= 256 ? 64 : (n32 <= 384 ? 96 : 128);
         const int minb = tprc == 64 ? 16 : (tprc == 96 ? 10 : 8);
-        if (4 * n32 > 3 * 4 * int64_t(tprc) &&
-            plan_cta_exact(s, 32, 4, tprc, minb, 1, tprc, tprc, INT_MAX,
+        if (plan_cta_exact(s, 32, 4, tprc, minb, 1, tprc, tprc, INT_MAX,
                            RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
             return RMSNORM_OK;
     }

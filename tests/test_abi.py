@@ -350,13 +350,14 @@ def test_epilogue_kernel_sets():
                                                                   rn.VARIANT_GRID)}
         # block-scaled outputs: the register and looped bodies except the 4-lane
         # group, the staged ring with register stores, and their own blocks of
-        # 64, 96 and 128 threads (compile-time size) with four 32-byte vectors
-        # per thread, register-capped at 64
+        # a compile-time size with four 32-byte vectors per thread: one warp
+        # (16 resident), 64, 96 and 128 threads (register-capped at 64)
         want = {key(k) for k in plain if (k["variant"] in (rn.VARIANT_WARP_PER_ROW,
                                                            rn.VARIANT_CTA_PER_ROW)
                                           and k["tpr"] != 4)
                 or (k["variant"] == rn.VARIANT_STAGED and k["cache_policy"] != 3)}
         want |= {(rn.VARIANT_CTA_PER_ROW, 32, t, 4, t, 1024 // t, 1) for t in (64, 96, 128)}
+        want.add((rn.VARIANT_CTA_PER_ROW, 32, 32, 4, 32, 16, 1))
         assert {key(k) for k in mx} == want
         for epi in (rn.EPI_MXFP4, rn.EPI_NVFP4):
             assert {key(k) for k in ks if k["dtype"] == dt and k["epilogue"] == epi} == want
@@ -379,25 +380,27 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                 nvec = hidden * (4 if dt == rn.F32 else 2) // 16
                 if epi == rn.EPI_MXFP8 and rows > SMS and 64 < nvec <= 2048:
                     # block-scaled prefill rows of 1-32 KiB: their own shapes
-                    # (a warp x 4 for 1-2 KiB rows, then 32-byte vectors, 2 or
-                    # 4 per thread)
+                    # (a warp x two 32-byte vectors for 1-2 KiB rows on 4 blocks
+                    # per SM, a one-warp block x four for 2-3 KiB rows, then
+                    # 32-byte vectors, 2 or 4 per thread)
                     if nvec <= 128:
-                        assert p.variant == rn.VARIANT_WARP_PER_ROW and p.vecs_per_thread == 4
+                        assert p.variant == rn.VARIANT_WARP_PER_ROW
+                        assert (p.vec_bytes, p.vecs_per_thread) == (32, 2)
+                        assert p.grid <= 4 * SMS
+                    elif nvec <= 192:
+                        k = ks[p.kernel_index]
+                        assert (k["tpr"], k["nv"], p.vec_bytes, p.block_threads) == (32, 4, 32, 32)
                     else:
                         assert p.vec_bytes == 32 and p.vecs_per_thread in (2, 4)
                         if 256 < nvec <= 1024:
-                            # a compile-time block of 64 / 96 / 128 threads x 4
-                            # vectors where the row fills >= 3/4 of its lanes,
-                            # else the register-capped 2-vector body
+                            # the smallest compile-time block of 64 / 96 / 128
+                            # threads x 4 vectors that holds the row
                             n32 = nvec // 2
                             tprc = 64 if n32 <= 256 else (96 if n32 <= 384 else 128)
-                            if 4 * n32 > 3 * 4 * tprc:
-                                k = ks[p.kernel_index]
-                                assert (k["tpr"], k["nv"], k["min_blocks"]) == \
-                                    (tprc, 4, 1024 // tprc), (rows, hidden, dt, k)
-                                assert p.block_threads == tprc
-                            else:
-                                assert ks[p.kernel_index]["min_blocks"] == 6
+                            k = ks[p.kernel_index]
+                            assert (k["tpr"], k["nv"], k["min_blocks"]) == \
+                                (tprc, 4, 1024 // tprc), (rows, hidden, dt, k)
+                            assert p.block_threads == tprc
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
