@@ -711,7 +711,7 @@ constexpr int kWarpBlock = 256;
         CTA_ENTRY(DT, 16, 3, 512, 3, 1, EPI), CTA_ENTRY(DT, 16, 4, 256, 6, 1, EPI),            \
         CTA_ENTRY(DT, 16, 4, 512, 2, 1, EPI), CTA_ENTRY(DT, 16, 8, 512, 0, 1, EPI),            \
         CTAF_ENTRY(DT, 16, 512, 1, 0, 0, EPI), LOOP_ENTRY(DT, 16, 512, 2, 1, EPI),             \
-        CTA_ENTRY(DT, 32, 2, 256, 6, 1, EPI)
+        CTA_ENTRY(DT, 32, 2, 256, 6, 1, EPI), CTA_ENTRY(DT, 32, 4, 320, 2, 1, EPI)
 
 #define ROWREG_SET(DT, EPI) WARP_ENTRY(DT, 16, 4, 1, 0, 0, EPI), ROWREG_SET_WIDE(DT, EPI)
 

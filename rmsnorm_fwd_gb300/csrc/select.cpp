@@ -389,7 +389,9 @@ int plan_staged_wide(const Shape &s, rmsnorm_plan_t *p)
     const int rc = plan_staged(s, 1, small ? 1 : 2, small ? 8 : 4, false, p);
     if (rc != RMSNORM_OK)
         return rc;
-    const int max_stages = s.row_bytes <= 40 * 1024 ? 4 : 2;
+    // Ring depth: 4 slots up to 40 KiB rows, 3 up to 48 KiB (1.6 % ahead of 2
+    // on 48 KiB rows), then 2.
+    const int max_stages = s.row_bytes <= 40 * 1024 ? 4 : (s.row_bytes <= 48 * 1024 ? 3 : 2);
     const int groups = p->rows_per_block;
     int stages = std::min(p->stages, max_stages) / groups * groups;
     if (stages < groups || stages < 2)
@@ -680,15 +682,17 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
 wide:
     // 16-24 KiB and 32-40 KiB rows: 32-byte vectors, 4 per thread, one block
     // per row (on the final sweep 2.6-6.8 % faster there than the persistent
-    // and staged bodies below; at 32 KiB the persistent one stays ahead).
-    // Plain output only: the weight-offset build of this body needs 107
-    // registers, which leaves one 320-thread block per SM instead of two
-    // (4.5 against 6.5 TB/s on 40 KiB rows).
-    if (s.epi == RMSNORM_EPI_PLAIN && s.a32 &&
+    // and staged bodies below; at 32 KiB the persistent one stays ahead), two
+    // blocks of <= 320 threads per SM.  The weight-offset output takes the
+    // build capped at 96 registers, so that its two blocks always fit.
+    if (s.epi <= RMSNORM_EPI_BIAS && s.a32 &&
         ((s.row_bytes > 16384 && s.row_bytes <= 24576) ||
          (s.row_bytes > 32768 && s.row_bytes <= 40960)) &&
-        plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), INT_MAX,
-                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+        (s.epi == RMSNORM_EPI_PLAIN
+             ? plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), INT_MAX,
+                              RMSNORM_VARIANT_CTA_PER_ROW, out)
+             : plan_cta_exact(s, 32, 4, 320, 2, 1, 0, tpr_for(nvec / 2, 4), INT_MAX,
+                              RMSNORM_VARIANT_CTA_PER_ROW, out)) == RMSNORM_OK)
         return RMSNORM_OK;
     // 16..32 KiB rows: the register bodies on a persistent grid.
     if (nvec <= 2048 && plan_prefill_wide(s, RMSNORM_VARIANT_PERSISTENT, true, out) == RMSNORM_OK)

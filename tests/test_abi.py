@@ -412,10 +412,14 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                 row_bytes = nvec * 16
                 if epi == rn.EPI_BIAS and rows > SMS and \
                         (16384 < row_bytes <= 24576 or 32768 < row_bytes <= 40960):
-                    # the plain output's 32-byte four-vector blocks are not
-                    # taken with the weight offset (one block per SM there)
+                    # the plain output's 32-byte four-vector blocks, in the
+                    # build capped at 96 registers for the weight offset (two
+                    # blocks of <= 320 threads per SM)
                     assert p0.vec_bytes == 32 and p0.vecs_per_thread == 4
-                    assert not (p.vec_bytes == 32 and p.vecs_per_thread == 4)
+                    assert (p.vec_bytes, p.vecs_per_thread, p.threads_per_row) == \
+                        (32, 4, p0.threads_per_row)
+                    k = ks[p.kernel_index]
+                    assert (k["block"], k["min_blocks"]) == (320, 2)
                     continue
                 if p0.variant not in (rn.VARIANT_CLUSTER, rn.VARIANT_GRID):
                     k, k0 = ks[p.kernel_index], ks[p0.kernel_index]
@@ -614,11 +618,14 @@ def test_prefill_rows_of_16_to_24_and_32_to_40_kib_take_32_byte_blocks():
         assert p.vecs_per_thread == 4 and p.grid == 16384, (hidden, p.as_dict())
     assert plan(16384, 16384, rn.BF16)[1].variant == rn.VARIANT_PERSISTENT   # 32 KiB rows
     assert plan(16384, 24576, rn.BF16)[1].variant == rn.VARIANT_STAGED       # 48 KiB rows
-    # the weight-offset output keeps the other bodies (its build of this one
-    # holds one block per SM, not two)
-    rc, p = rn.rmsnorm_plan_epilogue_status(A, 3 * A, 5 * A, 16384, 20480, rn.BF16,
-                                            rn.EPI_BIAS, SMS, OPTIN)
-    assert rc == rn.OK and p.variant == rn.VARIANT_STAGED
+    # the weight-offset output takes the same shape in its build capped at 96
+    # registers (two blocks of <= 320 threads per SM)
+    for hidden in (10240, 20480):
+        rc, p = rn.rmsnorm_plan_epilogue_status(A, 3 * A, 5 * A, 16384, hidden, rn.BF16,
+                                                rn.EPI_BIAS, SMS, OPTIN)
+        assert rc == rn.OK and p.variant == rn.VARIANT_CTA_PER_ROW and p.vec_bytes == 32
+        k = rn.kernels()[p.kernel_index]
+        assert (k["nv"], k["block"], k["min_blocks"]) == (4, 320, 2)
 
 
 def test_host_mapped_plan_caps_wide_row_grids_at_two_blocks_per_sm():
