@@ -353,6 +353,42 @@ def test_quant_exact_products_special_and_extreme_blocks(dtype, fmt, g):
 
 
 @pytest.mark.parametrize("fmt,g", QFMTS)
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_quant_exact_products_fallback_in_every_prefill_body(dtype, fmt, g):
+    """Prefill batches (more rows than SMs) at widths that reach every
+    block-scaled prefill body (16-bit elements) -- a warp per row (2 KiB
+    rows), the one-warp block (3 KiB), the 64-thread two-vector body (4 KiB),
+    the compile-time 64 / 96 / 128-thread four-vector blocks (5.6, 8, 10, 14
+    and 16 KiB rows, some with idle lanes) and the 24 KiB persistent body --
+    with blocks the
+    exact-product form hands back (zero, NaN, Inf, products below 2^-100) at
+    the start, middle and end of rows, so that the warp's one vote per row
+    fires for each vector slot of a thread; the other rows of the batch keep
+    the fast form.  Every row is compared with the oracle."""
+    rows = 160
+    for hidden in (1024, 1536, 2048, 2880, 4096, 5120, 7168, 8192, 12288):
+        rng = np.random.default_rng(hidden)
+        z = rng.standard_normal((rows, hidden)).astype(np.float32)
+        h32 = hidden // 32
+        at = lambda i: 32 * i
+        for r, blk in enumerate((0, h32 // 4, h32 // 2, 3 * h32 // 4, h32 - 1), start=1):
+            z[r, at(blk):at(blk) + 32] = 0.0              # one zero block per row
+        z[6, [at(b) for b in (0, h32 // 3, 2 * h32 // 3, h32 - 1)]] = np.nan
+        z[7, hidden - 1] = np.inf
+        z[8, :] = 0.0
+        for k in range(4):                               # a zero block per quarter
+            z[9, at(k * h32 // 4):at(k * h32 // 4) + 32] = 0.0
+        if dtype == "bf16":                              # products below 2^-100
+            z[10, at(h32 // 2):at(h32 // 2) + 32] *= 1e-32
+            z[11, hidden - 32:] *= 1e-32
+        x = inputs.to_storage(z, dtype)
+        w = inputs.to_storage(np.abs(rng.normal(1.0, 0.1, (1, hidden))).astype(np.float32),
+                              dtype)[0]
+        q, s = run_q(x, w, -0.0, 1e-6, dtype, fmt, g)
+        compare_quant(q, s, x, w, -0.0, 1e-6, dtype, fmt, g)
+
+
+@pytest.mark.parametrize("fmt,g", QFMTS)
 def test_quant_without_offset_every_forced_variant(fmt, g):
     """The exact-product path in every body that writes block-scaled rows:
     warp-per-row (short rows), block-per-row, persistent, looped (long rows)
