@@ -618,7 +618,11 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     //   4-16 KiB rows: blocks of 64, 96 or 128 threads (a compile-time size)
     //     with 4 32-byte vectors per thread, one block per row (16-byte
     //     vectors, 4 per thread, when unaligned for 32);
-    //   16-32 KiB rows: 32-byte vectors, 4 per thread, 4 blocks per SM.
+    //   16-24 KiB rows: 32-byte vectors, 4 per thread, capped at 96
+    //     registers, one block per row; 24-32 KiB rows: the same vectors
+    //     uncapped, 2 per thread on 2 blocks per SM (MX) or 4 on 4 (NVFP4);
+    //     32-40 KiB rows: the capped body on 6 blocks per SM; longer rows:
+    //     the looped body.
     const bool blockq = s.epi >= RMSNORM_EPI_MXFP8;
     if (blockq && s.a32 && nvec > 64 && nvec <= 128 &&
         plan_warp_exact(s, 32, 2, 0, int64_t(s.sm_count) * 4, out, 32) == RMSNORM_OK)
@@ -659,6 +663,28 @@ int plan_launch(const void *x, const void *w, const void *y, int64_t rows, int64
     if (blockq && nvec > 128 && nvec <= 1024 &&
         plan_cta_exact(s, 16, 4, 256, 6, 1, 0, tpr_for(nvec, 4), INT_MAX,
                        RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+        return RMSNORM_OK;
+    // 16-24 KiB and 32-40 KiB rows: the same vectors in the body capped at 96
+    // registers, one block per row, and on a persistent grid of 6 blocks per
+    // SM (interleaved timings on GB300, 20-40 KiB bf16 rows of the three
+    // formats: 17-39 % faster than the uncapped body and the looped one; at
+    // 24-32 KiB and 40-64 KiB those stay ahead or within 5 %).
+    if (blockq && s.a32 && nvec > 1024 && nvec <= 1536 &&
+        plan_cta_exact(s, 32, 4, 320, 2, 1, 0, tpr_for(nvec / 2, 4), INT_MAX,
+                       RMSNORM_VARIANT_CTA_PER_ROW, out) == RMSNORM_OK)
+        return RMSNORM_OK;
+    if (blockq && s.a32 && nvec > 2048 && nvec <= 2560) {
+        const int64_t cap = int64_t(s.sm_count) * 6;
+        if (plan_cta_exact(s, 32, 4, 320, 2, 1, 0, tpr_for(nvec / 2, 4), cap,
+                           cap < s.rows ? RMSNORM_VARIANT_PERSISTENT : RMSNORM_VARIANT_CTA_PER_ROW,
+                           out) == RMSNORM_OK)
+            return RMSNORM_OK;
+    }
+    // 24-32 KiB rows: MXFP8 / MXFP4 two 32-byte vectors per thread on 2
+    // blocks per SM (1-4.5 % ahead there), NVFP4 four on 4 blocks per SM.
+    if (blockq && s.a32 && nvec > 1536 && nvec <= 2048 && s.epi != RMSNORM_EPI_NVFP4 &&
+        plan_cta_exact(s, 32, 2, 1024, 0, 1, 0, tpr_for(nvec / 2, 2), int64_t(s.sm_count) * 2,
+                       RMSNORM_VARIANT_PERSISTENT, out) == RMSNORM_OK)
         return RMSNORM_OK;
     if (blockq && s.a32 && nvec > 1024 && nvec <= 2048 &&
         plan_cta_exact(s, 32, 4, 512, 0, 1, 0, tpr_for(nvec / 2, 4), int64_t(s.sm_count) * 4,

@@ -401,12 +401,29 @@ def test_epilogue_selector_matches_plain_bodies_outside_the_staged_range(epi):
                             assert (k["tpr"], k["nv"], k["min_blocks"]) == \
                                 (tprc, 4, 1024 // tprc), (rows, hidden, dt, k)
                             assert p.block_threads == tprc
+                        if 1536 < nvec <= 2048:
+                            # 24-32 KiB rows, MXFP8: two vectors per thread on
+                            # 2 blocks per SM
+                            assert p.vecs_per_thread == 2 and p.grid <= 2 * SMS
+                        if 1024 < nvec <= 1536:
+                            # 16-24 KiB rows: the body capped at 96 registers,
+                            # one block per row
+                            k = ks[p.kernel_index]
+                            assert (k["nv"], k["block"], k["min_blocks"]) == (4, 320, 2)
+                            assert p.grid == rows
                     assert p.threads_per_row * p.vecs_per_thread * p.vec_bytes >= nvec * 16, \
                         (rows, hidden, dt, p.as_dict())
                     continue
                 if epi == rn.EPI_MXFP8 and rows > SMS and nvec > 2048:
-                    # rows above 32 KiB: the looped body (not the ring, not the
-                    # plain output's 32-byte blocks)
+                    if nvec <= 2560:
+                        # 32-40 KiB rows: the capped 32-byte four-vector body on
+                        # 6 blocks per SM
+                        k = ks[p.kernel_index]
+                        assert (k["nv"], k["block"], k["min_blocks"]) == (4, 320, 2)
+                        assert p.grid == min(rows, 6 * SMS)
+                        continue
+                    # longer rows: the looped body (not the ring, not the plain
+                    # output's 32-byte blocks)
                     assert p.variant != rn.VARIANT_STAGED and p.vecs_per_thread == 0
                     continue
                 row_bytes = nvec * 16
