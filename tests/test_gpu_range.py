@@ -55,8 +55,10 @@ EXPS = {
              64, 70, 80, 90, 100, 110, 120, 126],
     "f32": [-145, -140, -133, -126, -120, -110, -100, -90, -80, -70, -64, -60, -50, 0, 50, 60,
             63, 64, 70, 80, 90, 100, 110, 120, 126],
-    # f16 squares stay inside fp32's range; its own range ends instead
-    "f16": [-24, -20, -14, -10, 0, 5, 10, 14, 15],
+    # f16 squares stay inside fp32's range; its own range ends instead (2^14 is
+    # the top binade that 3.9 * 2^e keeps below f16's largest value, 65504;
+    # Inf entries are the non-finite test's)
+    "f16": [-24, -20, -14, -10, 0, 5, 10, 13, 14],
 }
 
 
