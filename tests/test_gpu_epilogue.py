@@ -441,17 +441,23 @@ def test_fp4_argument_errors():
 @pytest.mark.parametrize("rows,hidden,dtype", [(2048, 20480, "bf16"), (1024, 32768, "f16"),
                                                (600, 9000, "f32"), (160, 36864, "bf16")])
 def test_epilogues_on_the_staged_ring(epi, rows, hidden, dtype):
-    """32-72 KiB rows: the weight-bias output runs on the shared-memory ring;
-    the block-scaled outputs on the looped body, and on the ring when forced."""
+    """32-72 KiB rows: the weight-bias output runs on the shared-memory ring
+    above 40 KiB (one block per row with 32-byte vectors on 32-40 KiB rows),
+    and on the ring when forced; the block-scaled outputs on the looped body,
+    and on the ring when forced."""
     x, w = inputs.random_case(rows, hidden, dtype, seed=hidden + 7)
     idx = sample_rows(rows, 48, seed=rows)
     xd, wd = to_device(x, dtype), to_device(w, dtype)
     if epi == "bias":
-        y = rn.rms_norm_bias(xd, wd, 0.5, 1e-6)
-        torch.cuda.synchronize()
-        if hidden * (4 if dtype == "f32" else 2) > 32768:
-            assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
-        compare(from_device(y, dtype), x, w, 1e-6, dtype, rows_idx=idx, bias=0.5)
+        row_bytes = hidden * (4 if dtype == "f32" else 2)
+        for v in (rn.VARIANT_AUTO, rn.VARIANT_STAGED):
+            y = rn.rms_norm_bias(xd, wd, 0.5, 1e-6, variant=v)
+            torch.cuda.synchronize()
+            if v == rn.VARIANT_STAGED or row_bytes > 40960:
+                assert rn.rmsnorm_last_variant() == rn.VARIANT_STAGED
+            elif row_bytes > 32768:
+                assert rn.rmsnorm_last_variant() == rn.VARIANT_CTA_PER_ROW
+            compare(from_device(y, dtype), x, w, 1e-6, dtype, rows_idx=idx, bias=0.5)
         return
     if hidden % 32:
         return
