@@ -7,6 +7,7 @@ Kernels are compiled for sm_103a only
 """
 from __future__ import annotations
 
+import fcntl
 import os
 import shutil
 import subprocess
@@ -47,12 +48,30 @@ def _newest_input() -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
+def _fresh() -> bool:
+    return os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input()
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile (if stale) and return the path of librmsnorm.so."""
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    """Compile (if stale) and return the path of librmsnorm.so.  Processes
+    that build at the same time (parallel test workers) take turns on a lock
+    file, so no two write the same object files; a process that waited finds
+    the library fresh and returns it."""
+    if not force and _fresh():
         return LIB
-    nvcc = _nvcc()
     os.makedirs(OUT, exist_ok=True)
+    with open(os.path.join(OUT, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            if not force and _fresh():
+                return LIB
+            return _build_locked(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool) -> str:
+    nvcc = _nvcc()
     common = [*CFLAGS, "-I", INCLUDE, "-I", CSRC]
 
     def compile_one(src: str) -> str:

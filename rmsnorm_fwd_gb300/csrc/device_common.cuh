@@ -514,6 +514,25 @@ __device__ inline void scale_packed(Vec<VB> &out, const Vec<VB> &xv, const Vec<V
                                            : Elem<DT>::narrow(f[k], 0.f);
 }
 
+// scale_bias() in the packed form: (x * r) * (w + bias), each operation an
+// IEEE fp32 one in the scalar order, so the same result.
+template <int DT, int VB>
+__device__ inline void scale_bias_packed(Vec<VB> &out, const Vec<VB> &xv, const Vec<VB> &wv,
+                                         float r, float bias)
+{
+    constexpr int P = VB / Elem<DT>::kSize / 2;
+    const uint64_t r2 = f2(r, r), b2 = f2(bias, bias);
+    float f[2 * P];
+#pragma unroll
+    for (int p = 0; p < P; ++p)
+        f2split(mul2(mul2(widen_pair<DT, VB>(xv, p), r2), add2(widen_pair<DT, VB>(wv, p), b2)),
+                f[2 * p], f[2 * p + 1]);
+#pragma unroll
+    for (int k = 0; k < Vec<VB>::kWords; ++k)
+        out.w[k] = Elem<DT>::kPerWord == 2 ? Elem<DT>::narrow(f[2 * k], f[2 * k + 1])
+                                           : Elem<DT>::narrow(f[k], 0.f);
+}
+
 // Sum of squares of one vector, element by element in the order sumsq()
 // uses, so the total is bit-identical to it.  16-bit elements go straight
 // into the mixed-precision fma (bf16 / f16 operands, fp32 accumulator): the

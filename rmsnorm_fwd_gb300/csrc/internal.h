@@ -33,7 +33,7 @@ struct LaunchArgs {
     float bias = -0.0f;     // weight offset (every epilogue but PLAIN); -0 adds nothing
     void *scales = nullptr; // block-scaled epilogues: the scales; y holds the codes
     float gscale = 1.0f;    // NVFP4: the per-tensor scale
-    void *scratch = nullptr; // grid variant: counters + partial sums (stream-ordered, per call)
+    void *scratch = nullptr; // grid variant: counters + partial sums (the context's, from create)
     bool xw = false;        // block-scaled output formed from exact x * w products (q_store)
 };
 

@@ -407,7 +407,7 @@ cta_rows_kernel(const void *x, const void *__restrict__ w, void *y, int64_t rows
                 else
                     ld_weight(wk, wt + k * stride);
                 if constexpr (EPI == RMSNORM_EPI_BIAS)
-                    scale_bias<DT, VB>(o, xv[k], wk, r, bias);
+                    scale_bias_packed<DT, VB>(o, xv[k], wk, r, bias);
                 else
                     scale_packed<DT, VB>(o, xv[k], wk, r);
                 st_stream<CP>(yr + k * stride, o);

@@ -1,7 +1,7 @@
 """Calls captured into CUDA graphs and replayed (the way decode loops run
 them), and calls from several host threads on their own streams at once:
 every body, including the cluster split and the grid barrier variant with
-its per-call stream-ordered scratch, against the oracle."""
+the context's scratch (allocated once at create), against the oracle."""
 import threading
 
 import pytest
