@@ -196,15 +196,17 @@ _COMMENT = re.compile(rb"/\*.*?\*/|//[^\n]*", re.S)
 def kernel_source_hash(dtype: str = "bf16") -> str:
     """Hash of the sources of the plain row kernels of `dtype` (the unit that
     compiles them and the headers it includes, plus the build flags), with
-    comments taken out: other kernels, host-only files such as the selector
-    and the wording of comments do not change them."""
+    comments taken out and runs of white space made one space: other kernels,
+    host-only files such as the selector, comments and layout do not change
+    them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "rmsnorm_fwd_gb300", "csrc")
     paths = [os.path.join(csrc, f) for f in (f"rowreg_{dtype}.cu",) + ROWREG_SOURCES]
     paths.append(os.path.join(ROOT, "include", "rmsnorm.h"))
     for p in paths:
         with open(p, "rb") as fh:
-            h.update(os.path.basename(p).encode() + _COMMENT.sub(b"", fh.read()))
+            code = re.sub(rb"\s+", b" ", _COMMENT.sub(b" ", fh.read())).strip()
+            h.update(os.path.basename(p).encode() + code)
     from rmsnorm_fwd_gb300 import _build
     h.update(repr((_build.GENCODE, _build.CFLAGS, _build.CUDA_FLAGS)).encode())
     return h.hexdigest()[:16]

@@ -40,3 +40,24 @@ def test_reference_arm_other_ranks_print_nothing():
     with redirect_stdout(buf):
         assert bench.run_reference(args, 2, 1) == 0
     assert buf.getvalue() == ""
+
+
+def test_traffic_record_follows_the_kernel_code_not_its_comments(tmp_path, monkeypatch):
+    """roofline.traffic is reported only while the row-kernel sources match the
+    capture: a changed comment keeps the hash, a changed statement does not."""
+    import shutil
+    h_repo = bench.kernel_source_hash("bf16")
+    root = tmp_path / "repo"
+    for d in ("rmsnorm_fwd_gb300/csrc", "include"):
+        (root / d).mkdir(parents=True)
+    for n in ["rowreg_bf16.cu", *bench.ROWREG_SOURCES]:
+        shutil.copy(f"{bench.ROOT}/rmsnorm_fwd_gb300/csrc/{n}", root / "rmsnorm_fwd_gb300/csrc" / n)
+    shutil.copy(f"{bench.ROOT}/include/rmsnorm.h", root / "include/rmsnorm.h")
+    monkeypatch.setattr(bench, "ROOT", str(root))
+    assert bench.kernel_source_hash("bf16") == h_repo
+    p = root / "rmsnorm_fwd_gb300/csrc/rowreg.cuh"
+    src = p.read_text()
+    p.write_text(src + "\n// a new comment\n/* and a\n   block comment */\n")
+    assert bench.kernel_source_hash("bf16") == h_repo
+    p.write_text(src.replace("__syncthreads();", "__syncthreads(); __syncthreads();", 1))
+    assert bench.kernel_source_hash("bf16") != h_repo
