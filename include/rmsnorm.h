@@ -24,9 +24,8 @@
  * element type.  All three are DEVICE pointers owned by the caller; the
  * library never frees or retains them.  The only memory the library itself
  * allocates is its per-device context, at rmsnorm_create: a 4-byte device
- * status word, the grid variant's fixed scratch (status word + fixed
- * scratch, allocated at create) and host-side state.  No call after
- * rmsnorm_create allocates device memory.
+ * status word, the grid variant's fixed scratch and host-side state.  No
+ * call after rmsnorm_create allocates device memory.
  *
  * Aliasing.  y == x (exactly in place) is allowed.  Any other overlap between
  * y and x, or between y and weight, is rejected with RMSNORM_ERR_ALIASING.
