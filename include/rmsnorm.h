@@ -169,7 +169,16 @@ int rmsnorm_fwd(const void *x, const void *weight, void *y, int64_t rows, int64_
  * and an optional plan override: when `plan` is non-NULL and plan->variant
  * is not AUTO, that exact plan is launched after validation against the
  * shape (benchmark sweeps); when `plan` is non-NULL and plan->variant is
- * AUTO, the chosen plan is written back into it. */
+ * AUTO, the chosen plan is written back into it.
+ *
+ * The environment variable RMSNORM_FORCE_VARIANT (a variant name without
+ * its prefix -- warp_per_row, cta_per_row, staged, persistent, generic,
+ * cluster, grid -- or its number), read once per process, replaces the
+ * automatic choice of every device call that asks for one (rmsnorm_fwd, the
+ * epilogue calls, and this call with variant AUTO and no explicit plan), so
+ * a program can be run on one body without code changes; a shape that body
+ * cannot take returns RMSNORM_ERR_VARIANT or RMSNORM_ERR_MISALIGNED.  The
+ * host-only planners (rmsnorm_plan, rmsnorm_plan_epilogue) ignore it. */
 int rmsnorm_fwd_ex(const void *x, const void *weight, void *y, int64_t rows, int64_t hidden,
                    float eps, int dtype, void *stream, int variant, rmsnorm_plan_t *plan);
 

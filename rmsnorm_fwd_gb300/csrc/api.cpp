@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <cstdio>
 #include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include <cuda_runtime.h>
@@ -148,6 +149,41 @@ bool pdl_enabled()
 }
 thread_local int t_last_variant = 0;
 
+// RMSNORM_FORCE_VARIANT: a variant name (warp_per_row, cta_per_row, staged,
+// persistent, generic, cluster, grid) or its number; read once.  It replaces
+// the automatic choice of every call that asks for one, so a program can be
+// timed or checked on one body without code changes; a shape that body
+// cannot take returns RMSNORM_ERR_VARIANT, as a forced rmsnorm_fwd_ex does.
+int forced_variant()
+{
+    static const int v = [] {
+        const char *e = std::getenv("RMSNORM_FORCE_VARIANT");
+        if (!e || !e[0])
+            return int(RMSNORM_VARIANT_AUTO);
+        static const struct {
+            const char *name;
+            int v;
+        } kNames[] = {{"warp_per_row", RMSNORM_VARIANT_WARP_PER_ROW},
+                      {"cta_per_row", RMSNORM_VARIANT_CTA_PER_ROW},
+                      {"staged", RMSNORM_VARIANT_STAGED},
+                      {"persistent", RMSNORM_VARIANT_PERSISTENT},
+                      {"generic", RMSNORM_VARIANT_GENERIC},
+                      {"cluster", RMSNORM_VARIANT_CLUSTER},
+                      {"grid", RMSNORM_VARIANT_GRID}};
+        for (const auto &n : kNames)
+            if (std::strcmp(e, n.name) == 0)
+                return n.v;
+        char *end = nullptr;
+        const long k = std::strtol(e, &end, 10);
+        if (end != e && *end == 0 && k >= RMSNORM_VARIANT_WARP_PER_ROW &&
+            k <= RMSNORM_VARIANT_GRID)
+            return int(k);
+        std::fprintf(stderr, "rmsnorm: RMSNORM_FORCE_VARIANT=%s not understood; ignored\n", e);
+        return int(RMSNORM_VARIANT_AUTO);
+    }();
+    return v;
+}
+
 bool log_enabled()
 {
     static const bool on = [] {
@@ -244,6 +280,8 @@ int launch(const void *x, const void *w, void *y, int64_t rows, int64_t hidden, 
         p = *plan;
         rc = validate_plan(p, x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, epi);
     } else {
+        if (variant == RMSNORM_VARIANT_AUTO)
+            variant = forced_variant();
         rc = plan_launch(x, w, y, rows, hidden, dtype, ctx.sm_count, ctx.smem_optin, variant, &p,
                          epi);
     }
