@@ -17,7 +17,7 @@ import oracle
 import rmsnorm_fwd_gb300 as rn
 from rmsnorm_fwd_gb300 import inputs
 
-from _parity import compare, from_device, sample_rows, to_device
+from _parity import compare, compare_quant, from_device, sample_rows, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -293,3 +293,60 @@ def test_prefill_20_to_40_kib_rows(hidden, dtype):
     x, w = inputs.random_case(rows, hidden, dtype, seed=hidden)
     y = run(x, w, 1e-6, dtype)
     compare(y, x, w, 1e-6, dtype, rows_idx=sample_rows(rows, 64, seed=hidden))
+
+
+# ------------------------------------------------------------------ 64-bit offsets
+
+def _accepts_far(rows, hidden, dtype, variant, epi=rn.EPI_PLAIN):
+    """accepts() with fake pointers far enough apart for tensors of several GiB."""
+    sms, optin = rn.rmsnorm_device_limits()
+    base = 1 << 40
+    p = rn.Plan()
+    rc = rn._load().rmsnorm_plan_epilogue(base, 3 * base, 5 * base, rows, hidden,
+                                          rn.DTYPE_CODES[dtype], epi, sms, optin, variant,
+                                          rn.ctypes.byref(p))
+    return rc == rn.OK
+
+
+@pytest.mark.parametrize("dtype,hidden", [("bf16", 4096), ("f32", 1000), ("f16", 2880)])
+def test_offsets_beyond_4_gib(dtype, hidden):
+    """Tensors of more than 2^32 bytes (and, for 16-bit types, 2^31 elements):
+    rows around and past those offsets, on every body that takes the shape (plain output), and the
+    weight-offset and MXFP8 outputs on the automatic plan, against the oracle.
+    The rows repeat a block of 64 seeded rows (rows are independent), so the
+    oracle runs on that block only."""
+    es = 4 if dtype == "f32" else 2
+    rows = (1 << 32) // (hidden * es) + 97        # the last 97 rows start beyond 4 GiB
+    assert rows * hidden * es > (1 << 32)
+    blk = 64
+    xs, w_np = inputs.random_case(blk, hidden, dtype, seed=hidden)
+    reps = -(-rows // blk)
+    x = to_device(xs, dtype).repeat(reps, 1)[:rows]
+    w = to_device(w_np, dtype)
+    # first rows, rows around 2^31 elements and 2^32 bytes, the last rows
+    marks = [0, (1 << 31) // hidden, (1 << 32) // (hidden * es)]
+    idx = np.unique(np.clip(np.concatenate(
+        [np.arange(m - 3, m + 4) for m in marks] + [np.arange(rows - 8, rows)]), 0, rows - 1))
+    sel = torch.from_numpy(idx).cuda()
+    x_sel = xs[idx % blk]
+    y = torch.empty_like(x)
+    ran = 0
+    for v in VARIANTS:
+        if not _accepts_far(rows, hidden, dtype, v):
+            continue
+        y.zero_()
+        rn.rms_norm(x, w, 1e-6, out=y, variant=v)
+        torch.cuda.synchronize()
+        compare(from_device(y.index_select(0, sel), dtype), x_sel, w_np, 1e-6, dtype)
+        ran += 1
+    assert ran >= 3
+    y.zero_()
+    rn.rms_norm_bias(x, w, 0.5, 1e-6, out=y)
+    torch.cuda.synchronize()
+    compare(from_device(y.index_select(0, sel), dtype), x_sel, w_np, 1e-6, dtype, bias=0.5)
+    del y
+    if hidden % 32 == 0:
+        q, s = rn.rms_norm_quant(x, w, 1e-6, "mxfp8")
+        torch.cuda.synchronize()
+        compare_quant(q.index_select(0, sel).cpu().numpy(), s.index_select(0, sel).cpu().numpy(),
+                      x_sel, w_np, -0.0, 1e-6, dtype, "mxfp8")

@@ -158,3 +158,35 @@ def test_qk_workloads_sampled_tokens(name):
                                   width - hq * d, 0.0, wl.eps, wl.dtype)
         ref = np.concatenate([ref[:hq * d], ref_k])
         check_equal_within(got[t], ref, wl.dtype)
+
+
+def test_qk_norm_fused_buffer_beyond_4_gib():
+    """A fused QKV buffer of more than 2^32 bytes (32 q + 8 k + 8 v heads of
+    128 bf16 per token): tokens around and past the 4 GiB offset against the
+    oracle, v untouched.  The tokens repeat a block of 64 seeded tokens
+    (heads are independent), so the oracle runs on that block only."""
+    dtype, hq, hk, d, blk = "bf16", 32, 8, 128, 64
+    width = (hq + 2 * hk) * d
+    T = (1 << 32) // (width * 2) + 40
+    small = rand(blk * width, dtype, 11)
+    qw, kw = rand(d, dtype, 12), rand(d, dtype, 13)
+    ref, _ = oracle.qk_norm(small, np.zeros(1, small.dtype), qw, kw, blk, hq, 0, d, width, 0,
+                            0.0, 1e-6, dtype)
+    _, ref_k = oracle.qk_norm(np.zeros(1, small.dtype), ref[hq * d:], qw, kw, blk, 0, hk, d, 0,
+                              width, 0.0, 1e-6, dtype)
+    ref = np.concatenate([ref[:hq * d], ref_k]).reshape(blk, width)
+    dbuf = to_device(small.reshape(blk, width), dtype).repeat(-(-T // blk), 1)[:T]
+    dqw, dkw = to_device(qw, dtype), to_device(kw, dtype)
+    qp = dbuf.data_ptr()
+    kp = qp + hq * d * dbuf.element_size()
+    rn.rmsnorm_qk_norm(qp, kp, dqw.data_ptr(), dkw.data_ptr(), T, hq, hk, d, width, width, 0.0,
+                       1e-6, rn.DTYPE_CODES[dtype], torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    mark = (1 << 32) // (width * 2)
+    idx = np.unique(np.concatenate([np.arange(0, 4), np.arange(mark - 4, mark + 4),
+                                    np.arange(T - 8, T)]))
+    got = from_device(dbuf.index_select(0, torch.from_numpy(idx).cuda()), dtype)
+    want = ref[idx % blk]
+    check_equal_within(got[:, :(hq + hk) * d].ravel(), want[:, :(hq + hk) * d].ravel(), dtype)
+    assert np.array_equal(got[:, (hq + hk) * d:],
+                          small.reshape(blk, width)[idx % blk][:, (hq + hk) * d:])
