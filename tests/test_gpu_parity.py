@@ -350,3 +350,30 @@ def test_offsets_beyond_4_gib(dtype, hidden):
         torch.cuda.synchronize()
         compare_quant(q.index_select(0, sel).cpu().numpy(), s.index_select(0, sel).cpu().numpy(),
                       x_sel, w_np, -0.0, 1e-6, dtype, "mxfp8")
+
+
+def test_more_rows_than_a_grid_holds_blocks_of():
+    """2^31 + 5 rows of 16 bytes (x and y 34 GB each): more rows than the
+    launch grid has blocks, so every body that takes the shape walks its rows
+    with a 64-bit grid-stride loop; the first rows, rows around 2^31 and the
+    last rows against the oracle.  The rows repeat a block of 64 seeded rows."""
+    dtype, hidden, blk = "bf16", 8, 64
+    rows = (1 << 31) + 5
+    xs, w_np = inputs.random_case(blk, hidden, dtype, seed=31)
+    x = to_device(xs, dtype).repeat(-(-rows // blk), 1)[:rows]
+    w = to_device(w_np, dtype)
+    idx = np.unique(np.concatenate([np.arange(0, 4), np.arange((1 << 31) - 4, rows)]))
+    sel = torch.from_numpy(idx).cuda()
+    y = torch.empty_like(x)
+    ran = []
+    for v in VARIANTS:
+        if not _accepts_far(rows, hidden, dtype, v):
+            continue
+        y.fill_(0)
+        p = rn.Plan()
+        rn.rms_norm(x, w, 1e-6, out=y, variant=v, plan=p)
+        torch.cuda.synchronize()
+        assert 0 < p.grid < rows
+        compare(from_device(y.index_select(0, sel), dtype), xs[idx % blk], w_np, 1e-6, dtype)
+        ran.append(p.variant)
+    assert len(set(ran)) >= 4, ran
