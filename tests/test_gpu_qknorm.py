@@ -190,3 +190,25 @@ def test_qk_norm_fused_buffer_beyond_4_gib():
     check_equal_within(got[:, :(hq + hk) * d].ravel(), want[:, :(hq + hk) * d].ravel(), dtype)
     assert np.array_equal(got[:, (hq + hk) * d:],
                           small.reshape(blk, width)[idx % blk][:, (hq + hk) * d:])
+
+
+def _draw_qk(i):
+    rng = np.random.default_rng(7000 + i)
+    dtype = ["bf16", "f16", "f32"][rng.integers(3)]
+    d = int(rng.choice([64, 128, 256, 512, 80, 96, 192])) if rng.random() < 0.7 else \
+        int(rng.integers(1, 600))
+    hq = int(rng.integers(0, 40))
+    hk = int(rng.integers(0 if hq else 1, 12))
+    T = int(np.exp(rng.uniform(0, np.log(max(2, min(3000, (1 << 21) // ((hq + 2 * hk) * d)))))))
+    bias = float([0.0, 1.0, 0.5][rng.integers(3)])
+    fused = hk > 0 and rng.random() < 0.6
+    return dtype, T, hq, hk, d, bias, fused
+
+
+@pytest.mark.parametrize("i", range(200))
+def test_qk_norm_random_cases(i):
+    """Seeded random head counts (q-only and k-only included), head sizes
+    (the vector bodies' sizes and arbitrary ones for the scalar body), token
+    counts, offsets, element types and layouts (separate q / k, or views into
+    one fused [q | k | v] buffer), every token against the oracle."""
+    test_qk_norm_matches_oracle(*_draw_qk(i))
