@@ -173,6 +173,87 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(inside)}
 
 
+class NvmlPoller:
+    """Read-only NVML queries (the driver's libnvidia-ml) of one GPU's SM
+    clock and clock-event reasons, every `period_s` on a background thread
+    while the timed regions run: nvidia-smi's own sampling gives one or two
+    samples over regions of a few milliseconds.  Silent when NVML cannot be
+    loaded (the nvidia-smi record stands alone then)."""
+
+    # NVML clock-event reason bits (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device, period_s: float = 0.0005):
+        self.period = period_s
+        self.samples: list[tuple[float, int, int]] = []
+        self.max_mhz = None
+        self.lib = self.handle = None
+        self.stop_flag = threading.Event()
+        self.thread = None
+        try:
+            import ctypes
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            h = ctypes.c_void_p()
+            pr = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(torch_device)
+            except Exception:
+                pass
+            ok = False
+            if pr is not None and hasattr(pr, "pci_bus_id"):
+                bus = (f"{getattr(pr, 'pci_domain_id', 0):08x}:{pr.pci_bus_id:02x}:"
+                       f"{pr.pci_device_id:02x}.0").encode()
+                ok = lib.nvmlDeviceGetHandleByPciBusId_v2(bus, ctypes.byref(h)) == 0
+            if not ok:
+                idx = torch_device.index if hasattr(torch_device, "index") else 0
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(idx or 0),
+                                                       ctypes.byref(h)) == 0
+            if not ok:
+                return
+            self.reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:  # 1 = SM clock
+                self.max_mhz = mx.value
+            self.lib, self.handle, self.ct = lib, h, ctypes
+        except Exception:
+            self.lib = None
+
+    def _run(self):
+        ct, lib, h = self.ct, self.lib, self.handle
+        clk, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self.stop_flag.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(clk)) == 0 and \
+                    self.reasons_fn(h, ct.byref(rs)) == 0:
+                self.samples.append((time.time(), clk.value, rs.value))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.lib is not None:
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+
+    def stop(self):
+        if self.thread is not None:
+            self.stop_flag.set()
+            self.thread.join(timeout=2)
+
+    def summary(self, t0: float, t1: float):
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if self.lib is None or not inside:
+            return None
+        reasons = sorted({name for _, _, r in inside for bit, name in self.REASONS.items()
+                          if r & bit})
+        mhz = [m for _, m, _ in inside]
+        return {"samples": len(inside), "sm_mhz": statistics.median(mhz), "sm_mhz_min": min(mhz),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "source": "NVML, every 0.5 ms inside the timed regions"}
+
+
 # ----------------------------------------------------------------- peaks, traffic
 
 def hbm_peak():
@@ -462,6 +543,8 @@ def run_ours(args, world, rank, local):
     R = max(1, args.regions)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
+    poller = NvmlPoller(device)
+    poller.start()
     t_wall0 = time.time()
     region_ms = []
     for reg in range(R):
@@ -476,6 +559,7 @@ def run_ours(args, world, rank, local):
         region_ms.append(reduce_max(start.elapsed_time(end), dist, device))
     t_wall1 = time.time()
     sampler.stop()
+    poller.stop()
     # Each timed region holds nothing but this kernel's K back-to-back
     # launches on one stream, so its average launch duration (launch gaps
     # included) is the region's time / K.  Reported: the median region (the
@@ -484,6 +568,9 @@ def run_ours(args, world, rank, local):
     max_ms = statistics.median(region_ms)
     max_kernel_ms = max_ms / K
     clocks = sampler.summary(t_wall0, t_wall1)
+    nv = poller.summary(t_wall0, t_wall1)
+    if nv is not None:
+        clocks["nvml"] = nv
     status = rn.rmsnorm_get_device_status()
 
     # ---- e2e through the public API: x from pinned host memory, y back to

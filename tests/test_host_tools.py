@@ -1,7 +1,7 @@
 """Host-side logic of the tuning sweep and the benchmark, on the CPU: the
 sweep's shared-memory formula agrees with the library's planner, its
-summary table, the benchmark's clock-sample reading and its lookup of the
-committed DRAM traffic figure."""
+summary table, the benchmark's clock-sample reading (nvidia-smi lines and
+NVML reason bits) and its lookup of the committed DRAM traffic figure."""
 import json
 
 import bench
@@ -101,3 +101,14 @@ def test_traffic_lookup_follows_workload_variant_and_sources():
     assert v is not None and abs(v / wl.bytes_per_call - 1) < 0.01
     assert bench.ncu_traffic(wl, "staged") is None
     assert bench.ncu_traffic(inputs.WORKLOADS["embed_bf16_8192x1024"], "cta_per_row") is None
+
+
+def test_nvml_summary_names_the_reason_bits_inside_the_window():
+    p = bench.NvmlPoller(None)          # no NVML here: a poller that reports nothing
+    assert p.summary(0.0, 1e12) is None
+    p.lib, p.max_mhz = object(), 2070   # stand-ins: summary() only reads the samples
+    p.samples = [(1.0, 1000, 0x8), (2.0, 2070, 0x0), (2.5, 2055, 0x4 | 0x20), (9.0, 900, 0x40)]
+    c = p.summary(1.5, 3.0)
+    assert c["samples"] == 2 and c["sm_mhz"] == 2062.5 and c["sm_mhz_min"] == 2055
+    assert c["reasons"] == ["sw_power_cap", "sw_thermal_slowdown"] and c["sm_max_mhz"] == 2070
+    assert p.summary(3.0, 4.0) is None
