@@ -49,7 +49,6 @@ constexpr uint64_t kDefaultWaitLimitNs = 1000000000ull; // one second
 // Host-buffer pipeline resources of one device (created on first use).
 constexpr int kPipeBuffers = 3;
 struct HostPipe {
-    bool ready = false;
     cudaStream_t in = nullptr, out = nullptr; // upload / download streams
     cudaEvent_t entry = nullptr;              // caller stream at entry
     cudaEvent_t loaded[kPipeBuffers] = {};    // upload of a buffer done
@@ -83,20 +82,20 @@ size_t grid_scratch_bytes(int sms)
 }
 std::mutex g_pipe_mu[kMaxDevices]; // one host-buffer call enqueues at a time per device
 
+// Releases whatever make_pipe created, also after it failed part way.
 void destroy_pipe(HostPipe *hp)
 {
     if (!hp)
         return;
-    if (hp->ready) {
-        cudaStreamDestroy(hp->in);
-        cudaStreamDestroy(hp->out);
+    for (cudaStream_t s : {hp->in, hp->out})
+        if (s)
+            cudaStreamDestroy(s);
+    if (hp->entry)
         cudaEventDestroy(hp->entry);
-        for (int b = 0; b < kPipeBuffers; ++b) {
-            cudaEventDestroy(hp->loaded[b]);
-            cudaEventDestroy(hp->computed[b]);
-            cudaEventDestroy(hp->drained[b]);
-        }
-    }
+    for (int b = 0; b < kPipeBuffers; ++b)
+        for (cudaEvent_t e : {hp->loaded[b], hp->computed[b], hp->drained[b]})
+            if (e)
+                cudaEventDestroy(e);
     delete hp;
 }
 
@@ -129,7 +128,6 @@ int make_pipe(HostPipe *hp)
             cudaEventCreateWithFlags(&hp->computed[b], ef) != cudaSuccess ||
             cudaEventCreateWithFlags(&hp->drained[b], ef) != cudaSuccess)
             return RMSNORM_ERR_CUDA;
-    hp->ready = true;
     return RMSNORM_OK;
 }
 std::atomic<uint64_t> g_wait_limit{kDefaultWaitLimitNs};
